@@ -1,0 +1,139 @@
+/*
+ * attn.h -- C ABI of libattn.so: tiled online-softmax scaled dot-product
+ * attention forward for NVIDIA GB300 (sm_103a).
+ *
+ * Plain C: every argument is a pointer or a scalar, no C++ or framework
+ * types.  All tensor pointers are DEVICE pointers owned by the caller; the
+ * library keeps no reference to them after the call returns, allocates no
+ * device memory and never synchronises inside attn_fwd.
+ */
+#ifndef GB300_ATTN_H
+#define GB300_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+enum attn_status {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1, /* a bad size, flag, null pointer or overlapping output      */
+    ATTN_ERR_UNSUPPORTED = 2, /* a valid request this build has no kernel for              */
+    ATTN_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed (see attn_last_cuda_error) */
+    ATTN_ERR_TIMEOUT = 4      /* a kernel gave up on a bounded wait (see attn_get_device_status) */
+};
+
+/* Element type of q, k, v and out. */
+enum attn_dtype { ATTN_F32 = 0, ATTN_F16 = 1, ATTN_BF16 = 2 };
+
+/* Layout of out. */
+enum attn_out_layout {
+    ATTN_OUT_HEAD_MAJOR = 0, /* [B, Hq, Sq, D]                                  */
+    ATTN_OUT_TOKEN_MAJOR = 1 /* [B, Sq, Hq*D]: out[(b*Sq + qi)*Hq*D + h*D + d]  */
+};
+
+/*
+ * attn_fwd -- attention forward for one batch of heads.
+ *
+ * Defined by "onnx-runtime-ep-cuda 0.1.0-dev.5, src/kernels/flash_attention.rs"
+ * (the kernel `flash_attention_body` and the host entry `run`): for every batch
+ * b, query head h and query row qi, with kv_head = h / (Hq / Hkv),
+ *
+ *   lsk        = total_lengths ? total_lengths[b] : Sk
+ *   causal_max = past_lengths ? past_lengths[b] + qi : lsk - Sq + qi
+ *   local_min  = local_window > 0 ? max(0, causal_max + 1 - local_window) : 0
+ *   key j in [0, Sk) is visible iff j < lsk, j >= local_min and
+ *                                     (causal == 0 or j <= causal_max)
+ *   s_j = scale * <q[b,h,qi,:], k[b,kv_head,j,:]>,
+ *         then softcap * tanh(s_j / softcap) when softcap > 0,
+ *         then + mask[plane, qi, j] when mask != NULL;
+ *   invisible keys get s_j = -inf (a select, never an add);
+ *   out[b,h,qi,:] = sum_j softmax(s)_j v[b,kv_head,j,:], or 0 when no key
+ *   has a finite score.
+ * The token-major layout is the transposed output of "pictor-kernels 0.1.0,
+ * src/gpu_backend/cuda_imagen_attn_kernels.rs" (module doc "The op"), with
+ * the batch outermost.
+ *
+ * Arguments (all pointers are device pointers, 16-byte aligned, caller-owned):
+ *   q             [B, Hq, Sq, D]            dtype
+ *   k, v          [B, Hkv, kv_capacity, D]  dtype; slots j >= min(lsk, Sk) may
+ *                                            hold any bits, NaN / Inf included:
+ *                                            they never reach the output
+ *   mask          NULL or f32 [mask_planes, Sq, Sk] (row stride Sk, 4-byte
+ *                 aligned); plane = b when mask_planes == B, b*Hq + h when
+ *                 mask_planes == B*Hq, else 0 (mask_planes == 1)
+ *   total_lengths NULL or int32 [B] (device): valid cache length per batch
+ *   past_lengths  NULL or int32 [B] (device): cached tokens before query row 0
+ *   out           output in the chosen layout, dtype; must not overlap q, k, v
+ *   B, Sq         >= 0 (0 is an empty problem: OK, nothing written)
+ *   Hq, Hkv, D    > 0, Hq % Hkv == 0
+ *   Sk            0 <= Sk <= kv_capacity; Sk == 0 writes zeros to out
+ *   causal        0 or 1;  local_window <= 0 means no window
+ *   scale         finite (callers usually pass 1/sqrt(D))
+ *   softcap       finite; <= 0 means no soft-capping
+ *   out_layout    enum attn_out_layout
+ *   mask_planes   0 (mask must be NULL), 1, B or B*Hq (mask must be non-NULL)
+ *   dtype         enum attn_dtype.  ATTN_F32 runs the fp32-exact CUDA-core
+ *                 kernel (1 <= D <= 128).  ATTN_F16 / ATTN_BF16 run the
+ *                 tensor-core (tcgen05) kernel: D must be 64 or 128, fp32
+ *                 accumulation, P rounded to the input type before P.V,
+ *                 output rounded to nearest even.
+ *   stream        a cudaStream_t (NULL = the legacy default stream)
+ *
+ * Behaviour: validates everything it can see on the host first; on any error
+ * it returns the status without launching or writing anything.  On success
+ * the work is enqueued on `stream` and the call returns without waiting.
+ * It allocates nothing, so it may be captured into a CUDA graph.
+ * Errors: ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED (D or dtype without a
+ * kernel, misaligned pointers or rows), ATTN_ERR_CUDA (launch failure).
+ * A kernel that times out on an internal wait is reported by
+ * attn_get_device_status, not by this call.
+ */
+int attn_fwd(const void *q, const void *k, const void *v, const float *mask,
+             const int32_t *total_lengths, const int32_t *past_lengths, void *out,
+             int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D,
+             int causal, int local_window, float scale, float softcap, int out_layout,
+             int mask_planes, int dtype, void *stream);
+
+/* Human-readable name of a status code; never NULL. */
+const char *attn_status_string(int status);
+
+/* The cudaError_t of the last CUDA failure seen by this library on the
+ * calling thread (0 if none). */
+int attn_last_cuda_error(void);
+
+/*
+ * attn_get_device_status -- synchronises `stream`, then reports and clears
+ * the device-side status word of the current device: ATTN_ERR_TIMEOUT if any
+ * kernel of this library gave up on a bounded wait since the last query,
+ * else ATTN_OK (or ATTN_ERR_CUDA if the synchronisation failed).
+ */
+int attn_get_device_status(void *stream);
+
+/*
+ * attn_set_wait_timeout_ns -- limit, in nanoseconds of %globaltimer, after
+ * which a kernel stops waiting on an internal barrier, records
+ * ATTN_ERR_TIMEOUT and exits.  Applies to launches made after the call.
+ * 0 restores the default (2 s).  Returns ATTN_OK.
+ */
+int attn_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/*
+ * attn_selftest_bounded_wait -- launches one small kernel that waits on a
+ * shared-memory barrier nobody arrives at, with the given limit, so that the
+ * timeout path can be exercised without hanging the GPU.  Synchronises
+ * `stream` and returns what attn_get_device_status would: ATTN_ERR_TIMEOUT
+ * when the wait ran out as designed.  timeout_ns must be in (0, 1e9].
+ */
+int attn_selftest_bounded_wait(uint64_t timeout_ns, void *stream);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_ATTN_H */

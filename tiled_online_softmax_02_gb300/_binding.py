@@ -1,0 +1,177 @@
+"""Thin ctypes binding over libattn.so (include/attn.h).
+
+Argument marshalling only: shapes are read off the tensors, the output is
+allocated with torch when the caller passes none, and the call goes to the C
+ABI on torch's current CUDA stream.  Every step of attention runs in the
+library's CUDA kernels; there is no fallback of any kind, and a missing
+library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
+ATTN_F32, ATTN_F16, ATTN_BF16 = 0, 1, 2
+DTYPE_CODES = {torch.float32: ATTN_F32, torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16}
+LAYOUTS = {"head": 0, "head_major": 0, 0: 0, "token": 1, "token_major": 1, 1: 1}
+
+# Every function include/attn.h declares, with its ctypes signature.
+_vp, _i32, _u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
+SIGNATURES = {
+    "attn_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                        _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                        _i32, _i32, ctypes.c_float, ctypes.c_float, _i32,
+                        _i32, _i32, _vp]),
+    "attn_status_string": (ctypes.c_char_p, [_i32]),
+    "attn_last_cuda_error": (_i32, []),
+    "attn_get_device_status": (_i32, [_vp]),
+    "attn_set_wait_timeout_ns": (_i32, [_u64]),
+    "attn_selftest_bounded_wait": (_i32, [_u64, _vp]),
+    "attn_version": (_i32, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library():
+    """Load libattn.so; raises if it has not been built (no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library {path} is missing: build it first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def attn_fwd(q, k, v, *, mask=None, total_lengths=None, past_lengths=None, causal=False,
+             local_window=0, scale=None, softcap=0.0, out_layout="head", seq_k=None, out=None):
+    """Attention forward through libattn.so.
+
+    q [B, Hq, Sq, D]; k, v [B, Hkv, kv_capacity, D] (same dtype: float32,
+    float16 or bfloat16); mask None or float32 [planes, Sq, Sk] (planes 1, B or
+    B*Hq; a 4-D [B, Hq, Sq, Sk] or [B, 1, Sq, Sk] mask is viewed as such);
+    total_lengths / past_lengths None or int32 [B]; seq_k = Sk (defaults to
+    kv_capacity).  out_layout "head" -> [B, Hq, Sq, D], "token" ->
+    [B, Sq, Hq*D].  scale defaults to 1/sqrt(D).
+
+    CUDA tensors: the call is enqueued on torch's current stream and returns
+    at once.  CPU tensors (ideally pinned): they are copied to the current
+    CUDA device, the kernel runs, and the output is copied back into a CPU
+    tensor (the end-to-end path).
+    """
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D: [B, H, S, D]")
+    B, Hq, Sq, D = q.shape
+    Hkv, kv_capacity = k.shape[1], k.shape[2]
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != D:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    if q.dtype not in DTYPE_CODES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype among float32 / float16 / bfloat16")
+    Sk = kv_capacity if seq_k is None else int(seq_k)
+    layout = LAYOUTS[out_layout]
+    mask_planes = 0
+    if mask is not None:
+        if mask.dtype != torch.float32:
+            raise ValueError("mask must be float32")
+        if mask.dim() == 4:
+            mask = mask.reshape(-1, mask.shape[-2], mask.shape[-1])
+        if mask.dim() != 3:
+            raise ValueError("mask must be [planes, Sq, Sk]")
+        mask_planes = mask.shape[0]
+    for name, t in (("total_lengths", total_lengths), ("past_lengths", past_lengths)):
+        if t is not None and (t.dtype != torch.int32 or t.numel() != B):
+            raise ValueError(f"{name} must be int32 [B]")
+    for t in (q, k, v, mask, total_lengths, past_lengths):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+        if t is not None and t.device != q.device:
+            raise ValueError("all tensors must be on the same device")
+    host = not q.is_cuda
+    host_out = None
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+
+        def up(t):
+            return None if t is None else t.to(dev, non_blocking=True)
+        q, k, v, mask, total_lengths, past_lengths = map(up, (q, k, v, mask, total_lengths,
+                                                               past_lengths))
+        host_out, out = out, None
+    shape = (B, Hq, Sq, D) if layout == 0 else (B, Sq, Hq * D)
+    if out is None:
+        out = torch.empty(shape, dtype=q.dtype, device=q.device)
+    elif tuple(out.shape) != shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous {q.dtype} tensor of shape {shape}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(total_lengths),
+                          _ptr(past_lengths), _ptr(out), B, Hq, Hkv, Sq, Sk, kv_capacity, D,
+                          int(bool(causal)), int(local_window), float(scale), float(softcap),
+                          layout, mask_planes, DTYPE_CODES[q.dtype], _stream_handle(q.device))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    if host:
+        if host_out is None:
+            host_out = torch.empty(shape, dtype=q.dtype, pin_memory=True)
+        host_out.copy_(out, non_blocking=True)
+        torch.cuda.current_stream(q.device).synchronize()
+        return host_out
+    return out
+
+
+def get_device_status(device=None) -> int:
+    """Synchronises the current stream and returns (and clears) the device
+    status word: ATTN_OK or ATTN_ERR_TIMEOUT."""
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        return load_library().attn_get_device_status(_stream_handle(dev))
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    load_library().attn_set_wait_timeout_ns(int(ns))
+
+
+def selftest_bounded_wait(timeout_ns: int, device=None) -> int:
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        return load_library().attn_selftest_bounded_wait(int(timeout_ns), _stream_handle(dev))

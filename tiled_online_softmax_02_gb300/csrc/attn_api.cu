@@ -1,0 +1,276 @@
+// attn_api.cu -- the C ABI of libattn.so (declared in include/attn.h):
+// argument validation, tensor-map encoding, kernel dispatch and the device
+// status word.
+//
+// Host entry modelled on `run` of "onnx-runtime-ep-cuda 0.1.0-dev.5,
+// src/kernels/flash_attention.rs": a capability gate (unsupported requests
+// return a distinct status, never a silent fallback), dtype dispatch, checked
+// narrowing of sizes and of the grid, then one launch.  Unlike that host code
+// the call is asynchronous (no synchronisation after the launch) and an
+// empty key range (Sk == 0) writes zeros instead of leaving the output
+// untouched.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/attn.h"
+#include "attn_internal.h"
+#include "device_common.cuh"
+
+namespace gb300_attn {
+namespace {
+
+__device__ int g_status_word;  // ORed kStatus* bits from every kernel
+
+thread_local int t_last_cuda_error = 0;
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return ATTN_ERR_CUDA;
+}
+
+// Device address of g_status_word on the current device (looked up once per
+// device with that device current).
+int* status_ptr(int* err) {
+  static std::mutex mu;
+  static int* cache[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 128) {
+    *err = cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice);
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_status_word);
+    if (e != cudaSuccess) {
+      *err = cuda_fail(e);
+      return nullptr;
+    }
+    cache[dev] = static_cast<int*>(ptr);
+  }
+  return cache[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn(int* err) {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static cudaError_t init_err = cudaSuccess;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    init_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                                cudaEnableDefault, &q);
+    if (init_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    else if (init_err == cudaSuccess)
+      init_err = cudaErrorSymbolNotFound;
+  });
+  if (!fn) *err = cuda_fail(init_err);
+  return fn;
+}
+
+// 16-bit tensor [planes, rows, D] as a 3-D TMA map with a {64, 128, 1} box and
+// the 128-byte swizzle the tcgen05 shared-memory descriptors expect.  Rows and
+// planes out of range read as zero.
+int encode_map(CUtensorMap* map, const void* base, bool bf16, int64_t planes, int64_t rows, int D) {
+  int err = ATTN_OK;
+  auto fn = encode_fn(&err);
+  if (!fn) return err;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * (cuuint64_t)D * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kTcBlockM, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return ATTN_OK;
+}
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  if (a < 0 || b < 0) return false;
+  if (a != 0 && b > (INT64_C(1) << 62) / a) return false;
+  *out = a * b;
+  return true;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+  if (!a || !b || abytes <= 0 || bbytes <= 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + (uintptr_t)bbytes && b0 < a0 + (uintptr_t)abytes;
+}
+
+__global__ void selftest_wait_kernel(uint64_t timeout_ns, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t a = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(a, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  // Nobody arrives on this barrier: the wait must run out and record it.
+  if (threadIdx.x == 0) mbar_wait(a, 0, timeout_ns, status);
+  __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, int* status, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(timeout_ns, status);
+  return cudaGetLastError();
+}
+
+}  // namespace gb300_attn
+
+using namespace gb300_attn;
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, const float* mask,
+                        const int32_t* total_lengths, const int32_t* past_lengths, void* out,
+                        int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D,
+                        int causal, int local_window, float scale, float softcap, int out_layout,
+                        int mask_planes, int dtype, void* stream) {
+  // ---------------------------------------------------------------- validation
+  if (dtype != ATTN_F32 && dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (B < 0 || Sq < 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (Sk < 0 || kv_capacity < Sk) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (out_layout != ATTN_OUT_HEAD_MAJOR && out_layout != ATTN_OUT_TOKEN_MAJOR) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !std::isfinite(softcap)) return ATTN_ERR_INVALID_ARG;
+  const int64_t BHq = (int64_t)B * Hq;
+  if (mask_planes < 0) return ATTN_ERR_INVALID_ARG;
+  if (mask_planes == 0 && mask != nullptr) return ATTN_ERR_INVALID_ARG;
+  if (mask_planes > 0) {
+    if (mask == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (mask_planes != 1 && mask_planes != B && (int64_t)mask_planes != BHq) return ATTN_ERR_INVALID_ARG;
+  }
+  const int64_t esize = dtype == ATTN_F32 ? 4 : 2;
+  int64_t q_elems, kv_elems, mask_elems = 0, t;
+  if (!mul_ok(BHq, Sq, &t) || !mul_ok(t, D, &q_elems)) return ATTN_ERR_INVALID_ARG;
+  if (!mul_ok((int64_t)B * Hkv, kv_capacity, &t) || !mul_ok(t, D, &kv_elems)) return ATTN_ERR_INVALID_ARG;
+  if (mask_planes > 0 && (!mul_ok(mask_planes, Sq, &t) || !mul_ok(t, Sk, &mask_elems)))
+    return ATTN_ERR_INVALID_ARG;
+  if (q_elems > (INT64_C(1) << 60) / esize || kv_elems > (INT64_C(1) << 60) / esize)
+    return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || Sq == 0) return ATTN_OK;  // empty problem: nothing to write
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hq > 65535) return ATTN_ERR_INVALID_ARG;  // grid.z / grid.y
+  const int64_t qbytes = q_elems * esize, kvbytes = kv_elems * esize, mbytes = mask_elems * 4;
+  if (overlaps(out, qbytes, q, qbytes) || overlaps(out, qbytes, k, kvbytes) ||
+      overlaps(out, qbytes, v, kvbytes) || overlaps(out, qbytes, mask, mbytes))
+    return ATTN_ERR_INVALID_ARG;
+
+  // capability gate: no kernel, no launch
+  if (dtype == ATTN_F32 && D > 128) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_F32 && D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return ATTN_ERR_UNSUPPORTED;
+  if (mask && !aligned(mask, 4)) return ATTN_ERR_UNSUPPORTED;
+  if ((total_lengths && !aligned(total_lengths, 4)) || (past_lengths && !aligned(past_lengths, 4)))
+    return ATTN_ERR_UNSUPPORTED;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (Sk == 0) {  // no key at all: every row is 0
+    cudaError_t e = cudaMemsetAsync(out, 0, (size_t)qbytes, st);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+  }
+
+  int err = ATTN_OK;
+  int* status = status_ptr(&err);
+  if (!status) return err;
+
+  CommonParams c{};
+  c.total_lengths = total_lengths;
+  c.past_lengths = past_lengths;
+  c.mask = mask_planes > 0 ? mask : nullptr;
+  c.out = out;
+  c.B = B; c.Hq = Hq; c.Hkv = Hkv; c.Sq = Sq; c.Sk = Sk; c.kv_capacity = kv_capacity; c.D = D;
+  c.group = Hq / Hkv;
+  c.causal = causal;
+  c.local_window = local_window > 0 ? local_window : 0;
+  c.out_layout = out_layout;
+  c.mask_planes = mask_planes;
+  c.mask_vec4 = (mask && aligned(mask, 16) && (Sk % 4) == 0) ? 1 : 0;
+  c.scale = scale;
+  c.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  c.softcap = softcap > 0.0f ? softcap : 0.0f;
+  c.inv_softcap = softcap > 0.0f ? 1.0f / softcap : 0.0f;
+  c.timeout_ns = g_timeout_ns.load();
+  c.status = status;
+
+  cudaError_t e;
+  if (dtype == ATTN_F32) {
+    F32Params fp{};
+    fp.q = static_cast<const float*>(q);
+    fp.k = static_cast<const float*>(k);
+    fp.v = static_cast<const float*>(v);
+    fp.c = c;
+    e = launch_attn_f32(fp, st);
+  } else {
+    const bool bf16 = dtype == ATTN_BF16;
+    TcParams tp{};
+    tp.c = c;
+    int rc = encode_map(&tp.tmap_q, q, bf16, BHq, Sq, D);
+    if (rc == ATTN_OK) rc = encode_map(&tp.tmap_k, k, bf16, (int64_t)B * Hkv, kv_capacity, D);
+    if (rc == ATTN_OK) rc = encode_map(&tp.tmap_v, v, bf16, (int64_t)B * Hkv, kv_capacity, D);
+    if (rc != ATTN_OK) return rc;
+    e = launch_attn_tc(tp, bf16, st);
+  }
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+extern "C" const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    default: return "ATTN_UNKNOWN_STATUS";
+  }
+}
+
+extern "C" int attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+extern "C" int attn_get_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (word != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return (word & kStatusTimeout) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+extern "C" int attn_set_wait_timeout_ns(uint64_t timeout_ns) {
+  g_timeout_ns.store(timeout_ns == 0 ? 2000000000ull : timeout_ns);
+  return ATTN_OK;
+}
+
+extern "C" int attn_selftest_bounded_wait(uint64_t timeout_ns, void* stream) {
+  if (timeout_ns == 0 || timeout_ns > 1000000000ull) return ATTN_ERR_INVALID_ARG;
+  int err = ATTN_OK;
+  int* status = status_ptr(&err);
+  if (!status) return err;
+  cudaError_t e = launch_selftest_wait(timeout_ns, status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return attn_get_device_status(stream);
+}
+
+extern "C" int attn_version(void) { return 100; }

@@ -1,0 +1,288 @@
+// attn_f32.cu -- fp32-exact attention forward on CUDA cores (FFMA), for
+// callers that need fp32 parity (no tensor cores, no 16-bit staging).
+//
+// Same method as the tensor-core kernel -- the tiled online softmax of
+// "onnx-runtime-ep-cuda 0.1.0-dev.5, src/kernels/flash_attention.rs"
+// (`flash_attention_body`) with every operand, score, probability and
+// accumulator in fp32, as the parity-first design of "pictor-kernels 0.1.0,
+// src/gpu_backend/cuda_imagen_attn_kernels.rs" (module doc "Parity-first
+// design") asks.  The pages' scalar kernels give each warp one query row and
+// re-read Q per key; here a 256-thread CTA owns 64 query rows and walks the
+// keys in tiles of 64, with both products register-tiled:
+//   S tile (64 x 64): thread (ty, tx) owns rows ty + 16 i and keys tx + 16 j
+//                     (i, j < 4), 16 FFMA per 8 shared-memory vector loads;
+//   O tile (64 x D):  thread owns rows ty + 16 i and columns 4 tx + 64 g.
+// Row max / sum reductions run over the 16 lanes that share a row.
+#include "device_common.cuh"
+
+namespace gb300_attn {
+namespace {
+
+constexpr int BM = kF32BlockM;  // 64 query rows
+constexpr int BN = 64;          // keys per tile
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int DP>
+struct F32Config {
+  static constexpr int kQStride = DP + 4;  // padded rows: conflict-free float4 reads
+  static constexpr int kKStride = DP + 4;
+  static constexpr int kVStride = DP;
+  static constexpr int kPStride = BN + 4;
+  static constexpr int kGroups = DP / 64;  // float4 column groups per O row per thread
+  static constexpr size_t kSmemFloats =
+      (size_t)BM * kQStride + (size_t)BN * kKStride + (size_t)BN * kVStride + (size_t)BM * kPStride;
+  static constexpr size_t kSmemBytes = kSmemFloats * sizeof(float);
+};
+
+// Loads rows [row0, row0 + nrows) of a [rows, D] fp32 matrix into shared memory
+// with row stride `sstride`, zero-filling rows >= valid_rows and columns >= D.
+template <int DP>
+__device__ __forceinline__ void load_rows(float* dst, int sstride, const float* src, int64_t row0,
+                                          int nrows, int64_t valid_rows, int D, bool vec4) {
+  if (vec4) {
+    constexpr int kVecPerRow = DP / 4;
+    for (int idx = threadIdx.x; idx < nrows * kVecPerRow; idx += kThreads) {
+      const int r = idx / kVecPerRow;
+      const int c = (idx % kVecPerRow) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (row0 + r < valid_rows && c < D)
+        v = __ldg(reinterpret_cast<const float4*>(src + (row0 + r) * (int64_t)D + c));
+      *reinterpret_cast<float4*>(dst + r * sstride + c) = v;
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < nrows * DP; idx += kThreads) {
+      const int r = idx / DP;
+      const int c = idx % DP;
+      float v = 0.f;
+      if (row0 + r < valid_rows && c < D) v = __ldg(src + (row0 + r) * (int64_t)D + c);
+      dst[r * sstride + c] = v;
+    }
+  }
+}
+
+template <int DP, bool SOFTCAP, bool MASK>
+__global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_constant__ F32Params P) {
+  using Cfg = F32Config<DP>;
+  const CommonParams& p = P.c;
+  extern __shared__ __align__(16) float fsm[];
+  float* Qs = fsm;
+  float* Ks = Qs + BM * Cfg::kQStride;
+  float* Vs = Ks + BN * Cfg::kKStride;
+  float* Ps = Vs + BN * Cfg::kVStride;
+
+  const int tx = threadIdx.x & 15;
+  const int ty = threadIdx.x >> 4;
+  const int n_qt = (p.Sq + BM - 1) / BM;
+  const int qt = n_qt - 1 - (int)blockIdx.x;
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int kvh = h / p.group;
+  const int64_t q0 = (int64_t)qt * BM;
+  const int D = p.D;
+  const bool vec4 = (D % 4) == 0;
+
+  const BatchLimits L = batch_limits(p, b);
+  const TileRange T = tile_range(p, L, q0, BM, BN);
+  int64_t zero_from = L.lsk < (int64_t)p.Sk ? L.lsk : (int64_t)p.Sk;  // garbage slots start here
+  if (zero_from < 0) zero_from = 0;
+
+  const float* qplane = P.q + ((int64_t)b * p.Hq + h) * (int64_t)p.Sq * D;
+  const float* kplane = P.k + ((int64_t)b * p.Hkv + kvh) * (int64_t)p.kv_capacity * D;
+  const float* vplane = P.v + ((int64_t)b * p.Hkv + kvh) * (int64_t)p.kv_capacity * D;
+  load_rows<DP>(Qs, Cfg::kQStride, qplane, q0, BM, p.Sq, D, vec4);
+
+  RowLimits R[4];
+  const float* mrow[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t qi = q0 + ty + 16 * i;
+    R[i] = row_limits(p, L, qi);
+    mrow[i] = nullptr;
+    if constexpr (MASK) {
+      int64_t plane = 0;
+      if (p.mask_planes == p.B) plane = b;
+      else if (p.mask_planes == p.B * p.Hq) plane = (int64_t)b * p.Hq + h;
+      if (qi < p.Sq) mrow[i] = p.mask + (plane * p.Sq + qi) * (int64_t)p.Sk;
+    }
+  }
+
+  float m[4], l[4];
+  float o[4][Cfg::kGroups][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+#pragma unroll
+    for (int g = 0; g < Cfg::kGroups; ++g)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) o[i][g][u] = 0.f;
+  }
+
+  for (int t = T.t_begin; t < T.t_end; ++t) {
+    const int64_t key0 = (int64_t)t * BN;
+    __syncthreads();  // previous tile's K / V / P no longer in use
+    load_rows<DP>(Ks, Cfg::kKStride, kplane, key0, BN, zero_from, D, vec4);
+    load_rows<DP>(Vs, Cfg::kVStride, vplane, key0, BN, zero_from, D, vec4);
+    __syncthreads();
+
+    // S = Q K^T for this thread's 4 x 4 block
+    float s[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+#pragma unroll 4
+    for (int d0 = 0; d0 < DP; d0 += 4) {
+      float4 qa[4], kb[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        qa[i] = *reinterpret_cast<const float4*>(Qs + (ty + 16 * i) * Cfg::kQStride + d0);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        kb[j] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * j) * Cfg::kKStride + d0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          s[i][j] = fmaf(qa[i].x, kb[j].x, s[i][j]);
+          s[i][j] = fmaf(qa[i].y, kb[j].y, s[i][j]);
+          s[i][j] = fmaf(qa[i].z, kb[j].z, s[i][j]);
+          s[i][j] = fmaf(qa[i].w, kb[j].w, s[i][j]);
+        }
+    }
+
+    // scores in log2 units; invisible keys -> -inf (a select)
+    const bool need_mask = !(key0 >= T.full_lo && key0 + BN <= T.full_hi);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t kj = key0 + tx + 16 * j;
+        float v;
+        if (SOFTCAP || MASK) {
+          v = s[i][j] * p.scale;
+          if constexpr (SOFTCAP) v = soft_cap(v, p.softcap, p.inv_softcap);
+          if constexpr (MASK) {
+            if (mrow[i] != nullptr && kj < (int64_t)p.Sk) v += __ldg(mrow[i] + kj);
+          }
+          v *= kLog2e;
+        } else {
+          v = s[i][j] * p.scale_log2;
+        }
+        if (need_mask && !(kj >= R[i].lo && kj < R[i].hi)) v = -INFINITY;
+        s[i][j] = v;
+      }
+    }
+
+    // online softmax update per row (the tile update of the page's kernel)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float mt = fmaxf(fmaxf(s[i][0], s[i][1]), fmaxf(s[i][2], s[i][3]));
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+      const float m_new = fmaxf(m[i], mt);
+      const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = (m[i] == -INFINITY) ? 0.f : fast_exp2(m[i] - m_new);
+      float rs = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float e = fast_exp2(s[i][j] - m_sub);
+        s[i][j] = e;
+        rs += e;
+      }
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) rs += __shfl_xor_sync(0xffffffffu, rs, off);
+      l[i] = l[i] * alpha + rs;
+      m[i] = m_new;
+#pragma unroll
+      for (int g = 0; g < Cfg::kGroups; ++g)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) o[i][g][u] *= alpha;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) Ps[(ty + 16 * i) * Cfg::kPStride + tx + 16 * j] = s[i][j];
+    }
+    __syncthreads();
+
+    // O += P V
+#pragma unroll 2
+    for (int k0 = 0; k0 < BN; k0 += 4) {
+      float4 pa[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        pa[i] = *reinterpret_cast<const float4*>(Ps + (ty + 16 * i) * Cfg::kPStride + k0);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+        for (int g = 0; g < Cfg::kGroups; ++g) {
+          const float4 vb = *reinterpret_cast<const float4*>(Vs + (k0 + kk) * Cfg::kVStride + g * 64 + tx * 4);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float pk = kk == 0 ? pa[i].x : kk == 1 ? pa[i].y : kk == 2 ? pa[i].z : pa[i].w;
+            o[i][g][0] = fmaf(pk, vb.x, o[i][g][0]);
+            o[i][g][1] = fmaf(pk, vb.y, o[i][g][1]);
+            o[i][g][2] = fmaf(pk, vb.z, o[i][g][2]);
+            o[i][g][3] = fmaf(pk, vb.w, o[i][g][3]);
+          }
+        }
+      }
+    }
+  }
+
+  // normalise and store
+  float* out = reinterpret_cast<float*>(p.out);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t qi = q0 + ty + 16 * i;
+    if (qi >= p.Sq) continue;
+    const float inv = l[i] > 0.f ? 1.0f / l[i] : 0.f;
+    int64_t base;
+    if (p.out_layout == 0)
+      base = (((int64_t)b * p.Hq + h) * p.Sq + qi) * D;
+    else
+      base = (((int64_t)b * p.Sq + qi) * p.Hq + h) * D;
+#pragma unroll
+    for (int g = 0; g < Cfg::kGroups; ++g) {
+      const int c = g * 64 + tx * 4;
+      if (vec4) {
+        if (c < D)
+          *reinterpret_cast<float4*>(out + base + c) =
+              make_float4(o[i][g][0] * inv, o[i][g][1] * inv, o[i][g][2] * inv, o[i][g][3] * inv);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (c + u < D) out[base + c + u] = o[i][g][u] * inv;
+      }
+    }
+  }
+}
+
+template <int DP, bool SOFTCAP, bool MASK>
+cudaError_t launch_variant(const F32Params& P, cudaStream_t stream) {
+  auto kernel = attn_fwd_f32_kernel<DP, SOFTCAP, MASK>;
+  constexpr size_t smem = F32Config<DP>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)((P.c.Sq + BM - 1) / BM), (unsigned)P.c.Hq, (unsigned)P.c.B);
+  kernel<<<grid, kThreads, smem, stream>>>(P);
+  return cudaGetLastError();
+}
+
+template <int DP>
+cudaError_t launch_dp(const F32Params& P, cudaStream_t stream) {
+  const bool sc = P.c.softcap > 0.0f;
+  const bool mk = P.c.mask != nullptr && P.c.mask_planes > 0;
+  if (sc && mk) return launch_variant<DP, true, true>(P, stream);
+  if (sc) return launch_variant<DP, true, false>(P, stream);
+  if (mk) return launch_variant<DP, false, true>(P, stream);
+  return launch_variant<DP, false, false>(P, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_f32(const F32Params& P, cudaStream_t stream) {
+  if (P.c.D <= 64) return launch_dp<64>(P, stream);
+  return launch_dp<128>(P, stream);
+}
+
+}  // namespace gb300_attn

@@ -1,0 +1,55 @@
+// attn_internal.h -- parameter blocks and launchers shared between the C ABI
+// layer (attn_api.cu) and the kernels (attn_tc.cu, attn_f32.cu).  Not part
+// of the public interface.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gb300_attn {
+
+// Problem description common to every kernel.  Sizes are validated by the
+// API layer before any kernel sees them.
+struct CommonParams {
+  const int32_t* total_lengths;  // [B] or nullptr
+  const int32_t* past_lengths;   // [B] or nullptr
+  const float* mask;             // [mask_planes, Sq, Sk] or nullptr
+  void* out;
+  int B, Hq, Hkv, Sq, Sk, kv_capacity, D, group;
+  int causal, local_window, out_layout, mask_planes;
+  int mask_vec4;      // 1: every mask row starts 16-byte aligned (Sk % 4 == 0)
+  float scale;        // softmax scale
+  float scale_log2;   // scale * log2(e)
+  float softcap;      // > 0: soft-cap value c
+  float inv_softcap;  // 1 / c
+  uint64_t timeout_ns;
+  int* status;        // device status word (timeouts)
+};
+
+// tcgen05 kernel: Q / K / V reach shared memory through TMA tensor maps.
+struct TcParams {
+  CUtensorMap tmap_q;  // dims {D, Sq, B*Hq},          box {64, 128, 1}, 128B swizzle
+  CUtensorMap tmap_k;  // dims {D, kv_capacity, B*Hkv}, box {64, 128, 1}, 128B swizzle
+  CUtensorMap tmap_v;  // same as tmap_k
+  CommonParams c;
+};
+
+// fp32 CUDA-core kernel.
+struct F32Params {
+  const float* q;
+  const float* k;
+  const float* v;
+  CommonParams c;
+};
+
+constexpr int kTcBlockM = 128;  // query rows per tcgen05 CTA
+constexpr int kTcBlockN = 128;  // keys per tcgen05 tile
+constexpr int kF32BlockM = 64;  // query rows per fp32 CTA
+
+// Launchers.  They assume validated parameters.
+cudaError_t launch_attn_tc(const TcParams& p, bool bf16, cudaStream_t stream);
+cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream);
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, int* status, cudaStream_t stream);
+
+}  // namespace gb300_attn
