@@ -58,8 +58,8 @@ struct TcConfig {
   static constexpr uint32_t kOffK = kOffQ + kTileBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
   static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
-  // q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], pv_done, drain
-  static constexpr int kNumBars = 1 + 3 * kStages + 2 + 2 + 1 + 1;
+  // q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], pv_done, drain, o_final
+  static constexpr int kNumBars = 1 + 3 * kStages + 2 + 2 + 1 + 1 + 1;
   static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kOffTmemSlot + 16 + 1024;  // + 1024 alignment slack
 };
@@ -97,6 +97,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
   auto bar_p = [&](int i) { return bar0 + 8u * (1 + 3 * S + 2 + i); };
   const uint32_t bar_pv = bar0 + 8u * (1 + 3 * S + 4);
   const uint32_t bar_drain = bar0 + 8u * (1 + 3 * S + 5);
+  // Completes once, after the last P.V.  The epilogue cannot wait on pv_done:
+  // by then pv_done may still be two phases short, which a parity wait cannot
+  // tell from done.
+  const uint32_t bar_o_final = bar0 + 8u * (1 + 3 * S + 6);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmemSlot);
 
   const int warp = threadIdx.x >> 5;
@@ -125,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
     }
     mbar_init(bar_pv, 1);
     mbar_init(bar_drain, 1);
+    mbar_init(bar_o_final, 1);
     mbar_init_fence();
   }
   if (warp == kTmaWarp && lane == 0) {
@@ -241,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
         __syncwarp();
         if (n >= 1 && !issue_pv(n - 1)) { ok = false; break; }
       }
-      if (ok) issue_pv(n_tiles - 1);
+      if (ok && issue_pv(n_tiles - 1) && lane == 0) tc_commit(bar_o_final);
       // Wait for every MMA this warp issued before tensor memory is freed.
       if (lane == 0) tc_commit(bar_drain);
       __syncwarp();
@@ -388,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
     // ---------------------------------------------------------- epilogue
     bool have_o = ok && n_tiles > 0;
     if (have_o) {
-      have_o = mbar_wait_warp(bar_pv, (n_tiles - 1) & 1, p.timeout_ns, p.status);
+      have_o = mbar_wait_warp(bar_o_final, 0, p.timeout_ns, p.status);
       tc_fence_after();
     }
     if (ok) {

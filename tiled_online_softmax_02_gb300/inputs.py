@@ -158,6 +158,7 @@ def sample_rows(w: Workload, n: int, seed: int = 7) -> np.ndarray:
     that matters plus seeded random rows.  Used to check full-size outputs on
     rows the oracle computes one by one."""
     rng = np.random.Generator(np.random.PCG64(seed))
+    n = min(n, w.B * w.Hq * w.Sq)  # never ask for more rows than exist
     picks = set()
     for b in {0, w.B - 1}:
         for h in {0, w.Hq - 1, min(w.group, w.Hq - 1)}:
