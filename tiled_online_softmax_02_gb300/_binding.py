@@ -48,7 +48,8 @@ class AttnError(RuntimeError):
 
 
 def library_path() -> str:
-    return _build.LIB
+    """The in-tree libattn.so, or the file GB300_ATTN_LIBRARY names."""
+    return os.environ.get("GB300_ATTN_LIBRARY") or _build.LIB
 
 
 def load_library():

@@ -43,15 +43,20 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: tuple[str, ...] = ()) -> str:
-    """Compile every csrc/*.cu for sm_103a and link libattn.so; returns its path."""
-    if not force and not extra_flags and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra_flags: tuple[str, ...] = (),
+          out_path: str | None = None) -> str:
+    """Compile every csrc/*.cu for sm_103a and link libattn.so; returns its path.
+    ``extra_flags`` / ``out_path`` build a variant next to (not over) the
+    default library, e.g. with a different -D setting."""
+    lib = out_path or LIB
+    if not force and not extra_flags and out_path is None and up_to_date():
         return LIB
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    objdir = BUILD if out_path is None else os.path.join(BUILD, "variant_" + os.path.basename(lib))
+    os.makedirs(objdir, exist_ok=True)
     procs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -67,10 +72,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags: tuple[str, ..
         objs.append(obj)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     subprocess.run([nvcc, "-shared", *ARCH, "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

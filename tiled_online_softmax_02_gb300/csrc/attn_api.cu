@@ -167,6 +167,8 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, const float
   if (B == 0 || Sq == 0) return ATTN_OK;  // empty problem: nothing to write
   if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
   if (B > 65535 || Hq > 65535) return ATTN_ERR_INVALID_ARG;  // grid.z / grid.y
+  if ((int64_t)((Sq + 2 * kTcBlockM - 1) / (2 * kTcBlockM)) * BHq > INT32_MAX)
+    return ATTN_ERR_INVALID_ARG;  // work items of the persistent tensor-core kernel
   const int64_t qbytes = q_elems * esize, kvbytes = kv_elems * esize, mbytes = mask_elems * 4;
   if (overlaps(out, qbytes, q, qbytes) || overlaps(out, qbytes, k, kvbytes) ||
       overlaps(out, qbytes, v, kvbytes) || overlaps(out, qbytes, mask, mbytes))

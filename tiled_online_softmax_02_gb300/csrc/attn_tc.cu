@@ -9,7 +9,11 @@
 // 8 query rows x 16 keys through shared memory with scalar FMAs (and a wmma
 // variant with 16x16 tiles); this kernel is a GB300 design of the same method.
 //
-// CTA = two 128-row query tiles (t = 0, 1) of one (b, h); key tiles of 128.
+// Work item = two 128-row query tiles (t = 0, 1) of one (b, h).  The kernel is
+// persistent: one CTA per SM walks a static snake order over the items
+// (latest query rows -- the longest causal rows -- first), and the K/V ring,
+// barrier phases and tensor memory carry over from item to item, so the next
+// item's loads overlap the current item's tail.
 //   warps 0-3   softmax for query tile 0, warps 4-7 for query tile 1: thread
 //               r of a warpgroup owns query row r (= TMEM lane r).  Reads its
 //               S row with tcgen05.ld, applies the structural masks (select to
@@ -18,7 +22,7 @@
 //               and rescales its O row when the max grew by more than 2^8
 //               (otherwise the old max is kept: the final O / l is exact
 //               either way).  Then normalises and stores the row.
-//   warp 8      TMA producer: both Q tiles once, then K_j / V_j into a ring.
+//   warp 8      TMA producer: both Q tiles per item, K_j / V_j into a ring.
 //   warp 9      MMA issuer (one thread) and owner of tensor memory.  Per key
 //               tile j, for t = 0, 1:  O_t += P_t(j-1) V(j-1), then
 //               S_t(j) = Q_t K(j)^T.  While warpgroup 0 turns S_0 into P_0,
@@ -47,7 +51,7 @@ namespace {
 
 constexpr int BM = kTcBlockM;   // rows per query tile
 constexpr int BN = kTcBlockN;   // keys per key tile
-constexpr int kQTiles = 2;      // query tiles per CTA
+constexpr int kQTiles = 2;      // query tiles per work item
 constexpr int kThreads = 320;   // 8 softmax warps + producer + MMA
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -66,11 +70,77 @@ struct TcConfig {
   static constexpr uint32_t kOffK = kOffQ + kQTiles * kTileBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
   static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
-  // q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_final[2], drain
-  static constexpr int kNumBars = 1 + 3 * kStages + 2 + 2 + 2 + 1;
+  // q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_final[2], drain
+  static constexpr int kNumBars = 2 + 3 * kStages + 2 + 2 + 2 + 1;
   static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kOffTmemSlot + 16 + 1024;  // + 1024 alignment slack
 };
+
+// Shared-memory addresses of the tiles and barriers.
+template <int D>
+struct Smem {
+  using Cfg = TcConfig<D>;
+  static constexpr int S = Cfg::kStages;
+  uint8_t* base;
+  uint32_t sQ, sK, sV, bar0;
+  __device__ uint32_t q_full() const { return bar0; }
+  __device__ uint32_t q_empty() const { return bar0 + 8u; }
+  __device__ uint32_t k_full(int s) const { return bar0 + 8u * (2 + s); }
+  __device__ uint32_t v_full(int s) const { return bar0 + 8u * (2 + S + s); }
+  __device__ uint32_t kv_empty(int s) const { return bar0 + 8u * (2 + 2 * S + s); }
+  __device__ uint32_t s_full(int t) const { return bar0 + 8u * (2 + 3 * S + t); }
+  __device__ uint32_t p_full(int t) const { return bar0 + 8u * (2 + 3 * S + 2 + t); }
+  // completes once per item, after query tile t's last P.V (the epilogue's wait)
+  __device__ uint32_t o_final(int t) const { return bar0 + 8u * (2 + 3 * S + 4 + t); }
+  __device__ uint32_t drain() const { return bar0 + 8u * (2 + 3 * S + 6); }
+};
+
+// One work item: two query tiles of one (b, h), their key-tile ranges and
+// the union [tb, tb + N) the item streams.
+struct Item {
+  int b, h, kvh;
+  int64_t q0;
+  BatchLimits L;
+  TileRange tr[kQTiles];
+  int tb, N;
+  __device__ bool active(int t, int j) const { return j >= tr[t].t_begin && j < tr[t].t_end; }
+};
+
+__device__ __forceinline__ Item make_item(const CommonParams& p, int idx) {
+  const int bh = p.B * p.Hq;
+  const int n_qp = (p.Sq + kQTiles * BM - 1) / (kQTiles * BM);
+  Item it;
+  const int qp = n_qp - 1 - idx / bh;  // latest query rows first
+  const int rem = idx - (idx / bh) * bh;
+  it.b = rem / p.Hq;
+  it.h = rem - it.b * p.Hq;  // heads of one kv group are consecutive items
+  it.kvh = it.h / p.group;
+  it.q0 = (int64_t)qp * (kQTiles * BM);
+  it.L = batch_limits(p, it.b);
+  int tb = 0, te = 0;
+  bool any = false;
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t) {
+    it.tr[t] = tile_range(p, it.L, it.q0 + t * BM, BM, BN);
+    if (it.tr[t].t_end > it.tr[t].t_begin) {
+      tb = any ? min(tb, it.tr[t].t_begin) : it.tr[t].t_begin;
+      te = any ? max(te, it.tr[t].t_end) : it.tr[t].t_end;
+      any = true;
+    }
+  }
+  it.tb = tb;
+  it.N = te - tb;
+  return it;
+}
+
+// Static snake schedule: round r gives CTA c item r*G + c (r even) or
+// r*G + G-1-c (r odd), so heavy and light items alternate between CTAs.
+__device__ __forceinline__ int item_of_round(int r, int n_items) {
+  const int G = gridDim.x;
+  const int c = blockIdx.x;
+  const int idx = r * G + ((r & 1) ? (G - 1 - c) : c);
+  return idx < n_items ? idx : -1;
+}
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -107,237 +177,206 @@ __device__ __forceinline__ float min128(const float (&x)[BN]) {
   return fminf(fminf(fminf(m[0], m[1]), fminf(m[2], m[3])), fminf(fminf(m[4], m[5]), fminf(m[6], m[7])));
 }
 
-template <int D, bool BF16, bool SOFTCAP, bool MASK>
-__global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ TcParams P) {
+// ------------------------------------------------------------------ producer
+// One thread.  Q tiles per item (after the previous item's QK^T products
+// released them), then the item's K / V tiles into the stage ring; the ring
+// index g runs on across items.
+template <int D>
+__device__ __forceinline__ void producer_role(const TcParams& P, const Smem<D>& sm, int n_items) {
   using Cfg = TcConfig<D>;
   constexpr int S = Cfg::kStages;
   const CommonParams& p = P.c;
+  int g = 0;        // K / V tiles issued so far (ring position)
+  int q_items = 0;  // items whose Q was loaded
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int idx = item_of_round(r, n_items);
+    if (idx < 0) break;
+    const Item it = make_item(p, idx);
+    if (it.N == 0) continue;
+    if (q_items > 0 && !mbar_wait(sm.q_empty(), (q_items - 1) & 1, p.timeout_ns, p.status)) break;
+    const int q_plane = it.b * p.Hq + it.h;
+    const int kv_plane = it.b * p.Hkv + it.kvh;
+    mbar_arrive_expect_tx(sm.q_full(), kQTiles * Cfg::kTileBytes);
+    for (int t = 0; t < kQTiles; ++t)
+      for (int s = 0; s < Cfg::kSub; ++s)
+        tma_load_3d(sm.sQ + t * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_q, sm.q_full(), s * 64,
+                    (int)(it.q0 + t * BM), q_plane);
+    ++q_items;
+    for (int n = 0; n < it.N; ++n, ++g) {
+      const int st = g % S;
+      const int key0 = (it.tb + n) * BN;
+      if (g >= S && !mbar_wait(sm.kv_empty(st), ((g / S) - 1) & 1, p.timeout_ns, p.status)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(sm.k_full(st), Cfg::kTileBytes);
+      for (int s = 0; s < Cfg::kSub; ++s)
+        tma_load_3d(sm.sK + st * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_k, sm.k_full(st), s * 64,
+                    key0, kv_plane);
+      mbar_arrive_expect_tx(sm.v_full(st), Cfg::kTileBytes);
+      for (int s = 0; s < Cfg::kSub; ++s)
+        tma_load_3d(sm.sV + st * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_v, sm.v_full(st), s * 64,
+                    key0, kv_plane);
+    }
+  }
+  // Let every copy this thread started land before the CTA can exit.
+  for (int n = (g > S ? g - S : 0); n < g; ++n) {
+    mbar_wait(sm.k_full(n % S), (n / S) & 1, p.timeout_ns, p.status);
+    mbar_wait(sm.v_full(n % S), (n / S) & 1, p.timeout_ns, p.status);
+  }
+  if (q_items > 0) mbar_wait(sm.q_full(), (q_items - 1) & 1, p.timeout_ns, p.status);
+}
 
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + Cfg::kOffQ;
-  const uint32_t sK = sbase + Cfg::kOffK;
-  const uint32_t sV = sbase + Cfg::kOffV;
-  const uint32_t bar0 = sbase + Cfg::kOffBar;
-  const uint32_t bar_q = bar0;
-  auto bar_k = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto bar_v = [&](int s) { return bar0 + 8u * (1 + S + s); };
-  auto bar_empty = [&](int s) { return bar0 + 8u * (1 + 2 * S + s); };
-  auto bar_s = [&](int t) { return bar0 + 8u * (1 + 3 * S + t); };
-  auto bar_p = [&](int t) { return bar0 + 8u * (1 + 3 * S + 2 + t); };
-  // completes once, after query tile t's last P.V (the epilogue's wait)
-  auto bar_o = [&](int t) { return bar0 + 8u * (1 + 3 * S + 4 + t); };
-  const uint32_t bar_drain = bar0 + 8u * (1 + 3 * S + 6);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmemSlot);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int n_qt = (p.Sq + kQTiles * BM - 1) / (kQTiles * BM);
-  const int qt = n_qt - 1 - (int)blockIdx.x;  // longest causal rows first
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
-  const int kvh = h / p.group;
-  const int64_t q0 = (int64_t)qt * (kQTiles * BM);
-
-  // key-tile range of each query tile, and their union [tb, te)
-  const BatchLimits L = batch_limits(p, b);
-  TileRange tr[kQTiles];
-  int tb = 0, te = 0;
-  bool any = false;
+// ------------------------------------------------------------------ MMA issuer
+// Whole warp waits; lane 0 issues.  Per item and key tile j (iteration n):
+// the P.V products of tile j-1, then the QK^T products of tile j, per query
+// tile in turn.  Returns after every MMA it issued has completed.
+template <int D, bool BF16>
+__device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, uint32_t tmem,
+                                         int n_items, int lane) {
+  using Cfg = TcConfig<D>;
+  constexpr int S = Cfg::kStages;
+  const CommonParams& p = P.c;
+  constexpr uint32_t idesc_qk = make_idesc_f16kind(BF16, BM, BN, false);
+  constexpr uint32_t idesc_pv = make_idesc_f16kind(BF16, BM, D, true);
+  int g0 = 0;                 // ring position of the item's first key tile
+  int q_items = 0;            // items whose Q was consumed
+  int pc[kQTiles] = {0, 0};   // P tiles consumed per query tile (all items)
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int idx = item_of_round(r, n_items);
+    if (idx < 0) break;
+    const Item it = make_item(p, idx);
+    if (it.N == 0) continue;
+    if (!mbar_wait_warp(sm.q_full(), q_items & 1, p.timeout_ns, p.status)) { ok = false; break; }
+    ++q_items;
+    int64_t zero_from = it.L.lsk < (int64_t)p.Sk ? it.L.lsk : (int64_t)p.Sk;
+    if (zero_from < 0) zero_from = 0;
+    bool first_pv[kQTiles] = {true, true};
+    for (int n = 0; ok && n <= it.N; ++n) {
+      const int j = it.tb + n;
+      bool k_ready = false;  // K(j) is waited for only before its first use
+      if (n >= 1) {
+        const int gp = g0 + n - 1;
+        const int ps = gp % S;
+        if (!mbar_wait_warp(sm.v_full(ps), (gp / S) & 1, p.timeout_ns, p.status)) { ok = false; break; }
+        const int64_t key0 = (int64_t)(j - 1) * BN;
+        if (zero_from < key0 + BN && zero_from < (int64_t)p.kv_capacity) {
+          // Cache slots past the valid length may hold NaN / Inf; P is 0
+          // there but 0 * NaN is not, so zero those V rows (whole 128-byte
+          // rows, so the swizzle does not matter).
+          const int r0 = zero_from > key0 ? (int)(zero_from - key0) : 0;
+          const int chunks = (BN - r0) * 8;
+          for (int s = 0; s < Cfg::kSub; ++s) {
+            uint8_t* vblk = sm.base + Cfg::kOffV + ps * Cfg::kTileBytes + s * Cfg::kSubBytes;
+            for (int c = lane; c < chunks; c += 32)
+              *reinterpret_cast<uint4*>(vblk + (size_t)(r0 + (c >> 3)) * 128 + (c & 7) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+      }
+      tc_fence_after();
 #pragma unroll
-  for (int t = 0; t < kQTiles; ++t) {
-    tr[t] = tile_range(p, L, q0 + t * BM, BM, BN);
-    if (tr[t].t_end > tr[t].t_begin) {
-      tb = any ? min(tb, tr[t].t_begin) : tr[t].t_begin;
-      te = any ? max(te, tr[t].t_end) : tr[t].t_end;
-      any = true;
-    }
-  }
-  const int N = te - tb;  // key tiles the CTA streams
-  auto active = [&](int t, int j) { return j >= tr[t].t_begin && j < tr[t].t_end; };
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
-    for (int s = 0; s < S; ++s) {
-      mbar_init(bar_k(s), 1);
-      mbar_init(bar_v(s), 1);
-      mbar_init(bar_empty(s), 1);
-    }
-    for (int t = 0; t < kQTiles; ++t) {
-      mbar_init(bar_s(t), 1);
-      mbar_init(bar_p(t), 4);  // one arrival per softmax warp of the tile
-      mbar_init(bar_o(t), 1);
-    }
-    mbar_init(bar_drain, 1);
-    mbar_init_fence();
-  }
-  if (warp == kTmaWarp && lane == 0) {
-    tma_prefetch_desc(&P.tmap_q);
-    tma_prefetch_desc(&P.tmap_k);
-    tma_prefetch_desc(&P.tmap_v);
-  }
-  if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-
-  if (warp == kTmaWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && N > 0) {
-      const int q_plane = b * p.Hq + h;
-      const int kv_plane = b * p.Hkv + kvh;
-      mbar_arrive_expect_tx(bar_q, kQTiles * Cfg::kTileBytes);
-      for (int t = 0; t < kQTiles; ++t)
-        for (int s = 0; s < Cfg::kSub; ++s)
-          tma_load_3d(sQ + t * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_q, bar_q, s * 64,
-                      (int)(q0 + t * BM), q_plane);
-      int issued = 0;
-      for (int n = 0; n < N; ++n) {
-        const int st = n % S;
-        const int key0 = (tb + n) * BN;
-        if (n >= S && !mbar_wait(bar_empty(st), ((n / S) - 1) & 1, p.timeout_ns, p.status)) break;
-        mbar_arrive_expect_tx(bar_k(st), Cfg::kTileBytes);
-        for (int s = 0; s < Cfg::kSub; ++s)
-          tma_load_3d(sK + st * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_k, bar_k(st), s * 64,
-                      key0, kv_plane);
-        mbar_arrive_expect_tx(bar_v(st), Cfg::kTileBytes);
-        for (int s = 0; s < Cfg::kSub; ++s)
-          tma_load_3d(sV + st * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_v, bar_v(st), s * 64,
-                      key0, kv_plane);
-        issued = n + 1;
-      }
-      // Let every copy this thread started land before the CTA can exit.
-      for (int n = (issued > S ? issued - S : 0); n < issued; ++n) {
-        mbar_wait(bar_k(n % S), (n / S) & 1, p.timeout_ns, p.status);
-        mbar_wait(bar_v(n % S), (n / S) & 1, p.timeout_ns, p.status);
-      }
-      mbar_wait(bar_q, 0, p.timeout_ns, p.status);
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    if (N > 0) {
-      constexpr uint32_t idesc_qk = make_idesc_f16kind(BF16, BM, BN, false);
-      constexpr uint32_t idesc_pv = make_idesc_f16kind(BF16, BM, D, true);
-      int64_t zero_from = L.lsk < (int64_t)p.Sk ? L.lsk : (int64_t)p.Sk;
-      if (zero_from < 0) zero_from = 0;
-      int pc[kQTiles] = {0, 0};  // P.V products issued per query tile
-
-      bool ok = mbar_wait_warp(bar_q, 0, p.timeout_ns, p.status);
-      // iteration n: P.V of key tile tb+n-1 (if n >= 1), S of key tile tb+n (if n < N)
-      for (int n = 0; ok && n <= N; ++n) {
-        const int j = tb + n;
-        bool k_ready = false;  // K(j) is waited for only before its first use
-        if (n >= 1) {
-          const int ps = (n - 1) % S;
-          if (!mbar_wait_warp(bar_v(ps), ((n - 1) / S) & 1, p.timeout_ns, p.status)) {
+      for (int t = 0; t < kQTiles; ++t) {
+        const bool do_pv = n >= 1 && it.active(t, j - 1);
+        const bool do_s = n < it.N && it.active(t, j);
+        if (do_pv) {
+          if (!mbar_wait_warp(sm.p_full(t), pc[t] & 1, p.timeout_ns, p.status)) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t vaddr = sm.sV + ((g0 + n - 1) % S) * Cfg::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B apart,
+              // 64-column blocks kSubBytes apart.
+              const uint64_t bdesc = make_sdesc_sw128(vaddr + kk * 2048, Cfg::kSubBytes, 1024);
+              mma_ts(tmem + kColO + t * 128, tmem + t * 128 + kk * 8, bdesc, idesc_pv,
+                     (!first_pv[t] || kk > 0) ? 1u : 0u);
+            }
+            if (!do_s) tc_commit(sm.o_final(t));  // query tile t has seen its last key tile
+          }
+          first_pv[t] = false;
+          ++pc[t];
+        }
+        if (do_s && !k_ready) {
+          const int gs = g0 + n;
+          if (!mbar_wait_warp(sm.k_full(gs % S), (gs / S) & 1, p.timeout_ns, p.status)) {
             ok = false;
             break;
           }
-          const int64_t key0 = (int64_t)(j - 1) * BN;
-          if (zero_from < key0 + BN && zero_from < (int64_t)p.kv_capacity) {
-            // Cache slots past the valid length may hold NaN / Inf; P is 0
-            // there but 0 * NaN is not, so zero those V rows (whole 128-byte
-            // rows, so the swizzle does not matter).
-            const int r0 = zero_from > key0 ? (int)(zero_from - key0) : 0;
-            const int chunks = (BN - r0) * 8;
-            for (int s = 0; s < Cfg::kSub; ++s) {
-              uint8_t* vblk = smem + Cfg::kOffV + ps * Cfg::kTileBytes + s * Cfg::kSubBytes;
-              for (int c = lane; c < chunks; c += 32)
-                *reinterpret_cast<uint4*>(vblk + (size_t)(r0 + (c >> 3)) * 128 + (c & 7) * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
+          tc_fence_after();
+          k_ready = true;
         }
-        tc_fence_after();
+        if (do_s && lane == 0) {
+          const uint32_t kaddr = sm.sK + ((g0 + n) % S) * Cfg::kTileBytes;
+          const uint32_t qaddr = sm.sQ + t * Cfg::kTileBytes;
 #pragma unroll
-        for (int t = 0; t < kQTiles; ++t) {
-          const bool do_pv = n >= 1 && active(t, j - 1);
-          const bool do_s = n < N && active(t, j);
-          if (do_pv) {
-            if (!mbar_wait_warp(bar_p(t), pc[t] & 1, p.timeout_ns, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            if (lane == 0) {
-              const uint32_t vaddr = sV + ((n - 1) % S) * Cfg::kTileBytes;
-#pragma unroll
-              for (int kk = 0; kk < BN / 16; ++kk) {
-                // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B
-                // apart, 64-column blocks kSubBytes apart.
-                const uint64_t bdesc = make_sdesc_sw128(vaddr + kk * 2048, Cfg::kSubBytes, 1024);
-                mma_ts(tmem + kColO + t * 128, tmem + t * 128 + kk * 8, bdesc, idesc_pv,
-                       (pc[t] > 0 || kk > 0) ? 1u : 0u);
-              }
-              if (!do_s) tc_commit(bar_o(t));  // query tile t has seen its last key tile
-            }
-            ++pc[t];
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * Cfg::kSubBytes + (kk & 3) * 32;
+            const uint64_t adesc = make_sdesc_sw128(qaddr + off, 16, 1024);
+            const uint64_t bdesc = make_sdesc_sw128(kaddr + off, 16, 1024);
+            mma_ss(tmem + t * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
           }
-          if (do_s && !k_ready) {
-            if (!mbar_wait_warp(bar_k(n % S), (n / S) & 1, p.timeout_ns, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            k_ready = true;
-          }
-          if (do_s && lane == 0) {
-            const uint32_t kaddr = sK + (n % S) * Cfg::kTileBytes;
-            const uint32_t qaddr = sQ + t * Cfg::kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * Cfg::kSubBytes + (kk & 3) * 32;
-              const uint64_t adesc = make_sdesc_sw128(qaddr + off, 16, 1024);
-              const uint64_t bdesc = make_sdesc_sw128(kaddr + off, 16, 1024);
-              mma_ss(tmem + t * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
-            }
-            tc_commit(bar_s(t));
-          }
-          __syncwarp();
+          tc_commit(sm.s_full(t));
         }
-        if (!ok) break;
-        if (n >= 1 && lane == 0) tc_commit(bar_empty((n - 1) % S));
         __syncwarp();
       }
-      // Wait for every MMA this warp issued before tensor memory is freed.
-      if (lane == 0) tc_commit(bar_drain);
+      if (!ok) break;
+      if (lane == 0) {
+        if (n >= 1) tc_commit(sm.kv_empty((g0 + n - 1) % S));
+        // the item's last QK^T products are issued: Q may be replaced once they finish
+        if (n == it.N - 1) tc_commit(sm.q_empty());
+      }
       __syncwarp();
-      mbar_wait_warp(bar_drain, 0, p.timeout_ns, p.status);
     }
-  } else {
-    // ------------------------------------------------------------ softmax
-    const int t = warp >> 2;  // query tile of this warpgroup
-    const int wq = warp & 3;  // TMEM lane quarter
-    const int row = wq * 32 + lane;
-    const int64_t qi = q0 + t * BM + row;
-    const TileRange T = t == 0 ? tr[0] : tr[1];  // a select keeps tr[] in registers
+    if (!ok) break;
+    g0 += it.N;
+  }
+  // Wait for every MMA this warp issued before tensor memory is freed.
+  if (lane == 0) tc_commit(sm.drain());
+  __syncwarp();
+  mbar_wait_warp(sm.drain(), 0, p.timeout_ns, p.status);
+}
+
+// ------------------------------------------------------------------ softmax
+// Warpgroup t (warps 4t..4t+3); thread = one query row of query tile t.
+template <int D, bool BF16, bool SOFTCAP, bool MASK>
+__device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& sm, uint32_t tmem,
+                                             int n_items, int warp, int lane) {
+  const CommonParams& p = P.c;
+  const int t = warp >> 2;  // query tile of this warpgroup
+  const int wq = warp & 3;  // TMEM lane quarter
+  const int row = wq * 32 + lane;
+  const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+  const uint32_t s_addr = tmem + lane_base + t * 128;
+  const uint32_t o_addr = tmem + lane_base + kColO + t * 128;
+  int sc = 0;  // S tiles consumed (all items)
+  int oc = 0;  // items whose O this warpgroup has read
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int idx = item_of_round(r, n_items);
+    if (idx < 0) break;
+    const Item it = make_item(p, idx);
+    const TileRange T = t == 0 ? it.tr[0] : it.tr[1];  // a select keeps tr[] in registers
     const int nt = T.t_end - T.t_begin;
-    const RowLimits R = row_limits(p, L, qi);
-    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const uint32_t s_addr = tmem + lane_base + t * 128;
-    const uint32_t o_addr = tmem + lane_base + kColO + t * 128;
+    const int64_t qi = it.q0 + t * BM + row;
+    const RowLimits R = row_limits(p, it.L, qi);
     const float* mrow = nullptr;
     if constexpr (MASK) {
       int64_t plane = 0;
-      if (p.mask_planes == p.B) plane = b;
-      else if (p.mask_planes == p.B * p.Hq) plane = (int64_t)b * p.Hq + h;
+      if (p.mask_planes == p.B) plane = it.b;
+      else if (p.mask_planes == p.B * p.Hq) plane = (int64_t)it.b * p.Hq + it.h;
       if (qi < p.Sq) mrow = p.mask + (plane * p.Sq + qi) * (int64_t)p.Sk;
     }
 
     float m_run = -INFINITY;  // running max, log2 units
     float l_run = 0.0f;       // running denominator
-    bool ok = true;
-    for (int c = 0; c < nt; ++c) {
+    for (int c = 0; c < nt; ++c, ++sc) {
       const int64_t key0 = (int64_t)(T.t_begin + c) * BN;
-      if (!mbar_wait_warp(bar_s(t), c & 1, p.timeout_ns, p.status)) { ok = false; break; }
+      if (!mbar_wait_warp(sm.s_full(t), sc & 1, p.timeout_ns, p.status)) { ok = false; break; }
       tc_fence_after();
       float x[BN];
       {
@@ -423,9 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float a0 = x[ch * 32 + 2 * i], a1 = x[ch * 32 + 2 * i + 1];
-          const float e0 = fast_exp2(fmaf(a0, xmul, -m_sub));
-          const float e1 = fast_exp2(fmaf(a1, xmul, -m_sub));
+          const float e0 = fast_exp2(fmaf(x[ch * 32 + 2 * i], xmul, -m_sub));
+          const float e1 = fast_exp2(fmaf(x[ch * 32 + 2 * i + 1], xmul, -m_sub));
           sum += e0 + e1;
           pk[i] = pack2<BF16>(e0, e1);
         }
@@ -435,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
       m_run = m_use;
 
       if (__any_sync(0xffffffffu, rescale)) {
-        // O_t already holds every earlier P.V (see the header)
+        // O_t already holds every earlier P.V of this item (see the header)
 #pragma unroll
         for (int k = 0; k < D / 32; ++k) {
           uint32_t o[32];
@@ -449,44 +487,105 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p(t));
+      if (lane == 0) mbar_arrive(sm.p_full(t));
     }
+    if (!ok) break;
 
     // ---------------------------------------------------------- epilogue
-    bool have_o = ok && nt > 0;
+    bool have_o = nt > 0;
     if (have_o) {
-      have_o = mbar_wait_warp(bar_o(t), 0, p.timeout_ns, p.status);
+      if (!mbar_wait_warp(sm.o_final(t), oc & 1, p.timeout_ns, p.status)) { ok = false; break; }
+      ++oc;
       tc_fence_after();
     }
-    if (ok) {
-      const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
-      uint16_t* out = reinterpret_cast<uint16_t*>(p.out);
-      int64_t base;
-      if (p.out_layout == 0)
-        base = (((int64_t)b * p.Hq + h) * p.Sq + qi) * D;
-      else
-        base = (((int64_t)b * p.Sq + qi) * p.Hq + h) * D;
+    const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+    uint16_t* out = reinterpret_cast<uint16_t*>(p.out);
+    int64_t base;
+    if (p.out_layout == 0)
+      base = (((int64_t)it.b * p.Hq + it.h) * p.Sq + qi) * D;
+    else
+      base = (((int64_t)it.b * p.Sq + qi) * p.Hq + it.h) * D;
 #pragma unroll
-      for (int k = 0; k < D / 32; ++k) {
-        uint32_t o[32];
-        if (have_o) {
-          tmem_ld32(o_addr + k * 32, o);
-          tmem_wait_ld();
-        } else {
+    for (int k = 0; k < D / 32; ++k) {
+      uint32_t o[32];
+      if (have_o) {
+        tmem_ld32(o_addr + k * 32, o);
+        tmem_wait_ld();
+      } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
-        }
-        uint32_t w[16];
+        for (int i = 0; i < 32; ++i) o[i] = 0u;
+      }
+      uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (qi < p.Sq) {
-          uint4* dst = reinterpret_cast<uint4*>(out + base + k * 32);
+      for (int i = 0; i < 16; ++i)
+        w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+      if (qi < p.Sq) {
+        uint4* dst = reinterpret_cast<uint4*>(out + base + k * 32);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-        }
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       }
     }
+    // The next item's first P.V into O_t waits for this warpgroup's next
+    // p_full arrival, which comes after these reads (fence before arrive).
+  }
+}
+
+template <int D, bool BF16, bool SOFTCAP, bool MASK>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ TcParams P) {
+  using Cfg = TcConfig<D>;
+  constexpr int S = Cfg::kStages;
+  const CommonParams& p = P.c;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Smem<D> sm;
+  sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm.base);
+  sm.sQ = sbase + Cfg::kOffQ;
+  sm.sK = sbase + Cfg::kOffK;
+  sm.sV = sbase + Cfg::kOffV;
+  sm.bar0 = sbase + Cfg::kOffBar;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm.base + Cfg::kOffTmemSlot);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_items = ((p.Sq + kQTiles * BM - 1) / (kQTiles * BM)) * p.B * p.Hq;
+
+  if (threadIdx.x == 0) {
+    mbar_init(sm.q_full(), 1);
+    mbar_init(sm.q_empty(), 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(sm.k_full(s), 1);
+      mbar_init(sm.v_full(s), 1);
+      mbar_init(sm.kv_empty(s), 1);
+    }
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(sm.s_full(t), 1);
+      mbar_init(sm.p_full(t), 4);  // one arrival per softmax warp of the tile
+      mbar_init(sm.o_final(t), 1);
+    }
+    mbar_init(sm.drain(), 1);
+    mbar_init_fence();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&P.tmap_q);
+    tma_prefetch_desc(&P.tmap_k);
+    tma_prefetch_desc(&P.tmap_v);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp == kTmaWarp) {
+    if (lane == 0) producer_role<D>(P, sm, n_items);
+  } else if (warp == kMmaWarp) {
+    mma_role<D, BF16>(P, sm, tmem, n_items, lane);
+  } else {
+    softmax_role<D, BF16, SOFTCAP, MASK>(P, sm, tmem, n_items, warp, lane);
   }
 
   tc_fence_before();
@@ -503,8 +602,13 @@ cudaError_t launch_variant(const TcParams& P, cudaStream_t stream) {
   constexpr uint32_t smem = TcConfig<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((P.c.Sq + kQTiles * BM - 1) / (kQTiles * BM)), (unsigned)P.c.Hq,
-                  (unsigned)P.c.B);
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int64_t n_items =
+      (int64_t)((P.c.Sq + kQTiles * BM - 1) / (kQTiles * BM)) * P.c.B * P.c.Hq;
+  if (n_items > INT32_MAX) return cudaErrorInvalidConfiguration;
+  const int grid = (int)(n_items < sms ? n_items : sms);  // one persistent CTA per SM
   kernel<<<grid, kThreads, smem, stream>>>(P);
   return cudaGetLastError();
 }

@@ -120,20 +120,31 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-// try_wait with a suspend-time hint: a waiting warp sleeps (and leaves the
-// issue slots to the warps doing work) until the phase completes or the hint
-// runs out.
-constexpr uint32_t kWaitSuspendHintNs = 100000;
+// Optional suspend-time hint for try_wait (ns).  0 (the default) uses the
+// plain form, whose suspension limit the hardware picks.
+#ifndef GB300_WAIT_HINT_NS
+#define GB300_WAIT_HINT_NS 0
+#endif
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
+#if GB300_WAIT_HINT_NS > 0
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kWaitSuspendHintNs)
+      : "r"(bar), "r"(parity), "r"((uint32_t)GB300_WAIT_HINT_NS)
       : "memory");
+#else
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+#endif
   return ok != 0;
 }
 
@@ -145,9 +156,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
                                           int* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (;;) {
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > timeout_ns) {
+    if ((it & 15u) == 0u && global_timer_ns() - t0 > timeout_ns) {
       if (status) atomicOr(status, kStatusTimeout);
       return false;
     }
