@@ -41,7 +41,12 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of the tcgen05 kernel, keyed by workload, with the hash of the
 # kernel sources they were taken on; reported as null once the sources change.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    "gqa_causal_bf16": {"bytes_per_launch": 128702976, "source_hash": "54537ca6e2fed12d"},
+    "window_softcap_bf16": {"bytes_per_launch": 409761792, "source_hash": "54537ca6e2fed12d"},
+    "ragged_kvcache_f16": {"bytes_per_launch": 48567040, "source_hash": "54537ca6e2fed12d"},
+    "dit_f32": {"bytes_per_launch": 59015936, "source_hash": "54537ca6e2fed12d"},
+}
 
 
 # ----------------------------------------------------------------- FLOP count
@@ -253,14 +258,23 @@ def oracle_sample(w: Workload, x: dict, budget_s: float, seed: int = 3):
         oracle.attn_rows(qf, kf, vf, rows, **kw)
         return time.perf_counter() - t, 4 * w.D * int(cnt[rows[:, 0], rows[:, 2]].sum())
 
-    n = 4 * threads
-    dt, fl = run(pick(n))
-    rate = fl / max(dt, 1e-6)
-    per_row = max(fl / n, 1.0)
-    n2 = int(max(threads, min(5_000_000, budget_s * rate / per_row)))
-    rows = pick(n2)
-    dt2, fl2 = run(rows)
-    return fl + fl2, dt + dt2, threads, n + n2
+    # grow a calibration sample until its timing means something, then size
+    # the rest of the sample to the budget
+    n, tot_s, tot_fl, tot_rows = 4 * threads, 0.0, 0, 0
+    while True:
+        dt, fl = run(pick(n))
+        tot_s, tot_fl, tot_rows = tot_s + dt, tot_fl + fl, tot_rows + n
+        if dt >= 0.5 or n >= 2_000_000 or tot_s + 4 * dt > budget_s:
+            break
+        n *= 4
+    rate = tot_fl / max(tot_s, 1e-6)
+    per_row = max(tot_fl / tot_rows, 1.0)
+    left = budget_s - tot_s
+    if left > 0.2:
+        n2 = int(max(threads, min(5_000_000, left * rate / per_row)))
+        dt, fl = run(pick(n2))
+        tot_s, tot_fl, tot_rows = tot_s + dt, tot_fl + fl, tot_rows + n2
+    return tot_fl, tot_s, threads, tot_rows
 
 
 def reference_arm(args, world, rank):
@@ -269,7 +283,8 @@ def reference_arm(args, world, rank):
     w = WORKLOADS[args.workload]
     x = make_inputs(w)
     flops, flops_excl = flops_of(w, x)
-    per_step_budget = max(1.0, args.ref_seconds / max(1, args.steps + args.warmup))
+    # the whole arm (warm-up included) stays within about --ref-seconds
+    per_step_budget = max(0.02, args.ref_seconds / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_sample(w, x, per_step_budget, seed=11)
     tot_fl, tot_s, threads, rows = 0, 0.0, 0, 0
@@ -278,7 +293,7 @@ def reference_arm(args, world, rank):
         tot_fl, tot_s, rows = tot_fl + fl, tot_s + s, rows + r
     value = tot_fl / tot_s / 1e12
     sample = (f"{rows} seeded random (b, h, qi) rows of {w.name}, oracle_attn_rows, "
-              f"{args.steps} steps of ~{per_step_budget:.1f} s")
+              f"{args.steps} steps of ~{per_step_budget:.2f} s")
     line = {"metric": "attention fwd TFLOP/s (unmasked FLOPs)", "impl": "reference",
             "value": value, "unit": "TFLOP/s", "n_gpus": 0, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": tot_s * 1e3 / args.steps,

@@ -362,6 +362,21 @@ def pin_brute_force_tiny(lib):
                         _close(got[0, 0, qi], expect, 1e-13, f"tiny {Sq}x{Sk}x{D} c={causal}")
 
 
-PINS = [pin_closed_forms, pin_torch_sdpa, pin_streaming_recurrences, pin_uniform_v,
+def pin_rows_equal_full(lib):
+    """oracle_attn_rows (rows one by one, any order) equals the full forward."""
+    rng = np.random.default_rng(19)
+    B, Hq, Hkv, Sq, Sk, D = 2, 4, 2, 9, 13, 5
+    q, k, v = _rand(rng, B, Hq, Sq, D), _rand(rng, B, Hkv, Sk, D), _rand(rng, B, Hkv, Sk, D)
+    am = _rand(rng, B * Hq, Sq, Sk)
+    kw = dict(B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, kv_capacity=Sk, D=D, causal=True,
+              local_window=5, scale=0.7, softcap=2.0, mask=am, mask_planes=B * Hq, nthreads=3,
+              lib=lib)
+    full = oracle.attn_fwd(q, k, v, **kw)
+    rows = np.array([(b, h, i) for b in range(B) for h in range(Hq) for i in range(Sq)])[::-1]
+    got = oracle.attn_rows(q, k, v, rows, **kw)
+    _close(got, full[rows[:, 0], rows[:, 1], rows[:, 2]], 0.0, "rows = full")
+
+
+PINS = [pin_rows_equal_full, pin_closed_forms, pin_torch_sdpa, pin_streaming_recurrences, pin_uniform_v,
         pin_mask_properties, pin_window_and_softcap_limits, pin_gqa_and_layout, pin_ragged,
         pin_brute_force_tiny]
