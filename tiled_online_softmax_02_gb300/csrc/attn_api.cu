@@ -209,6 +209,12 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, const float
   c.scale_log2 = (float)((double)scale * 1.4426950408889634);
   c.softcap = softcap > 0.0f ? softcap : 0.0f;
   c.inv_softcap = softcap > 0.0f ? 1.0f / softcap : 0.0f;
+  if (softcap > 0.0f) {
+    const double l2e = 1.4426950408889634;
+    c.sc_k1 = (float)(2.0 * l2e * (double)scale / (double)softcap);
+    c.sc_k2 = (float)(-2.0 * (double)softcap * l2e);
+    c.sc_k3 = (float)((double)softcap * l2e);
+  }
   c.timeout_ns = g_timeout_ns.load();
   c.status = status;
 

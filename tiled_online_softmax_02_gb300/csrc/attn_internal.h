@@ -23,6 +23,9 @@ struct CommonParams {
   float scale_log2;   // scale * log2(e)
   float softcap;      // > 0: soft-cap value c
   float inv_softcap;  // 1 / c
+  // soft-cap folded into log2 units: softcap(scale*s)*log2(e) = k2 * r + k3,
+  // r = 1 / (2^(k1 * s) + 1), k1 = 2 log2(e) scale / c, k2 = -2 c log2(e), k3 = c log2(e)
+  float sc_k1, sc_k2, sc_k3;
   uint64_t timeout_ns;
   int* status;        // device status word (timeouts)
 };

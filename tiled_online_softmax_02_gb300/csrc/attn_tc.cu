@@ -392,51 +392,58 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
 
       const bool need_mask = !(key0 >= T.full_lo && key0 + BN <= T.full_hi);
       float m_tile;
-      bool scaled;  // x already in log2 units (else raw Q.K, scaled inside the exp)
-      if (SOFTCAP || MASK || need_mask) {
-        // general path: x_j = ((softcap(scale s_j)) + mask_j) * log2 e, or -inf
+      bool scaled = false;  // x already in log2 units (else raw Q.K, scaled inside the exp)
+      if constexpr (SOFTCAP) {
+        // c tanh(scale s / c), already in log2 units
+#pragma unroll
+        for (int i = 0; i < BN; ++i) x[i] = soft_cap_log2(x[i], p.sc_k1, p.sc_k2, p.sc_k3);
+        scaled = true;
+      } else if constexpr (MASK) {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) x[i] *= p.scale_log2;
+        scaled = true;
+      }
+      if constexpr (MASK) {
+        // + mask (log2 units); rows past Sq have no mask row
+        if (mrow != nullptr) {
+#pragma unroll
+          for (int c4 = 0; c4 < BN; c4 += 4) {
+            const int64_t j0 = key0 + c4;
+            float mv[4] = {0.f, 0.f, 0.f, 0.f};
+            if (p.mask_vec4 && j0 + 3 < (int64_t)p.Sk) {
+              const float4 m4 = __ldg(reinterpret_cast<const float4*>(mrow + j0));
+              mv[0] = m4.x; mv[1] = m4.y; mv[2] = m4.z; mv[3] = m4.w;
+            } else {
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                if (j0 + u < (int64_t)p.Sk) mv[u] = __ldg(mrow + j0 + u);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) x[c4 + u] = fmaf(mv[u], kLog2e, x[c4 + u]);
+          }
+        }
+      }
+      if (need_mask) {
+        // structural limits of this row: keys outside [lo, hi) become -inf
+        if (!scaled) {
+#pragma unroll
+          for (int i = 0; i < BN; ++i) x[i] *= p.scale_log2;
+          scaled = true;
+        }
         int64_t lo = R.lo - key0, hi = R.hi - key0;
         lo = lo < 0 ? 0 : (lo > BN ? BN : lo);
         hi = hi < 0 ? 0 : (hi > BN ? BN : hi);
         const int lo_rel = (int)lo;
         const uint32_t span = hi > lo ? (uint32_t)(hi - lo) : 0u;
 #pragma unroll
-        for (int c4 = 0; c4 < BN; c4 += 4) {
-          float mv[4] = {0.f, 0.f, 0.f, 0.f};
-          if constexpr (MASK) {
-            const int64_t j0 = key0 + c4;
-            if (mrow != nullptr) {
-              if (p.mask_vec4 && j0 + 3 < (int64_t)p.Sk) {
-                const float4 m4 = __ldg(reinterpret_cast<const float4*>(mrow + j0));
-                mv[0] = m4.x; mv[1] = m4.y; mv[2] = m4.z; mv[3] = m4.w;
-              } else {
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                  if (j0 + u < (int64_t)p.Sk) mv[u] = __ldg(mrow + j0 + u);
-              }
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float v;
-            if constexpr (SOFTCAP || MASK) {
-              v = x[c4 + u] * p.scale;
-              if constexpr (SOFTCAP) v = soft_cap(v, p.softcap, p.inv_softcap);
-              if constexpr (MASK) v += mv[u];
-              v *= kLog2e;
-            } else {
-              v = x[c4 + u] * p.scale_log2;
-            }
-            x[c4 + u] = ((uint32_t)(c4 + u - lo_rel) < span) ? v : -INFINITY;
-          }
-        }
+        for (int i = 0; i < BN; ++i) x[i] = ((uint32_t)(i - lo_rel) < span) ? x[i] : -INFINITY;
+      }
+      if (scaled) {
         m_tile = max128(x);
-        scaled = true;
       } else {
         // every key of this tile is visible to every row: the extreme raw
         // score times the (signed) scale is the max of the scaled scores
         m_tile = (p.scale_log2 >= 0.0f ? max128(x) : min128(x)) * p.scale_log2;
-        scaled = false;
       }
 
       // online update, keeping the old max unless it grew by more than 2^8

@@ -337,6 +337,12 @@ __device__ __forceinline__ float fast_rcp(float x) {
 
 // c * tanh(s / c) through tanh(y) = 1 - 2 / (2^(2 y log2 e) + 1): one ex2 and
 // one reciprocal; exact limits +-c for |y| -> inf, absolute error ~1e-7 * c.
+// The same soft-cap on a raw score s, returned in log2 units, with the
+// constants folded (see CommonParams::sc_k*): one FMUL, ex2, FADD, rcp, FFMA.
+__device__ __forceinline__ float soft_cap_log2(float s, float k1, float k2, float k3) {
+  return fmaf(k2, fast_rcp(fast_exp2(s * k1) + 1.0f), k3);
+}
+
 __device__ __forceinline__ float soft_cap(float s, float cap, float inv_cap) {
   const float e = fast_exp2(s * inv_cap * 2.8853900817779268f);  // 2 * log2(e)
   return cap * (1.0f - 2.0f * fast_rcp(e + 1.0f));
