@@ -59,6 +59,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.0f;  // keep the old max while it is within 2^8
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxOrderB = 256;  // batches ranked by cost when B <= this
 
 template <int D>
 struct TcConfig {
@@ -70,10 +71,13 @@ struct TcConfig {
   static constexpr uint32_t kOffK = kOffQ + kQTiles * kTileBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
   static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
-  // q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_final[2], drain
-  static constexpr int kNumBars = 2 + 3 * kStages + 2 + 2 + 2 + 1;
+  // q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_final[2],
+  // drain, merge_full, merge_done
+  static constexpr int kNumBars = 2 + 3 * kStages + 2 + 2 + 2 + 3;
   static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
-  static constexpr uint32_t kSmemBytes = kOffTmemSlot + 16 + 1024;  // + 1024 alignment slack
+  static constexpr uint32_t kOffMerge = kOffTmemSlot + 16;          // float2 [128] (key-split merge)
+  static constexpr uint32_t kOffOrder = kOffMerge + BM * 8;         // int [kMaxOrderB] batch order
+  static constexpr uint32_t kSmemBytes = kOffOrder + kMaxOrderB * 4 + 1024;  // + alignment slack
 };
 
 // Shared-memory addresses of the tiles and barriers.
@@ -93,30 +97,68 @@ struct Smem {
   // completes once per item, after query tile t's last P.V (the epilogue's wait)
   __device__ uint32_t o_final(int t) const { return bar0 + 8u * (2 + 3 * S + 4 + t); }
   __device__ uint32_t drain() const { return bar0 + 8u * (2 + 3 * S + 6); }
+  // key-split merge hand-over: lane 1's row max / sum written (128 arrivals),
+  // then lane 1's O read by warpgroup 0 (128 arrivals)
+  __device__ uint32_t merge_full() const { return bar0 + 8u * (2 + 3 * S + 7); }
+  __device__ uint32_t merge_done() const { return bar0 + 8u * (2 + 3 * S + 8); }
+  __device__ float2* merge() const { return reinterpret_cast<float2*>(base + Cfg::kOffMerge); }
+  __device__ const int* order() const { return reinterpret_cast<const int*>(base + Cfg::kOffOrder); }
 };
 
-// One work item: two query tiles of one (b, h), their key-tile ranges and
-// the union [tb, tb + N) the item streams.
+// One work item of one (b, h): two lanes t = 0, 1, each a 128-row query tile
+// with its own S / O in tensor memory, visiting key tiles
+// tr[t].t_begin, + stride, ... < tr[t].t_end.  Normally lane t is query tile t
+// (stride 1).  When the second query tile would have no rows (short Sq, e.g.
+// decode or chunked prefill), both lanes take the same 128 rows and split the
+// key tiles even / odd (stride 2), so the tensor core still alternates
+// between two softmax warpgroups; warpgroup 0 merges the two partial rows.
+// The item streams the key tiles [tb, tb + N).
 struct Item {
   int b, h, kvh;
   int64_t q0;
   BatchLimits L;
   TileRange tr[kQTiles];
-  int tb, N;
-  __device__ bool active(int t, int j) const { return j >= tr[t].t_begin && j < tr[t].t_end; }
+  int tb, N, stride;
+  bool split;
+  __device__ bool active(int t, int j) const {
+    return j >= tr[t].t_begin && j < tr[t].t_end && ((j - tr[t].t_begin) & (stride - 1)) == 0;
+  }
+  __device__ bool last(int t, int j) const { return j + stride >= tr[t].t_end; }
+  __device__ int tiles(int t) const {
+    return tr[t].t_end > tr[t].t_begin ? (tr[t].t_end - tr[t].t_begin + stride - 1) / stride : 0;
+  }
+  __device__ int64_t row0(int t) const { return q0 + (split ? 0 : t * BM); }
 };
 
-__device__ __forceinline__ Item make_item(const CommonParams& p, int idx) {
+template <bool KSPLIT>
+__device__ __forceinline__ Item make_item(const CommonParams& p, int idx, const int* border) {
   const int bh = p.B * p.Hq;
   const int n_qp = (p.Sq + kQTiles * BM - 1) / (kQTiles * BM);
   Item it;
   const int qp = n_qp - 1 - idx / bh;  // latest query rows first
   const int rem = idx - (idx / bh) * bh;
-  it.b = rem / p.Hq;
-  it.h = rem - it.b * p.Hq;  // heads of one kv group are consecutive items
+  const int br = rem / p.Hq;
+  it.b = border ? border[br] : br;  // costliest batches first
+  it.h = rem - br * p.Hq;           // heads of one kv group are consecutive items
   it.kvh = it.h / p.group;
   it.q0 = (int64_t)qp * (kQTiles * BM);
   it.L = batch_limits(p, it.b);
+  it.split = KSPLIT && it.q0 + BM >= (int64_t)p.Sq;
+  if (it.split) {
+    const TileRange t0 = tile_range(p, it.L, it.q0, BM, BN);
+    it.tr[0] = t0;
+    it.tr[1] = t0;
+    it.stride = 2;
+    if (t0.t_end > t0.t_begin + 1) {
+      it.tr[1].t_begin = t0.t_begin + 1;
+    } else {
+      it.tr[1].t_begin = it.tr[1].t_end = 0;  // one key tile: lane 1 stays empty
+    }
+    it.tb = t0.t_begin;
+    it.N = t0.t_end > t0.t_begin ? t0.t_end - t0.t_begin : 0;
+    return it;
+  }
+  it.stride = 1;
   int tb = 0, te = 0;
   bool any = false;
 #pragma unroll
@@ -131,6 +173,25 @@ __device__ __forceinline__ Item make_item(const CommonParams& p, int idx) {
   it.tb = tb;
   it.N = te - tb;
   return it;
+}
+
+// Batches ranked by their number of valid key tiles (descending, ties by
+// index), written to order[rank] = b.  Threads 0..B-1 each rank one batch.
+__device__ __forceinline__ void rank_batches(const CommonParams& p, int* order) {
+  const int b = threadIdx.x;
+  if (b >= p.B) return;
+  auto cost = [&](int i) {
+    const BatchLimits L = batch_limits(p, i);
+    int64_t n = L.lsk < (int64_t)p.Sk ? L.lsk : (int64_t)p.Sk;
+    return n > 0 ? n : (int64_t)0;
+  };
+  const int64_t c = cost(b);
+  int rank = 0;
+  for (int i = 0; i < p.B; ++i) {
+    const int64_t ci = cost(i);
+    rank += (ci > c || (ci == c && i < b)) ? 1 : 0;
+  }
+  order[rank] = b;
 }
 
 // Static snake schedule: round r gives CTA c item r*G + c (r even) or
@@ -181,18 +242,21 @@ __device__ __forceinline__ float min128(const float (&x)[BN]) {
 // One thread.  Q tiles per item (after the previous item's QK^T products
 // released them), then the item's K / V tiles into the stage ring; the ring
 // index g runs on across items.
-template <int D>
+template <int D, bool KSPLIT>
 __device__ __forceinline__ void producer_role(const TcParams& P, const Smem<D>& sm, int n_items) {
   using Cfg = TcConfig<D>;
   constexpr int S = Cfg::kStages;
   const CommonParams& p = P.c;
   int g = 0;        // K / V tiles issued so far (ring position)
   int q_items = 0;  // items whose Q was loaded
+  // batch ranking only in the key-split variant (short query ranges, where
+  // ragged lengths decide the cost); elsewhere the pointer stays out of registers
+  const int* border = (KSPLIT && p.B <= kMaxOrderB) ? sm.order() : nullptr;
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int idx = item_of_round(r, n_items);
     if (idx < 0) break;
-    const Item it = make_item(p, idx);
+    const Item it = make_item<KSPLIT>(p, idx, border);
     if (it.N == 0) continue;
     if (q_items > 0 && !mbar_wait(sm.q_empty(), (q_items - 1) & 1, p.timeout_ns, p.status)) break;
     const int q_plane = it.b * p.Hq + it.h;
@@ -201,7 +265,7 @@ __device__ __forceinline__ void producer_role(const TcParams& P, const Smem<D>& 
     for (int t = 0; t < kQTiles; ++t)
       for (int s = 0; s < Cfg::kSub; ++s)
         tma_load_3d(sm.sQ + t * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_q, sm.q_full(), s * 64,
-                    (int)(it.q0 + t * BM), q_plane);
+                    (int)it.row0(t), q_plane);
     ++q_items;
     for (int n = 0; n < it.N; ++n, ++g) {
       const int st = g % S;
@@ -228,26 +292,60 @@ __device__ __forceinline__ void producer_role(const TcParams& P, const Smem<D>& 
   if (q_items > 0) mbar_wait(sm.q_full(), (q_items - 1) & 1, p.timeout_ns, p.status);
 }
 
+// S_t = Q_t K^T for one key tile (K tile at kaddr), then commit s_full(t).
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_qk(const Smem<D>& sm, uint32_t tmem, int t, uint32_t kaddr) {
+  using Cfg = TcConfig<D>;
+  constexpr uint32_t idesc_qk = make_idesc_f16kind(BF16, BM, BN, false);
+  const uint32_t qaddr = sm.sQ + t * Cfg::kTileBytes;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * Cfg::kSubBytes + (kk & 3) * 32;
+    const uint64_t adesc = make_sdesc_sw128(qaddr + off, 16, 1024);
+    const uint64_t bdesc = make_sdesc_sw128(kaddr + off, 16, 1024);
+    mma_ss(tmem + t * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+  }
+  tc_commit(sm.s_full(t));
+}
+
+// O_t (+)= P_t V for one key tile (V tile at vaddr; P_t in tensor memory over
+// the first half of S_t).
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_pv(const Smem<D>& sm, uint32_t tmem, int t, uint32_t vaddr,
+                                         bool accumulate) {
+  using Cfg = TcConfig<D>;
+  constexpr uint32_t idesc_pv = make_idesc_f16kind(BF16, BM, D, true);
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk) {
+    // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B apart, 64-column
+    // blocks kSubBytes apart.
+    const uint64_t bdesc = make_sdesc_sw128(vaddr + kk * 2048, Cfg::kSubBytes, 1024);
+    mma_ts(tmem + kColO + t * 128, tmem + t * 128 + kk * 8, bdesc, idesc_pv,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
 // ------------------------------------------------------------------ MMA issuer
 // Whole warp waits; lane 0 issues.  Per item and key tile j (iteration n):
 // the P.V products of tile j-1, then the QK^T products of tile j, per query
 // tile in turn.  Returns after every MMA it issued has completed.
-template <int D, bool BF16>
+template <int D, bool BF16, bool KSPLIT>
 __device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, uint32_t tmem,
                                          int n_items, int lane) {
   using Cfg = TcConfig<D>;
   constexpr int S = Cfg::kStages;
   const CommonParams& p = P.c;
-  constexpr uint32_t idesc_qk = make_idesc_f16kind(BF16, BM, BN, false);
-  constexpr uint32_t idesc_pv = make_idesc_f16kind(BF16, BM, D, true);
   int g0 = 0;                 // ring position of the item's first key tile
   int q_items = 0;            // items whose Q was consumed
-  int pc[kQTiles] = {0, 0};   // P tiles consumed per query tile (all items)
+  int pc[kQTiles] = {0, 0};   // P tiles consumed per lane (all items)
+  // batch ranking only in the key-split variant (short query ranges, where
+  // ragged lengths decide the cost); elsewhere the pointer stays out of registers
+  const int* border = (KSPLIT && p.B <= kMaxOrderB) ? sm.order() : nullptr;
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int idx = item_of_round(r, n_items);
     if (idx < 0) break;
-    const Item it = make_item(p, idx);
+    const Item it = make_item<KSPLIT>(p, idx, border);
     if (it.N == 0) continue;
     if (!mbar_wait_warp(sm.q_full(), q_items & 1, p.timeout_ns, p.status)) { ok = false; break; }
     ++q_items;
@@ -279,51 +377,95 @@ __device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, u
         }
       }
       tc_fence_after();
-#pragma unroll
-      for (int t = 0; t < kQTiles; ++t) {
-        const bool do_pv = n >= 1 && it.active(t, j - 1);
-        const bool do_s = n < it.N && it.active(t, j);
-        if (do_pv) {
-          if (!mbar_wait_warp(sm.p_full(t), pc[t] & 1, p.timeout_ns, p.status)) { ok = false; break; }
+      const bool pv0 = n >= 1 && it.active(0, j - 1), pv1 = n >= 1 && it.active(1, j - 1);
+      const bool s0 = n < it.N && it.active(0, j), s1 = n < it.N && it.active(1, j);
+      const uint32_t kaddr = sm.sK + ((g0 + n) % S) * Cfg::kTileBytes;
+      const uint32_t vaddr = sm.sV + ((g0 + n - 1 + S) % S) * Cfg::kTileBytes;
+      // K(j) is waited for only right before the first S that reads it, so a
+      // late K never holds back the P.V products of tile j-1.
+      auto wait_k = [&]() -> bool {
+        if (k_ready) return true;
+        const int gs = g0 + n;
+        if (!mbar_wait_warp(sm.k_full(gs % S), (gs / S) & 1, p.timeout_ns, p.status)) return false;
+        tc_fence_after();
+        k_ready = true;
+        return true;
+      };
+      // A lane with no P.V pending gets its S first (key-split lanes
+      // alternate), so the tensor core has work while the other lane's
+      // softmax runs.  S_t(j) overwrites the S region that held the lane's
+      // previous P, whose P.V this thread issued earlier.
+      if (!KSPLIT) {
+        // both lanes are query tiles: P.V then S, lane by lane
+        if (pv0) {
+          if (!mbar_wait_warp(sm.p_full(0), pc[0] & 1, p.timeout_ns, p.status)) { ok = false; break; }
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t vaddr = sm.sV + ((g0 + n - 1) % S) * Cfg::kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B apart,
-              // 64-column blocks kSubBytes apart.
-              const uint64_t bdesc = make_sdesc_sw128(vaddr + kk * 2048, Cfg::kSubBytes, 1024);
-              mma_ts(tmem + kColO + t * 128, tmem + t * 128 + kk * 8, bdesc, idesc_pv,
-                     (!first_pv[t] || kk > 0) ? 1u : 0u);
-            }
-            if (!do_s) tc_commit(sm.o_final(t));  // query tile t has seen its last key tile
+            issue_pv<D, BF16>(sm, tmem, 0, vaddr, !first_pv[0]);
+            if (it.last(0, j - 1)) tc_commit(sm.o_final(0));  // lane 0 has seen its last key tile
           }
-          first_pv[t] = false;
-          ++pc[t];
+          first_pv[0] = false;
+          ++pc[0];
         }
-        if (do_s && !k_ready) {
-          const int gs = g0 + n;
-          if (!mbar_wait_warp(sm.k_full(gs % S), (gs / S) & 1, p.timeout_ns, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          k_ready = true;
-        }
-        if (do_s && lane == 0) {
-          const uint32_t kaddr = sm.sK + ((g0 + n) % S) * Cfg::kTileBytes;
-          const uint32_t qaddr = sm.sQ + t * Cfg::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * Cfg::kSubBytes + (kk & 3) * 32;
-            const uint64_t adesc = make_sdesc_sw128(qaddr + off, 16, 1024);
-            const uint64_t bdesc = make_sdesc_sw128(kaddr + off, 16, 1024);
-            mma_ss(tmem + t * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          tc_commit(sm.s_full(t));
+        if (s0) {
+          if (!wait_k()) { ok = false; break; }
+          if (lane == 0) issue_qk<D, BF16>(sm, tmem, 0, kaddr);
         }
         __syncwarp();
+        if (pv1) {
+          if (!mbar_wait_warp(sm.p_full(1), pc[1] & 1, p.timeout_ns, p.status)) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            issue_pv<D, BF16>(sm, tmem, 1, vaddr, !first_pv[1]);
+            if (it.last(1, j - 1)) tc_commit(sm.o_final(1));
+          }
+          first_pv[1] = false;
+          ++pc[1];
+        }
+        if (s1) {
+          if (!wait_k()) { ok = false; break; }
+          if (lane == 0) issue_qk<D, BF16>(sm, tmem, 1, kaddr);
+        }
+        __syncwarp();
+      } else {
+      if (s0 && !pv0) {
+        if (!wait_k()) { ok = false; break; }
+        if (lane == 0) issue_qk<D, BF16>(sm, tmem, 0, kaddr);
       }
+      if (s1 && !pv1) {
+        if (!wait_k()) { ok = false; break; }
+        if (lane == 0) issue_qk<D, BF16>(sm, tmem, 1, kaddr);
+      }
+      if (pv0) {
+        if (!mbar_wait_warp(sm.p_full(0), pc[0] & 1, p.timeout_ns, p.status)) { ok = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          issue_pv<D, BF16>(sm, tmem, 0, vaddr, !first_pv[0]);
+          if (it.last(0, j - 1)) tc_commit(sm.o_final(0));  // lane 0 has seen its last key tile
+        }
+        first_pv[0] = false;
+        ++pc[0];
+        if (s0) {
+          if (!wait_k()) { ok = false; break; }
+          if (lane == 0) issue_qk<D, BF16>(sm, tmem, 0, kaddr);
+        }
+      }
+      if (pv1) {
+        if (!mbar_wait_warp(sm.p_full(1), pc[1] & 1, p.timeout_ns, p.status)) { ok = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          issue_pv<D, BF16>(sm, tmem, 1, vaddr, !first_pv[1]);
+          if (it.last(1, j - 1)) tc_commit(sm.o_final(1));
+        }
+        first_pv[1] = false;
+        ++pc[1];
+        if (s1) {
+          if (!wait_k()) { ok = false; break; }
+          if (lane == 0) issue_qk<D, BF16>(sm, tmem, 1, kaddr);
+        }
+      }
+      }  // KSPLIT
+      __syncwarp();
       if (!ok) break;
       if (lane == 0) {
         if (n >= 1) tc_commit(sm.kv_empty((g0 + n - 1) % S));
@@ -343,7 +485,7 @@ __device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, u
 
 // ------------------------------------------------------------------ softmax
 // Warpgroup t (warps 4t..4t+3); thread = one query row of query tile t.
-template <int D, bool BF16, bool SOFTCAP, bool MASK>
+template <int D, bool BF16, bool SOFTCAP, bool MASK, bool KSPLIT>
 __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& sm, uint32_t tmem,
                                              int n_items, int warp, int lane) {
   const CommonParams& p = P.c;
@@ -353,16 +495,22 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
   const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
   const uint32_t s_addr = tmem + lane_base + t * 128;
   const uint32_t o_addr = tmem + lane_base + kColO + t * 128;
-  int sc = 0;  // S tiles consumed (all items)
-  int oc = 0;  // items whose O this warpgroup has read
+  int sc = 0;                // S tiles this lane consumed (all items)
+  int oc[kQTiles] = {0, 0};  // o_final completions per lane so far (both warpgroups track both)
+  int mc = 0;                // key-split items merged so far
+  // batch ranking only in the key-split variant (short query ranges, where
+  // ragged lengths decide the cost); elsewhere the pointer stays out of registers
+  const int* border = (KSPLIT && p.B <= kMaxOrderB) ? sm.order() : nullptr;
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int idx = item_of_round(r, n_items);
     if (idx < 0) break;
-    const Item it = make_item(p, idx);
-    const TileRange T = t == 0 ? it.tr[0] : it.tr[1];  // a select keeps tr[] in registers
-    const int nt = T.t_end - T.t_begin;
-    const int64_t qi = it.q0 + t * BM + row;
+    const Item it = make_item<KSPLIT>(p, idx, border);
+    // selects, not it.tr[t]: a runtime index would put the item in local memory
+    const TileRange T = t == 0 ? it.tr[0] : it.tr[1];
+    const int nt0 = it.tiles(0), nt1 = it.tiles(1);
+    const int nt = t == 0 ? nt0 : nt1;
+    const int64_t qi = (t == 0 ? it.row0(0) : it.row0(1)) + row;
     const RowLimits R = row_limits(p, it.L, qi);
     const float* mrow = nullptr;
     if constexpr (MASK) {
@@ -375,7 +523,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
     float m_run = -INFINITY;  // running max, log2 units
     float l_run = 0.0f;       // running denominator
     for (int c = 0; c < nt; ++c, ++sc) {
-      const int64_t key0 = (int64_t)(T.t_begin + c) * BN;
+      const int64_t key0 = (int64_t)(T.t_begin + c * (KSPLIT ? it.stride : 1)) * BN;
       if (!mbar_wait_warp(sm.s_full(t), sc & 1, p.timeout_ns, p.status)) { ok = false; break; }
       tc_fence_after();
       float x[BN];
@@ -430,7 +578,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
           for (int i = 0; i < BN; ++i) x[i] *= p.scale_log2;
           scaled = true;
         }
-        int64_t lo = R.lo - key0, hi = R.hi - key0;
+        int lo = R.lo - (int)key0, hi = R.hi - (int)key0;
         lo = lo < 0 ? 0 : (lo > BN ? BN : lo);
         hi = hi < 0 ? 0 : (hi > BN ? BN : hi);
         const int lo_rel = (int)lo;
@@ -499,19 +647,50 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
     if (!ok) break;
 
     // ---------------------------------------------------------- epilogue
-    bool have_o = nt > 0;
-    if (have_o) {
-      if (!mbar_wait_warp(sm.o_final(t), oc & 1, p.timeout_ns, p.status)) { ok = false; break; }
-      ++oc;
-      tc_fence_after();
+    float2* merge = sm.merge();
+    float a0 = 1.0f, a1 = 0.0f, inv_l = 0.0f;  // out = (a0 O_t + a1 O_1) * inv_l
+    bool have_o = nt > 0, have_o1 = false;
+    if (KSPLIT && it.split) {
+      // key-split lanes: warpgroup 1 hands its row max / sum to warpgroup 0,
+      // which combines both partial rows
+      if (t == 1) {
+        merge[row] = make_float2(m_run, l_run);
+        mbar_arrive(sm.merge_full());
+        // O_1 must not be overwritten by this lane's next item before warpgroup 0 read it
+        if (!mbar_wait_warp(sm.merge_done(), mc & 1, p.timeout_ns, p.status)) { ok = false; break; }
+        tc_fence_after();
+        ++mc;
+        oc[0] += nt0 > 0;
+        oc[1] += nt1 > 0;
+        continue;
+      }
+      if (nt1 > 0) {
+        if (!mbar_wait_warp(sm.o_final(1), oc[1] & 1, p.timeout_ns, p.status)) { ok = false; break; }
+        have_o1 = true;
+      }
+      if (!mbar_wait_warp(sm.merge_full(), mc & 1, p.timeout_ns, p.status)) { ok = false; break; }
+      const float2 ml1 = merge[row];
+      const float m = fmaxf(m_run, ml1.x);
+      a0 = m_run == -INFINITY ? 0.0f : fast_exp2(m_run - m);
+      a1 = ml1.x == -INFINITY ? 0.0f : fast_exp2(ml1.x - m);
+      const float l = a0 * l_run + a1 * ml1.y;
+      inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+    } else {
+      inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
     }
-    const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+    if (have_o) {
+      if (!mbar_wait_warp(sm.o_final(t), (t == 0 ? oc[0] : oc[1]) & 1, p.timeout_ns, p.status)) { ok = false; break; }
+    }
+    oc[0] += nt0 > 0;
+    oc[1] += nt1 > 0;
+    tc_fence_after();
     uint16_t* out = reinterpret_cast<uint16_t*>(p.out);
     int64_t base;
     if (p.out_layout == 0)
       base = (((int64_t)it.b * p.Hq + it.h) * p.Sq + qi) * D;
     else
       base = (((int64_t)it.b * p.Sq + qi) * p.Hq + it.h) * D;
+    const uint32_t o1_addr = tmem + lane_base + kColO + 128;
 #pragma unroll
     for (int k = 0; k < D / 32; ++k) {
       uint32_t o[32];
@@ -521,6 +700,14 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = 0u;
+      }
+      if (KSPLIT && have_o1) {  // key-split: fold in lane 1's partial row
+        uint32_t o1[32];
+        tmem_ld32(o1_addr + k * 32, o1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          o[i] = __float_as_uint(a0 * __uint_as_float(o[i]) + a1 * __uint_as_float(o1[i]));
       }
       uint32_t w[16];
 #pragma unroll
@@ -532,12 +719,18 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
         for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       }
     }
+    if (KSPLIT && it.split) {
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(sm.merge_done());  // lane 1 may now start its next item
+      ++mc;
+    }
     // The next item's first P.V into O_t waits for this warpgroup's next
     // p_full arrival, which comes after these reads (fence before arrive).
   }
 }
 
-template <int D, bool BF16, bool SOFTCAP, bool MASK>
+template <int D, bool BF16, bool SOFTCAP, bool MASK, bool KSPLIT>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ TcParams P) {
   using Cfg = TcConfig<D>;
   constexpr int S = Cfg::kStages;
@@ -571,8 +764,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
       mbar_init(sm.o_final(t), 1);
     }
     mbar_init(sm.drain(), 1);
+    mbar_init(sm.merge_full(), BM);
+    mbar_init(sm.merge_done(), BM);
     mbar_init_fence();
   }
+  if (KSPLIT && p.B <= kMaxOrderB) rank_batches(p, reinterpret_cast<int*>(sm.base + Cfg::kOffOrder));
   if (warp == kTmaWarp && lane == 0) {
     tma_prefetch_desc(&P.tmap_q);
     tma_prefetch_desc(&P.tmap_k);
@@ -588,11 +784,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
   if (warp == kTmaWarp) {
-    if (lane == 0) producer_role<D>(P, sm, n_items);
+    if (lane == 0) producer_role<D, KSPLIT>(P, sm, n_items);
   } else if (warp == kMmaWarp) {
-    mma_role<D, BF16>(P, sm, tmem, n_items, lane);
+    mma_role<D, BF16, KSPLIT>(P, sm, tmem, n_items, lane);
   } else {
-    softmax_role<D, BF16, SOFTCAP, MASK>(P, sm, tmem, n_items, warp, lane);
+    softmax_role<D, BF16, SOFTCAP, MASK, KSPLIT>(P, sm, tmem, n_items, warp, lane);
   }
 
   tc_fence_before();
@@ -603,9 +799,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
   }
 }
 
-template <int D, bool BF16, bool SOFTCAP, bool MASK>
+template <int D, bool BF16, bool SOFTCAP, bool MASK, bool KSPLIT>
 cudaError_t launch_variant(const TcParams& P, cudaStream_t stream) {
-  auto kernel = attn_fwd_tc_kernel<D, BF16, SOFTCAP, MASK>;
+  auto kernel = attn_fwd_tc_kernel<D, BF16, SOFTCAP, MASK, KSPLIT>;
   constexpr uint32_t smem = TcConfig<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -620,14 +816,23 @@ cudaError_t launch_variant(const TcParams& P, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int D, bool BF16>
-cudaError_t launch_d(const TcParams& P, cudaStream_t stream) {
+template <int D, bool BF16, bool KSPLIT>
+cudaError_t launch_k(const TcParams& P, cudaStream_t stream) {
   const bool sc = P.c.softcap > 0.0f;
   const bool mk = P.c.mask != nullptr && P.c.mask_planes > 0;
-  if (sc && mk) return launch_variant<D, BF16, true, true>(P, stream);
-  if (sc) return launch_variant<D, BF16, true, false>(P, stream);
-  if (mk) return launch_variant<D, BF16, false, true>(P, stream);
-  return launch_variant<D, BF16, false, false>(P, stream);
+  if (sc && mk) return launch_variant<D, BF16, true, true, KSPLIT>(P, stream);
+  if (sc) return launch_variant<D, BF16, true, false, KSPLIT>(P, stream);
+  if (mk) return launch_variant<D, BF16, false, true, KSPLIT>(P, stream);
+  return launch_variant<D, BF16, false, false, KSPLIT>(P, stream);
+}
+
+template <int D, bool BF16>
+cudaError_t launch_d(const TcParams& P, cudaStream_t stream) {
+  // Key-split lanes are compiled in only when some item has an empty second
+  // query tile: the last query pair holds at most 128 rows.
+  const int rem = P.c.Sq - ((P.c.Sq - 1) / (kQTiles * BM)) * (kQTiles * BM);
+  if (rem <= BM) return launch_k<D, BF16, true>(P, stream);
+  return launch_k<D, BF16, false>(P, stream);
 }
 
 }  // namespace

@@ -21,7 +21,7 @@ namespace gb300_attn {
 // Rows outside [0, Sq) see nothing.  64-bit arithmetic throughout.
 // ---------------------------------------------------------------------------
 struct RowLimits {
-  int64_t lo, hi;  // visible keys are [lo, hi); empty when hi <= lo
+  int lo, hi;  // visible keys are [lo, hi), 0 <= lo <= hi <= Sk (empty when equal)
 };
 
 struct BatchLimits {
@@ -38,17 +38,21 @@ __device__ __forceinline__ BatchLimits batch_limits(const CommonParams& p, int b
 
 __device__ __forceinline__ RowLimits row_limits(const CommonParams& p, const BatchLimits& L,
                                                 int64_t qi) {
-  RowLimits r;
   const int64_t causal_max = L.causal_base + qi;
-  r.lo = 0;
+  int64_t lo = 0;
   if (p.local_window > 0) {
-    r.lo = causal_max + 1 - (int64_t)p.local_window;
-    if (r.lo < 0) r.lo = 0;
+    lo = causal_max + 1 - (int64_t)p.local_window;
+    if (lo < 0) lo = 0;
   }
   int64_t hi = L.lsk < (int64_t)p.Sk ? L.lsk : (int64_t)p.Sk;
   if (p.causal && causal_max + 1 < hi) hi = causal_max + 1;
-  if (qi < 0 || qi >= (int64_t)p.Sq) hi = r.lo;  // rows past Sq see nothing
-  r.hi = hi;
+  if (qi < 0 || qi >= (int64_t)p.Sq) hi = lo;  // rows past Sq see nothing
+  // clamp into [0, Sk] (keeps the visible set; fits 32 bits)
+  if (lo > (int64_t)p.Sk) lo = p.Sk;
+  if (hi < lo) hi = lo;
+  RowLimits r;
+  r.lo = (int)lo;
+  r.hi = (int)hi;
   return r;
 }
 
@@ -57,8 +61,8 @@ __device__ __forceinline__ RowLimits row_limits(const CommonParams& p, const Bat
 // the block sees every key (no per-element masking needed there).  lo and hi
 // are non-decreasing in qi, so the extremes come from the first and last row.
 struct TileRange {
-  int t_begin, t_end;      // tiles to visit
-  int64_t full_lo, full_hi;  // keys [full_lo, full_hi) visible to every row
+  int t_begin, t_end;  // tiles to visit
+  int full_lo, full_hi;  // keys [full_lo, full_hi) visible to every row
 };
 
 __device__ __forceinline__ TileRange tile_range(const CommonParams& p, const BatchLimits& L,
@@ -70,8 +74,8 @@ __device__ __forceinline__ TileRange tile_range(const CommonParams& p, const Bat
   const RowLimits last = row_limits(p, L, q_last);
   // union of the visible ranges of all rows (rows with an empty range included
   // in the bounds is harmless: their scores are all masked)
-  const int64_t lo = first.lo;
-  const int64_t hi = last.hi;
+  const int lo = first.lo;
+  const int hi = last.hi;
   if (hi <= lo || q0 >= (int64_t)p.Sq) {
     t.t_begin = t.t_end = 0;
   } else {
