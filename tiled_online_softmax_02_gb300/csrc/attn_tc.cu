@@ -59,7 +59,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.0f;  // keep the old max while it is within 2^8
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxOrderB = 256;  // batches ranked by cost when B <= this
+constexpr int kMaxOrderB = 64;   // batches ranked by cost when B <= this
+constexpr uint32_t kMaskBufBytes = 32 * 32 * 4;  // per softmax warp: 32 rows x 32 keys of f32
 
 template <int D>
 struct TcConfig {
@@ -77,7 +78,9 @@ struct TcConfig {
   static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffMerge = kOffTmemSlot + 16;          // float2 [128] (key-split merge)
   static constexpr uint32_t kOffOrder = kOffMerge + BM * 8;         // int [kMaxOrderB] batch order
-  static constexpr uint32_t kSmemBytes = kOffOrder + kMaxOrderB * 4 + 1024;  // + alignment slack
+  static constexpr uint32_t kOffMaskBuf = (kOffOrder + kMaxOrderB * 4 + 127) / 128 * 128;
+  static constexpr uint32_t kSmemBytes = kOffMaskBuf + 8 * kMaskBufBytes + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 // Shared-memory addresses of the tiles and barriers.
@@ -103,6 +106,7 @@ struct Smem {
   __device__ uint32_t merge_done() const { return bar0 + 8u * (2 + 3 * S + 8); }
   __device__ float2* merge() const { return reinterpret_cast<float2*>(base + Cfg::kOffMerge); }
   __device__ const int* order() const { return reinterpret_cast<const int*>(base + Cfg::kOffOrder); }
+  __device__ uint8_t* mask_buf(int warp) const { return base + Cfg::kOffMaskBuf + warp * kMaskBufBytes; }
 };
 
 // One work item of one (b, h): two lanes t = 0, 1, each a 128-row query tile
@@ -483,6 +487,62 @@ __device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, u
   mbar_wait_warp(sm.drain(), 0, p.timeout_ns, p.status);
 }
 
+// Mask block of one warp -- 32 rows (mask rows mwarp, mwarp + Sk, ...) by the
+// 128 keys [key0, key0 + 128) -- into x of the lane that owns each row
+// (natural units; 0 for rows >= nrows and keys >= Sk).  A lane-per-row load
+// would touch 32 cache lines per instruction; instead each instruction loads
+// 4 rows x 128 contiguous bytes, and a 4 KB per-warp buffer (16-byte chunks
+// XOR-swizzled by row, conflict-free both ways) turns rows into lanes.  Needs
+// vec4: mask rows are 16-byte aligned (Sk % 4 == 0) and loads are float4;
+// otherwise each 16-byte chunk is four scalar loads with per-element bounds.
+__device__ __forceinline__ void mask_rows_coalesced(float (&x)[BN], const float* mwarp, int nrows,
+                                                    int Sk, int key0, bool vec4, uint8_t* buf,
+                                                    int lane) {
+  const int rsub = lane >> 3;  // row within a group of 4
+  const int csub = lane & 7;   // 16-byte chunk within a 128-byte row segment
+  // one 32-key chunk in flight per lane (8 float4); the other lane's warps
+  // cover the latency
+  float4 v[8];
+  auto load = [&](int k, float4 (&dst)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int row = 4 * i + rsub;
+      const int key = key0 + 32 * k + 4 * csub;
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float* src = mwarp + (int64_t)row * Sk + key;
+      if (vec4) {
+        if (row < nrows && key + 3 < Sk) t = __ldg(reinterpret_cast<const float4*>(src));
+      } else if (row < nrows) {
+        if (key + 0 < Sk) t.x = __ldg(src + 0);
+        if (key + 1 < Sk) t.y = __ldg(src + 1);
+        if (key + 2 < Sk) t.z = __ldg(src + 2);
+        if (key + 3 < Sk) t.w = __ldg(src + 3);
+      }
+      dst[i] = t;
+    }
+  };
+  load(0, v);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int row = 4 * i + rsub;
+      *reinterpret_cast<float4*>(buf + row * 128 + ((csub ^ (row & 7)) << 4)) = v[i];
+    }
+    if (k + 1 < 4) load(k + 1, v);
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float4 t = *reinterpret_cast<const float4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4));
+      x[32 * k + 4 * c + 0] = t.x;
+      x[32 * k + 4 * c + 1] = t.y;
+      x[32 * k + 4 * c + 2] = t.z;
+      x[32 * k + 4 * c + 3] = t.w;
+    }
+    __syncwarp();
+  }
+}
+
 // ------------------------------------------------------------------ softmax
 // Warpgroup t (warps 4t..4t+3); thread = one query row of query tile t.
 template <int D, bool BF16, bool SOFTCAP, bool MASK, bool KSPLIT>
@@ -512,63 +572,65 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
     const int nt = t == 0 ? nt0 : nt1;
     const int64_t qi = (t == 0 ? it.row0(0) : it.row0(1)) + row;
     const RowLimits R = row_limits(p, it.L, qi);
-    const float* mrow = nullptr;
+    const float* mwarp = nullptr;  // this warp's first mask row
+    int mrows = 0;
     if constexpr (MASK) {
       int64_t plane = 0;
       if (p.mask_planes == p.B) plane = it.b;
       else if (p.mask_planes == p.B * p.Hq) plane = (int64_t)it.b * p.Hq + it.h;
-      if (qi < p.Sq) mrow = p.mask + (plane * p.Sq + qi) * (int64_t)p.Sk;
+      const int64_t qw0 = qi - lane;  // this warp's first row
+      mwarp = p.mask + (plane * p.Sq + (qw0 < p.Sq ? qw0 : 0)) * (int64_t)p.Sk;
+      mrows = qw0 < p.Sq ? (int)min((int64_t)32, (int64_t)p.Sq - qw0) : 0;
     }
 
     float m_run = -INFINITY;  // running max, log2 units
     float l_run = 0.0f;       // running denominator
     for (int c = 0; c < nt; ++c, ++sc) {
       const int64_t key0 = (int64_t)(T.t_begin + c * (KSPLIT ? it.stride : 1)) * BN;
+      float x[BN];
+      if constexpr (MASK) {
+        // this tile's mask rows into x (natural units), before the S wait:
+        // the loads overlap the tensor core's work
+        mask_rows_coalesced(x, mwarp, mrows, p.Sk, (int)key0, p.mask_vec4 != 0, sm.mask_buf(warp),
+                            lane);
+      }
       if (!mbar_wait_warp(sm.s_full(t), sc & 1, p.timeout_ns, p.status)) { ok = false; break; }
       tc_fence_after();
-      float x[BN];
-      {
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_ld32(s_addr + k * 32, sr[k]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[k * 32 + i] = __uint_as_float(sr[k][i]);
-      }
 
       const bool need_mask = !(key0 >= T.full_lo && key0 + BN <= T.full_hi);
       float m_tile;
       bool scaled = false;  // x already in log2 units (else raw Q.K, scaled inside the exp)
-      if constexpr (SOFTCAP) {
-        // c tanh(scale s / c), already in log2 units
-#pragma unroll
-        for (int i = 0; i < BN; ++i) x[i] = soft_cap_log2(x[i], p.sc_k1, p.sc_k2, p.sc_k3);
-        scaled = true;
-      } else if constexpr (MASK) {
-#pragma unroll
-        for (int i = 0; i < BN; ++i) x[i] *= p.scale_log2;
-        scaled = true;
-      }
       if constexpr (MASK) {
-        // + mask (log2 units); rows past Sq have no mask row
-        if (mrow != nullptr) {
+        // x = transform(S) + mask * log2 e, 32 columns at a time
 #pragma unroll
-          for (int c4 = 0; c4 < BN; c4 += 4) {
-            const int64_t j0 = key0 + c4;
-            float mv[4] = {0.f, 0.f, 0.f, 0.f};
-            if (p.mask_vec4 && j0 + 3 < (int64_t)p.Sk) {
-              const float4 m4 = __ldg(reinterpret_cast<const float4*>(mrow + j0));
-              mv[0] = m4.x; mv[1] = m4.y; mv[2] = m4.z; mv[3] = m4.w;
-            } else {
+        for (int k = 0; k < 4; ++k) {
+          uint32_t sr[32];
+          tmem_ld32(s_addr + k * 32, sr);
+          tmem_wait_ld();
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
-                if (j0 + u < (int64_t)p.Sk) mv[u] = __ldg(mrow + j0 + u);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) x[c4 + u] = fmaf(mv[u], kLog2e, x[c4 + u]);
+          for (int i = 0; i < 32; ++i) {
+            const float sv = __uint_as_float(sr[i]);
+            const float v = SOFTCAP ? soft_cap_log2(sv, p.sc_k1, p.sc_k2, p.sc_k3) : sv * p.scale_log2;
+            x[32 * k + i] = fmaf(x[32 * k + i], kLog2e, v);
           }
+        }
+        scaled = true;
+      } else {
+        {
+          uint32_t sr[4][32];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tmem_ld32(s_addr + k * 32, sr[k]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[k * 32 + i] = __uint_as_float(sr[k][i]);
+        }
+        if constexpr (SOFTCAP) {
+          // c tanh(scale s / c), already in log2 units
+#pragma unroll
+          for (int i = 0; i < BN; ++i) x[i] = soft_cap_log2(x[i], p.sc_k1, p.sc_k2, p.sc_k3);
+          scaled = true;
         }
       }
       if (need_mask) {
