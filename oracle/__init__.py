@@ -65,6 +65,11 @@ def _bind(lib):
                                      i64, i64, i64, i64, i64, i64, i64,
                                      ctypes.c_int, i64, ctypes.c_double, ctypes.c_double,
                                      i64, ctypes.c_int]
+    lib.oracle_attn_fwd_lse.restype = ctypes.c_int
+    lib.oracle_attn_fwd_lse.argtypes = [f32p, f32p, f32p, f32p, i32p, i32p, f64p, f64p,
+                                        i64, i64, i64, i64, i64, i64, i64,
+                                        ctypes.c_int, i64, ctypes.c_double, ctypes.c_double,
+                                        ctypes.c_int, i64, ctypes.c_int]
     lib.oracle_default_threads.restype = ctypes.c_int
     lib.oracle_default_threads.argtypes = []
     return lib
@@ -162,3 +167,31 @@ def attn_rows(q, k, v, rows, *, B, Hq, Hkv, Sq, Sk, kv_capacity, D, causal=False
     if rc != 0:
         raise ValueError(f"oracle_attn_rows failed with code {rc}")
     return out
+
+
+def attn_fwd_lse(q, k, v, *, B, Hq, Hkv, Sq, Sk, kv_capacity, D, causal=False,
+                 local_window=0, scale=None, softcap=0.0, out_layout=0, mask=None,
+                 mask_planes=0, total_lengths=None, past_lengths=None, nthreads=0, lib=None):
+    """Full forward in fp64 plus the per-row log-sum-exp of the scores
+    (natural log, -inf for rows without a finite score).  Returns (out, lse)
+    with lse float64 [B, Hq, Sq]."""
+    lib = lib or load()
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(D))
+    qa, qp = _f32(_as_numpy(q))
+    ka, kp = _f32(_as_numpy(k))
+    va, vp = _f32(_as_numpy(v))
+    ma, mp = _f32(_as_numpy(mask))
+    ta, tp = _i32(_as_numpy(total_lengths))
+    pa, pp = _i32(_as_numpy(past_lengths))
+    shape = (B, Hq, Sq, D) if out_layout == 0 else (B, Sq, Hq * D)
+    out = np.zeros(shape, dtype=np.float64)
+    lse = np.zeros((B, Hq, Sq), dtype=np.float64)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    rc = lib.oracle_attn_fwd_lse(qp, kp, vp, mp, tp, pp, out.ctypes.data_as(f64p),
+                                 lse.ctypes.data_as(f64p), B, Hq, Hkv, Sq, Sk, kv_capacity, D,
+                                 int(bool(causal)), int(local_window), float(scale),
+                                 float(softcap), int(out_layout), int(mask_planes), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_fwd_lse failed with code {rc}")
+    return out, lse

@@ -22,6 +22,7 @@
  *          S[j] = S[j] + mask[plane, qi, j]            if a mask is given
  *   M = max_j S[j];  the row is 0 if M = -inf
  *   O[d] = sum_j exp(S[j] - M) V[j,d] / sum_j exp(S[j] - M)
+ *   lse  = log sum_j exp(S[j]) = M + log sum_j exp(S[j] - M)   (-inf if M = -inf)
  *
  * Sources: "onnx-runtime-ep-cuda 0.1.0-dev.5, src/kernels/flash_attention.rs"
  * -- the kernel `flash_attention_body` (per-row limits, the masking rule, the
@@ -61,9 +62,10 @@ typedef struct {
     int64_t mask_planes;
 } problem_t;
 
-/* One output row: the definition written out. `s` is scratch of Sk doubles. */
+/* One output row: the definition written out. `s` is scratch of Sk doubles.
+ * Also returns the row's log-sum-exp of the scores in *lse. */
 static void oracle_row(const problem_t *p, int64_t b, int64_t h, int64_t qi,
-                       double *s, double *o)
+                       double *s, double *o, double *lse)
 {
     const int64_t group = p->Hq / p->Hkv;
     const int64_t kvh = h / group;
@@ -102,6 +104,7 @@ static void oracle_row(const problem_t *p, int64_t b, int64_t h, int64_t qi,
     }
 
     for (int64_t d = 0; d < p->D; ++d) o[d] = 0.0;
+    *lse = -INFINITY;
     if (m == -INFINITY) return; /* no finite visible score: the row is 0 */
 
     double l = 0.0;
@@ -115,6 +118,7 @@ static void oracle_row(const problem_t *p, int64_t b, int64_t h, int64_t qi,
         for (int64_t d = 0; d < p->D; ++d) o[d] += s[j] * (double)vrow[d];
     }
     for (int64_t d = 0; d < p->D; ++d) o[d] /= l;
+    *lse = m + log(l);
 }
 
 typedef struct {
@@ -122,6 +126,7 @@ typedef struct {
     const int64_t *rows; /* NULL: all rows, enumerated (b, h, qi) */
     int64_t n_rows, begin, end;
     double *out;
+    double *lse;    /* NULL, or one value per row: [B,Hq,Sq] (rows == NULL) or [n_rows] */
     int out_layout; /* only used when rows == NULL */
     int failed;
 } task_t;
@@ -137,7 +142,7 @@ static void *worker(void *arg)
     }
     for (int64_t r = t->begin; r < t->end; ++r) {
         int64_t b, h, qi;
-        double *o;
+        double *o, lse;
         if (t->rows) {
             b = t->rows[3 * r + 0];
             h = t->rows[3 * r + 1];
@@ -152,14 +157,15 @@ static void *worker(void *arg)
             else
                 o = t->out + ((b * p->Sq + qi) * p->Hq + h) * p->D;
         }
-        oracle_row(p, b, h, qi, s, o);
+        oracle_row(p, b, h, qi, s, o, &lse);
+        if (t->lse) t->lse[t->rows ? r : (b * p->Hq + h) * p->Sq + qi] = lse;
     }
     free(s);
     return NULL;
 }
 
 static int run_tasks(const problem_t *p, const int64_t *rows, int64_t n_rows,
-                     double *out, int out_layout, int nthreads)
+                     double *out, double *lse, int out_layout, int nthreads)
 {
     if (nthreads <= 0) {
         long n = sysconf(_SC_NPROCESSORS_ONLN);
@@ -182,6 +188,7 @@ static int run_tasks(const problem_t *p, const int64_t *rows, int64_t n_rows,
         tasks[i].rows = rows;
         tasks[i].n_rows = n_rows;
         tasks[i].out = out;
+        tasks[i].lse = lse;
         tasks[i].out_layout = out_layout;
         tasks[i].begin = 0;
         tasks[i].end = 0;
@@ -239,7 +246,21 @@ int oracle_attn_fwd(const float *q, const float *k, const float *v, const float 
     problem_t p = {q, k, v, mask, total_lengths, past_lengths, B, Hq, Hkv, Sq, Sk,
                    kv_capacity, D, causal, local_window, scale, softcap, mask_planes};
     if (check(&p) || !out || (out_layout != 0 && out_layout != 1)) return 1;
-    return run_tasks(&p, NULL, B * Hq * Sq, out, out_layout, nthreads);
+    return run_tasks(&p, NULL, B * Hq * Sq, out, NULL, out_layout, nthreads);
+}
+
+/* Full forward plus the per-row log-sum-exp of the scores, lse [B,Hq,Sq]. */
+int oracle_attn_fwd_lse(const float *q, const float *k, const float *v, const float *mask,
+                        const int32_t *total_lengths, const int32_t *past_lengths, double *out,
+                        double *lse, int64_t B, int64_t Hq, int64_t Hkv, int64_t Sq, int64_t Sk,
+                        int64_t kv_capacity, int64_t D, int causal, int64_t local_window,
+                        double scale, double softcap, int out_layout, int64_t mask_planes,
+                        int nthreads)
+{
+    problem_t p = {q, k, v, mask, total_lengths, past_lengths, B, Hq, Hkv, Sq, Sk,
+                   kv_capacity, D, causal, local_window, scale, softcap, mask_planes};
+    if (check(&p) || !out || !lse || (out_layout != 0 && out_layout != 1)) return 1;
+    return run_tasks(&p, NULL, B * Hq * Sq, out, lse, out_layout, nthreads);
 }
 
 /* Selected rows only: rows is [n_rows][3] of (b, h, qi); out_rows is
@@ -259,7 +280,7 @@ int oracle_attn_rows(const float *q, const float *k, const float *v, const float
             rows[3 * r + 1] >= Hq || rows[3 * r + 2] < 0 || rows[3 * r + 2] >= Sq)
             return 1;
     }
-    return run_tasks(&p, rows, n_rows, out_rows, 0, nthreads);
+    return run_tasks(&p, rows, n_rows, out_rows, NULL, 0, nthreads);
 }
 
 /* Number of worker threads a call with nthreads <= 0 uses. */

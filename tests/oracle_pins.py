@@ -377,6 +377,42 @@ def pin_rows_equal_full(lib):
     _close(got, full[rows[:, 0], rows[:, 1], rows[:, 2]], 0.0, "rows = full")
 
 
-PINS = [pin_rows_equal_full, pin_closed_forms, pin_torch_sdpa, pin_streaming_recurrences, pin_uniform_v,
+def pin_lse(lib):
+    """The row log-sum-exp: hand-worked values, scipy's logsumexp over the
+    explicitly formed score rows, and the shift a constant mask row causes."""
+    from scipy.special import logsumexp
+    eye = np.eye(2, dtype=np.float32).reshape(1, 1, 2, 2)
+    v = np.array([[1, 2], [3, 4]], np.float32).reshape(1, 1, 2, 2)
+    kw = dict(B=1, Hq=1, Hkv=1, Sq=2, Sk=2, kv_capacity=2, D=2, scale=1.0, nthreads=1, lib=lib)
+    _, lse = oracle.attn_fwd_lse(eye, eye, v, **kw)
+    _close(lse[0, 0], [math.log(math.e + 1), math.log(1 + math.e)], 1e-14, "lse plain 2x2")
+    _, lse = oracle.attn_fwd_lse(eye, eye, v, causal=True, **kw)
+    _close(lse[0, 0], [1.0, math.log(1 + math.e)], 1e-14, "lse causal 2x2")
+    m = np.array([[[-np.inf, -np.inf], [0, 0]]], np.float32)
+    _, lse = oracle.attn_fwd_lse(eye, eye, v, mask=m, mask_planes=1, **kw)
+    assert lse[0, 0, 0] == -np.inf, "fully masked row must have lse -inf"
+    rng = np.random.default_rng(20)
+    B, Hq, Hkv, Sq, Sk, D = 2, 4, 2, 7, 11, 6
+    q, k, vv = _rand(rng, B, Hq, Sq, D), _rand(rng, B, Hkv, Sk, D), _rand(rng, B, Hkv, Sk, D)
+    am = (np.round(_rand(rng, B, Sq, Sk) * 256) / 256).astype(np.float32)
+    scale, c = 0.6, 3.0
+    kw = dict(B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, kv_capacity=Sk, D=D, scale=scale, causal=True,
+              softcap=c, mask=am, mask_planes=B, nthreads=2, lib=lib)
+    out, lse = oracle.attn_fwd_lse(q, k, vv, **kw)
+    _close(out, _run(lib, q, k, vv, causal=True, scale=scale, softcap=c, mask=am, mask_planes=B),
+           0.0, "attn_fwd_lse output = attn_fwd output")
+    g = Hq // Hkv
+    for b in range(B):
+        for h in range(Hq):
+            s = scale * (q[b, h].astype(np.float64) @ k[b, h // g].astype(np.float64).T)
+            s = c * np.tanh(s / c) + am[b].astype(np.float64)
+            s[np.triu(np.ones((Sq, Sk), bool), k=Sk - Sq + 1)] = -np.inf
+            _close(lse[b, h], logsumexp(s, axis=1), 1e-12, f"lse vs scipy b={b} h={h}")
+    shift = rng.integers(-3, 4, size=(B, Sq, 1)).astype(np.float32)
+    _, lse2 = oracle.attn_fwd_lse(q, k, vv, **dict(kw, mask=am + shift))
+    _close(lse2, lse + np.repeat(shift[:, None, :, 0], Hq, axis=1), 1e-12, "lse shift")
+
+
+PINS = [pin_rows_equal_full, pin_lse, pin_closed_forms, pin_torch_sdpa, pin_streaming_recurrences, pin_uniform_v,
         pin_mask_properties, pin_window_and_softcap_limits, pin_gqa_and_layout, pin_ragged,
         pin_brute_force_tiny]

@@ -45,6 +45,8 @@ MUTANTS = {
     "dot_q_with_q": ("(double)qrow[d] * (double)krow[d]", "(double)qrow[d] * (double)qrow[d]"),
     "softcap_without_inner_divide": ("p->softcap * tanh(score / p->softcap)",
                                      "p->softcap * tanh(score)"),
+    "lse_drops_max": ("*lse = m + log(l);", "*lse = log(l);"),
+    "lse_log2": ("*lse = m + log(l);", "*lse = m + log2(l);"),
     "kv_plane_ignores_batch": ("const int64_t kv_plane = (b * p->Hkv + kvh) * p->kv_capacity;",
                                "const int64_t kv_plane = kvh * p->kv_capacity;"),
 }
