@@ -10,6 +10,7 @@
 #ifndef GB300_ATTN_H
 #define GB300_ATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -96,6 +97,49 @@ int attn_fwd(const void *q, const void *k, const void *v, const float *mask,
              int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D,
              int causal, int local_window, float scale, float softcap, int out_layout,
              int mask_planes, int dtype, void *stream);
+
+/*
+ * attn_fwd_splitkv -- attn_fwd with each query tile's keys split into
+ * `num_splits` contiguous ranges computed by different CTAs, then merged
+ * (the flash-decoding arrangement: for decode-like shapes with few query rows
+ * and long key ranges).  The result is the same attention output; it can
+ * also return each row's log-sum-exp of its scores.
+ *
+ * The definition is attn_fwd's.  The merge combines ranges r with partial
+ * outputs O_r and log-sum-exps L_r as O = sum_r w_r O_r / sum_r w_r,
+ * w_r = exp(L_r - max L), L = max L + log sum_r w_r -- the online-softmax
+ * rescale of "onnx-runtime-ep-cuda 0.1.0-dev.5, src/kernels/flash_attention.rs"
+ * (`flash_attention_body`, alpha / beta update) applied to whole key ranges.
+ *
+ * Arguments as attn_fwd, plus:
+ *   dtype           ATTN_F16 or ATTN_BF16 only (ATTN_F32: ATTN_ERR_UNSUPPORTED)
+ *   num_splits      0 = chosen by the library (attn_splitkv_num_splits), else 1..64
+ *   lse             NULL or f32 [B, Hq, Sq] device: log sum_j exp(s_j) per row,
+ *                   natural log, -inf for rows without a finite score
+ *   workspace       device scratch of at least attn_splitkv_workspace_bytes(
+ *                   B, Hq, Sq, D, splits) bytes, 16-byte aligned, caller-owned,
+ *                   not overlapping any other argument; unused (may be NULL)
+ *                   when the split count is 1.  Calls that share a workspace
+ *                   must not overlap on the GPU.
+ * Launches the attention kernel and, when split, one merge kernel, on
+ * `stream`; allocates and synchronises nothing.  Errors as attn_fwd;
+ * ATTN_ERR_INVALID_ARG also for a split count outside 0..64 or a missing /
+ * too small workspace.
+ */
+int attn_fwd_splitkv(const void *q, const void *k, const void *v, const float *mask,
+                     const int32_t *total_lengths, const int32_t *past_lengths, void *out,
+                     int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D,
+                     int causal, int local_window, float scale, float softcap, int out_layout,
+                     int mask_planes, int dtype, int num_splits, float *lse, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/* The split count attn_fwd_splitkv uses for num_splits == 0 on the current
+ * device (about two work items per SM, at most one split per 128-key tile). */
+int attn_splitkv_num_splits(int B, int Hq, int Sq, int Sk);
+
+/* Workspace bytes attn_fwd_splitkv needs for a split count (0 when <= 1):
+ * num_splits * B * Hq * Sq * (D + 1) * 4. */
+size_t attn_splitkv_workspace_bytes(int B, int Hq, int Sq, int D, int num_splits);
 
 /* Human-readable name of a status code; never NULL. */
 const char *attn_status_string(int status);

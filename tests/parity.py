@@ -85,3 +85,41 @@ def run_and_check(w: Workload, seed: int | None = None, what: str = ""):
     out = run_gpu(w, x)
     ref = run_oracle(w, x)
     return check(w, out.double().cpu().numpy(), ref, what or w.name)
+
+
+def run_oracle_lse(w: Workload, x: dict):
+    return oracle.attn_fwd_lse(x["q"], x["k"], x["v"], B=w.B, Hq=w.Hq, Hkv=w.Hkv, Sq=w.Sq, Sk=w.Sk,
+                               kv_capacity=w.kv_capacity, D=w.D, causal=w.causal,
+                               local_window=w.local_window, scale=w.softmax_scale,
+                               softcap=w.softcap, out_layout=w.out_layout, mask=x["mask"],
+                               mask_planes=w.mask_planes, total_lengths=x["total_lengths"],
+                               past_lengths=x["past_lengths"])
+
+
+def run_gpu_splitkv(w: Workload, x: dict, num_splits: int):
+    g = to_dev(x)
+    o, lse = attn.attn_fwd_splitkv(g["q"], g["k"], g["v"], mask=g["mask"],
+                                   total_lengths=g["total_lengths"], past_lengths=g["past_lengths"],
+                                   causal=w.causal, local_window=w.local_window,
+                                   scale=w.softmax_scale, softcap=w.softcap,
+                                   out_layout=w.out_layout, seq_k=w.Sk, num_splits=num_splits)
+    torch.cuda.synchronize()
+    st = attn.get_device_status()
+    assert st == attn.ATTN_OK, f"device status {attn.status_string(st)}"
+    return o, lse
+
+
+# log-sum-exp: fp32 scores and sums against fp64
+LSE_ATOL, LSE_RTOL = 2e-3, 1e-4
+
+
+def check_lse(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    both_inf = np.isneginf(got) & np.isneginf(ref)
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref)), f"{what}: -inf rows differ"
+    g, r = got[~both_inf], ref[~both_inf]
+    assert np.isfinite(g).all(), f"{what}: non-finite lse"
+    bad = np.abs(g - r) > LSE_ATOL + LSE_RTOL * np.abs(r)
+    assert not bad.any(), f"{what}: {int(bad.sum())} lse values out of tolerance " \
+                          f"(max err {float(np.abs(g - r).max()):.3e})"

@@ -117,6 +117,29 @@ def test_unsupported_requests(lib, case):
     assert call(lib, **UNSUPPORTED[case]) == attn.ATTN_ERR_UNSUPPORTED
 
 
+def call_splitkv(lib, splits, ws=None, ws_bytes=0, lse=None, **kw):
+    a = dict(GOOD, **kw)
+    return lib.attn_fwd_splitkv(a["q"], a["k"], a["v"], a["mask"], a["total"], a["past"], a["out"],
+                                a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Sk"], a["cap"], a["D"],
+                                a["causal"], a["window"], a["scale"], a["softcap"], a["layout"],
+                                a["planes"], a["dtype"], splits, lse, ws, ws_bytes, None)
+
+
+def test_splitkv_validation(lib):
+    assert call_splitkv(lib, -1) == attn.ATTN_ERR_INVALID_ARG
+    assert call_splitkv(lib, 65) == attn.ATTN_ERR_INVALID_ARG
+    assert call_splitkv(lib, 4, dtype=0) == attn.ATTN_ERR_UNSUPPORTED
+    assert call_splitkv(lib, 4) == attn.ATTN_ERR_INVALID_ARG  # no workspace
+    need = lib.attn_splitkv_workspace_bytes(2, 4, 200, 64, 4)
+    assert need == 4 * 2 * 4 * 200 * 65 * 4
+    assert call_splitkv(lib, 4, ws=0x78000000, ws_bytes=need - 4) == attn.ATTN_ERR_INVALID_ARG
+    assert call_splitkv(lib, 4, ws=0x78000008, ws_bytes=need) == attn.ATTN_ERR_UNSUPPORTED
+    assert call_splitkv(lib, 4, ws=Q, ws_bytes=need) == attn.ATTN_ERR_INVALID_ARG  # overlaps q
+    assert call_splitkv(lib, 2, lse=0x7C000002) == attn.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_splitkv_workspace_bytes(2, 4, 200, 64, 1) == 0
+    assert call_splitkv(lib, 4, B=0) == attn.ATTN_OK
+
+
 def test_valid_plane_counts_pass_validation_order(lib):
     # plane counts 1, B and B*Hq are accepted; with D=96 the request still
     # fails, but on the capability gate, proving the plane check passed

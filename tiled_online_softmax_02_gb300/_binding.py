@@ -29,6 +29,12 @@ SIGNATURES = {
                         _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                         _i32, _i32, ctypes.c_float, ctypes.c_float, _i32,
                         _i32, _i32, _vp]),
+    "attn_fwd_splitkv": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                _i32, _i32, ctypes.c_float, ctypes.c_float, _i32,
+                                _i32, _i32, _i32, _vp, _vp, ctypes.c_size_t, _vp]),
+    "attn_splitkv_num_splits": (_i32, [_i32, _i32, _i32, _i32]),
+    "attn_splitkv_workspace_bytes": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, _i32]),
     "attn_status_string": (ctypes.c_char_p, [_i32]),
     "attn_last_cuda_error": (_i32, []),
     "attn_get_device_status": (_i32, [_vp]),
@@ -158,6 +164,51 @@ def attn_fwd(q, k, v, *, mask=None, total_lengths=None, past_lengths=None, causa
         torch.cuda.current_stream(q.device).synchronize()
         return host_out
     return out
+
+
+def attn_fwd_splitkv(q, k, v, *, mask=None, total_lengths=None, past_lengths=None, causal=False,
+                     local_window=0, scale=None, softcap=0.0, out_layout="head", seq_k=None,
+                     num_splits=0, out=None, lse=None, workspace=None):
+    """Split-KV attention forward (CUDA tensors, bf16 / f16): the same output
+    as attn_fwd, computed over `num_splits` key ranges and merged (0 = the
+    library's choice).  Returns (out, lse) with lse float32 [B, Hq, Sq], the
+    natural-log log-sum-exp of each row's scores.  The fp32 workspace is
+    allocated with torch when not given."""
+    B, Hq, Sq, D = q.shape
+    Hkv, kv_capacity = k.shape[1], k.shape[2]
+    Sk = kv_capacity if seq_k is None else int(seq_k)
+    lib = load_library()
+    layout = LAYOUTS[out_layout]
+    shape = (B, Hq, Sq, D) if layout == 0 else (B, Sq, Hq * D)
+    if q.dtype not in (torch.float16, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("split-KV needs float16 or bfloat16 q, k, v of one dtype")
+    for t in (q, k, v, mask, total_lengths, past_lengths):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("split-KV takes contiguous CUDA tensors")
+    mask_planes = 0
+    if mask is not None:
+        if mask.dim() == 4:
+            mask = mask.reshape(-1, mask.shape[-2], mask.shape[-1])
+        mask_planes = mask.shape[0]
+    with torch.cuda.device(q.device):
+        splits = int(num_splits) or lib.attn_splitkv_num_splits(B, Hq, Sq, max(Sk, 1))
+        need = lib.attn_splitkv_workspace_bytes(B, Hq, Sq, D, splits)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need // 4, dtype=torch.float32, device=q.device)
+        if out is None:
+            out = torch.empty(shape, dtype=q.dtype, device=q.device)
+        if lse is None:
+            lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        rc = lib.attn_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(total_lengths),
+                                  _ptr(past_lengths), _ptr(out), B, Hq, Hkv, Sq, Sk, kv_capacity,
+                                  D, int(bool(causal)), int(local_window),
+                                  float(1.0 / math.sqrt(D) if scale is None else scale),
+                                  float(softcap), layout, mask_planes, DTYPE_CODES[q.dtype], splits,
+                                  _ptr(lse), _ptr(workspace), ws_bytes, _stream_handle(q.device))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_splitkv")
+    return out, lse
 
 
 def get_device_status(device=None) -> int:

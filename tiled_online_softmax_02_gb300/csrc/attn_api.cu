@@ -136,11 +136,34 @@ cudaError_t launch_selftest_wait(uint64_t timeout_ns, int* status, cudaStream_t 
 
 using namespace gb300_attn;
 
-extern "C" int attn_fwd(const void* q, const void* k, const void* v, const float* mask,
-                        const int32_t* total_lengths, const int32_t* past_lengths, void* out,
-                        int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D,
-                        int causal, int local_window, float scale, float softcap, int out_layout,
-                        int mask_planes, int dtype, void* stream) {
+namespace {
+
+constexpr int kMaxSplits = 64;
+
+int tile_count(int Sk) { return (Sk + kTcBlockN - 1) / kTcBlockN; }
+
+int64_t splitkv_rows(int B, int Hq, int Sq) { return (int64_t)B * Hq * Sq; }
+
+// Split count chosen when the caller passes 0: enough work items for about
+// two per SM, never more splits than key tiles.
+int auto_splits(int B, int Hq, int Sq, int Sk) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t items = (int64_t)((Sq + 2 * kTcBlockM - 1) / (2 * kTcBlockM)) * B * Hq;
+  if (items <= 0) return 1;
+  int64_t s = (2 * (int64_t)sms + items - 1) / items;
+  const int tiles = tile_count(Sk);
+  if (s > tiles) s = tiles;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return s < 1 ? 1 : (int)s;
+}
+
+int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
+             const int32_t* total_lengths, const int32_t* past_lengths, void* out,
+             int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D,
+             int causal, int local_window, float scale, float softcap, int out_layout,
+             int mask_planes, int dtype, void* stream, bool splitkv_api, int num_splits, float* lse,
+             void* workspace, size_t workspace_bytes) {
   // ---------------------------------------------------------------- validation
   if (dtype != ATTN_F32 && dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   if (B < 0 || Sq < 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
@@ -176,6 +199,12 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, const float
 
   // capability gate: no kernel, no launch
   if (dtype == ATTN_F32 && D > 128) return ATTN_ERR_UNSUPPORTED;
+  if (splitkv_api) {
+    if (num_splits < 0 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+    if (dtype == ATTN_F32) return ATTN_ERR_UNSUPPORTED;  // split-KV is a tensor-core path
+    if (lse && !aligned(lse, 4)) return ATTN_ERR_UNSUPPORTED;
+    if (lse && overlaps(lse, splitkv_rows(B, Hq, Sq) * 4, out, qbytes)) return ATTN_ERR_INVALID_ARG;
+  }
   if (dtype != ATTN_F32 && D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
     return ATTN_ERR_UNSUPPORTED;
@@ -184,9 +213,22 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, const float
     return ATTN_ERR_UNSUPPORTED;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (Sk == 0) {  // no key at all: every row is 0
+  if (Sk == 0) {  // no key at all: every row is 0 (and its log-sum-exp -inf)
     cudaError_t e = cudaMemsetAsync(out, 0, (size_t)qbytes, st);
+    if (e == cudaSuccess && lse) e = launch_fill_f32(lse, splitkv_rows(B, Hq, Sq), -INFINITY, st);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+  }
+  int splits = 1;
+  if (splitkv_api) {
+    splits = num_splits == 0 ? auto_splits(B, Hq, Sq, Sk) : num_splits;
+    if (splits > 1) {
+      const size_t need = (size_t)splits * (size_t)splitkv_rows(B, Hq, Sq) * (size_t)(D + 1) * 4;
+      if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+      if (!aligned(workspace, 16)) return ATTN_ERR_UNSUPPORTED;
+      if (overlaps(workspace, (int64_t)need, out, qbytes) || overlaps(workspace, (int64_t)need, q, qbytes) ||
+          overlaps(workspace, (int64_t)need, k, kvbytes) || overlaps(workspace, (int64_t)need, v, kvbytes))
+        return ATTN_ERR_INVALID_ARG;
+    }
   }
 
   int err = ATTN_OK;
@@ -217,6 +259,12 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, const float
   }
   c.timeout_ns = g_timeout_ns.load();
   c.status = status;
+  c.num_splits = splits;
+  c.lse = lse;
+  if (splits > 1) {
+    c.ws_o = static_cast<float*>(workspace);
+    c.ws_lse = c.ws_o + (size_t)splits * (size_t)splitkv_rows(B, Hq, Sq) * D;
+  }
 
   cudaError_t e;
   if (dtype == ATTN_F32) {
@@ -235,8 +283,53 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, const float
     if (rc == ATTN_OK) rc = encode_map(&tp.tmap_v, v, bf16, (int64_t)B * Hkv, kv_capacity, D);
     if (rc != ATTN_OK) return rc;
     e = launch_attn_tc(tp, bf16, st);
+    if (e == cudaSuccess && splits > 1) {
+      MergeParams mp{};
+      mp.ws_o = c.ws_o;
+      mp.ws_lse = c.ws_lse;
+      mp.out = out;
+      mp.lse = lse;
+      mp.B = B; mp.Hq = Hq; mp.Sq = Sq; mp.D = D;
+      mp.num_splits = splits;
+      mp.out_layout = out_layout;
+      mp.bf16 = bf16;
+      e = launch_attn_merge(mp, st);
+    }
   }
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, const float* mask,
+                        const int32_t* total_lengths, const int32_t* past_lengths, void* out,
+                        int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D,
+                        int causal, int local_window, float scale, float softcap, int out_layout,
+                        int mask_planes, int dtype, void* stream) {
+  return fwd_impl(q, k, v, mask, total_lengths, past_lengths, out, B, Hq, Hkv, Sq, Sk, kv_capacity,
+                  D, causal, local_window, scale, softcap, out_layout, mask_planes, dtype, stream,
+                  false, 1, nullptr, nullptr, 0);
+}
+
+extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, const float* mask,
+                                const int32_t* total_lengths, const int32_t* past_lengths,
+                                void* out, int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity,
+                                int D, int causal, int local_window, float scale, float softcap,
+                                int out_layout, int mask_planes, int dtype, int num_splits,
+                                float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_impl(q, k, v, mask, total_lengths, past_lengths, out, B, Hq, Hkv, Sq, Sk, kv_capacity,
+                  D, causal, local_window, scale, softcap, out_layout, mask_planes, dtype, stream,
+                  true, num_splits, lse, workspace, workspace_bytes);
+}
+
+extern "C" int attn_splitkv_num_splits(int B, int Hq, int Sq, int Sk) {
+  if (B <= 0 || Hq <= 0 || Sq <= 0 || Sk <= 0) return 1;
+  return auto_splits(B, Hq, Sq, Sk);
+}
+
+extern "C" size_t attn_splitkv_workspace_bytes(int B, int Hq, int Sq, int D, int num_splits) {
+  if (B <= 0 || Hq <= 0 || Sq <= 0 || D <= 0 || num_splits <= 1) return 0;
+  return (size_t)num_splits * (size_t)splitkv_rows(B, Hq, Sq) * (size_t)(D + 1) * 4;
 }
 
 extern "C" const char* attn_status_string(int status) {

@@ -28,6 +28,22 @@ struct CommonParams {
   float sc_k1, sc_k2, sc_k3;
   uint64_t timeout_ns;
   int* status;        // device status word (timeouts)
+  // split-KV (tensor-core kernel): each query tile's key tiles are cut into
+  // num_splits contiguous ranges handled by different CTAs
+  int num_splits;     // 1: no split, rows are finished in the kernel
+  float* ws_o;        // num_splits > 1: partial rows [num_splits, B, Hq, Sq, D], each O / l
+  float* ws_lse;      // num_splits > 1: partial log-sum-exp [num_splits, B, Hq, Sq]
+  float* lse;         // nullable: the row log-sum-exp [B, Hq, Sq] (natural log)
+};
+
+// Combines split-KV partial rows into the output (and the log-sum-exp).
+struct MergeParams {
+  const float* ws_o;
+  const float* ws_lse;
+  void* out;
+  float* lse;  // nullable
+  int B, Hq, Sq, D, num_splits, out_layout;
+  bool bf16;
 };
 
 // tcgen05 kernel: Q / K / V reach shared memory through TMA tensor maps.
@@ -54,5 +70,7 @@ constexpr int kF32BlockM = 64;  // query rows per fp32 CTA
 cudaError_t launch_attn_tc(const TcParams& p, bool bf16, cudaStream_t stream);
 cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream);
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, int* status, cudaStream_t stream);
+cudaError_t launch_attn_merge(const MergeParams& p, cudaStream_t stream);
+cudaError_t launch_fill_f32(float* dst, int64_t n, float value, cudaStream_t stream);
 
 }  // namespace gb300_attn

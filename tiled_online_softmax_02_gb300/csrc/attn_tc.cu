@@ -1,907 +1,18 @@
-// attn_tc.cu -- tensor-core (tcgen05) attention forward for bf16 / f16 inputs
-// on GB300 (sm_103a).
-//
-// The method is the tiled online softmax of "onnx-runtime-ep-cuda
-// 0.1.0-dev.5, src/kernels/flash_attention.rs" (module doc and
-// `flash_attention_body`): scores of one key tile at a time, a running row
-// maximum and denominator, and the output numerator rescaled when the maximum
-// moves, so no [B,H,Sq,Sk] score tensor ever exists.  The page's kernel stages
-// 8 query rows x 16 keys through shared memory with scalar FMAs (and a wmma
-// variant with 16x16 tiles); this kernel is a GB300 design of the same method.
-//
-// Work item = two 128-row query tiles (t = 0, 1) of one (b, h).  The kernel is
-// persistent: one CTA per SM walks a static snake order over the items
-// (latest query rows -- the longest causal rows -- first), and the K/V ring,
-// barrier phases and tensor memory carry over from item to item, so the next
-// item's loads overlap the current item's tail.
-//   warps 0-3   softmax for query tile 0, warps 4-7 for query tile 1: thread
-//               r of a warpgroup owns query row r (= TMEM lane r).  Reads its
-//               S row with tcgen05.ld, applies the structural masks (select to
-//               -inf), soft-cap and additive mask, updates the running max /
-//               sum in registers, writes P (input dtype) back over its S row,
-//               and rescales its O row when the max grew by more than 2^8
-//               (otherwise the old max is kept: the final O / l is exact
-//               either way).  Then normalises and stores the row.
-//   warp 8      TMA producer: both Q tiles per item, K_j / V_j into a ring.
-//   warp 9      MMA issuer (one thread) and owner of tensor memory.  Per key
-//               tile j, for t = 0, 1:  O_t += P_t(j-1) V(j-1), then
-//               S_t(j) = Q_t K(j)^T.  While warpgroup 0 turns S_0 into P_0,
-//               the tensor core works on tile 1, and the other way round.
-//               Because S_t(j) is issued after O_t's P.V and a commit covers
-//               every earlier MMA of the thread, "S_t(j) ready" also means
-//               "O_t up to date", so a rescale never waits.
-// Each query tile visits only its own key-tile range (causal / window /
-// length limits), so the diagonal and window edges cost no extra MMAs.
-//
-// Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384),
-// O_1 [384,512).  Shared memory: Q_0, Q_1, kStages x (K, V) tiles, barriers;
-// every tile is stored as 64-column (128-byte) blocks in the 128-byte swizzle
-// TMA writes.
-//
-// Every barrier wait is bounded (mbar_wait); on a timeout the kernel records
-// ATTN_ERR_TIMEOUT in the status word, drains what it issued, frees tensor
-// memory and exits.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-
-#include "device_common.cuh"
+// attn_tc.cu -- dispatch of the tcgen05 attention kernels by input type and
+// head dim (the kernels live in attn_tc.cuh, instantiated per type and head
+// dim in attn_tc_<type>_d<D>.cu).
+#include "attn_internal.h"
 
 namespace gb300_attn {
-namespace {
 
-constexpr int BM = kTcBlockM;   // rows per query tile
-constexpr int BN = kTcBlockN;   // keys per key tile
-constexpr int kQTiles = 2;      // query tiles per work item
-constexpr int kThreads = 320;   // 8 softmax warps + producer + MMA
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;
-constexpr float kRescaleLog2 = 8.0f;  // keep the old max while it is within 2^8
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxOrderB = 64;   // batches ranked by cost when B <= this
-constexpr uint32_t kMaskBufBytes = 32 * 32 * 4;  // per softmax warp: 32 rows x 32 keys of f32
-
-template <int D>
-struct TcConfig {
-  static constexpr int kSub = D / 64;                   // 128-byte column blocks per row
-  static constexpr uint32_t kSubBytes = BM * 128;       // [128 rows][64 cols] of 16-bit
-  static constexpr uint32_t kTileBytes = kSub * kSubBytes;
-  static constexpr int kStages = (D == 64) ? 4 : 2;
-  static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffK = kOffQ + kQTiles * kTileBytes;
-  static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
-  static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
-  // q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_final[2],
-  // drain, merge_full, merge_done
-  static constexpr int kNumBars = 2 + 3 * kStages + 2 + 2 + 2 + 3;
-  static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
-  static constexpr uint32_t kOffMerge = kOffTmemSlot + 16;          // float2 [128] (key-split merge)
-  static constexpr uint32_t kOffOrder = kOffMerge + BM * 8;         // int [kMaxOrderB] batch order
-  static constexpr uint32_t kOffMaskBuf = (kOffOrder + kMaxOrderB * 4 + 127) / 128 * 128;
-  static constexpr uint32_t kSmemBytes = kOffMaskBuf + 8 * kMaskBufBytes + 1024;  // + alignment slack
-  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-};
-
-// Shared-memory addresses of the tiles and barriers.
-template <int D>
-struct Smem {
-  using Cfg = TcConfig<D>;
-  static constexpr int S = Cfg::kStages;
-  uint8_t* base;
-  uint32_t sQ, sK, sV, bar0;
-  __device__ uint32_t q_full() const { return bar0; }
-  __device__ uint32_t q_empty() const { return bar0 + 8u; }
-  __device__ uint32_t k_full(int s) const { return bar0 + 8u * (2 + s); }
-  __device__ uint32_t v_full(int s) const { return bar0 + 8u * (2 + S + s); }
-  __device__ uint32_t kv_empty(int s) const { return bar0 + 8u * (2 + 2 * S + s); }
-  __device__ uint32_t s_full(int t) const { return bar0 + 8u * (2 + 3 * S + t); }
-  __device__ uint32_t p_full(int t) const { return bar0 + 8u * (2 + 3 * S + 2 + t); }
-  // completes once per item, after query tile t's last P.V (the epilogue's wait)
-  __device__ uint32_t o_final(int t) const { return bar0 + 8u * (2 + 3 * S + 4 + t); }
-  __device__ uint32_t drain() const { return bar0 + 8u * (2 + 3 * S + 6); }
-  // key-split merge hand-over: lane 1's row max / sum written (128 arrivals),
-  // then lane 1's O read by warpgroup 0 (128 arrivals)
-  __device__ uint32_t merge_full() const { return bar0 + 8u * (2 + 3 * S + 7); }
-  __device__ uint32_t merge_done() const { return bar0 + 8u * (2 + 3 * S + 8); }
-  __device__ float2* merge() const { return reinterpret_cast<float2*>(base + Cfg::kOffMerge); }
-  __device__ const int* order() const { return reinterpret_cast<const int*>(base + Cfg::kOffOrder); }
-  __device__ uint8_t* mask_buf(int warp) const { return base + Cfg::kOffMaskBuf + warp * kMaskBufBytes; }
-};
-
-// One work item of one (b, h): two lanes t = 0, 1, each a 128-row query tile
-// with its own S / O in tensor memory, visiting key tiles
-// tr[t].t_begin, + stride, ... < tr[t].t_end.  Normally lane t is query tile t
-// (stride 1).  When the second query tile would have no rows (short Sq, e.g.
-// decode or chunked prefill), both lanes take the same 128 rows and split the
-// key tiles even / odd (stride 2), so the tensor core still alternates
-// between two softmax warpgroups; warpgroup 0 merges the two partial rows.
-// The item streams the key tiles [tb, tb + N).
-struct Item {
-  int b, h, kvh;
-  int64_t q0;
-  BatchLimits L;
-  TileRange tr[kQTiles];
-  int tb, N, stride;
-  bool split;
-  __device__ bool active(int t, int j) const {
-    return j >= tr[t].t_begin && j < tr[t].t_end && ((j - tr[t].t_begin) & (stride - 1)) == 0;
-  }
-  __device__ bool last(int t, int j) const { return j + stride >= tr[t].t_end; }
-  __device__ int tiles(int t) const {
-    return tr[t].t_end > tr[t].t_begin ? (tr[t].t_end - tr[t].t_begin + stride - 1) / stride : 0;
-  }
-  __device__ int64_t row0(int t) const { return q0 + (split ? 0 : t * BM); }
-};
-
-template <bool KSPLIT>
-__device__ __forceinline__ Item make_item(const CommonParams& p, int idx, const int* border) {
-  const int bh = p.B * p.Hq;
-  const int n_qp = (p.Sq + kQTiles * BM - 1) / (kQTiles * BM);
-  Item it;
-  const int qp = n_qp - 1 - idx / bh;  // latest query rows first
-  const int rem = idx - (idx / bh) * bh;
-  const int br = rem / p.Hq;
-  it.b = border ? border[br] : br;  // costliest batches first
-  it.h = rem - br * p.Hq;           // heads of one kv group are consecutive items
-  it.kvh = it.h / p.group;
-  it.q0 = (int64_t)qp * (kQTiles * BM);
-  it.L = batch_limits(p, it.b);
-  it.split = KSPLIT && it.q0 + BM >= (int64_t)p.Sq;
-  if (it.split) {
-    const TileRange t0 = tile_range(p, it.L, it.q0, BM, BN);
-    it.tr[0] = t0;
-    it.tr[1] = t0;
-    it.stride = 2;
-    if (t0.t_end > t0.t_begin + 1) {
-      it.tr[1].t_begin = t0.t_begin + 1;
-    } else {
-      it.tr[1].t_begin = it.tr[1].t_end = 0;  // one key tile: lane 1 stays empty
-    }
-    it.tb = t0.t_begin;
-    it.N = t0.t_end > t0.t_begin ? t0.t_end - t0.t_begin : 0;
-    return it;
-  }
-  it.stride = 1;
-  int tb = 0, te = 0;
-  bool any = false;
-#pragma unroll
-  for (int t = 0; t < kQTiles; ++t) {
-    it.tr[t] = tile_range(p, it.L, it.q0 + t * BM, BM, BN);
-    if (it.tr[t].t_end > it.tr[t].t_begin) {
-      tb = any ? min(tb, it.tr[t].t_begin) : it.tr[t].t_begin;
-      te = any ? max(te, it.tr[t].t_end) : it.tr[t].t_end;
-      any = true;
-    }
-  }
-  it.tb = tb;
-  it.N = te - tb;
-  return it;
-}
-
-// Batches ranked by their number of valid key tiles (descending, ties by
-// index), written to order[rank] = b.  Threads 0..B-1 each rank one batch.
-__device__ __forceinline__ void rank_batches(const CommonParams& p, int* order) {
-  const int b = threadIdx.x;
-  if (b >= p.B) return;
-  auto cost = [&](int i) {
-    const BatchLimits L = batch_limits(p, i);
-    int64_t n = L.lsk < (int64_t)p.Sk ? L.lsk : (int64_t)p.Sk;
-    return n > 0 ? n : (int64_t)0;
-  };
-  const int64_t c = cost(b);
-  int rank = 0;
-  for (int i = 0; i < p.B; ++i) {
-    const int64_t ci = cost(i);
-    rank += (ci > c || (ci == c && i < b)) ? 1 : 0;
-  }
-  order[rank] = b;
-}
-
-// Static snake schedule: round r gives CTA c item r*G + c (r even) or
-// r*G + G-1-c (r odd), so heavy and light items alternate between CTAs.
-__device__ __forceinline__ int item_of_round(int r, int n_items) {
-  const int G = gridDim.x;
-  const int c = blockIdx.x;
-  const int idx = r * G + ((r & 1) ? (G - 1 - c) : c);
-  return idx < n_items ? idx : -1;
-}
-
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  if constexpr (BF16) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  } else {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  }
-}
-
-// Maximum / minimum of 128 values as eight independent chains (short
-// dependency depth instead of one 127-long chain).
-__device__ __forceinline__ float max128(const float (&x)[BN]) {
-  float m[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) m[k] = x[k];
-#pragma unroll
-  for (int i = 8; i < BN; i += 8)
-#pragma unroll
-    for (int k = 0; k < 8; ++k) m[k] = fmaxf(m[k], x[i + k]);
-  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
-}
-
-__device__ __forceinline__ float min128(const float (&x)[BN]) {
-  float m[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) m[k] = x[k];
-#pragma unroll
-  for (int i = 8; i < BN; i += 8)
-#pragma unroll
-    for (int k = 0; k < 8; ++k) m[k] = fminf(m[k], x[i + k]);
-  return fminf(fminf(fminf(m[0], m[1]), fminf(m[2], m[3])), fminf(fminf(m[4], m[5]), fminf(m[6], m[7])));
-}
-
-// ------------------------------------------------------------------ producer
-// One thread.  Q tiles per item (after the previous item's QK^T products
-// released them), then the item's K / V tiles into the stage ring; the ring
-// index g runs on across items.
-template <int D, bool KSPLIT>
-__device__ __forceinline__ void producer_role(const TcParams& P, const Smem<D>& sm, int n_items) {
-  using Cfg = TcConfig<D>;
-  constexpr int S = Cfg::kStages;
-  const CommonParams& p = P.c;
-  int g = 0;        // K / V tiles issued so far (ring position)
-  int q_items = 0;  // items whose Q was loaded
-  // batch ranking only in the key-split variant (short query ranges, where
-  // ragged lengths decide the cost); elsewhere the pointer stays out of registers
-  const int* border = (KSPLIT && p.B <= kMaxOrderB) ? sm.order() : nullptr;
-  bool ok = true;
-  for (int r = 0; ok; ++r) {
-    const int idx = item_of_round(r, n_items);
-    if (idx < 0) break;
-    const Item it = make_item<KSPLIT>(p, idx, border);
-    if (it.N == 0) continue;
-    if (q_items > 0 && !mbar_wait(sm.q_empty(), (q_items - 1) & 1, p.timeout_ns, p.status)) break;
-    const int q_plane = it.b * p.Hq + it.h;
-    const int kv_plane = it.b * p.Hkv + it.kvh;
-    mbar_arrive_expect_tx(sm.q_full(), kQTiles * Cfg::kTileBytes);
-    for (int t = 0; t < kQTiles; ++t)
-      for (int s = 0; s < Cfg::kSub; ++s)
-        tma_load_3d(sm.sQ + t * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_q, sm.q_full(), s * 64,
-                    (int)it.row0(t), q_plane);
-    ++q_items;
-    for (int n = 0; n < it.N; ++n, ++g) {
-      const int st = g % S;
-      const int key0 = (it.tb + n) * BN;
-      if (g >= S && !mbar_wait(sm.kv_empty(st), ((g / S) - 1) & 1, p.timeout_ns, p.status)) {
-        ok = false;
-        break;
-      }
-      mbar_arrive_expect_tx(sm.k_full(st), Cfg::kTileBytes);
-      for (int s = 0; s < Cfg::kSub; ++s)
-        tma_load_3d(sm.sK + st * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_k, sm.k_full(st), s * 64,
-                    key0, kv_plane);
-      mbar_arrive_expect_tx(sm.v_full(st), Cfg::kTileBytes);
-      for (int s = 0; s < Cfg::kSub; ++s)
-        tma_load_3d(sm.sV + st * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_v, sm.v_full(st), s * 64,
-                    key0, kv_plane);
-    }
-  }
-  // Let every copy this thread started land before the CTA can exit.
-  for (int n = (g > S ? g - S : 0); n < g; ++n) {
-    mbar_wait(sm.k_full(n % S), (n / S) & 1, p.timeout_ns, p.status);
-    mbar_wait(sm.v_full(n % S), (n / S) & 1, p.timeout_ns, p.status);
-  }
-  if (q_items > 0) mbar_wait(sm.q_full(), (q_items - 1) & 1, p.timeout_ns, p.status);
-}
-
-// S_t = Q_t K^T for one key tile (K tile at kaddr), then commit s_full(t).
-template <int D, bool BF16>
-__device__ __forceinline__ void issue_qk(const Smem<D>& sm, uint32_t tmem, int t, uint32_t kaddr) {
-  using Cfg = TcConfig<D>;
-  constexpr uint32_t idesc_qk = make_idesc_f16kind(BF16, BM, BN, false);
-  const uint32_t qaddr = sm.sQ + t * Cfg::kTileBytes;
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * Cfg::kSubBytes + (kk & 3) * 32;
-    const uint64_t adesc = make_sdesc_sw128(qaddr + off, 16, 1024);
-    const uint64_t bdesc = make_sdesc_sw128(kaddr + off, 16, 1024);
-    mma_ss(tmem + t * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
-  }
-  tc_commit(sm.s_full(t));
-}
-
-// O_t (+)= P_t V for one key tile (V tile at vaddr; P_t in tensor memory over
-// the first half of S_t).
-template <int D, bool BF16>
-__device__ __forceinline__ void issue_pv(const Smem<D>& sm, uint32_t tmem, int t, uint32_t vaddr,
-                                         bool accumulate) {
-  using Cfg = TcConfig<D>;
-  constexpr uint32_t idesc_pv = make_idesc_f16kind(BF16, BM, D, true);
-#pragma unroll
-  for (int kk = 0; kk < BN / 16; ++kk) {
-    // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B apart, 64-column
-    // blocks kSubBytes apart.
-    const uint64_t bdesc = make_sdesc_sw128(vaddr + kk * 2048, Cfg::kSubBytes, 1024);
-    mma_ts(tmem + kColO + t * 128, tmem + t * 128 + kk * 8, bdesc, idesc_pv,
-           (accumulate || kk > 0) ? 1u : 0u);
-  }
-}
-
-// ------------------------------------------------------------------ MMA issuer
-// Whole warp waits; lane 0 issues.  Per item and key tile j (iteration n):
-// the P.V products of tile j-1, then the QK^T products of tile j, per query
-// tile in turn.  Returns after every MMA it issued has completed.
-template <int D, bool BF16, bool KSPLIT>
-__device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, uint32_t tmem,
-                                         int n_items, int lane) {
-  using Cfg = TcConfig<D>;
-  constexpr int S = Cfg::kStages;
-  const CommonParams& p = P.c;
-  int g0 = 0;                 // ring position of the item's first key tile
-  int q_items = 0;            // items whose Q was consumed
-  int pc[kQTiles] = {0, 0};   // P tiles consumed per lane (all items)
-  // batch ranking only in the key-split variant (short query ranges, where
-  // ragged lengths decide the cost); elsewhere the pointer stays out of registers
-  const int* border = (KSPLIT && p.B <= kMaxOrderB) ? sm.order() : nullptr;
-  bool ok = true;
-  for (int r = 0; ok; ++r) {
-    const int idx = item_of_round(r, n_items);
-    if (idx < 0) break;
-    const Item it = make_item<KSPLIT>(p, idx, border);
-    if (it.N == 0) continue;
-    if (!mbar_wait_warp(sm.q_full(), q_items & 1, p.timeout_ns, p.status)) { ok = false; break; }
-    ++q_items;
-    int64_t zero_from = it.L.lsk < (int64_t)p.Sk ? it.L.lsk : (int64_t)p.Sk;
-    if (zero_from < 0) zero_from = 0;
-    bool first_pv[kQTiles] = {true, true};
-    for (int n = 0; ok && n <= it.N; ++n) {
-      const int j = it.tb + n;
-      bool k_ready = false;  // K(j) is waited for only before its first use
-      if (n >= 1) {
-        const int gp = g0 + n - 1;
-        const int ps = gp % S;
-        if (!mbar_wait_warp(sm.v_full(ps), (gp / S) & 1, p.timeout_ns, p.status)) { ok = false; break; }
-        const int64_t key0 = (int64_t)(j - 1) * BN;
-        if (zero_from < key0 + BN && zero_from < (int64_t)p.kv_capacity) {
-          // Cache slots past the valid length may hold NaN / Inf; P is 0
-          // there but 0 * NaN is not, so zero those V rows (whole 128-byte
-          // rows, so the swizzle does not matter).
-          const int r0 = zero_from > key0 ? (int)(zero_from - key0) : 0;
-          const int chunks = (BN - r0) * 8;
-          for (int s = 0; s < Cfg::kSub; ++s) {
-            uint8_t* vblk = sm.base + Cfg::kOffV + ps * Cfg::kTileBytes + s * Cfg::kSubBytes;
-            for (int c = lane; c < chunks; c += 32)
-              *reinterpret_cast<uint4*>(vblk + (size_t)(r0 + (c >> 3)) * 128 + (c & 7) * 16) =
-                  make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-      }
-      tc_fence_after();
-      const bool pv0 = n >= 1 && it.active(0, j - 1), pv1 = n >= 1 && it.active(1, j - 1);
-      const bool s0 = n < it.N && it.active(0, j), s1 = n < it.N && it.active(1, j);
-      const uint32_t kaddr = sm.sK + ((g0 + n) % S) * Cfg::kTileBytes;
-      const uint32_t vaddr = sm.sV + ((g0 + n - 1 + S) % S) * Cfg::kTileBytes;
-      // K(j) is waited for only right before the first S that reads it, so a
-      // late K never holds back the P.V products of tile j-1.
-      auto wait_k = [&]() -> bool {
-        if (k_ready) return true;
-        const int gs = g0 + n;
-        if (!mbar_wait_warp(sm.k_full(gs % S), (gs / S) & 1, p.timeout_ns, p.status)) return false;
-        tc_fence_after();
-        k_ready = true;
-        return true;
-      };
-      // A lane with no P.V pending gets its S first (key-split lanes
-      // alternate), so the tensor core has work while the other lane's
-      // softmax runs.  S_t(j) overwrites the S region that held the lane's
-      // previous P, whose P.V this thread issued earlier.
-      if (!KSPLIT) {
-        // both lanes are query tiles: P.V then S, lane by lane
-        if (pv0) {
-          if (!mbar_wait_warp(sm.p_full(0), pc[0] & 1, p.timeout_ns, p.status)) { ok = false; break; }
-          tc_fence_after();
-          if (lane == 0) {
-            issue_pv<D, BF16>(sm, tmem, 0, vaddr, !first_pv[0]);
-            if (it.last(0, j - 1)) tc_commit(sm.o_final(0));  // lane 0 has seen its last key tile
-          }
-          first_pv[0] = false;
-          ++pc[0];
-        }
-        if (s0) {
-          if (!wait_k()) { ok = false; break; }
-          if (lane == 0) issue_qk<D, BF16>(sm, tmem, 0, kaddr);
-        }
-        __syncwarp();
-        if (pv1) {
-          if (!mbar_wait_warp(sm.p_full(1), pc[1] & 1, p.timeout_ns, p.status)) { ok = false; break; }
-          tc_fence_after();
-          if (lane == 0) {
-            issue_pv<D, BF16>(sm, tmem, 1, vaddr, !first_pv[1]);
-            if (it.last(1, j - 1)) tc_commit(sm.o_final(1));
-          }
-          first_pv[1] = false;
-          ++pc[1];
-        }
-        if (s1) {
-          if (!wait_k()) { ok = false; break; }
-          if (lane == 0) issue_qk<D, BF16>(sm, tmem, 1, kaddr);
-        }
-        __syncwarp();
-      } else {
-      if (s0 && !pv0) {
-        if (!wait_k()) { ok = false; break; }
-        if (lane == 0) issue_qk<D, BF16>(sm, tmem, 0, kaddr);
-      }
-      if (s1 && !pv1) {
-        if (!wait_k()) { ok = false; break; }
-        if (lane == 0) issue_qk<D, BF16>(sm, tmem, 1, kaddr);
-      }
-      if (pv0) {
-        if (!mbar_wait_warp(sm.p_full(0), pc[0] & 1, p.timeout_ns, p.status)) { ok = false; break; }
-        tc_fence_after();
-        if (lane == 0) {
-          issue_pv<D, BF16>(sm, tmem, 0, vaddr, !first_pv[0]);
-          if (it.last(0, j - 1)) tc_commit(sm.o_final(0));  // lane 0 has seen its last key tile
-        }
-        first_pv[0] = false;
-        ++pc[0];
-        if (s0) {
-          if (!wait_k()) { ok = false; break; }
-          if (lane == 0) issue_qk<D, BF16>(sm, tmem, 0, kaddr);
-        }
-      }
-      if (pv1) {
-        if (!mbar_wait_warp(sm.p_full(1), pc[1] & 1, p.timeout_ns, p.status)) { ok = false; break; }
-        tc_fence_after();
-        if (lane == 0) {
-          issue_pv<D, BF16>(sm, tmem, 1, vaddr, !first_pv[1]);
-          if (it.last(1, j - 1)) tc_commit(sm.o_final(1));
-        }
-        first_pv[1] = false;
-        ++pc[1];
-        if (s1) {
-          if (!wait_k()) { ok = false; break; }
-          if (lane == 0) issue_qk<D, BF16>(sm, tmem, 1, kaddr);
-        }
-      }
-      }  // KSPLIT
-      __syncwarp();
-      if (!ok) break;
-      if (lane == 0) {
-        if (n >= 1) tc_commit(sm.kv_empty((g0 + n - 1) % S));
-        // the item's last QK^T products are issued: Q may be replaced once they finish
-        if (n == it.N - 1) tc_commit(sm.q_empty());
-      }
-      __syncwarp();
-    }
-    if (!ok) break;
-    g0 += it.N;
-  }
-  // Wait for every MMA this warp issued before tensor memory is freed.
-  if (lane == 0) tc_commit(sm.drain());
-  __syncwarp();
-  mbar_wait_warp(sm.drain(), 0, p.timeout_ns, p.status);
-}
-
-// Mask block of one warp -- 32 rows (mask rows mwarp, mwarp + Sk, ...) by the
-// 128 keys [key0, key0 + 128) -- into x of the lane that owns each row
-// (natural units; 0 for rows >= nrows and keys >= Sk).  A lane-per-row load
-// would touch 32 cache lines per instruction; instead each instruction loads
-// 4 rows x 128 contiguous bytes, and a 4 KB per-warp buffer (16-byte chunks
-// XOR-swizzled by row, conflict-free both ways) turns rows into lanes.  Needs
-// vec4: mask rows are 16-byte aligned (Sk % 4 == 0) and loads are float4;
-// otherwise each 16-byte chunk is four scalar loads with per-element bounds.
-__device__ __forceinline__ void mask_rows_coalesced(float (&x)[BN], const float* mwarp, int nrows,
-                                                    int Sk, int key0, bool vec4, uint8_t* buf,
-                                                    int lane) {
-  const int rsub = lane >> 3;  // row within a group of 4
-  const int csub = lane & 7;   // 16-byte chunk within a 128-byte row segment
-  // one 32-key chunk in flight per lane (8 float4); the other lane's warps
-  // cover the latency
-  float4 v[8];
-  auto load = [&](int k, float4 (&dst)[8]) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int row = 4 * i + rsub;
-      const int key = key0 + 32 * k + 4 * csub;
-      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float* src = mwarp + (int64_t)row * Sk + key;
-      if (vec4) {
-        if (row < nrows && key + 3 < Sk) t = __ldg(reinterpret_cast<const float4*>(src));
-      } else if (row < nrows) {
-        if (key + 0 < Sk) t.x = __ldg(src + 0);
-        if (key + 1 < Sk) t.y = __ldg(src + 1);
-        if (key + 2 < Sk) t.z = __ldg(src + 2);
-        if (key + 3 < Sk) t.w = __ldg(src + 3);
-      }
-      dst[i] = t;
-    }
-  };
-  load(0, v);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int row = 4 * i + rsub;
-      *reinterpret_cast<float4*>(buf + row * 128 + ((csub ^ (row & 7)) << 4)) = v[i];
-    }
-    if (k + 1 < 4) load(k + 1, v);
-    __syncwarp();
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const float4 t = *reinterpret_cast<const float4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4));
-      x[32 * k + 4 * c + 0] = t.x;
-      x[32 * k + 4 * c + 1] = t.y;
-      x[32 * k + 4 * c + 2] = t.z;
-      x[32 * k + 4 * c + 3] = t.w;
-    }
-    __syncwarp();
-  }
-}
-
-// ------------------------------------------------------------------ softmax
-// Warpgroup t (warps 4t..4t+3); thread = one query row of query tile t.
-template <int D, bool BF16, bool SOFTCAP, bool MASK, bool KSPLIT>
-__device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& sm, uint32_t tmem,
-                                             int n_items, int warp, int lane) {
-  const CommonParams& p = P.c;
-  const int t = warp >> 2;  // query tile of this warpgroup
-  const int wq = warp & 3;  // TMEM lane quarter
-  const int row = wq * 32 + lane;
-  const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-  const uint32_t s_addr = tmem + lane_base + t * 128;
-  const uint32_t o_addr = tmem + lane_base + kColO + t * 128;
-  int sc = 0;                // S tiles this lane consumed (all items)
-  int oc[kQTiles] = {0, 0};  // o_final completions per lane so far (both warpgroups track both)
-  int mc = 0;                // key-split items merged so far
-  // batch ranking only in the key-split variant (short query ranges, where
-  // ragged lengths decide the cost); elsewhere the pointer stays out of registers
-  const int* border = (KSPLIT && p.B <= kMaxOrderB) ? sm.order() : nullptr;
-  bool ok = true;
-  for (int r = 0; ok; ++r) {
-    const int idx = item_of_round(r, n_items);
-    if (idx < 0) break;
-    const Item it = make_item<KSPLIT>(p, idx, border);
-    // selects, not it.tr[t]: a runtime index would put the item in local memory
-    const TileRange T = t == 0 ? it.tr[0] : it.tr[1];
-    const int nt0 = it.tiles(0), nt1 = it.tiles(1);
-    const int nt = t == 0 ? nt0 : nt1;
-    const int64_t qi = (t == 0 ? it.row0(0) : it.row0(1)) + row;
-    const RowLimits R = row_limits(p, it.L, qi);
-    const float* mwarp = nullptr;  // this warp's first mask row
-    int mrows = 0;
-    if constexpr (MASK) {
-      int64_t plane = 0;
-      if (p.mask_planes == p.B) plane = it.b;
-      else if (p.mask_planes == p.B * p.Hq) plane = (int64_t)it.b * p.Hq + it.h;
-      const int64_t qw0 = qi - lane;  // this warp's first row
-      mwarp = p.mask + (plane * p.Sq + (qw0 < p.Sq ? qw0 : 0)) * (int64_t)p.Sk;
-      mrows = qw0 < p.Sq ? (int)min((int64_t)32, (int64_t)p.Sq - qw0) : 0;
-    }
-
-    float m_run = -INFINITY;  // running max, log2 units
-    float l_run = 0.0f;       // running denominator
-    for (int c = 0; c < nt; ++c, ++sc) {
-      const int64_t key0 = (int64_t)(T.t_begin + c * (KSPLIT ? it.stride : 1)) * BN;
-      float x[BN];
-      if constexpr (MASK) {
-        // this tile's mask rows into x (natural units), before the S wait:
-        // the loads overlap the tensor core's work
-        mask_rows_coalesced(x, mwarp, mrows, p.Sk, (int)key0, p.mask_vec4 != 0, sm.mask_buf(warp),
-                            lane);
-      }
-      if (!mbar_wait_warp(sm.s_full(t), sc & 1, p.timeout_ns, p.status)) { ok = false; break; }
-      tc_fence_after();
-
-      const bool need_mask = !(key0 >= T.full_lo && key0 + BN <= T.full_hi);
-      float m_tile;
-      bool scaled = false;  // x already in log2 units (else raw Q.K, scaled inside the exp)
-      if constexpr (MASK) {
-        // x = transform(S) + mask * log2 e, 32 columns at a time
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint32_t sr[32];
-          tmem_ld32(s_addr + k * 32, sr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float sv = __uint_as_float(sr[i]);
-            const float v = SOFTCAP ? soft_cap_log2(sv, p.sc_k1, p.sc_k2, p.sc_k3) : sv * p.scale_log2;
-            x[32 * k + i] = fmaf(x[32 * k + i], kLog2e, v);
-          }
-        }
-        scaled = true;
-      } else {
-        {
-          uint32_t sr[4][32];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) tmem_ld32(s_addr + k * 32, sr[k]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[k * 32 + i] = __uint_as_float(sr[k][i]);
-        }
-        if constexpr (SOFTCAP) {
-          // c tanh(scale s / c), already in log2 units
-#pragma unroll
-          for (int i = 0; i < BN; ++i) x[i] = soft_cap_log2(x[i], p.sc_k1, p.sc_k2, p.sc_k3);
-          scaled = true;
-        }
-      }
-      if (need_mask) {
-        // structural limits of this row: keys outside [lo, hi) become -inf
-        if (!scaled) {
-#pragma unroll
-          for (int i = 0; i < BN; ++i) x[i] *= p.scale_log2;
-          scaled = true;
-        }
-        int lo = R.lo - (int)key0, hi = R.hi - (int)key0;
-        lo = lo < 0 ? 0 : (lo > BN ? BN : lo);
-        hi = hi < 0 ? 0 : (hi > BN ? BN : hi);
-        const int lo_rel = (int)lo;
-        const uint32_t span = hi > lo ? (uint32_t)(hi - lo) : 0u;
-#pragma unroll
-        for (int i = 0; i < BN; ++i) x[i] = ((uint32_t)(i - lo_rel) < span) ? x[i] : -INFINITY;
-      }
-      if (scaled) {
-        m_tile = max128(x);
-      } else {
-        // every key of this tile is visible to every row: the extreme raw
-        // score times the (signed) scale is the max of the scaled scores
-        m_tile = (p.scale_log2 >= 0.0f ? max128(x) : min128(x)) * p.scale_log2;
-      }
-
-      // online update, keeping the old max unless it grew by more than 2^8
-      const float m_new = fmaxf(m_run, m_tile);
-      float alpha = 1.0f;
-      bool rescale = false;
-      float m_use = m_run;
-      if (m_run == -INFINITY) {
-        m_use = m_new;  // first live tile: this row's O is still exactly 0
-      } else if (m_new - m_run > kRescaleLog2) {
-        m_use = m_new;
-        alpha = fast_exp2(m_run - m_new);
-        rescale = true;
-      }
-      const float m_sub = (m_use == -INFINITY) ? 0.0f : m_use;
-      const float xmul = scaled ? 1.0f : p.scale_log2;  // brings x to log2 units
-
-      // P = 2^(x - m) in four 32-column chunks, each packed into 16 columns
-      // of 16-bit pairs over the first half of this S row
-      float sum = 0.0f;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float e0 = fast_exp2(fmaf(x[ch * 32 + 2 * i], xmul, -m_sub));
-          const float e1 = fast_exp2(fmaf(x[ch * 32 + 2 * i + 1], xmul, -m_sub));
-          sum += e0 + e1;
-          pk[i] = pack2<BF16>(e0, e1);
-        }
-        tmem_st16(s_addr + ch * 16, pk);
-      }
-      l_run = l_run * alpha + sum;
-      m_run = m_use;
-
-      if (__any_sync(0xffffffffu, rescale)) {
-        // O_t already holds every earlier P.V of this item (see the header)
-#pragma unroll
-        for (int k = 0; k < D / 32; ++k) {
-          uint32_t o[32];
-          tmem_ld32(o_addr + k * 32, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(o_addr + k * 32, o);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.p_full(t));
-    }
-    if (!ok) break;
-
-    // ---------------------------------------------------------- epilogue
-    float2* merge = sm.merge();
-    float a0 = 1.0f, a1 = 0.0f, inv_l = 0.0f;  // out = (a0 O_t + a1 O_1) * inv_l
-    bool have_o = nt > 0, have_o1 = false;
-    if (KSPLIT && it.split) {
-      // key-split lanes: warpgroup 1 hands its row max / sum to warpgroup 0,
-      // which combines both partial rows
-      if (t == 1) {
-        merge[row] = make_float2(m_run, l_run);
-        mbar_arrive(sm.merge_full());
-        // O_1 must not be overwritten by this lane's next item before warpgroup 0 read it
-        if (!mbar_wait_warp(sm.merge_done(), mc & 1, p.timeout_ns, p.status)) { ok = false; break; }
-        tc_fence_after();
-        ++mc;
-        oc[0] += nt0 > 0;
-        oc[1] += nt1 > 0;
-        continue;
-      }
-      if (nt1 > 0) {
-        if (!mbar_wait_warp(sm.o_final(1), oc[1] & 1, p.timeout_ns, p.status)) { ok = false; break; }
-        have_o1 = true;
-      }
-      if (!mbar_wait_warp(sm.merge_full(), mc & 1, p.timeout_ns, p.status)) { ok = false; break; }
-      const float2 ml1 = merge[row];
-      const float m = fmaxf(m_run, ml1.x);
-      a0 = m_run == -INFINITY ? 0.0f : fast_exp2(m_run - m);
-      a1 = ml1.x == -INFINITY ? 0.0f : fast_exp2(ml1.x - m);
-      const float l = a0 * l_run + a1 * ml1.y;
-      inv_l = l > 0.0f ? 1.0f / l : 0.0f;
-    } else {
-      inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
-    }
-    if (have_o) {
-      if (!mbar_wait_warp(sm.o_final(t), (t == 0 ? oc[0] : oc[1]) & 1, p.timeout_ns, p.status)) { ok = false; break; }
-    }
-    oc[0] += nt0 > 0;
-    oc[1] += nt1 > 0;
-    tc_fence_after();
-    uint16_t* out = reinterpret_cast<uint16_t*>(p.out);
-    int64_t base;
-    if (p.out_layout == 0)
-      base = (((int64_t)it.b * p.Hq + it.h) * p.Sq + qi) * D;
-    else
-      base = (((int64_t)it.b * p.Sq + qi) * p.Hq + it.h) * D;
-    const uint32_t o1_addr = tmem + lane_base + kColO + 128;
-#pragma unroll
-    for (int k = 0; k < D / 32; ++k) {
-      uint32_t o[32];
-      if (have_o) {
-        tmem_ld32(o_addr + k * 32, o);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0u;
-      }
-      if (KSPLIT && have_o1) {  // key-split: fold in lane 1's partial row
-        uint32_t o1[32];
-        tmem_ld32(o1_addr + k * 32, o1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          o[i] = __float_as_uint(a0 * __uint_as_float(o[i]) + a1 * __uint_as_float(o1[i]));
-      }
-      uint32_t w[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-      if (qi < p.Sq) {
-        uint4* dst = reinterpret_cast<uint4*>(out + base + k * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-      }
-    }
-    if (KSPLIT && it.split) {
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(sm.merge_done());  // lane 1 may now start its next item
-      ++mc;
-    }
-    // The next item's first P.V into O_t waits for this warpgroup's next
-    // p_full arrival, which comes after these reads (fence before arrive).
-  }
-}
-
-template <int D, bool BF16, bool SOFTCAP, bool MASK, bool KSPLIT>
-__global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ TcParams P) {
-  using Cfg = TcConfig<D>;
-  constexpr int S = Cfg::kStages;
-  const CommonParams& p = P.c;
-
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  Smem<D> sm;
-  sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(sm.base);
-  sm.sQ = sbase + Cfg::kOffQ;
-  sm.sK = sbase + Cfg::kOffK;
-  sm.sV = sbase + Cfg::kOffV;
-  sm.bar0 = sbase + Cfg::kOffBar;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm.base + Cfg::kOffTmemSlot);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int n_items = ((p.Sq + kQTiles * BM - 1) / (kQTiles * BM)) * p.B * p.Hq;
-
-  if (threadIdx.x == 0) {
-    mbar_init(sm.q_full(), 1);
-    mbar_init(sm.q_empty(), 1);
-    for (int s = 0; s < S; ++s) {
-      mbar_init(sm.k_full(s), 1);
-      mbar_init(sm.v_full(s), 1);
-      mbar_init(sm.kv_empty(s), 1);
-    }
-    for (int t = 0; t < kQTiles; ++t) {
-      mbar_init(sm.s_full(t), 1);
-      mbar_init(sm.p_full(t), 4);  // one arrival per softmax warp of the tile
-      mbar_init(sm.o_final(t), 1);
-    }
-    mbar_init(sm.drain(), 1);
-    mbar_init(sm.merge_full(), BM);
-    mbar_init(sm.merge_done(), BM);
-    mbar_init_fence();
-  }
-  if (KSPLIT && p.B <= kMaxOrderB) rank_batches(p, reinterpret_cast<int*>(sm.base + Cfg::kOffOrder));
-  if (warp == kTmaWarp && lane == 0) {
-    tma_prefetch_desc(&P.tmap_q);
-    tma_prefetch_desc(&P.tmap_k);
-    tma_prefetch_desc(&P.tmap_v);
-  }
-  if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-
-  if (warp == kTmaWarp) {
-    if (lane == 0) producer_role<D, KSPLIT>(P, sm, n_items);
-  } else if (warp == kMmaWarp) {
-    mma_role<D, BF16, KSPLIT>(P, sm, tmem, n_items, lane);
-  } else {
-    softmax_role<D, BF16, SOFTCAP, MASK, KSPLIT>(P, sm, tmem, n_items, warp, lane);
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-template <int D, bool BF16, bool SOFTCAP, bool MASK, bool KSPLIT>
-cudaError_t launch_variant(const TcParams& P, cudaStream_t stream) {
-  auto kernel = attn_fwd_tc_kernel<D, BF16, SOFTCAP, MASK, KSPLIT>;
-  constexpr uint32_t smem = TcConfig<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const int64_t n_items =
-      (int64_t)((P.c.Sq + kQTiles * BM - 1) / (kQTiles * BM)) * P.c.B * P.c.Hq;
-  if (n_items > INT32_MAX) return cudaErrorInvalidConfiguration;
-  const int grid = (int)(n_items < sms ? n_items : sms);  // one persistent CTA per SM
-  kernel<<<grid, kThreads, smem, stream>>>(P);
-  return cudaGetLastError();
-}
-
-template <int D, bool BF16, bool KSPLIT>
-cudaError_t launch_k(const TcParams& P, cudaStream_t stream) {
-  const bool sc = P.c.softcap > 0.0f;
-  const bool mk = P.c.mask != nullptr && P.c.mask_planes > 0;
-  if (sc && mk) return launch_variant<D, BF16, true, true, KSPLIT>(P, stream);
-  if (sc) return launch_variant<D, BF16, true, false, KSPLIT>(P, stream);
-  if (mk) return launch_variant<D, BF16, false, true, KSPLIT>(P, stream);
-  return launch_variant<D, BF16, false, false, KSPLIT>(P, stream);
-}
-
-template <int D, bool BF16>
-cudaError_t launch_d(const TcParams& P, cudaStream_t stream) {
-  // Key-split lanes are compiled in only when some item has an empty second
-  // query tile: the last query pair holds at most 128 rows.
-  const int rem = P.c.Sq - ((P.c.Sq - 1) / (kQTiles * BM)) * (kQTiles * BM);
-  if (rem <= BM) return launch_k<D, BF16, true>(P, stream);
-  return launch_k<D, BF16, false>(P, stream);
-}
-
-}  // namespace
+cudaError_t launch_attn_tc_bf16_d64(const TcParams& P, cudaStream_t stream);
+cudaError_t launch_attn_tc_bf16_d128(const TcParams& P, cudaStream_t stream);
+cudaError_t launch_attn_tc_f16_d64(const TcParams& P, cudaStream_t stream);
+cudaError_t launch_attn_tc_f16_d128(const TcParams& P, cudaStream_t stream);
 
 cudaError_t launch_attn_tc(const TcParams& P, bool bf16, cudaStream_t stream) {
-  if (P.c.D == 64) return bf16 ? launch_d<64, true>(P, stream) : launch_d<64, false>(P, stream);
-  return bf16 ? launch_d<128, true>(P, stream) : launch_d<128, false>(P, stream);
+  if (P.c.D == 64) return bf16 ? launch_attn_tc_bf16_d64(P, stream) : launch_attn_tc_f16_d64(P, stream);
+  return bf16 ? launch_attn_tc_bf16_d128(P, stream) : launch_attn_tc_f16_d128(P, stream);
 }
 
 }  // namespace gb300_attn

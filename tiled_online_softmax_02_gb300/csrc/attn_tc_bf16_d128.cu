@@ -1,0 +1,12 @@
+// attn_tc_bf16_d128.cu -- instantiates the tcgen05 attention kernels for
+// bf16 inputs and head dim 128 (one translation unit per type and head
+// dim, so they compile in parallel).
+#include "attn_tc.cuh"
+
+namespace gb300_attn {
+
+cudaError_t launch_attn_tc_bf16_d128(const TcParams& P, cudaStream_t stream) {
+  return launch_attn_tc_dd<128, true>(P, stream);
+}
+
+}  // namespace gb300_attn
