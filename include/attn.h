@@ -141,6 +141,40 @@ int attn_splitkv_num_splits(int B, int Hq, int Sq, int Sk);
  * num_splits * B * Hq * Sq * (D + 1) * 4. */
 size_t attn_splitkv_workspace_bytes(int B, int Hq, int Sq, int D, int num_splits);
 
+/* Size of the library-owned buffer attn_fwd_splitkv_noalloc uses (8 MiB). */
+#define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * attn_fwd_splitkv_noalloc -- attn_fwd_splitkv for callers that cannot
+ * allocate device memory when they run attention: runtimes and plugin hosts
+ * that plan all device memory ahead of time and forbid allocation during
+ * execution, code where a cudaMalloc would synchronise the device or disturb
+ * other work, or integrations with no allocator available.  The split-KV
+ * scratch lives in a buffer the library owns, ATTN_NOALLOC_SCRATCH_BYTES in
+ * size, present on every GPU the library is loaded on until the process
+ * exits.  This entry point has no counterpart in the source pages; it is a
+ * deployment convenience around the same kernels.
+ *
+ * Arguments and results as attn_fwd_splitkv, without the workspace.  It calls
+ * no cudaMalloc / cudaFree and no allocating library routine.
+ *   - Problems whose partial rows need more than ATTN_NOALLOC_SCRATCH_BYTES
+ *     (attn_splitkv_workspace_bytes for the split count used) are refused
+ *     with ATTN_ERR_INVALID_ARG before anything is launched.
+ *   - The first call on a device looks up the buffer's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call uses the same buffer and leaves its partial rows there.
+ *     Nothing in it has to start at zero: each call writes every value it
+ *     later reads.  Calls that overlap on the GPU (different streams, or
+ *     different host threads) race on the buffer; serialise them.
+ */
+int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, const float *mask,
+                             const int32_t *total_lengths, const int32_t *past_lengths, void *out,
+                             int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D,
+                             int causal, int local_window, float scale, float softcap,
+                             int out_layout, int mask_planes, int dtype, int num_splits,
+                             float *lse, void *stream);
+
 /* Human-readable name of a status code; never NULL. */
 const char *attn_status_string(int status);
 

@@ -33,6 +33,10 @@ SIGNATURES = {
                                 _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                 _i32, _i32, ctypes.c_float, ctypes.c_float, _i32,
                                 _i32, _i32, _i32, _vp, _vp, ctypes.c_size_t, _vp]),
+    "attn_fwd_splitkv_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                        _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                        _i32, _i32, ctypes.c_float, ctypes.c_float, _i32,
+                                        _i32, _i32, _i32, _vp, _vp]),
     "attn_splitkv_num_splits": (_i32, [_i32, _i32, _i32, _i32]),
     "attn_splitkv_workspace_bytes": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, _i32]),
     "attn_status_string": (ctypes.c_char_p, [_i32]),

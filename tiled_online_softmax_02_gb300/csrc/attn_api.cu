@@ -375,3 +375,68 @@ extern "C" int attn_selftest_bounded_wait(uint64_t timeout_ns, void* stream) {
 }
 
 extern "C" int attn_version(void) { return 100; }
+
+// ---------------------------------------------------------------------------
+// Allocation-free split-KV entry point.
+//
+// Some callers cannot allocate device memory at the point where they run
+// attention: inference runtimes and plugin hosts that plan all device memory
+// ahead of time and forbid allocation while executing, code running inside a
+// region where cudaMalloc would synchronise the device or disturb other work,
+// or embedded integrations with no allocator at hand.  For them this entry
+// point keeps the split-KV scratch in a fixed buffer that the library itself
+// owns.  The buffer below lives in every GPU's memory once the library is
+// loaded on it, until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of g_noalloc_scratch on the current device.  Host code may
+// not use the symbol itself as a device pointer, so it is looked up once per
+// device, with that device current, and cached.
+void* noalloc_scratch(int* err) {
+  static std::mutex mu;
+  static void* cache[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 128) {
+    *err = cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice);
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      *err = cuda_fail(e);
+      return nullptr;
+    }
+    cache[dev] = ptr;
+  }
+  return cache[dev];
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v,
+                                        const float* mask, const int32_t* total_lengths,
+                                        const int32_t* past_lengths, void* out, int B, int Hq,
+                                        int Hkv, int Sq, int Sk, int kv_capacity, int D,
+                                        int causal, int local_window, float scale, float softcap,
+                                        int out_layout, int mask_planes, int dtype, int num_splits,
+                                        float* lse, void* stream) {
+  // Problems whose partial rows do not fit the fixed buffer are refused up
+  // front, before anything is launched.
+  if (B > 0 && Hq > 0 && Sq > 0 && Sk > 0 && D > 0 && num_splits >= 0 && num_splits <= kMaxSplits) {
+    const int splits = num_splits == 0 ? auto_splits(B, Hq, Sq, Sk) : num_splits;
+    if (attn_splitkv_workspace_bytes(B, Hq, Sq, D, splits) > (size_t)ATTN_NOALLOC_SCRATCH_BYTES)
+      return ATTN_ERR_INVALID_ARG;
+  }
+  int err = ATTN_OK;
+  void* scratch = noalloc_scratch(&err);
+  if (!scratch) return err;
+  return fwd_impl(q, k, v, mask, total_lengths, past_lengths, out, B, Hq, Hkv, Sq, Sk, kv_capacity,
+                  D, causal, local_window, scale, softcap, out_layout, mask_planes, dtype, stream,
+                  true, num_splits, lse, scratch, (size_t)ATTN_NOALLOC_SCRATCH_BYTES);
+}
