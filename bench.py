@@ -33,7 +33,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from tiled_online_softmax_02_gb300.inputs import WORKLOADS, Workload, make_inputs  # noqa: E402
+from tiled_online_softmax_02_gb300.inputs import (EXTRA_WORKLOADS, WORKLOADS, Workload,  # noqa: E402
+                                                  make_inputs)
+
+ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}
 
 DEFAULT_WORKLOAD = "gqa_causal_bf16"
 L2_FLUSH_BYTES = 256 << 20
@@ -42,10 +45,10 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # ncu capture of the tcgen05 kernel, keyed by workload, with the hash of the
 # kernel sources they were taken on; reported as null once the sources change.
 NCU_TRAFFIC = {
-    "gqa_causal_bf16": {"bytes_per_launch": 128702976, "source_hash": "54537ca6e2fed12d"},
-    "window_softcap_bf16": {"bytes_per_launch": 409761792, "source_hash": "54537ca6e2fed12d"},
-    "ragged_kvcache_f16": {"bytes_per_launch": 48567040, "source_hash": "54537ca6e2fed12d"},
-    "dit_f32": {"bytes_per_launch": 59015936, "source_hash": "54537ca6e2fed12d"},
+    "gqa_causal_bf16": {"bytes_per_launch": 128877056, "source_hash": "331a807deb69b300"},
+    "window_softcap_bf16": {"bytes_per_launch": 402496000, "source_hash": "331a807deb69b300"},
+    "ragged_kvcache_f16": {"bytes_per_launch": 48678656, "source_hash": "331a807deb69b300"},
+    "dit_f32": {"bytes_per_launch": 58580736, "source_hash": "390c7581ed4dd12a"},
 }
 
 
@@ -99,6 +102,36 @@ def flops_of(w: Workload, x: dict) -> tuple[int, int]:
     return flops, excl
 
 
+def algorithmic_bytes(w: Workload, x: dict) -> int:
+    """Bytes a launch must move at least: Q read and O written once, each kv
+    head's visible key and value rows read once, and every mask entry that
+    some visible (row, key) pair uses read once per plane."""
+    es = 4 if w.dtype == "f32" else 2
+    tot = x["total_lengths"].numpy() if x["total_lengths"] is not None else None
+    pst = x["past_lengths"].numpy() if x["past_lengths"] is not None else None
+    qi = np.arange(w.Sq, dtype=np.int64)
+    nbytes = 2 * w.B * w.Hq * w.Sq * w.D * es
+    for b in range(w.B):
+        lsk = int(tot[b]) if tot is not None else w.Sk
+        base = int(pst[b]) if pst is not None else lsk - w.Sq
+        cmax = base + qi
+        lo = np.maximum(0, cmax + 1 - w.local_window) if w.local_window > 0 else np.zeros_like(qi)
+        hi = np.full_like(qi, min(lsk, w.Sk))
+        if w.causal:
+            hi = np.minimum(hi, cmax + 1)
+        hi = np.maximum(hi, lo)
+        if w.Sq:
+            # union of the rows' visible key ranges (each is an interval)
+            keys = int(hi.max()) - int(lo.min()) if hi.max() > lo.min() else 0
+            nbytes += 2 * w.Hkv * keys * w.D * es
+        if x["mask"] is not None:
+            planes = 1 if w.mask_planes == w.B else (w.Hq if w.mask_planes == w.B * w.Hq else 0)
+            nbytes += 4 * int((hi - lo).sum()) * planes
+    if x["mask"] is not None and w.mask_planes == 1:
+        nbytes += 4 * w.Sq * w.Sk
+    return nbytes
+
+
 # ------------------------------------------------------------------- helpers
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -110,14 +143,26 @@ def read_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+# Sources of each kernel family (the kernel, its launcher and the headers it
+# includes): an ncu traffic figure stays valid while these are unchanged.
+KERNEL_SOURCES = {
+    "tc": ("attn_tc.cuh", "attn_tc.cu", "attn_tc_bf16_d64.cu", "attn_tc_bf16_d128.cu",
+           "attn_tc_f16_d64.cu", "attn_tc_f16_d128.cu", "device_common.cuh", "attn_internal.h"),
+    "f32": ("attn_f32.cu", "device_common.cuh", "attn_internal.h"),
+}
+
+
+def kernel_family(w: Workload, splitkv: bool = False) -> str:
+    return "f32" if w.dtype == "f32" else "tc"
+
+
+def kernel_source_hash(family: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tiled_online_softmax_02_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES[family]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -280,7 +325,7 @@ def oracle_sample(w: Workload, x: dict, budget_s: float, seed: int = 3):
 def reference_arm(args, world, rank):
     if rank != 0:
         return 0
-    w = WORKLOADS[args.workload]
+    w = ALL_WORKLOADS[args.workload]
     x = make_inputs(w)
     flops, flops_excl = flops_of(w, x)
     # the whole arm (warm-up included) stays within about --ref-seconds
@@ -318,16 +363,34 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     attn.load_library()
-    w = WORKLOADS[args.workload]
+    w = ALL_WORKLOADS[args.workload]
     x = make_inputs(w)
     flops, flops_excl = flops_of(w, x)
+    abytes = algorithmic_bytes(w, x)
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     out = torch.empty((w.B, w.Hq, w.Sq, w.D) if w.out_layout == 0 else (w.B, w.Sq, w.Hq * w.D),
                       dtype=g["q"].dtype, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    launches_per_step = 1
+    if args.splitkv:
+        lib = attn.load_library()
+        splits = lib.attn_splitkv_num_splits(w.B, w.Hq, w.Hkv, w.Sq, w.Sk)
+        need = lib.attn_splitkv_workspace_bytes(w.B, w.Hq, w.Sq, w.D, splits)
+        ws_buf = torch.empty(max(need // 4, 4), dtype=torch.float32, device=dev)
+        lse_buf = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+        launches_per_step = 2 if splits > 1 else 1
+
     def step():
+        if args.splitkv:
+            attn.attn_fwd_splitkv(g["q"], g["k"], g["v"], mask=g["mask"],
+                                  total_lengths=g["total_lengths"], past_lengths=g["past_lengths"],
+                                  causal=w.causal, local_window=w.local_window,
+                                  scale=w.softmax_scale, softcap=w.softcap,
+                                  out_layout=w.out_layout, seq_k=w.Sk, num_splits=splits,
+                                  out=out, lse=lse_buf, workspace=ws_buf)
+            return
         attn.attn_fwd(g["q"], g["k"], g["v"], mask=g["mask"], total_lengths=g["total_lengths"],
                       past_lengths=g["past_lengths"], causal=w.causal,
                       local_window=w.local_window, scale=w.softmax_scale, softcap=w.softcap,
@@ -398,7 +461,13 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return 0
     peaks, src = read_peaks()
-    if w.dtype == "f32":
+    hbm_gbs = abytes / avg_launch_s / 1e9
+    ridge = float(peaks["bf16_tflops"]) * 1e3 / float(peaks["hbm_gbs"])  # FLOP per byte
+    if w.dtype != "f32" and flops / max(abytes, 1) < ridge:
+        # below the ridge point HBM, not the tensor pipe, bounds the launch
+        peak, bound = float(peaks["hbm_gbs"]), "hbm"
+        src = f"{src} hbm_gbs"
+    elif w.dtype == "f32":
         # fp32 FFMA on CUDA cores: SMs x 128 FMA/clk x 2 FLOP x max SM clock
         props = torch.cuda.get_device_properties(dev)
         mhz = float(peaks.get("sm_max_mhz", 2070.0))
@@ -408,9 +477,10 @@ def run_ours(args, world, rank, local):
         peak, bound = float(peaks["bf16_tflops"]), "tensor"
         src = f"{src} bf16_tflops (burst)"
     achieved = flops / avg_launch_s / 1e12
+    roof = hbm_gbs if bound == "hbm" else achieved
     traffic = None
-    ent = NCU_TRAFFIC.get(w.name)
-    if ent and ent.get("source_hash") == kernel_source_hash():
+    ent = NCU_TRAFFIC.get(w.name + ("+splitkv" if args.splitkv else ""))
+    if ent and ent.get("source_hash") == kernel_source_hash(kernel_family(w, args.splitkv)):
         traffic = ent["bytes_per_launch"]
     cpu = None
     if not args.no_cpu_baseline:
@@ -424,16 +494,20 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": max_s * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded, shaped like the pages' workloads)",
-        "config": workload_config(w, flops, flops_excl, world),
-        "frac_of_peak": achieved / peak,
-        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic, "peak_source": src,
+        "config": dict(workload_config(w, flops, flops_excl, world),
+                       entry="attn_fwd_splitkv" if args.splitkv else "attn_fwd",
+                       **({"num_splits": splits} if args.splitkv else {})),
+        "frac_of_peak": roof / peak,
+        "roofline": {"bound": bound, "achieved": roof, "peak": peak,
+                     "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+                     "frac": roof / peak, "traffic": traffic, "peak_source": src,
+                     "algorithmic_bytes": abytes, "hbm_gbs": hbm_gbs,
                      "frac_of_sustained": (achieved / float(peaks.get("bf16_tflops_sustained", peak))
                                            if bound == "tensor" else None)},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
         "cpu_baseline": cpu,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clock_info,
         "wall_s_timed_region": wall,
     }
@@ -447,7 +521,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", choices=list(ALL_WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--splitkv", action="store_true",
+                    help="time attn_fwd_splitkv with the library's split count")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)

@@ -134,8 +134,10 @@ int attn_fwd_splitkv(const void *q, const void *k, const void *v, const float *m
                      size_t workspace_bytes, void *stream);
 
 /* The split count attn_fwd_splitkv uses for num_splits == 0 on the current
- * device (about two work items per SM, at most one split per 128-key tile). */
-int attn_splitkv_num_splits(int B, int Hq, int Sq, int Sk);
+ * device, at most one split per 128-key tile: with (Hq / Hkv) * Sq <= 32 query
+ * rows per kv head (the decode kernel) about four CTAs per SM over
+ * B * Hkv * splits, otherwise about two query-tile work items per SM. */
+int attn_splitkv_num_splits(int B, int Hq, int Hkv, int Sq, int Sk);
 
 /* Workspace bytes attn_fwd_splitkv needs for a split count (0 when <= 1):
  * num_splits * B * Hq * Sq * (D + 1) * 4. */

@@ -37,7 +37,7 @@ SIGNATURES = {
                                         _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                         _i32, _i32, ctypes.c_float, ctypes.c_float, _i32,
                                         _i32, _i32, _i32, _vp, _vp]),
-    "attn_splitkv_num_splits": (_i32, [_i32, _i32, _i32, _i32]),
+    "attn_splitkv_num_splits": (_i32, [_i32, _i32, _i32, _i32, _i32]),
     "attn_splitkv_workspace_bytes": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, _i32]),
     "attn_status_string": (ctypes.c_char_p, [_i32]),
     "attn_last_cuda_error": (_i32, []),
@@ -195,7 +195,7 @@ def attn_fwd_splitkv(q, k, v, *, mask=None, total_lengths=None, past_lengths=Non
             mask = mask.reshape(-1, mask.shape[-2], mask.shape[-1])
         mask_planes = mask.shape[0]
     with torch.cuda.device(q.device):
-        splits = int(num_splits) or lib.attn_splitkv_num_splits(B, Hq, Sq, max(Sk, 1))
+        splits = int(num_splits) or lib.attn_splitkv_num_splits(B, Hq, Hkv, Sq, max(Sk, 1))
         need = lib.attn_splitkv_workspace_bytes(B, Hq, Sq, D, splits)
         if workspace is None and need > 0:
             workspace = torch.empty(need // 4, dtype=torch.float32, device=q.device)

@@ -20,6 +20,7 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/attn.h"
+#include "attn_decode.h"
 #include "attn_internal.h"
 #include "device_common.cuh"
 
@@ -144,14 +145,23 @@ int tile_count(int Sk) { return (Sk + kTcBlockN - 1) / kTcBlockN; }
 
 int64_t splitkv_rows(int B, int Hq, int Sq) { return (int64_t)B * Hq * Sq; }
 
-// Split count chosen when the caller passes 0: enough work items for about
-// two per SM, never more splits than key tiles.
-int auto_splits(int B, int Hq, int Sq, int Sk) {
+// Few query rows per kv head go to the decode kernel (16-bit types).
+bool decode_shape(int Hq, int Hkv, int Sq) {
+  return Hkv > 0 && Hq % Hkv == 0 && (int64_t)(Hq / Hkv) * Sq <= kDecodeMaxRows;
+}
+
+// Split count chosen when the caller passes 0, never more splits than key
+// tiles.  Decode kernel: CTAs = B * Hkv * splits, about two waves of two CTAs
+// per SM.  Tensor-core kernel: about two work items per SM.
+int auto_splits(int B, int Hq, int Hkv, int Sq, int Sk) {
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t items = (int64_t)((Sq + 2 * kTcBlockM - 1) / (2 * kTcBlockM)) * B * Hq;
+  const int64_t items = decode_shape(Hq, Hkv, Sq)
+                            ? (int64_t)B * Hkv
+                            : (int64_t)((Sq + 2 * kTcBlockM - 1) / (2 * kTcBlockM)) * B * Hq;
   if (items <= 0) return 1;
-  int64_t s = (2 * (int64_t)sms + items - 1) / items;
+  const int64_t target = decode_shape(Hq, Hkv, Sq) ? 4 * (int64_t)sms : 2 * (int64_t)sms;
+  int64_t s = (target + items - 1) / items;
   const int tiles = tile_count(Sk);
   if (s > tiles) s = tiles;
   if (s > kMaxSplits) s = kMaxSplits;
@@ -220,7 +230,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
   }
   int splits = 1;
   if (splitkv_api) {
-    splits = num_splits == 0 ? auto_splits(B, Hq, Sq, Sk) : num_splits;
+    splits = num_splits == 0 ? auto_splits(B, Hq, Hkv, Sq, Sk) : num_splits;
     if (splits > 1) {
       const size_t need = (size_t)splits * (size_t)splitkv_rows(B, Hq, Sq) * (size_t)(D + 1) * 4;
       if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
@@ -274,6 +284,15 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
     fp.v = static_cast<const float*>(v);
     fp.c = c;
     e = launch_attn_f32(fp, st);
+  } else if (decode_shape(Hq, Hkv, Sq)) {
+    const bool bf16 = dtype == ATTN_BF16;
+    DecodeParams dp{};
+    dp.q = q;
+    dp.c = c;
+    int rc = encode_map(&dp.tmap_k, k, bf16, (int64_t)B * Hkv, kv_capacity, D);
+    if (rc == ATTN_OK) rc = encode_map(&dp.tmap_v, v, bf16, (int64_t)B * Hkv, kv_capacity, D);
+    if (rc != ATTN_OK) return rc;
+    e = launch_attn_decode(dp, bf16, st);
   } else {
     const bool bf16 = dtype == ATTN_BF16;
     TcParams tp{};
@@ -283,6 +302,9 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
     if (rc == ATTN_OK) rc = encode_map(&tp.tmap_v, v, bf16, (int64_t)B * Hkv, kv_capacity, D);
     if (rc != ATTN_OK) return rc;
     e = launch_attn_tc(tp, bf16, st);
+  }
+  if (dtype != ATTN_F32) {
+    const bool bf16 = dtype == ATTN_BF16;
     if (e == cudaSuccess && splits > 1) {
       MergeParams mp{};
       mp.ws_o = c.ws_o;
@@ -322,9 +344,9 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, con
                   true, num_splits, lse, workspace, workspace_bytes);
 }
 
-extern "C" int attn_splitkv_num_splits(int B, int Hq, int Sq, int Sk) {
-  if (B <= 0 || Hq <= 0 || Sq <= 0 || Sk <= 0) return 1;
-  return auto_splits(B, Hq, Sq, Sk);
+extern "C" int attn_splitkv_num_splits(int B, int Hq, int Hkv, int Sq, int Sk) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0) return 1;
+  return auto_splits(B, Hq, Hkv, Sq, Sk);
 }
 
 extern "C" size_t attn_splitkv_workspace_bytes(int B, int Hq, int Sq, int D, int num_splits) {
@@ -428,8 +450,9 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
                                         float* lse, void* stream) {
   // Problems whose partial rows do not fit the fixed buffer are refused up
   // front, before anything is launched.
-  if (B > 0 && Hq > 0 && Sq > 0 && Sk > 0 && D > 0 && num_splits >= 0 && num_splits <= kMaxSplits) {
-    const int splits = num_splits == 0 ? auto_splits(B, Hq, Sq, Sk) : num_splits;
+  if (B > 0 && Hq > 0 && Hkv > 0 && Sq > 0 && Sk > 0 && D > 0 && num_splits >= 0 &&
+      num_splits <= kMaxSplits) {
+    const int splits = num_splits == 0 ? auto_splits(B, Hq, Hkv, Sq, Sk) : num_splits;
     if (attn_splitkv_workspace_bytes(B, Hq, Sq, D, splits) > (size_t)ATTN_NOALLOC_SCRATCH_BYTES)
       return ATTN_ERR_INVALID_ARG;
   }

@@ -95,6 +95,14 @@ _add(4, Workload("ragged_kvcache_f16", B=8, Hq=32, Hkv=4, Sq=128, Sk=4096, kv_ca
 
 WORKLOAD_ORDER = list(WORKLOADS)
 
+# Shapes beyond the five: decode (one new token per sequence over a long
+# ragged cache), the case split-KV serves.
+EXTRA_WORKLOADS: dict[str, Workload] = {
+    "decode_bf16": Workload("decode_bf16", B=8, Hq=32, Hkv=8, Sq=1, Sk=32768, kv_capacity=32768,
+                            D=128, dtype="bf16", causal=True, ragged=True, garbage="finite",
+                            seed=SEED_BASE + 10),
+}
+
 
 def _round(x: np.ndarray, dtype: str) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(TORCH_DTYPES[dtype])
