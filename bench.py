@@ -41,14 +41,17 @@ ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}
 DEFAULT_WORKLOAD = "gqa_causal_bf16"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# ncu capture of the tcgen05 kernel, keyed by workload, with the hash of the
-# kernel sources they were taken on; reported as null once the sources change.
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# dominant kernel from one ncu capture, keyed by workload (+splitkv: the
+# attn_fwd_splitkv entry), with the hash of that kernel's sources at the time;
+# reported as null once those sources change.
 NCU_TRAFFIC = {
     "gqa_causal_bf16": {"bytes_per_launch": 128877056, "source_hash": "331a807deb69b300"},
     "window_softcap_bf16": {"bytes_per_launch": 402496000, "source_hash": "331a807deb69b300"},
     "ragged_kvcache_f16": {"bytes_per_launch": 48678656, "source_hash": "331a807deb69b300"},
     "dit_f32": {"bytes_per_launch": 58580736, "source_hash": "390c7581ed4dd12a"},
+    "decode_bf16": {"bytes_per_launch": 771968256, "source_hash": "3819eeef5b6fb131"},
+    "decode_bf16+splitkv": {"bytes_per_launch": 772924416, "source_hash": "3819eeef5b6fb131"},
 }
 
 
@@ -149,11 +152,14 @@ KERNEL_SOURCES = {
     "tc": ("attn_tc.cuh", "attn_tc.cu", "attn_tc_bf16_d64.cu", "attn_tc_bf16_d128.cu",
            "attn_tc_f16_d64.cu", "attn_tc_f16_d128.cu", "device_common.cuh", "attn_internal.h"),
     "f32": ("attn_f32.cu", "device_common.cuh", "attn_internal.h"),
+    "decode": ("attn_decode.cu", "attn_decode.h", "device_common.cuh", "attn_internal.h"),
 }
 
 
 def kernel_family(w: Workload, splitkv: bool = False) -> str:
-    return "f32" if w.dtype == "f32" else "tc"
+    if w.dtype == "f32":
+        return "f32"
+    return "decode" if w.group * w.Sq <= 32 else "tc"
 
 
 def kernel_source_hash(family: str) -> str:
@@ -272,7 +278,8 @@ def workload_config(w: Workload, flops: int, flops_excl: int, n: int) -> dict:
            "local_window": w.local_window, "softcap": w.softcap, "mask_planes": w.mask_planes,
            "ragged": w.ragged, "out_layout": ["head_major", "token_major"][w.out_layout],
            "seed": w.seed, "flops_per_step": flops, "parallelism": f"replicas x{n}",
-           "l2": "flushed between timed steps (256 MiB write outside the timed events)"}
+           "l2": "flushed between timed steps outside the timed events: a 256 MiB write, then a "
+                 "256 MiB read so no dirty line is left to be written back inside the next step"}
     if flops_excl != flops:
         cfg["flops_per_step_excluding_neg_inf_mask"] = flops_excl
     return cfg
@@ -371,12 +378,20 @@ def run_ours(args, world, rank, local):
     out = torch.empty((w.B, w.Hq, w.Sq, w.D) if w.out_layout == 0 else (w.B, w.Sq, w.Hq * w.D),
                       dtype=g["q"].dtype, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def evict_l2():
+        # A write larger than L2 evicts it, but leaves it full of dirty lines
+        # whose write-back would land inside the next timed launch; reading
+        # another buffer larger than L2 writes them back here instead.
+        flush.zero_()
+        flush_rd.max()
     stream = torch.cuda.current_stream(dev)
 
     launches_per_step = 1
     if args.splitkv:
         lib = attn.load_library()
-        splits = lib.attn_splitkv_num_splits(w.B, w.Hq, w.Hkv, w.Sq, w.Sk)
+        splits = args.splits or lib.attn_splitkv_num_splits(w.B, w.Hq, w.Hkv, w.Sq, w.Sk)
         need = lib.attn_splitkv_workspace_bytes(w.B, w.Hq, w.Sq, w.D, splits)
         ws_buf = torch.empty(max(need // 4, 4), dtype=torch.float32, device=dev)
         lse_buf = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
@@ -397,7 +412,7 @@ def run_ours(args, world, rank, local):
                       out_layout=w.out_layout, seq_k=w.Sk, out=out)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        evict_l2()
         step()
     torch.cuda.synchronize()
     if attn.get_device_status() != attn.ATTN_OK:
@@ -415,7 +430,7 @@ def run_ours(args, world, rank, local):
         clocks.mark(True)
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.zero_()                 # evict L2 outside the timed events
+        evict_l2()                    # outside the timed events
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -523,7 +538,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(ALL_WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--splitkv", action="store_true",
-                    help="time attn_fwd_splitkv with the library's split count")
+                    help="time attn_fwd_splitkv (split count: --splits, else the library's choice)")
+    ap.add_argument("--splits", type=int, default=0, help="split count for --splitkv (0: library)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)

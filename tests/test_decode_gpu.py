@@ -57,7 +57,7 @@ def test_row_counts_attn_fwd(shape, dtype, D):
     check(w, run_gpu(w, x).double().cpu().numpy(), run_oracle(w, x), f"{shape} {dtype} D={D}")
 
 
-@pytest.mark.parametrize("splits", [2, 5, 0])
+@pytest.mark.parametrize("splits", [1, 2, 5, 0])
 @pytest.mark.parametrize("shape", ["rows2", "rows16_sq4", "rows17", "rows32_sq2"])
 def test_row_counts_splitkv(shape, splits):
     Hq, Hkv, Sq = ROW_SHAPES[shape]

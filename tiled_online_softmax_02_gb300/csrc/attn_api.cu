@@ -150,6 +150,19 @@ bool decode_shape(int Hq, int Hkv, int Sq) {
   return Hkv > 0 && Hq % Hkv == 0 && (int64_t)(Hq / Hkv) * Sq <= kDecodeMaxRows;
 }
 
+// Thread-block cluster size of the decode kernel when the key tiles are not
+// split across launches: enough CTAs for about two waves of two per SM, at
+// most 8 (the portable cluster size) and at most one CTA per key tile.
+int decode_cluster(int B, int Hkv, int Sk) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t units = (int64_t)B * Hkv;
+  int64_t cl = (4 * (int64_t)sms + units - 1) / units;
+  if (cl > tile_count(Sk)) cl = tile_count(Sk);
+  if (cl > 8) cl = 8;
+  return cl < 1 ? 1 : (int)cl;
+}
+
 // Split count chosen when the caller passes 0, never more splits than key
 // tiles.  Decode kernel: CTAs = B * Hkv * splits, about two waves of two CTAs
 // per SM.  Tensor-core kernel: about two work items per SM.
@@ -289,6 +302,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
     DecodeParams dp{};
     dp.q = q;
     dp.c = c;
+    dp.cluster = splits == 1 ? decode_cluster(B, Hkv, Sk) : 1;
     int rc = encode_map(&dp.tmap_k, k, bf16, (int64_t)B * Hkv, kv_capacity, D);
     if (rc == ATTN_OK) rc = encode_map(&dp.tmap_v, v, bf16, (int64_t)B * Hkv, kv_capacity, D);
     if (rc != ATTN_OK) return rc;

@@ -21,8 +21,11 @@
 // shared-memory exchange through a bounded mbarrier).
 //
 // Roles (224 threads): warps 0-3 softmax, warp 4 K loads (TMA), warp 5 V loads
-// (TMA), warp 6 MMA issue.  With num_splits > 1 the CTA writes its rows'
-// partial O / l and log-sum-exp for the merge kernel; otherwise the output.
+// (TMA), warp 6 MMA issue.  A kv head's key tiles can be cut into parts in two
+// ways, combinable: a thread-block cluster of up to 8 CTAs whose partial rows
+// are merged through distributed shared memory by the cluster's first CTA,
+// and num_splits key ranges whose partial O / l and log-sum-exp go to a
+// workspace for the merge kernel.  With neither, the CTA writes the output.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -39,13 +42,25 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only past a 256x growth
 
+// Stage counts of the K and V rings for D = 128 (D = 64 uses 3 and 2) and the
+// CTAs per SM the 16-row variant is compiled for.
+#ifndef GB300_DEC_K_STAGES
+#define GB300_DEC_K_STAGES 2
+#endif
+#ifndef GB300_DEC_V_STAGES
+#define GB300_DEC_V_STAGES 1
+#endif
+#ifndef GB300_DEC_MIN_BLOCKS
+#define GB300_DEC_MIN_BLOCKS 2
+#endif
+
 template <int D, int NR>
 struct DecConfig {
   static constexpr int kSub = D / 64;                  // 64-column (128-byte) blocks per row
   static constexpr int kSubBytes = kDecKeys * 128;      // one 64-column block of a K / V tile
   static constexpr int kTileBytes = kSub * kSubBytes;   // one K or V tile
-  static constexpr int kSK = D == 128 ? 2 : 3;          // K stages
-  static constexpr int kSV = D == 128 ? 1 : 2;          // V stages
+  static constexpr int kSK = D == 128 ? GB300_DEC_K_STAGES : 3;  // K stages
+  static constexpr int kSV = D == 128 ? GB300_DEC_V_STAGES : 2;  // V stages
   static constexpr int kRowBlock = NR * 128;            // one 64-column block of Q or P^T
   static constexpr int kQBytes = kSub * kRowBlock;
   static constexpr int kPBytes = 2 * kRowBlock;         // 128 keys = two 64-key blocks
@@ -65,6 +80,7 @@ struct DecConfig {
   static constexpr uint32_t kTmemCols = 3 * NR <= 64 ? 64u : 128u;
   static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kRowBlock % 1024 == 0, "SW128 alignment");
   static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert((NR * D + NR) * 4 <= kSK * kTileBytes, "cluster exchange fits in the K ring");
 };
 
 template <int D, int NR>
@@ -91,20 +107,27 @@ struct DecLayout {
   __device__ uint32_t pv_done(int i) const { return s + C::kOffBar + (2 * C::kSK + 2 * C::kSV + 4 + i) * 8; }
   __device__ uint32_t red_bar() const { return s + C::kOffBar + (2 * C::kSK + 2 * C::kSV + 6) * 8; }
   __device__ uint32_t* slot() const { return reinterpret_cast<uint32_t*>(base + C::kOffSlot); }
+  // cluster exchange, over the K ring once every S^T product is done:
+  // normalised partial rows [NR][D] and their log-sum-exps (log2 units) [NR]
+  __device__ float* xo() const { return reinterpret_cast<float*>(base + C::kOffK); }
+  __device__ float* xl() const { return xo() + NR * D; }
 };
 
 // The (batch, kv head, part) of a CTA and its key tiles.
 struct DecUnit {
-  int b, kvh, part;
+  int b, kvh;
+  int part;        // key range (split) index; its partial row goes to the workspace
+  int rank;        // CTA index within the cluster
   int R;           // query rows of this kv head: group * Sq
   int64_t row0;    // first row (b * Hq + kvh * group) * Sq in [B*Hq*Sq]
   int t0, n;       // key tiles [t0, t0 + n)
   int64_t zero_from;  // V rows at or past this key hold no valid data
 };
 
-__device__ __forceinline__ DecUnit dec_unit(const CommonParams& p) {
+__device__ __forceinline__ DecUnit dec_unit(const CommonParams& p, int P_cluster) {
   DecUnit u;
-  u.part = blockIdx.x;
+  u.part = blockIdx.x / P_cluster;
+  u.rank = blockIdx.x % P_cluster;
   u.kvh = blockIdx.y;
   u.b = blockIdx.z;
   u.R = p.group * p.Sq;
@@ -118,8 +141,9 @@ __device__ __forceinline__ DecUnit dec_unit(const CommonParams& p) {
     te = (last.hi + kDecKeys - 1) / kDecKeys;
   }
   const int total = te - tb;
-  const int per = (total + p.num_splits - 1) / p.num_splits;
-  int a = tb + u.part * per, e = a + per;
+  const int parts = p.num_splits * P_cluster;  // = gridDim.x
+  const int per = (total + parts - 1) / parts;
+  int a = tb + (int)blockIdx.x * per, e = a + per;
   if (a > te) a = te;
   if (e > te) e = te;
   u.t0 = a;
@@ -308,6 +332,46 @@ __device__ __forceinline__ uint16_t dec_to_bits(float x) {
   else return __half_as_ushort(__float2half_rn(x));
 }
 
+// Row r of the unit, column d = tid: the normalised value and the row's
+// log-sum-exp in log2 units, to the workspace (split) or the output.
+template <int D, bool BF16>
+__device__ __forceinline__ void dec_store_row(const CommonParams& p, const DecUnit& u, int r, int tid,
+                                              float val, float lse2) {
+  const int64_t rows = (int64_t)p.B * p.Hq * p.Sq;
+  const int64_t row = u.row0 + r;
+  const float lse = lse2 * kLn2;  // -inf stays -inf
+  if (p.num_splits > 1) {
+    if (tid < D) p.ws_o[((int64_t)u.part * rows + row) * D + tid] = val;
+    if (tid == r) p.ws_lse[(int64_t)u.part * rows + row] = lse;
+    return;
+  }
+  if (tid < D) {
+    int64_t idx = row * D + tid;
+    if (p.out_layout != 0) {
+      const int qi = r % p.Sq, h = u.kvh * p.group + r / p.Sq;
+      idx = (((int64_t)u.b * p.Sq + qi) * p.Hq + h) * D + tid;
+    }
+    reinterpret_cast<uint16_t*>(p.out)[idx] = dec_to_bits<BF16>(val);
+  }
+  if (p.lse != nullptr && tid == r) p.lse[row] = lse;
+}
+
+// Distributed shared memory: a 32-bit load from CTA `rank` of the cluster at
+// the offset of this CTA's shared address `saddr`.
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t saddr, int rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// Every thread of every CTA of the cluster arrives; release / acquire order
+// shared-memory writes before the other CTAs' reads.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ softmax
 // Thread tid of warps 0-3 owns key tid of every tile (TMEM lane tid of S^T)
 // and, in the epilogue, column d = tid of O^T.  Scores are kept in log2
@@ -315,7 +379,8 @@ __device__ __forceinline__ uint16_t dec_to_bits(float x) {
 // only when a tile raises it by more than kRescaleThreshold.
 template <int D, int NR, bool BF16>
 __device__ __forceinline__ void dec_softmax(const CommonParams& p, const DecLayout<D, NR>& sm,
-                                            const DecUnit& u, uint32_t tmem, int warp, int lane) {
+                                            const DecUnit& u, uint32_t tmem, int cluster, int warp,
+                                            int lane) {
   using C = DecConfig<D, NR>;
   const int tid = warp * 32 + lane;
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
@@ -434,35 +499,51 @@ __device__ __forceinline__ void dec_softmax(const CommonParams& p, const DecLayo
 #pragma unroll
     for (int r = 0; r < NR; ++r) o[r] = 0.0f;
   }
-  const int64_t rows = (int64_t)p.B * p.Hq * p.Sq;
-  const bool split = p.num_splits > 1;
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
     if (r >= u.R) break;
     const float Lr = red[r] + red[NR + r] + red[2 * NR + r] + red[3 * NR + r];
     const float inv = Lr > 0.0f ? 1.0f / Lr : 0.0f;
-    const float lse = Lr > 0.0f ? (m[r] + log2f(Lr)) * kLn2 : -INFINITY;
-    const int64_t row = u.row0 + r;
-    if (split) {
-      if (tid < D) p.ws_o[((int64_t)u.part * rows + row) * D + tid] = o[r] * inv;
-      if (tid == r) p.ws_lse[(int64_t)u.part * rows + row] = lse;
+    const float lse2 = Lr > 0.0f ? m[r] + log2f(Lr) : -INFINITY;
+    if (cluster > 1) {  // to shared memory, for the cluster's first CTA to merge
+      if (tid < D) sm.xo()[r * D + tid] = o[r] * inv;
+      if (tid == r) sm.xl()[r] = lse2;
     } else {
-      if (tid < D) {
-        int64_t idx = row * D + tid;
-        if (p.out_layout != 0) {
-          const int qi = r % p.Sq, h = u.kvh * p.group + r / p.Sq;
-          idx = (((int64_t)u.b * p.Sq + qi) * p.Hq + h) * D + tid;
-        }
-        reinterpret_cast<uint16_t*>(p.out)[idx] = dec_to_bits<BF16>(o[r] * inv);
-      }
-      if (p.lse != nullptr && tid == r) p.lse[row] = lse;
+      dec_store_row<D, BF16>(p, u, r, tid, o[r] * inv, lse2);
     }
+  }
+}
+
+// Cluster merge, by the softmax threads of the cluster's first CTA: row r of
+// the CTAs' parts combines as O = sum_k w_k O_k / sum_k w_k with
+// w_k = 2^(lse_k - max lse), read from each CTA's shared memory.
+template <int D, int NR, bool BF16>
+__device__ __forceinline__ void dec_cluster_merge(const CommonParams& p, const DecLayout<D, NR>& sm,
+                                                  const DecUnit& u, int cluster, int tid) {
+  const uint32_t xo = smem_u32(sm.xo()), xl = smem_u32(sm.xl());
+  for (int r = 0; r < u.R; ++r) {
+    float lk[8];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      lk[k] = k < cluster ? ld_dsmem_f32(xl + r * 4, k) : -INFINITY;
+      mx = fmaxf(mx, lk[k]);
+    }
+    float wsum = 0.0f, acc = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float w = lk[k] == -INFINITY ? 0.0f : exp2f(lk[k] - mx);
+      wsum += w;
+      if (w > 0.0f && tid < D) acc = fmaf(w, ld_dsmem_f32(xo + (uint32_t)(r * D + tid) * 4, k), acc);
+    }
+    dec_store_row<D, BF16>(p, u, r, tid, wsum > 0.0f ? acc / wsum : 0.0f,
+                           wsum > 0.0f ? mx + log2f(wsum) : -INFINITY);
   }
 }
 
 // -------------------------------------------------------------------- kernel
 template <int D, int NR, bool BF16>
-__global__ void __launch_bounds__(kDecThreads, NR == 16 ? 2 : 1) attn_decode_kernel(const __grid_constant__ DecodeParams P) {
+__global__ void __launch_bounds__(kDecThreads, NR == 16 ? GB300_DEC_MIN_BLOCKS : 1) attn_decode_kernel(const __grid_constant__ DecodeParams P) {
   using C = DecConfig<D, NR>;
   const CommonParams& p = P.c;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -470,7 +551,7 @@ __global__ void __launch_bounds__(kDecThreads, NR == 16 ? 2 : 1) attn_decode_ker
   sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   sm.s = smem_u32(sm.base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const DecUnit u = dec_unit(p);
+  const DecUnit u = dec_unit(p, P.cluster);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kSK; ++i) {
@@ -531,13 +612,18 @@ __global__ void __launch_bounds__(kDecThreads, NR == 16 ? 2 : 1) attn_decode_ker
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm.slot());
 
   if (warp < 4) {
-    dec_softmax<D, NR, BF16>(p, sm, u, tmem, warp, lane);
+    dec_softmax<D, NR, BF16>(p, sm, u, tmem, P.cluster, warp, lane);
   } else if (warp == kKWarp) {
     if (lane == 0) dec_loader<D, NR, C::kSK>(p, &P.tmap_k, u, sm.k_tile(0), sm.k_full(0), sm.k_empty(0));
   } else if (warp == kVWarp) {
     if (lane == 0) dec_loader<D, NR, C::kSV>(p, &P.tmap_v, u, sm.v_tile(0), sm.v_full(0), sm.v_empty(0));
   } else {
     dec_mma<D, NR, BF16>(p, sm, u, tmem, lane);
+  }
+  if (P.cluster > 1) {
+    cluster_sync_all();  // every CTA's partial rows are in its shared memory
+    if (u.rank == 0 && warp < 4) dec_cluster_merge<D, NR, BF16>(p, sm, u, P.cluster, threadIdx.x);
+    cluster_sync_all();  // ... and have been read: no CTA's shared memory goes away earlier
   }
 
   tc_fence_before();
@@ -557,9 +643,24 @@ cudaError_t launch_dec(const DecodeParams& P, cudaStream_t stream) {
   // the whole carve-out as shared memory, so two CTAs fit on an SM where the size allows
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)P.c.num_splits, (unsigned)P.c.Hkv, (unsigned)P.c.B);
-  kernel<<<grid, kDecThreads, smem, stream>>>(P);
-  return cudaGetLastError();
+  const dim3 grid((unsigned)(P.c.num_splits * P.cluster), (unsigned)P.c.Hkv, (unsigned)P.c.B);
+  if (P.cluster <= 1) {
+    kernel<<<grid, kDecThreads, smem, stream>>>(P);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kDecThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)P.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, P);
 }
 
 template <int D, bool BF16>
@@ -571,7 +672,8 @@ cudaError_t launch_dec_d(const DecodeParams& P, cudaStream_t stream) {
 
 cudaError_t launch_attn_decode(const DecodeParams& P, bool bf16, cudaStream_t stream) {
   const int64_t rows = (int64_t)P.c.group * P.c.Sq;
-  if (rows < 1 || rows > kDecodeMaxRows || P.c.num_splits < 1 || (P.c.D != 64 && P.c.D != 128))
+  if (rows < 1 || rows > kDecodeMaxRows || P.c.num_splits < 1 || P.cluster < 1 || P.cluster > 8 ||
+      (P.c.D != 64 && P.c.D != 128))
     return cudaErrorInvalidValue;
   if (P.c.D == 128) return bf16 ? launch_dec_d<128, true>(P, stream) : launch_dec_d<128, false>(P, stream);
   return bf16 ? launch_dec_d<64, true>(P, stream) : launch_dec_d<64, false>(P, stream);

@@ -17,7 +17,10 @@ struct DecodeParams {
   CUtensorMap tmap_k;  // dims {D, kv_capacity, B*Hkv}, box {64, 128, 1}, 128B swizzle
   CUtensorMap tmap_v;  // same as tmap_k
   const void* q;       // [B, Hq, Sq, D]
-  CommonParams c;      // c.num_splits parts per kv head; > 1 writes partial rows to c.ws_o / c.ws_lse
+  int cluster;         // CTAs per thread-block cluster (1..8): each takes a part of the key
+                       // tiles, and the cluster merges its partial rows in shared memory
+  CommonParams c;      // c.num_splits key ranges per kv head (each one cluster); > 1 writes
+                       // partial rows to c.ws_o / c.ws_lse for the merge kernel
 };
 
 cudaError_t launch_attn_decode(const DecodeParams& p, bool bf16, cudaStream_t stream);
