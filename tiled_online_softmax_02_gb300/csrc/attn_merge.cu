@@ -15,29 +15,32 @@
 namespace gb300_attn {
 namespace {
 
-// One thread per (row, 4 output columns).
+// One thread per (row, 2 output columns); the per-split loads are issued
+// unconditionally (a range without keys holds -inf and weight 0, and its
+// partial row is never multiplied in), so they overlap instead of forming a
+// chain of dependent branches.
 __global__ void attn_merge_kernel(const MergeParams p) {
-  const int64_t groups = p.D / 4;
+  const int64_t groups = p.D / 2;
   const int64_t rows = (int64_t)p.B * p.Hq * p.Sq;
   const int64_t plane = rows * p.D;  // floats per split in ws_o
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < rows * groups;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int64_t row = idx / groups;  // (b * Hq + h) * Sq + qi
-    const int c = (int)(idx - row * groups) * 4;
+    const int c = (int)(idx - row * groups) * 2;
     float m = -INFINITY;
+#pragma unroll 8
     for (int s = 0; s < p.num_splits; ++s) m = fmaxf(m, __ldg(p.ws_lse + s * rows + row));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float2 acc = make_float2(0.f, 0.f);
     float wsum = 0.f;
     if (m != -INFINITY) {
+#pragma unroll 8
       for (int s = 0; s < p.num_splits; ++s) {
         const float ls = __ldg(p.ws_lse + s * rows + row);
-        if (ls == -INFINITY) continue;
-        const float w = __expf(ls - m);
-        const float4 o = __ldg(reinterpret_cast<const float4*>(p.ws_o + s * plane + row * p.D + c));
-        acc.x = fmaf(w, o.x, acc.x);
-        acc.y = fmaf(w, o.y, acc.y);
-        acc.z = fmaf(w, o.z, acc.z);
-        acc.w = fmaf(w, o.w, acc.w);
+        const float2 o = __ldg(reinterpret_cast<const float2*>(p.ws_o + s * plane + row * p.D + c));
+        const bool live = ls != -INFINITY;
+        const float w = live ? __expf(ls - m) : 0.f;
+        acc.x += live ? w * o.x : 0.f;
+        acc.y += live ? w * o.y : 0.f;
         wsum += w;
       }
     }
@@ -46,17 +49,15 @@ __global__ void attn_merge_kernel(const MergeParams p) {
     const int64_t bh = row / p.Sq;
     const int64_t h = bh % p.Hq, b = bh / p.Hq;
     const int64_t base = p.out_layout == 0 ? row * p.D : ((b * p.Sq + qi) * p.Hq + h) * p.D;
-    uint2 packed;
+    uint32_t packed;
     if (p.bf16) {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-      packed = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+      __nv_bfloat162 v = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      packed = *reinterpret_cast<uint32_t*>(&v);
     } else {
-      __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
-      __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
-      packed = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+      __half2 v = __floats2half2_rn(acc.x * inv, acc.y * inv);
+      packed = *reinterpret_cast<uint32_t*>(&v);
     }
-    *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) + base + c) = packed;
+    *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.out) + base + c) = packed;
     if (p.lse != nullptr && c == 0) p.lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
   }
 }
@@ -69,8 +70,8 @@ __global__ void fill_f32_kernel(float* dst, int64_t n, float value) {
 }  // namespace
 
 cudaError_t launch_attn_merge(const MergeParams& p, cudaStream_t stream) {
-  const int64_t work = (int64_t)p.B * p.Hq * p.Sq * (p.D / 4);
-  const int threads = 256;
+  const int64_t work = (int64_t)p.B * p.Hq * p.Sq * (p.D / 2);
+  const int threads = 128;
   const int64_t blocks = (work + threads - 1) / threads;
   attn_merge_kernel<<<(unsigned)(blocks < 65535 * 8 ? blocks : 65535 * 8), threads, 0, stream>>>(p);
   return cudaGetLastError();
