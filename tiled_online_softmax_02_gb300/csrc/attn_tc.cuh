@@ -75,9 +75,9 @@ struct TcConfig {
   static constexpr uint32_t kOffK = kOffQ + kQTiles * kTileBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
   static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
-  // q_full, q_empty, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_final[2],
-  // drain, merge_full, merge_done
-  static constexpr int kNumBars = 2 + 3 * kStages + 2 + 2 + 2 + 3;
+  // q_full, q_empty, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2],
+  // o_final[2], drain, merge_full, merge_done
+  static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 3;
   static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffMerge = kOffTmemSlot + 16;          // float2 [128] (key-split merge)
   static constexpr uint32_t kOffOrder = kOffMerge + BM * 8;         // int [kMaxOrderB] batch order
@@ -97,16 +97,19 @@ struct Smem {
   __device__ uint32_t q_empty() const { return bar0 + 8u; }
   __device__ uint32_t k_full(int s) const { return bar0 + 8u * (2 + s); }
   __device__ uint32_t v_full(int s) const { return bar0 + 8u * (2 + S + s); }
-  __device__ uint32_t kv_empty(int s) const { return bar0 + 8u * (2 + 2 * S + s); }
-  __device__ uint32_t s_full(int t) const { return bar0 + 8u * (2 + 3 * S + t); }
-  __device__ uint32_t p_full(int t) const { return bar0 + 8u * (2 + 3 * S + 2 + t); }
+  // K and V slots are released separately: a K tile is free once both
+  // query tiles' QK^T products read it, one key tile before its V is
+  __device__ uint32_t k_empty(int s) const { return bar0 + 8u * (2 + 2 * S + s); }
+  __device__ uint32_t v_empty(int s) const { return bar0 + 8u * (2 + 3 * S + s); }
+  __device__ uint32_t s_full(int t) const { return bar0 + 8u * (2 + 4 * S + t); }
+  __device__ uint32_t p_full(int t) const { return bar0 + 8u * (2 + 4 * S + 2 + t); }
   // completes once per item, after query tile t's last P.V (the epilogue's wait)
-  __device__ uint32_t o_final(int t) const { return bar0 + 8u * (2 + 3 * S + 4 + t); }
-  __device__ uint32_t drain() const { return bar0 + 8u * (2 + 3 * S + 6); }
+  __device__ uint32_t o_final(int t) const { return bar0 + 8u * (2 + 4 * S + 4 + t); }
+  __device__ uint32_t drain() const { return bar0 + 8u * (2 + 4 * S + 6); }
   // key-split merge hand-over: lane 1's row max / sum written (128 arrivals),
   // then lane 1's O read by warpgroup 0 (128 arrivals)
-  __device__ uint32_t merge_full() const { return bar0 + 8u * (2 + 3 * S + 7); }
-  __device__ uint32_t merge_done() const { return bar0 + 8u * (2 + 3 * S + 8); }
+  __device__ uint32_t merge_full() const { return bar0 + 8u * (2 + 4 * S + 7); }
+  __device__ uint32_t merge_done() const { return bar0 + 8u * (2 + 4 * S + 8); }
   __device__ float2* merge() const { return reinterpret_cast<float2*>(base + Cfg::kOffMerge); }
   __device__ const int* order() const { return reinterpret_cast<const int*>(base + Cfg::kOffOrder); }
   __device__ uint8_t* mask_buf(int warp) const { return base + Cfg::kOffMaskBuf + warp * kMaskBufBytes; }
@@ -238,28 +241,28 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-// Maximum / minimum of 128 values as eight independent chains (short
-// dependency depth instead of one 127-long chain).
+// Maximum / minimum of 128 values: three-input max / min in eight
+// independent chains (68 instructions, dependency depth 9).
 __device__ __forceinline__ float max128(const float (&x)[BN]) {
   float m[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) m[k] = x[k];
+  for (int k = 0; k < 8; ++k) m[k] = fmaxf(x[k], x[k + 8]);
 #pragma unroll
-  for (int i = 8; i < BN; i += 8)
+  for (int i = 16; i < BN; i += 16)
 #pragma unroll
-    for (int k = 0; k < 8; ++k) m[k] = fmaxf(m[k], x[i + k]);
-  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+    for (int k = 0; k < 8; ++k) m[k] = fmax3(m[k], x[i + k], x[i + 8 + k]);
+  return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], fmax3(m[5], m[6], m[7])));
 }
 
 __device__ __forceinline__ float min128(const float (&x)[BN]) {
   float m[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) m[k] = x[k];
+  for (int k = 0; k < 8; ++k) m[k] = fminf(x[k], x[k + 8]);
 #pragma unroll
-  for (int i = 8; i < BN; i += 8)
+  for (int i = 16; i < BN; i += 16)
 #pragma unroll
-    for (int k = 0; k < 8; ++k) m[k] = fminf(m[k], x[i + k]);
-  return fminf(fminf(fminf(m[0], m[1]), fminf(m[2], m[3])), fminf(fminf(m[4], m[5]), fminf(m[6], m[7])));
+    for (int k = 0; k < 8; ++k) m[k] = fmin3(m[k], x[i + k], x[i + 8 + k]);
+  return fminf(fmin3(m[0], m[1], m[2]), fmin3(m[3], m[4], fmin3(m[5], m[6], m[7])));
 }
 
 // ------------------------------------------------------------------ producer
@@ -294,7 +297,10 @@ __device__ __forceinline__ void producer_role(const TcParams& P, const Smem<D>& 
     for (int n = 0; n < it.N; ++n, ++g) {
       const int st = g % S;
       const int key0 = (it.tb + n) * BN;
-      if (g >= S && !mbar_wait(sm.kv_empty(st), ((g / S) - 1) & 1, p.timeout_ns, p.status)) {
+      // K(g) reuses the slot of K(g - S), freed after that tile's QK^T
+      // products; V(g) the slot of V(g - S), freed one key tile later (after
+      // its P.V products).  So K runs a key tile further ahead than V.
+      if (g >= S && !mbar_wait(sm.k_empty(st), ((g / S) - 1) & 1, p.timeout_ns, p.status)) {
         ok = false;
         break;
       }
@@ -302,6 +308,10 @@ __device__ __forceinline__ void producer_role(const TcParams& P, const Smem<D>& 
       for (int s = 0; s < Cfg::kSub; ++s)
         tma_load_3d(sm.sK + st * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_k, sm.k_full(st), s * 64,
                     key0, kv_plane);
+      if (g >= S && !mbar_wait(sm.v_empty(st), ((g / S) - 1) & 1, p.timeout_ns, p.status)) {
+        ok = false;
+        break;
+      }
       mbar_arrive_expect_tx(sm.v_full(st), Cfg::kTileBytes);
       for (int s = 0; s < Cfg::kSub; ++s)
         tma_load_3d(sm.sV + st * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_v, sm.v_full(st), s * 64,
@@ -317,36 +327,38 @@ __device__ __forceinline__ void producer_role(const TcParams& P, const Smem<D>& 
 }
 
 // S_t = Q_t K^T for one key tile (K tile at kaddr), then commit s_full(t).
+// Warp-collective: the whole MMA warp calls it, one elected lane issues.
 template <int D, bool BF16>
 __device__ __forceinline__ void issue_qk(const Smem<D>& sm, uint32_t tmem, int t, uint32_t kaddr) {
   using Cfg = TcConfig<D>;
   constexpr uint32_t idesc_qk = make_idesc_f16kind(BF16, BM, BN, false);
-  const uint32_t qaddr = sm.sQ + t * Cfg::kTileBytes;
+  const uint64_t adesc0 = make_sdesc_sw128(sm.sQ + t * Cfg::kTileBytes, 16, 1024);
+  const uint64_t bdesc0 = make_sdesc_sw128(kaddr, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * Cfg::kSubBytes + (kk & 3) * 32;
-    const uint64_t adesc = make_sdesc_sw128(qaddr + off, 16, 1024);
-    const uint64_t bdesc = make_sdesc_sw128(kaddr + off, 16, 1024);
-    mma_ss(tmem + t * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+    // K step kk: 32 bytes into a 128-byte row, 64-column blocks kSubBytes
+    // apart; the start address field counts 16-byte units
+    const uint32_t off16 = ((kk >> 2) * Cfg::kSubBytes + (kk & 3) * 32) >> 4;
+    mma_ss_elect(tmem + t * 128, adesc0 + off16, bdesc0 + off16, idesc_qk, kk > 0 ? 1u : 0u);
   }
-  tc_commit(sm.s_full(t));
+  tc_commit_elect(sm.s_full(t));
 }
 
 // O_t (+)= P_t V for one key tile (V tile at vaddr; P_t in tensor memory over
 // the first half of S_t).
+// Warp-collective, like issue_qk.
 template <int D, bool BF16>
 __device__ __forceinline__ void issue_pv(const Smem<D>& sm, uint32_t tmem, int t, uint32_t vaddr,
                                          bool accumulate) {
   using Cfg = TcConfig<D>;
   constexpr uint32_t idesc_pv = make_idesc_f16kind(BF16, BM, D, true);
+  // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B apart, 64-column
+  // blocks kSubBytes apart.
+  const uint64_t bdesc0 = make_sdesc_sw128(vaddr, Cfg::kSubBytes, 1024);
 #pragma unroll
-  for (int kk = 0; kk < BN / 16; ++kk) {
-    // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B apart, 64-column
-    // blocks kSubBytes apart.
-    const uint64_t bdesc = make_sdesc_sw128(vaddr + kk * 2048, Cfg::kSubBytes, 1024);
-    mma_ts(tmem + kColO + t * 128, tmem + t * 128 + kk * 8, bdesc, idesc_pv,
-           (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < BN / 16; ++kk)
+    mma_ts_elect(tmem + kColO + t * 128, tmem + t * 128 + kk * 8, bdesc0 + (uint32_t)(kk * 2048 >> 4),
+                 idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -424,86 +436,77 @@ __device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, u
         if (pv0) {
           if (!mbar_wait_warp(sm.p_full(0), pc[0] & 1, p.timeout_ns, p.status)) { ok = false; break; }
           tc_fence_after();
-          if (lane == 0) {
-            issue_pv<D, BF16>(sm, tmem, 0, vaddr, !first_pv[0]);
-            if (it.last(0, j - 1)) tc_commit(sm.o_final(0));  // lane 0 has seen its last key tile
-          }
+          issue_pv<D, BF16>(sm, tmem, 0, vaddr, !first_pv[0]);
+          if (it.last(0, j - 1)) tc_commit_elect(sm.o_final(0));  // lane 0 has seen its last key tile
           first_pv[0] = false;
           ++pc[0];
         }
         if (s0) {
           if (!wait_k()) { ok = false; break; }
-          if (lane == 0) issue_qk<D, BF16>(sm, tmem, 0, kaddr);
+          issue_qk<D, BF16>(sm, tmem, 0, kaddr);
         }
         __syncwarp();
         if (pv1) {
           if (!mbar_wait_warp(sm.p_full(1), pc[1] & 1, p.timeout_ns, p.status)) { ok = false; break; }
           tc_fence_after();
-          if (lane == 0) {
-            issue_pv<D, BF16>(sm, tmem, 1, vaddr, !first_pv[1]);
-            if (it.last(1, j - 1)) tc_commit(sm.o_final(1));
-          }
+          issue_pv<D, BF16>(sm, tmem, 1, vaddr, !first_pv[1]);
+          if (it.last(1, j - 1)) tc_commit_elect(sm.o_final(1));
           first_pv[1] = false;
           ++pc[1];
         }
         if (s1) {
           if (!wait_k()) { ok = false; break; }
-          if (lane == 0) issue_qk<D, BF16>(sm, tmem, 1, kaddr);
+          issue_qk<D, BF16>(sm, tmem, 1, kaddr);
         }
         __syncwarp();
       } else {
       if (s0 && !pv0) {
         if (!wait_k()) { ok = false; break; }
-        if (lane == 0) issue_qk<D, BF16>(sm, tmem, 0, kaddr);
+        issue_qk<D, BF16>(sm, tmem, 0, kaddr);
       }
       if (s1 && !pv1) {
         if (!wait_k()) { ok = false; break; }
-        if (lane == 0) issue_qk<D, BF16>(sm, tmem, 1, kaddr);
+        issue_qk<D, BF16>(sm, tmem, 1, kaddr);
       }
       if (pv0) {
         if (!mbar_wait_warp(sm.p_full(0), pc[0] & 1, p.timeout_ns, p.status)) { ok = false; break; }
         tc_fence_after();
-        if (lane == 0) {
-          issue_pv<D, BF16>(sm, tmem, 0, vaddr, !first_pv[0]);
-          if (it.last(0, j - 1)) tc_commit(sm.o_final(0));  // lane 0 has seen its last key tile
-        }
+        issue_pv<D, BF16>(sm, tmem, 0, vaddr, !first_pv[0]);
+        if (it.last(0, j - 1)) tc_commit_elect(sm.o_final(0));  // lane 0 has seen its last key tile
         first_pv[0] = false;
         ++pc[0];
         if (s0) {
           if (!wait_k()) { ok = false; break; }
-          if (lane == 0) issue_qk<D, BF16>(sm, tmem, 0, kaddr);
+          issue_qk<D, BF16>(sm, tmem, 0, kaddr);
         }
       }
       if (pv1) {
         if (!mbar_wait_warp(sm.p_full(1), pc[1] & 1, p.timeout_ns, p.status)) { ok = false; break; }
         tc_fence_after();
-        if (lane == 0) {
-          issue_pv<D, BF16>(sm, tmem, 1, vaddr, !first_pv[1]);
-          if (it.last(1, j - 1)) tc_commit(sm.o_final(1));
-        }
+        issue_pv<D, BF16>(sm, tmem, 1, vaddr, !first_pv[1]);
+        if (it.last(1, j - 1)) tc_commit_elect(sm.o_final(1));
         first_pv[1] = false;
         ++pc[1];
         if (s1) {
           if (!wait_k()) { ok = false; break; }
-          if (lane == 0) issue_qk<D, BF16>(sm, tmem, 1, kaddr);
+          issue_qk<D, BF16>(sm, tmem, 1, kaddr);
         }
       }
       }  // KSPLIT
       __syncwarp();
       if (!ok) break;
-      if (lane == 0) {
-        if (n >= 1) tc_commit(sm.kv_empty((g0 + n - 1) % S));
-        // the item's last QK^T products are issued: Q may be replaced once they finish
-        if (n == it.N - 1) tc_commit(sm.q_empty());
-      }
+      // K(j) was read by this iteration's QK^T products, V(j-1) by its P.V
+      if (n < it.N) tc_commit_elect(sm.k_empty((g0 + n) % S));
+      if (n >= 1) tc_commit_elect(sm.v_empty((g0 + n - 1) % S));
+      // the item's last QK^T products are issued: Q may be replaced once they finish
+      if (n == it.N - 1) tc_commit_elect(sm.q_empty());
       __syncwarp();
     }
     if (!ok) break;
     g0 += it.N;
   }
   // Wait for every MMA this warp issued before tensor memory is freed.
-  if (lane == 0) tc_commit(sm.drain());
-  __syncwarp();
+  tc_commit_elect(sm.drain());
   mbar_wait_warp(sm.drain(), 0, p.timeout_ns, p.status);
 }
 
@@ -627,11 +630,21 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
           uint32_t sr[32];
           tmem_ld32(s_addr + k * 32, sr);
           tmem_wait_ld();
+          if constexpr (SOFTCAP) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float sv = __uint_as_float(sr[i]);
-            const float v = SOFTCAP ? soft_cap_log2(sv, p.sc_k1, p.sc_k2, p.sc_k3) : sv * p.scale_log2;
-            x[32 * k + i] = fmaf(x[32 * k + i], kLog2e, v);
+            for (int i = 0; i < 32; ++i) {
+              const float v = soft_cap_log2(__uint_as_float(sr[i]), p.sc_k1, p.sc_k2, p.sc_k3);
+              x[32 * k + i] = fmaf(x[32 * k + i], kLog2e, v);
+            }
+          } else {
+            // (mask, mask) * log2 e + (s, s) * scale log2 e, two keys per instruction
+            const uint64_t sc2 = f2(p.scale_log2, p.scale_log2);
+            const uint64_t le2 = f2(kLog2e, kLog2e);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const uint64_t sv = fmul2(f2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sc2);
+              f2_split(ffma2(f2(x[32 * k + i], x[32 * k + i + 1]), le2, sv), x[32 * k + i], x[32 * k + i + 1]);
+            }
           }
         }
         scaled = true;
@@ -654,8 +667,9 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
         }
       }
       if (need_mask) {
-        // structural limits of this row: keys outside [lo, hi) become -inf
-        if (!scaled) {
+        // structural limits of this row: keys outside [lo, hi) become -inf;
+        // with a positive scale the raw scores can be selected directly
+        if (!scaled && !(p.scale_log2 > 0.0f)) {
 #pragma unroll
           for (int i = 0; i < BN; ++i) x[i] *= p.scale_log2;
           scaled = true;
@@ -670,10 +684,14 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
       }
       if (scaled) {
         m_tile = max128(x);
-      } else {
+      } else if (!need_mask) {
         // every key of this tile is visible to every row: the extreme raw
         // score times the (signed) scale is the max of the scaled scores
         m_tile = (p.scale_log2 >= 0.0f ? max128(x) : min128(x)) * p.scale_log2;
+      } else {
+        // raw scores with -inf outside the row's keys, positive scale
+        const float mr = max128(x);
+        m_tile = mr == -INFINITY ? -INFINITY : mr * p.scale_log2;
       }
 
       // online update, keeping the old max unless it grew by more than 2^8
@@ -692,20 +710,28 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
       const float xmul = scaled ? 1.0f : p.scale_log2;  // brings x to log2 units
 
       // P = 2^(x - m) in four 32-column chunks, each packed into 16 columns
-      // of 16-bit pairs over the first half of this S row
-      float sum = 0.0f;
+      // of 16-bit pairs over the first half of this S row.  The argument and
+      // the row sum take one packed instruction per two keys; the sum runs
+      // in four independent pairs of accumulators.
+      const uint64_t mul2 = f2(xmul, xmul), sub2 = f2(-m_sub, -m_sub);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float e0 = fast_exp2(fmaf(x[ch * 32 + 2 * i], xmul, -m_sub));
-          const float e1 = fast_exp2(fmaf(x[ch * 32 + 2 * i + 1], xmul, -m_sub));
-          sum += e0 + e1;
+          float a0, a1;
+          f2_split(ffma2(f2(x[ch * 32 + 2 * i], x[ch * 32 + 2 * i + 1]), mul2, sub2), a0, a1);
+          const float e0 = fast_exp2(a0);
+          const float e1 = fast_exp2(a1);
+          acc[i & 3] = fadd2(acc[i & 3], f2(e0, e1));
           pk[i] = pack2<BF16>(e0, e1);
         }
         tmem_st16(s_addr + ch * 16, pk);
       }
+      float sum, sum_hi;
+      f2_split(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), sum, sum_hi);
+      sum += sum_hi;
       l_run = l_run * alpha + sum;
       m_run = m_use;
 
@@ -860,7 +886,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
     for (int s = 0; s < S; ++s) {
       mbar_init(sm.k_full(s), 1);
       mbar_init(sm.v_full(s), 1);
-      mbar_init(sm.kv_empty(s), 1);
+      mbar_init(sm.k_empty(s), 1);
+      mbar_init(sm.v_empty(s), 1);
     }
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(sm.s_full(t), 1);
