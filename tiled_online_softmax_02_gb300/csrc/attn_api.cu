@@ -279,6 +279,8 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
     c.sc_k1 = (float)(2.0 * l2e * (double)scale / (double)softcap);
     c.sc_k2 = (float)(-2.0 * (double)softcap * l2e);
     c.sc_k3 = (float)((double)softcap * l2e);
+    c.sc_in = (float)((double)scale / (double)softcap);
+    c.sc_out = (float)((double)softcap * l2e);
   }
   c.timeout_ns = g_timeout_ns.load();
   c.status = status;

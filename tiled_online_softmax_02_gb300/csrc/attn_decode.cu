@@ -290,18 +290,16 @@ __device__ __forceinline__ void dec_mma(const CommonParams& p, const DecLayout<D
       __syncwarp();
     }
     tc_fence_after();
-    if (lane == 0) {
-      const uint32_t vaddr = sm.v_tile(vs), paddr = sm.p_buf(t & 1);
+    // the converged warp issues; one elected lane starts the MMAs (see mma_ss_elect)
+    const uint64_t adesc0 = make_sdesc_sw128(sm.v_tile(vs), v_lbo, 1024);
+    const uint64_t bdesc0 = make_sdesc_sw128(sm.p_buf(t & 1), 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < kDecKeys / 16; ++kk) {
-        const uint64_t adesc = make_sdesc_sw128(vaddr + kk * 2048, v_lbo, 1024);
-        const uint64_t bdesc = make_sdesc_sw128(paddr + (kk >> 2) * C::kRowBlock + (kk & 3) * 32, 16, 1024);
-        mma_ss(tmem + C::kColO, adesc, bdesc, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
-      }
-      tc_commit(sm.pv_done(t & 1));
-      tc_commit(sm.v_empty(vs));
-    }
-    __syncwarp();
+    for (int kk = 0; kk < kDecKeys / 16; ++kk)
+      mma_ss_elect(tmem + C::kColO, adesc0 + (uint32_t)((kk * 2048) >> 4),
+                   bdesc0 + (uint32_t)(((kk >> 2) * C::kRowBlock + (kk & 3) * 32) >> 4), idesc_o,
+                   (t > 0 || kk > 0) ? 1u : 0u);
+    tc_commit_elect(sm.pv_done(t & 1));
+    tc_commit_elect(sm.v_empty(vs));
     return true;
   };
 
@@ -309,18 +307,17 @@ __device__ __forceinline__ void dec_mma(const CommonParams& p, const DecLayout<D
     const int ks = n % C::kSK;
     if (!mbar_wait_warp(sm.k_full(ks), (n / C::kSK) & 1, p.timeout_ns, p.status)) return;
     tc_fence_after();
-    if (lane == 0) {
-      const uint32_t kaddr = sm.k_tile(ks), qaddr = sm.q();
+    {
+      const uint64_t adesc0 = make_sdesc_sw128(sm.k_tile(ks), 16, 1024);
+      const uint64_t bdesc0 = make_sdesc_sw128(sm.q(), 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t adesc = make_sdesc_sw128(kaddr + (kk >> 2) * C::kSubBytes + (kk & 3) * 32, 16, 1024);
-        const uint64_t bdesc = make_sdesc_sw128(qaddr + (kk >> 2) * C::kRowBlock + (kk & 3) * 32, 16, 1024);
-        mma_ss(tmem + (n & 1) * NR, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
-      }
-      tc_commit(sm.s_full(n & 1));
-      tc_commit(sm.k_empty(ks));
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss_elect(tmem + (n & 1) * NR, adesc0 + (uint32_t)(((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4),
+                     bdesc0 + (uint32_t)(((kk >> 2) * C::kRowBlock + (kk & 3) * 32) >> 4), idesc_s,
+                     kk > 0 ? 1u : 0u);
+      tc_commit_elect(sm.s_full(n & 1));
+      tc_commit_elect(sm.k_empty(ks));
     }
-    __syncwarp();
     if (n >= 1 && !pv(n - 1)) return;
   }
   if (u.n >= 1) pv(u.n - 1);

@@ -26,6 +26,9 @@ struct CommonParams {
   // soft-cap folded into log2 units: softcap(scale*s)*log2(e) = k2 * r + k3,
   // r = 1 / (2^(k1 * s) + 1), k1 = 2 log2(e) scale / c, k2 = -2 c log2(e), k3 = c log2(e)
   float sc_k1, sc_k2, sc_k3;
+  // the same through the hardware tanh: softcap(scale*s)*log2(e) = sc_out * tanh(sc_in * s),
+  // sc_in = scale / c, sc_out = c log2(e) (tensor-core kernels)
+  float sc_in, sc_out;
   uint64_t timeout_ns;
   int* status;        // device status word (timeouts)
   // split-KV (tensor-core kernel): each query tile's key tiles are cut into

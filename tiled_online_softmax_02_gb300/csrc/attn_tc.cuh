@@ -622,7 +622,11 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
 
       const bool need_mask = !(key0 >= T.full_lo && key0 + BN <= T.full_hi);
       float m_tile;
-      bool scaled = false;  // x already in log2 units (else raw Q.K, scaled inside the exp)
+      // x is either already in log2 units (scaled) or a raw value that xs
+      // brings there: the raw Q.K (xs = scale log2 e) or, with a soft-cap,
+      // tanh(scale Q.K / c) (xs = c log2 e > 0)
+      bool scaled = false;
+      const float xs = SOFTCAP ? p.sc_out : p.scale_log2;
       if constexpr (MASK) {
         // x = transform(S) + mask * log2 e, 32 columns at a time
 #pragma unroll
@@ -631,10 +635,16 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
           tmem_ld32(s_addr + k * 32, sr);
           tmem_wait_ld();
           if constexpr (SOFTCAP) {
+            // (mask, mask) * log2 e + c log2 e * tanh(scale s / c)
+            const uint64_t in2 = f2(p.sc_in, p.sc_in), out2 = f2(p.sc_out, p.sc_out);
+            const uint64_t le2 = f2(kLog2e, kLog2e);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float v = soft_cap_log2(__uint_as_float(sr[i]), p.sc_k1, p.sc_k2, p.sc_k3);
-              x[32 * k + i] = fmaf(x[32 * k + i], kLog2e, v);
+            for (int i = 0; i < 32; i += 2) {
+              float a0, a1;
+              f2_split(fmul2(f2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), in2), a0, a1);
+              const uint64_t tv = f2(fast_tanh(a0), fast_tanh(a1));
+              f2_split(ffma2(tv, out2, fmul2(f2(x[32 * k + i], x[32 * k + i + 1]), le2)), x[32 * k + i],
+                       x[32 * k + i + 1]);
             }
           } else {
             // (mask, mask) * log2 e + (s, s) * scale log2 e, two keys per instruction
@@ -660,18 +670,23 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
             for (int i = 0; i < 32; ++i) x[k * 32 + i] = __uint_as_float(sr[k][i]);
         }
         if constexpr (SOFTCAP) {
-          // c tanh(scale s / c), already in log2 units
+          // tanh(scale s / c); xs = c log2 e brings it to log2 units
+          const uint64_t in2 = f2(p.sc_in, p.sc_in);
 #pragma unroll
-          for (int i = 0; i < BN; ++i) x[i] = soft_cap_log2(x[i], p.sc_k1, p.sc_k2, p.sc_k3);
-          scaled = true;
+          for (int i = 0; i < BN; i += 2) {
+            float a0, a1;
+            f2_split(fmul2(f2(x[i], x[i + 1]), in2), a0, a1);
+            x[i] = fast_tanh(a0);
+            x[i + 1] = fast_tanh(a1);
+          }
         }
       }
       if (need_mask) {
         // structural limits of this row: keys outside [lo, hi) become -inf;
         // with a positive scale the raw scores can be selected directly
-        if (!scaled && !(p.scale_log2 > 0.0f)) {
+        if (!scaled && !(xs > 0.0f)) {
 #pragma unroll
-          for (int i = 0; i < BN; ++i) x[i] *= p.scale_log2;
+          for (int i = 0; i < BN; ++i) x[i] *= xs;
           scaled = true;
         }
         int lo = R.lo - (int)key0, hi = R.hi - (int)key0;
@@ -687,11 +702,11 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
       } else if (!need_mask) {
         // every key of this tile is visible to every row: the extreme raw
         // score times the (signed) scale is the max of the scaled scores
-        m_tile = (p.scale_log2 >= 0.0f ? max128(x) : min128(x)) * p.scale_log2;
+        m_tile = (xs >= 0.0f ? max128(x) : min128(x)) * xs;
       } else {
         // raw scores with -inf outside the row's keys, positive scale
         const float mr = max128(x);
-        m_tile = mr == -INFINITY ? -INFINITY : mr * p.scale_log2;
+        m_tile = mr == -INFINITY ? -INFINITY : mr * xs;
       }
 
       // online update, keeping the old max unless it grew by more than 2^8
@@ -707,7 +722,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
         rescale = true;
       }
       const float m_sub = (m_use == -INFINITY) ? 0.0f : m_use;
-      const float xmul = scaled ? 1.0f : p.scale_log2;  // brings x to log2 units
+      const float xmul = scaled ? 1.0f : xs;  // brings x to log2 units
 
       // P = 2^(x - m) in four 32-column chunks, each packed into 16 columns
       // of 16-bit pairs over the first half of this S row.  The argument and
