@@ -46,12 +46,12 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # attn_fwd_splitkv entry), with the hash of that kernel's sources at the time;
 # reported as null once those sources change.
 NCU_TRAFFIC = {
-    "gqa_causal_bf16": {"bytes_per_launch": 128877056, "source_hash": "331a807deb69b300"},
-    "window_softcap_bf16": {"bytes_per_launch": 402496000, "source_hash": "331a807deb69b300"},
-    "ragged_kvcache_f16": {"bytes_per_launch": 48678656, "source_hash": "331a807deb69b300"},
-    "dit_f32": {"bytes_per_launch": 58580736, "source_hash": "390c7581ed4dd12a"},
-    "decode_bf16": {"bytes_per_launch": 771968256, "source_hash": "3819eeef5b6fb131"},
-    "decode_bf16+splitkv": {"bytes_per_launch": 772924416, "source_hash": "3819eeef5b6fb131"},
+    "gqa_causal_bf16": {"bytes_per_launch": 127573248, "source_hash": "edfb8aacc86b1fc1"},
+    "window_softcap_bf16": {"bytes_per_launch": 396639488, "source_hash": "edfb8aacc86b1fc1"},
+    "ragged_kvcache_f16": {"bytes_per_launch": 48539904, "source_hash": "edfb8aacc86b1fc1"},
+    "dit_f32": {"bytes_per_launch": 57720576, "source_hash": "0d1800f9038e6334"},
+    "decode_bf16": {"bytes_per_launch": 775716096, "source_hash": "12ff4660b69f949f"},
+    "decode_bf16+splitkv": {"bytes_per_launch": 776804352, "source_hash": "12ff4660b69f949f"},
 }
 
 
