@@ -153,12 +153,13 @@ KERNEL_SOURCES = {
            "attn_tc_f16_d64.cu", "attn_tc_f16_d128.cu", "device_common.cuh", "attn_internal.h"),
     "f32": ("attn_f32.cu", "device_common.cuh", "attn_internal.h"),
     "decode": ("attn_decode.cu", "attn_decode.h", "device_common.cuh", "attn_internal.h"),
+    "f32tc": ("attn_f32tc.cu", "device_common.cuh", "attn_internal.h"),
 }
 
 
-def kernel_family(w: Workload, splitkv: bool = False) -> str:
+def kernel_family(w: Workload, splitkv: bool = False, f32split: bool = False) -> str:
     if w.dtype == "f32":
-        return "f32"
+        return "f32tc" if f32split else "f32"
     return "decode" if w.group * w.Sq <= 32 else "tc"
 
 
@@ -389,6 +390,14 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
 
     launches_per_step = 1
+    # fp32 workloads run the tensor-core entry (attn_fwd_f32_split) for the
+    # head dims it covers unless --f32-path exact asks for the CUDA-core kernel
+    f32split = w.dtype == "f32" and args.f32_path == "split" and w.D in (64, 128)
+    if f32split:
+        lib = attn.load_library()
+        ws_f32 = torch.empty(lib.attn_f32_split_workspace_bytes(w.B, w.Hkv, w.kv_capacity, w.D),
+                             dtype=torch.uint8, device=dev)
+        launches_per_step = 2  # the K / V split, then the attention kernel
     if args.splitkv:
         lib = attn.load_library()
         splits = args.splits or lib.attn_splitkv_num_splits(w.B, w.Hq, w.Hkv, w.Sq, w.Sk)
@@ -405,6 +414,13 @@ def run_ours(args, world, rank, local):
                                   scale=w.softmax_scale, softcap=w.softcap,
                                   out_layout=w.out_layout, seq_k=w.Sk, num_splits=splits,
                                   out=out, lse=lse_buf, workspace=ws_buf)
+            return
+        if f32split:
+            attn.attn_fwd_f32_split(g["q"], g["k"], g["v"], mask=g["mask"],
+                                    total_lengths=g["total_lengths"], past_lengths=g["past_lengths"],
+                                    causal=w.causal, local_window=w.local_window,
+                                    scale=w.softmax_scale, softcap=w.softcap,
+                                    out_layout=w.out_layout, seq_k=w.Sk, out=out, workspace=ws_f32)
             return
         attn.attn_fwd(g["q"], g["k"], g["v"], mask=g["mask"], total_lengths=g["total_lengths"],
                       past_lengths=g["past_lengths"], causal=w.causal,
@@ -455,6 +471,14 @@ def run_ours(args, world, rank, local):
     d2h = int(host_out.numel() * host_out.element_size())
 
     def e2e_step():
+        if f32split:
+            attn.attn_fwd_f32_split(host["q"], host["k"], host["v"], mask=host["mask"],
+                                    total_lengths=host["total_lengths"],
+                                    past_lengths=host["past_lengths"], causal=w.causal,
+                                    local_window=w.local_window, scale=w.softmax_scale,
+                                    softcap=w.softcap, out_layout=w.out_layout, seq_k=w.Sk,
+                                    out=host_out, workspace=ws_f32)
+            return
         attn.attn_fwd(host["q"], host["k"], host["v"], mask=host["mask"],
                       total_lengths=host["total_lengths"], past_lengths=host["past_lengths"],
                       causal=w.causal, local_window=w.local_window, scale=w.softmax_scale,
@@ -482,6 +506,10 @@ def run_ours(args, world, rank, local):
         # below the ridge point HBM, not the tensor pipe, bounds the launch
         peak, bound = float(peaks["hbm_gbs"]), "hbm"
         src = f"{src} hbm_gbs"
+    elif f32split:
+        # bf16 tensor cores doing 4.5 MMAs per fp32 MMA (6 for QK^T, 3 for P.V)
+        peak, bound = float(peaks["bf16_tflops"]) / 4.5, "tensor"
+        src = f"{src} bf16_tflops (burst) / 4.5 bf16 MMAs per fp32 MMA (6 for QK^T, 3 for PV)"
     elif w.dtype == "f32":
         # fp32 FFMA on CUDA cores: SMs x 128 FMA/clk x 2 FLOP x max SM clock
         props = torch.cuda.get_device_properties(dev)
@@ -494,8 +522,8 @@ def run_ours(args, world, rank, local):
     achieved = flops / avg_launch_s / 1e12
     roof = hbm_gbs if bound == "hbm" else achieved
     traffic = None
-    ent = NCU_TRAFFIC.get(w.name + ("+splitkv" if args.splitkv else ""))
-    if ent and ent.get("source_hash") == kernel_source_hash(kernel_family(w, args.splitkv)):
+    ent = NCU_TRAFFIC.get(w.name + ("+splitkv" if args.splitkv else "") + ("+f32split" if f32split else ""))
+    if ent and ent.get("source_hash") == kernel_source_hash(kernel_family(w, args.splitkv, f32split)):
         traffic = ent["bytes_per_launch"]
     cpu = None
     if not args.no_cpu_baseline:
@@ -510,14 +538,16 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded, shaped like the pages' workloads)",
         "config": dict(workload_config(w, flops, flops_excl, world),
-                       entry="attn_fwd_splitkv" if args.splitkv else "attn_fwd",
+                       entry=("attn_fwd_splitkv" if args.splitkv else
+                              "attn_fwd_f32_split" if f32split else "attn_fwd"),
                        **({"num_splits": splits} if args.splitkv else {})),
         "frac_of_peak": roof / peak,
         "roofline": {"bound": bound, "achieved": roof, "peak": peak,
                      "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
                      "frac": roof / peak, "traffic": traffic, "peak_source": src,
                      "algorithmic_bytes": abytes, "hbm_gbs": hbm_gbs,
-                     "frac_of_sustained": (achieved / float(peaks.get("bf16_tflops_sustained", peak))
+                     "frac_of_sustained": (achieved / (float(peaks.get("bf16_tflops_sustained", peak))
+                                                       / (4.5 if f32split else 1.0))
                                            if bound == "tensor" else None)},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
@@ -540,6 +570,9 @@ def main(argv=None):
     ap.add_argument("--splitkv", action="store_true",
                     help="time attn_fwd_splitkv (split count: --splits, else the library's choice)")
     ap.add_argument("--splits", type=int, default=0, help="split count for --splitkv (0: library)")
+    ap.add_argument("--f32-path", choices=["split", "exact"], default="split",
+                    help="fp32 workloads: the tensor-core entry attn_fwd_f32_split (D 64 / 128) or "
+                         "the fp32-exact CUDA-core kernel of attn_fwd")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)

@@ -143,6 +143,49 @@ int attn_splitkv_num_splits(int B, int Hq, int Hkv, int Sq, int Sk);
  * num_splits * B * Hq * Sq * (D + 1) * 4. */
 size_t attn_splitkv_workspace_bytes(int B, int Hq, int Sq, int D, int num_splits);
 
+/*
+ * attn_fwd_f32_split -- attn_fwd for fp32 q, k, v, out on the tensor cores.
+ *
+ * The definition is attn_fwd's, in fp32 as "pictor-kernels 0.1.0,
+ * src/gpu_backend/cuda_imagen_attn_kernels.rs" ("Parity-first design") asks
+ * of its DiT joint attention. That page keeps the products on CUDA cores and
+ * leaves tensor-core tuning for later. This entry runs both products as bf16
+ * tcgen05 MMAs with fp32 accumulation, each fp32 operand carried as a sum of
+ * bf16 pieces (x0 = bf16(x), x1 = bf16(x - x0), x2 = bf16(x - x0 - x1)):
+ *   S = Q K^T   three pieces of Q and K, six products
+ *               (q0k0 + q0k1 + q1k0 + q0k2 + q1k1 + q2k0). The dropped terms
+ *               are below about 3 * 2^-24 |q k|, so the scores keep fp32
+ *               accuracy even where |s| is large.
+ *   O = P V     two pieces of P and V (residual <= 2^-16), three products
+ *               (p0v0 + p0v1 + p1v0). The output is a P-weighted average of
+ *               V, so its error stays near 2^-16 max|v|.
+ * The result is held to the fp32 path's 1e-4 bound, including on sharply
+ * peaked softmax rows. The fp32-exact CUDA-core kernel stays available as
+ * attn_fwd with ATTN_F32.
+ *
+ * Arguments as attn_fwd with dtype fixed to fp32, plus:
+ *   D               64 or 128 (others: ATTN_ERR_UNSUPPORTED)
+ *   workspace       device scratch of at least attn_f32_split_workspace_bytes(
+ *                   B, Hkv, kv_capacity, D) bytes, 16-byte aligned,
+ *                   caller-owned, not overlapping any other argument.  The
+ *                   call first writes the bf16 pieces of k (three) and v (two) there (rows
+ *                   at or past a batch's valid length as zeros), then runs
+ *                   the attention kernel.  Calls that share a workspace must
+ *                   not overlap on the GPU.
+ * Launches two kernels on `stream`; allocates and synchronises nothing.
+ * Errors as attn_fwd; ATTN_ERR_INVALID_ARG also for a missing or too small
+ * workspace, or more than 2^31 / 5 key-value planes (B * Hkv).
+ */
+int attn_fwd_f32_split(const float *q, const float *k, const float *v, const float *mask,
+                       const int32_t *total_lengths, const int32_t *past_lengths, float *out,
+                       int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D,
+                       int causal, int local_window, float scale, float softcap, int out_layout,
+                       int mask_planes, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes attn_fwd_f32_split needs: 5 * B * Hkv * kv_capacity * D * 2
+ * (three bf16 pieces of k, two of v); 0 for non-positive sizes. */
+size_t attn_f32_split_workspace_bytes(int B, int Hkv, int kv_capacity, int D);
+
 /* Size of the library-owned buffer attn_fwd_splitkv_noalloc uses (8 MiB). */
 #define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -35,6 +35,20 @@ def run_gpu(w: Workload, x: dict, *, out=None):
     return o
 
 
+def run_gpu_f32split(w: Workload, x: dict, *, out=None, workspace=None):
+    """The fp32 tensor-core entry (attn_fwd_f32_split) on the same inputs."""
+    g = to_dev(x)
+    o = attn.attn_fwd_f32_split(g["q"], g["k"], g["v"], mask=g["mask"],
+                                total_lengths=g["total_lengths"], past_lengths=g["past_lengths"],
+                                causal=w.causal, local_window=w.local_window,
+                                scale=w.softmax_scale, softcap=w.softcap, out_layout=w.out_layout,
+                                seq_k=w.Sk, out=out, workspace=workspace)
+    torch.cuda.synchronize()
+    st = attn.get_device_status()
+    assert st == attn.ATTN_OK, f"device status {attn.status_string(st)}"
+    return o
+
+
 def run_oracle(w: Workload, x: dict):
     return oracle.attn_fwd(x["q"], x["k"], x["v"], B=w.B, Hq=w.Hq, Hkv=w.Hkv, Sq=w.Sq, Sk=w.Sk,
                            kv_capacity=w.kv_capacity, D=w.D, causal=w.causal,

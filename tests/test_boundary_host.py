@@ -169,3 +169,30 @@ def test_binding_rejects_bad_tensors():
         attn.attn_fwd(q, torch.zeros(1, 1, 4, 32), torch.zeros(1, 1, 4, 32))
     with pytest.raises(ValueError):
         attn.attn_fwd(q, q.double(), q.double())
+
+
+def call_f32split(lib, ws=None, ws_bytes=0, **kw):
+    a = dict(GOOD, **dict(dict(D=64), **kw))
+    return lib.attn_fwd_f32_split(a["q"], a["k"], a["v"], a["mask"], a["total"], a["past"], a["out"],
+                                  a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Sk"], a["cap"], a["D"],
+                                  a["causal"], a["window"], a["scale"], a["softcap"], a["layout"],
+                                  a["planes"], ws, ws_bytes, None)
+
+
+def test_f32_split_validation(lib):
+    need = lib.attn_f32_split_workspace_bytes(2, 2, 200, 64)
+    assert need == 5 * 2 * 2 * 200 * 64 * 2  # k0, k1, k2, v0, v1 in bf16
+    assert lib.attn_f32_split_workspace_bytes(0, 2, 200, 64) == 0
+    WS = 0x7A000000
+    assert call_f32split(lib) == attn.ATTN_ERR_INVALID_ARG                            # no workspace
+    assert call_f32split(lib, ws=WS, ws_bytes=need - 1) == attn.ATTN_ERR_INVALID_ARG  # too small
+    assert call_f32split(lib, ws=WS + 8, ws_bytes=need) == attn.ATTN_ERR_UNSUPPORTED  # misaligned
+    assert call_f32split(lib, ws=K, ws_bytes=need) == attn.ATTN_ERR_INVALID_ARG       # overlaps k
+    assert call_f32split(lib, ws=WS, ws_bytes=need, D=96) == attn.ATTN_ERR_UNSUPPORTED
+    assert call_f32split(lib, ws=WS, ws_bytes=need, D=256) == attn.ATTN_ERR_UNSUPPORTED
+    assert call_f32split(lib, ws=WS, ws_bytes=need, Hq=5) == attn.ATTN_ERR_INVALID_ARG
+    assert call_f32split(lib, ws=WS, ws_bytes=need, q=Q + 8) == attn.ATTN_ERR_UNSUPPORTED
+    assert call_f32split(lib, ws=WS, ws_bytes=need, B=0) == attn.ATTN_OK              # empty problem
+    # B * Hkv beyond the TMA plane coordinates of the four pieces
+    assert call_f32split(lib, ws=WS, ws_bytes=2**62, B=40000, Hq=40000, Hkv=40000, Sq=1, Sk=1,
+                         cap=1) == attn.ATTN_ERR_INVALID_ARG

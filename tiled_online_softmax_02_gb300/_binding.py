@@ -37,6 +37,11 @@ SIGNATURES = {
                                         _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                         _i32, _i32, ctypes.c_float, ctypes.c_float, _i32,
                                         _i32, _i32, _i32, _vp, _vp]),
+    "attn_fwd_f32_split": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                  _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                  _i32, _i32, ctypes.c_float, ctypes.c_float, _i32,
+                                  _i32, _vp, ctypes.c_size_t, _vp]),
+    "attn_f32_split_workspace_bytes": (ctypes.c_size_t, [_i32, _i32, _i32, _i32]),
     "attn_splitkv_num_splits": (_i32, [_i32, _i32, _i32, _i32, _i32]),
     "attn_splitkv_workspace_bytes": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, _i32]),
     "attn_status_string": (ctypes.c_char_p, [_i32]),
@@ -94,7 +99,8 @@ def _stream_handle(device) -> ctypes.c_void_p:
 
 
 def attn_fwd(q, k, v, *, mask=None, total_lengths=None, past_lengths=None, causal=False,
-             local_window=0, scale=None, softcap=0.0, out_layout="head", seq_k=None, out=None):
+             local_window=0, scale=None, softcap=0.0, out_layout="head", seq_k=None, out=None,
+             _f32_split=False, workspace=None):
     """Attention forward through libattn.so.
 
     q [B, Hq, Sq, D]; k, v [B, Hkv, kv_capacity, D] (same dtype: float32,
@@ -155,12 +161,21 @@ def attn_fwd(q, k, v, *, mask=None, total_lengths=None, past_lengths=None, causa
         scale = 1.0 / math.sqrt(D)
     lib = load_library()
     with torch.cuda.device(q.device):
-        rc = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(total_lengths),
-                          _ptr(past_lengths), _ptr(out), B, Hq, Hkv, Sq, Sk, kv_capacity, D,
-                          int(bool(causal)), int(local_window), float(scale), float(softcap),
-                          layout, mask_planes, DTYPE_CODES[q.dtype], _stream_handle(q.device))
+        args = (_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(total_lengths), _ptr(past_lengths),
+                _ptr(out), B, Hq, Hkv, Sq, Sk, kv_capacity, D, int(bool(causal)),
+                int(local_window), float(scale), float(softcap), layout, mask_planes)
+        if _f32_split:
+            need = lib.attn_f32_split_workspace_bytes(B, Hkv, kv_capacity, D)
+            if workspace is None or not workspace.is_cuda:
+                workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+            ws_bytes = workspace.numel() * workspace.element_size()
+            rc = lib.attn_fwd_f32_split(*args, _ptr(workspace), ws_bytes, _stream_handle(q.device))
+            what = "attn_fwd_f32_split"
+        else:
+            rc = lib.attn_fwd(*args, DTYPE_CODES[q.dtype], _stream_handle(q.device))
+            what = "attn_fwd"
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_fwd")
+        raise AttnError(rc, what)
     if host:
         if host_out is None:
             host_out = torch.empty(shape, dtype=q.dtype, pin_memory=True)
@@ -168,6 +183,22 @@ def attn_fwd(q, k, v, *, mask=None, total_lengths=None, past_lengths=None, causa
         torch.cuda.current_stream(q.device).synchronize()
         return host_out
     return out
+
+
+def attn_fwd_f32_split(q, k, v, *, mask=None, total_lengths=None, past_lengths=None,
+                       causal=False, local_window=0, scale=None, softcap=0.0, out_layout="head",
+                       seq_k=None, out=None, workspace=None):
+    """fp32 attention forward on the tensor cores (attn_fwd_f32_split in the C
+    ABI): q, k, v float32 with D = 64 or 128, each product taken as three bf16
+    MMAs over two-piece operands.  Arguments and result as attn_fwd (CUDA or,
+    end to end, CPU tensors).  The bf16 workspace for the split K / V
+    (attn_f32_split_workspace_bytes) is allocated with torch when not given."""
+    if q.dtype != torch.float32:
+        raise ValueError("attn_fwd_f32_split takes float32 q, k, v")
+    return attn_fwd(q, k, v, mask=mask, total_lengths=total_lengths, past_lengths=past_lengths,
+                    causal=causal, local_window=local_window, scale=scale, softcap=softcap,
+                    out_layout=out_layout, seq_k=seq_k, out=out, _f32_split=True,
+                    workspace=workspace)
 
 
 def attn_fwd_splitkv(q, k, v, *, mask=None, total_lengths=None, past_lengths=None, causal=False,

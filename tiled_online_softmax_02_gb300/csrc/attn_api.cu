@@ -79,16 +79,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn(int* err) {
   return fn;
 }
 
-// 16-bit tensor [planes, rows, D] as a 3-D TMA map with a {64, 128, 1} box and
-// the 128-byte swizzle the tcgen05 shared-memory descriptors expect.  Rows and
-// planes out of range read as zero.
-int encode_map(CUtensorMap* map, const void* base, bool bf16, int64_t planes, int64_t rows, int D) {
+// 16-bit tensor [planes, rows, D] as a 3-D TMA map with a {64, box_rows, 1}
+// box and the 128-byte swizzle the tcgen05 shared-memory descriptors expect.
+// Rows and planes out of range read as zero.
+int encode_map(CUtensorMap* map, const void* base, bool bf16, int64_t planes, int64_t rows, int D,
+               int box_rows = kTcBlockM) {
   int err = ATTN_OK;
   auto fn = encode_fn(&err);
   if (!fn) return err;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)planes};
   const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * (cuuint64_t)D * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)kTcBlockM, 1};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -186,7 +187,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
              int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D,
              int causal, int local_window, float scale, float softcap, int out_layout,
              int mask_planes, int dtype, void* stream, bool splitkv_api, int num_splits, float* lse,
-             void* workspace, size_t workspace_bytes) {
+             void* workspace, size_t workspace_bytes, bool f32split = false) {
   // ---------------------------------------------------------------- validation
   if (dtype != ATTN_F32 && dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   if (B < 0 || Sq < 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
@@ -222,6 +223,18 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
 
   // capability gate: no kernel, no launch
   if (dtype == ATTN_F32 && D > 128) return ATTN_ERR_UNSUPPORTED;
+  if (f32split) {
+    if (dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+    if ((int64_t)B * Hkv > INT32_MAX / kF32TcPlanesPerKv) return ATTN_ERR_INVALID_ARG;  // TMA planes
+    const size_t need = f32tc_workspace_bytes(kv_elems);
+    if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return ATTN_ERR_UNSUPPORTED;
+    if (overlaps(workspace, (int64_t)need, out, qbytes) || overlaps(workspace, (int64_t)need, q, qbytes) ||
+        overlaps(workspace, (int64_t)need, k, kvbytes) || overlaps(workspace, (int64_t)need, v, kvbytes) ||
+        overlaps(workspace, (int64_t)need, mask, mbytes))
+      return ATTN_ERR_INVALID_ARG;
+  }
   if (splitkv_api) {
     if (num_splits < 0 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
     if (dtype == ATTN_F32) return ATTN_ERR_UNSUPPORTED;  // split-KV is a tensor-core path
@@ -292,7 +305,15 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
   }
 
   cudaError_t e;
-  if (dtype == ATTN_F32) {
+  if (f32split) {
+    F32TcParams fp{};
+    fp.q = static_cast<const float*>(q);
+    fp.ws = workspace;
+    fp.c = c;
+    int rc = encode_map(&fp.tmap_ws, workspace, true, kF32TcPlanesPerKv * (int64_t)B * Hkv, kv_capacity, D, 64);
+    if (rc != ATTN_OK) return rc;
+    e = launch_attn_f32tc(fp, static_cast<const float*>(k), static_cast<const float*>(v), st);
+  } else if (dtype == ATTN_F32) {
     F32Params fp{};
     fp.q = static_cast<const float*>(q);
     fp.k = static_cast<const float*>(k);
@@ -358,6 +379,22 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, con
   return fwd_impl(q, k, v, mask, total_lengths, past_lengths, out, B, Hq, Hkv, Sq, Sk, kv_capacity,
                   D, causal, local_window, scale, softcap, out_layout, mask_planes, dtype, stream,
                   true, num_splits, lse, workspace, workspace_bytes);
+}
+
+extern "C" int attn_fwd_f32_split(const float* q, const float* k, const float* v, const float* mask,
+                                  const int32_t* total_lengths, const int32_t* past_lengths, float* out,
+                                  int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D,
+                                  int causal, int local_window, float scale, float softcap,
+                                  int out_layout, int mask_planes, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return fwd_impl(q, k, v, mask, total_lengths, past_lengths, out, B, Hq, Hkv, Sq, Sk, kv_capacity,
+                  D, causal, local_window, scale, softcap, out_layout, mask_planes, ATTN_F32, stream,
+                  false, 1, nullptr, workspace, workspace_bytes, true);
+}
+
+extern "C" size_t attn_f32_split_workspace_bytes(int B, int Hkv, int kv_capacity, int D) {
+  if (B <= 0 || Hkv <= 0 || kv_capacity <= 0 || D <= 0) return 0;
+  return f32tc_workspace_bytes((int64_t)B * Hkv * kv_capacity * D);
 }
 
 extern "C" int attn_splitkv_num_splits(int B, int Hq, int Hkv, int Sq, int Sk) {

@@ -65,6 +65,17 @@ struct F32Params {
   CommonParams c;
 };
 
+// fp32 on the tensor cores: K / V split into bf16 pieces in a workspace
+// (k0, k1, k2, v0, v1, each [B, Hkv, kv_capacity, D]) read through one TMA
+// map over [5 * B * Hkv planes, kv_capacity rows, D]; Q (fp32) is split in
+// the kernel.
+struct F32TcParams {
+  CUtensorMap tmap_ws;  // box {64, 64, 1}, 128B swizzle
+  const float* q;
+  void* ws;
+  CommonParams c;
+};
+
 constexpr int kTcBlockM = 128;  // query rows per tcgen05 CTA
 constexpr int kTcBlockN = 128;  // keys per tcgen05 tile
 constexpr int kF32BlockM = 64;  // query rows per fp32 CTA
@@ -72,6 +83,10 @@ constexpr int kF32BlockM = 64;  // query rows per fp32 CTA
 // Launchers.  They assume validated parameters.
 cudaError_t launch_attn_tc(const TcParams& p, bool bf16, cudaStream_t stream);
 cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream);
+cudaError_t launch_attn_f32tc(const F32TcParams& p, const float* k, const float* v, cudaStream_t stream);
+// workspace bytes of the fp32 tensor-core path for B * Hkv * kv_capacity * D elements of K (and of V)
+size_t f32tc_workspace_bytes(int64_t kv_elems);
+constexpr int kF32TcPlanesPerKv = 5;  // k0, k1, k2, v0, v1
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, int* status, cudaStream_t stream);
 cudaError_t launch_attn_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_fill_f32(float* dst, int64_t n, float value, cudaStream_t stream);
