@@ -301,12 +301,13 @@ __device__ __forceinline__ void f_mma(const F32TcParams& P, const FSmem<D>& sm, 
         const uint64_t d0 = make_sdesc_sw128(vb, C::kSubBytes, 1024);
         const uint64_t d1 = make_sdesc_sw128(vb + C::kPieceBytes, C::kSubBytes, 1024);
         const uint32_t pa = tmem + kFColS + 64 * (m & 1);  // p0 in its first 32 columns, p1 in the next 32
+        // two K steps (16 keys each, 2048 bytes of V apart) per issue block
 #pragma unroll
-        for (int kk = 0; kk < FN / 16; ++kk) {
-          const uint32_t off16 = (uint32_t)(kk * 2048) >> 4;
-          mma_ts_elect(tmem + kFColO, pa + kk * 8, d0 + off16, id_pv, (m == 0 && kk == 0) ? 0u : 1u);
-          mma_ts_elect(tmem + kFColO, pa + kk * 8, d1 + off16, id_pv, 1u);
-          mma_ts_elect(tmem + kFColO, pa + 32 + kk * 8, d0 + off16, id_pv, 1u);
+        for (int kk = 0; kk < FN / 16; kk += 2) {
+          const uint32_t o0 = (uint32_t)(kk * 2048) >> 4, o1 = (uint32_t)((kk + 1) * 2048) >> 4;
+          mma_ts6_elect(tmem + kFColO, pa + kk * 8, d0 + o0, pa + kk * 8, d1 + o0, pa + 32 + kk * 8, d0 + o0,
+                        pa + (kk + 1) * 8, d0 + o1, pa + (kk + 1) * 8, d1 + o1, pa + 32 + (kk + 1) * 8, d0 + o1,
+                        id_pv, (m == 0 && kk == 0) ? 0u : 1u);
         }
         tc_commit_elect(sm.v_empty(gv % S));
         tc_commit_elect(sm.pv_done());
@@ -321,17 +322,14 @@ __device__ __forceinline__ void f_mma(const F32TcParams& P, const FSmem<D>& sm, 
         uint64_t kd[kKPieces];
 #pragma unroll
         for (int pc = 0; pc < kKPieces; ++pc) kd[pc] = make_sdesc_sw128(kb + pc * C::kPieceBytes, 16, 1024);
-        const uint32_t sdst = tmem + kFColS + 64 * (n & 1);
-        constexpr int qa[6] = {0, 0, 1, 0, 1, 2};
-        constexpr int kbp[6] = {0, 1, 0, 2, 1, 0};
+        const uint32_t sd = tmem + kFColS + 64 * (n & 1);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // K step kk: 32 bytes into a 128-byte row, 64-column blocks kSubBytes apart
           const uint32_t off16 = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
-#pragma unroll
-          for (int t = 0; t < 6; ++t)
-            mma_ts_elect(sdst, tmem + kFColQ + qa[t] * kQPiece + kk * 8, kd[kbp[t]] + off16, id_qk,
-                         (kk > 0 || t > 0) ? 1u : 0u);
+          const uint32_t q0 = tmem + kFColQ + kk * 8, q1 = q0 + kQPiece, q2 = q0 + 2 * kQPiece;
+          mma_ts6_elect(sd, q0, kd[0] + off16, q0, kd[1] + off16, q1, kd[0] + off16, q0, kd[2] + off16,
+                        q1, kd[1] + off16, q2, kd[0] + off16, id_qk, kk > 0 ? 1u : 0u);
         }
         tc_commit_elect(sm.s_full(n & 1));
         tc_commit_elect(sm.k_empty(gs % S));

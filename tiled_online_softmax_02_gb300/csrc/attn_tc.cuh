@@ -334,12 +334,13 @@ __device__ __forceinline__ void issue_qk(const Smem<D>& sm, uint32_t tmem, int t
   constexpr uint32_t idesc_qk = make_idesc_f16kind(BF16, BM, BN, false);
   const uint64_t adesc0 = make_sdesc_sw128(sm.sQ + t * Cfg::kTileBytes, 16, 1024);
   const uint64_t bdesc0 = make_sdesc_sw128(kaddr, 16, 1024);
+  // K steps kk = 4s..4s+3 lie in 64-column block s (kSubBytes apart), 32
+  // bytes into each 128-byte row; the start address field counts 16 bytes
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    // K step kk: 32 bytes into a 128-byte row, 64-column blocks kSubBytes
-    // apart; the start address field counts 16-byte units
-    const uint32_t off16 = ((kk >> 2) * Cfg::kSubBytes + (kk & 3) * 32) >> 4;
-    mma_ss_elect(tmem + t * 128, adesc0 + off16, bdesc0 + off16, idesc_qk, kk > 0 ? 1u : 0u);
+  for (int s = 0; s < D / 64; ++s) {
+    const uint32_t o = (s * Cfg::kSubBytes) >> 4;
+    mma_ss4_elect(tmem + t * 128, adesc0 + o, bdesc0 + o, adesc0 + o + 2, bdesc0 + o + 2, adesc0 + o + 4,
+                  bdesc0 + o + 4, adesc0 + o + 6, bdesc0 + o + 6, idesc_qk, s > 0 ? 1u : 0u);
   }
   tc_commit_elect(sm.s_full(t));
 }
@@ -355,10 +356,13 @@ __device__ __forceinline__ void issue_pv(const Smem<D>& sm, uint32_t tmem, int t
   // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B apart, 64-column
   // blocks kSubBytes apart.
   const uint64_t bdesc0 = make_sdesc_sw128(vaddr, Cfg::kSubBytes, 1024);
+  // four K steps (16 keys, 2048 bytes of V, 8 columns of P each) per issue block
+  const uint32_t d = tmem + kColO + t * 128, a = tmem + t * 128;
 #pragma unroll
-  for (int kk = 0; kk < BN / 16; ++kk)
-    mma_ts_elect(tmem + kColO + t * 128, tmem + t * 128 + kk * 8, bdesc0 + (uint32_t)(kk * 2048 >> 4),
-                 idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < BN / 16; kk += 4)
+    mma_ts4_elect(d, a + kk * 8, bdesc0 + (uint32_t)(kk * 128), a + (kk + 1) * 8,
+                  bdesc0 + (uint32_t)((kk + 1) * 128), a + (kk + 2) * 8, bdesc0 + (uint32_t)((kk + 2) * 128),
+                  a + (kk + 3) * 8, bdesc0 + (uint32_t)((kk + 3) * 128), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // ------------------------------------------------------------------ MMA issuer

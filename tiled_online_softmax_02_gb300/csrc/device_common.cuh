@@ -283,6 +283,63 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// Several MMAs into one accumulator from one asm block and one elect.sync:
+// the issuing lane then needs no further issue slots between them, which
+// keeps MMAs back to back even while other warps of the sub-partition issue
+// (N = 64 MMAs: 32 cycles each this way, 39 when issued one asm block at a
+// time next to one arithmetic-heavy warp).  The first MMA accumulates iff
+// acc0 != 0, the others always.
+__device__ __forceinline__ void mma_ss4_elect(uint32_t d, uint64_t a0, uint64_t b0, uint64_t a1, uint64_t b1,
+                                              uint64_t a2, uint64_t b2, uint64_t a3, uint64_t b3,
+                                              uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "setp.ne.b32 q, %10, 0;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %9, q;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %9, 1;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %9, 1;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %9, 1;\n\t}" ::"r"(d),
+      "l"(a0), "l"(b0), "l"(a1), "l"(b1), "l"(a2), "l"(b2), "l"(a3), "l"(b3), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+
+// Four MMAs with A in tensor memory (addresses a_i).
+__device__ __forceinline__ void mma_ts4_elect(uint32_t d, uint32_t a0, uint64_t b0, uint32_t a1, uint64_t b1,
+                                              uint32_t a2, uint64_t b2, uint32_t a3, uint64_t b3,
+                                              uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "setp.ne.b32 q, %10, 0;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %9, q;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %9, 1;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %9, 1;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %9, 1;\n\t}" ::"r"(d),
+      "r"(a0), "l"(b0), "r"(a1), "l"(b1), "r"(a2), "l"(b2), "r"(a3), "l"(b3), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+
+// Six MMAs with A in tensor memory.
+__device__ __forceinline__ void mma_ts6_elect(uint32_t d, uint32_t a0, uint64_t b0, uint32_t a1, uint64_t b1,
+                                              uint32_t a2, uint64_t b2, uint32_t a3, uint64_t b3,
+                                              uint32_t a4, uint64_t b4, uint32_t a5, uint64_t b5,
+                                              uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "setp.ne.b32 q, %14, 0;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %13, q;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %13, 1;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %13, 1;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %13, 1;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %13, 1;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%11], %12, %13, 1;\n\t}" ::"r"(d),
+      "r"(a0), "l"(b0), "r"(a1), "l"(b1), "r"(a2), "l"(b2), "r"(a3), "l"(b3), "r"(a4), "l"(b4),
+      "r"(a5), "l"(b5), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+
 // tc_commit by the elected lane (the lane that issued the warp's MMAs).
 __device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
   asm volatile(
