@@ -74,14 +74,17 @@ struct FCfg {
   static constexpr uint32_t kPieceBytes = kSub * kSubBytes;    // one piece of one tile
   static constexpr uint32_t kKTileBytes = kKPieces * kPieceBytes;
   static constexpr uint32_t kVTileBytes = kVPieces * kPieceBytes;
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  // K and V of a key tile arrive together (one barrier); a V slot is freed
+  // a key tile later than its K slot, so V has one stage more
+  static constexpr int kKStages = (D == 64) ? 4 : 2;
+  static constexpr int kVStages = kKStages + 1;
   static constexpr uint32_t kOffK = 0;
-  static constexpr uint32_t kOffV = kOffK + kStages * kKTileBytes;
-  static constexpr uint32_t kOffMaskBuf = kOffV + kStages * kVTileBytes;
+  static constexpr uint32_t kOffV = kOffK + kKStages * kKTileBytes;
+  static constexpr uint32_t kOffMaskBuf = kOffV + kVStages * kVTileBytes;
   static constexpr uint32_t kOffBar = kOffMaskBuf + 4 * kFMaskBufBytes;
-  // k_full[S], k_empty[S], v_full[S], v_empty[S], q_full, q_empty, s_full[2],
+  // kv_full[KS], k_empty[KS], v_empty[VS], q_full, q_empty, s_full[2],
   // p_full[2], pv_done, o_final, drain
-  static constexpr int kNumBars = 4 * kStages + 2 + 2 + 2 + 3;
+  static constexpr int kNumBars = 2 * kKStages + kVStages + 2 + 2 + 2 + 3;
   static constexpr uint32_t kOffSlot = kOffBar + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -90,24 +93,25 @@ struct FCfg {
 template <int D>
 struct FSmem {
   using C = FCfg<D>;
-  static constexpr int S = C::kStages;
+  static constexpr int KS = C::kKStages, VS = C::kVStages;
+  static constexpr int kB = 2 * KS + VS;  // first barrier after the rings
   uint8_t* base;
   uint32_t sK, sV, bar0;
-  __device__ uint32_t k_full(int s) const { return bar0 + 8u * s; }
-  __device__ uint32_t k_empty(int s) const { return bar0 + 8u * (S + s); }
-  __device__ uint32_t v_full(int s) const { return bar0 + 8u * (2 * S + s); }
-  __device__ uint32_t v_empty(int s) const { return bar0 + 8u * (3 * S + s); }
-  __device__ uint32_t q_full() const { return bar0 + 8u * (4 * S); }
-  __device__ uint32_t q_empty() const { return bar0 + 8u * (4 * S + 1); }
+  // K and V of key tile g, on ring index g % KS (V slot g % VS)
+  __device__ uint32_t kv_full(int s) const { return bar0 + 8u * s; }
+  __device__ uint32_t k_empty(int s) const { return bar0 + 8u * (KS + s); }
+  __device__ uint32_t v_empty(int s) const { return bar0 + 8u * (2 * KS + s); }
+  __device__ uint32_t q_full() const { return bar0 + 8u * kB; }
+  __device__ uint32_t q_empty() const { return bar0 + 8u * (kB + 1); }
   // per S buffer b: the scores of its next tile are in (s_full), its P is
   // written (p_full, 4 arrivals).  A buffer's next scores wait for the P.V of
   // its previous P, so neither barrier can run two phases ahead of its waiter.
-  __device__ uint32_t s_full(int b) const { return bar0 + 8u * (4 * S + 2 + b); }
-  __device__ uint32_t p_full(int b) const { return bar0 + 8u * (4 * S + 4 + b); }
+  __device__ uint32_t s_full(int b) const { return bar0 + 8u * (kB + 2 + b); }
+  __device__ uint32_t p_full(int b) const { return bar0 + 8u * (kB + 4 + b); }
   // one completion per P.V (the softmax waits on it only before rescaling O)
-  __device__ uint32_t pv_done() const { return bar0 + 8u * (4 * S + 6); }
-  __device__ uint32_t o_final() const { return bar0 + 8u * (4 * S + 7); }
-  __device__ uint32_t drain() const { return bar0 + 8u * (4 * S + 8); }
+  __device__ uint32_t pv_done() const { return bar0 + 8u * (kB + 6); }
+  __device__ uint32_t o_final() const { return bar0 + 8u * (kB + 7); }
+  __device__ uint32_t drain() const { return bar0 + 8u * (kB + 8); }
   __device__ uint8_t* mask_buf(int warp) const { return base + C::kOffMaskBuf + warp * kFMaskBufBytes; }
 };
 
@@ -213,13 +217,15 @@ __device__ __forceinline__ int f_item_of_round(int r, int n_items) {
 }
 
 // ------------------------------------------------------------------ producer
-// One thread.  Per key tile: the K pieces into the K ring, the V pieces into
-// the V ring.  A K slot is freed by the tile's QK^T products, a V slot by its
-// P.V products (two key tiles later).
+// One thread.  Per key tile g: the K pieces into K slot g % KS and the V
+// pieces into V slot g % VS, both completing kv_full(g % KS).  A K slot is
+// freed by its tile's QK^T products, a V slot by its P.V products.  At each
+// item start it also prefetches the item's Q rows into L2, so the softmax
+// warps' Q loads come from L2.
 template <int D>
 __device__ __forceinline__ void f_producer(const F32TcParams& P, const FSmem<D>& sm, int n_items) {
   using C = FCfg<D>;
-  constexpr int S = C::kStages;
+  constexpr int KS = C::kKStages, VS = C::kVStages;
   const CommonParams& p = P.c;
   const int kvp = p.B * p.Hkv;  // planes per piece in the workspace map
   int g = 0;
@@ -229,53 +235,56 @@ __device__ __forceinline__ void f_producer(const F32TcParams& P, const FSmem<D>&
     if (idx < 0) break;
     const FItem it = make_fitem(p, idx);
     if (it.N == 0) continue;
+    {
+      const int64_t rows = (int64_t)p.Sq - it.q0 < FM ? (int64_t)p.Sq - it.q0 : FM;
+      const float* qsrc = P.q + (((int64_t)it.b * p.Hq + it.h) * p.Sq + it.q0) * D;
+      bulk_prefetch_l2(qsrc, (uint32_t)(rows * D * 4));
+    }
     const int kv_plane = it.b * p.Hkv + it.kvh;
     for (int n = 0; n < it.N; ++n, ++g) {
-      const int st = g % S;
+      const int ks = g % KS, vs = g % VS;
       const int key0 = (it.tb + n) * FN;
-      if (g >= S && !mbar_wait(sm.k_empty(st), ((g / S) - 1) & 1, p.timeout_ns, p.status)) {
+      if (g >= KS && !mbar_wait(sm.k_empty(ks), ((g / KS) - 1) & 1, p.timeout_ns, p.status)) {
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(sm.k_full(st), C::kKTileBytes);
+      if (g >= VS && !mbar_wait(sm.v_empty(vs), ((g / VS) - 1) & 1, p.timeout_ns, p.status)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(sm.kv_full(ks), C::kKTileBytes + C::kVTileBytes);
       for (int pc = 0; pc < kKPieces; ++pc)
         for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d(sm.sK + st * C::kKTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_ws,
-                      sm.k_full(st), s * 64, key0, pc * kvp + kv_plane);
-      if (g >= S && !mbar_wait(sm.v_empty(st), ((g / S) - 1) & 1, p.timeout_ns, p.status)) {
-        ok = false;
-        break;
-      }
-      mbar_arrive_expect_tx(sm.v_full(st), C::kVTileBytes);
+          tma_load_3d(sm.sK + ks * C::kKTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_ws,
+                      sm.kv_full(ks), s * 64, key0, pc * kvp + kv_plane);
       for (int pc = 0; pc < kVPieces; ++pc)
         for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d(sm.sV + st * C::kVTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_ws,
-                      sm.v_full(st), s * 64, key0, (kKPieces + pc) * kvp + kv_plane);
+          tma_load_3d(sm.sV + vs * C::kVTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_ws,
+                      sm.kv_full(ks), s * 64, key0, (kKPieces + pc) * kvp + kv_plane);
     }
   }
   // Let every copy this thread started land before the CTA can exit.
-  for (int n = (g > S ? g - S : 0); n < g; ++n) {
-    mbar_wait(sm.k_full(n % S), (n / S) & 1, p.timeout_ns, p.status);
-    mbar_wait(sm.v_full(n % S), (n / S) & 1, p.timeout_ns, p.status);
-  }
+  for (int n = (g > KS ? g - KS : 0); n < g; ++n) mbar_wait(sm.kv_full(n % KS), (n / KS) & 1, p.timeout_ns, p.status);
 }
 
 // ------------------------------------------------------------------ MMA issuer
 // The whole warp runs this; elect.sync picks the issuing lane.  Step n of an
-// item: the P.V products of tile n - 2 (once its P is written), which frees
-// the S buffer n % 2, then the scores of tile n into it.  Tensor-core
-// operations of one thread run in issue order, so S(n) never overwrites a P
-// before its P.V read it.
+// item: the scores of tile n into S buffer n % 2 (once its K / V are in), then
+// the P.V products of tile n - 1 (once its P is written).  One barrier wait
+// sits between consecutive issue blocks, while the block before is still
+// queued on the tensor core.  S(n) overwrites the P of tile n - 2, whose P.V
+// this warp issued one step earlier (tensor-core operations of one thread run
+// in issue order).
 template <int D>
 __device__ __forceinline__ void f_mma(const F32TcParams& P, const FSmem<D>& sm, uint32_t tmem, int n_items) {
   using C = FCfg<D>;
-  constexpr int S = C::kStages;
+  constexpr int KS = C::kKStages, VS = C::kVStages;
   constexpr uint32_t id_qk = make_idesc_f16kind(true, FM, FN, false);
   constexpr uint32_t id_pv = make_idesc_f16kind(true, FM, D, true);
   constexpr uint32_t kQPiece = D / 2;  // tensor-memory columns per piece of Q
   const CommonParams& p = P.c;
-  int g0 = 0;       // ring position of the item's first key tile
-  int q_items = 0;  // items whose Q was consumed
+  int g0 = 0;          // ring position of the item's first key tile
+  int q_items = 0;     // items whose Q was consumed
   int pb[2] = {0, 0};  // P tiles consumed per S buffer (all items)
   bool ok = true;
   for (int r = 0; ok; ++r) {
@@ -286,39 +295,13 @@ __device__ __forceinline__ void f_mma(const F32TcParams& P, const FSmem<D>& sm, 
     if (!mbar_wait_warp(sm.q_full(), q_items & 1, p.timeout_ns, p.status)) break;
     ++q_items;
     tc_fence_after();
-    for (int n = 0; ok && n < it.N + 2; ++n) {
-      if (n >= 2) {
-        // O (+)= P_{n-2} V_{n-2}: p0 v0 + p0 v1 + p1 v0
-        const int m = n - 2;
-        const int gv = g0 + m;
-        if (!mbar_wait_warp(sm.p_full(m & 1), pb[m & 1] & 1, p.timeout_ns, p.status)) { ok = false; break; }
-        ++pb[m & 1];
-        if (!mbar_wait_warp(sm.v_full(gv % S), (gv / S) & 1, p.timeout_ns, p.status)) { ok = false; break; }
-        tc_fence_after();
-        // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B apart,
-        // 64-column blocks kSubBytes apart
-        const uint32_t vb = sm.sV + (gv % S) * C::kVTileBytes;
-        const uint64_t d0 = make_sdesc_sw128(vb, C::kSubBytes, 1024);
-        const uint64_t d1 = make_sdesc_sw128(vb + C::kPieceBytes, C::kSubBytes, 1024);
-        const uint32_t pa = tmem + kFColS + 64 * (m & 1);  // p0 in its first 32 columns, p1 in the next 32
-        // two K steps (16 keys each, 2048 bytes of V apart) per issue block
-#pragma unroll
-        for (int kk = 0; kk < FN / 16; kk += 2) {
-          const uint32_t o0 = (uint32_t)(kk * 2048) >> 4, o1 = (uint32_t)((kk + 1) * 2048) >> 4;
-          mma_ts6_elect(tmem + kFColO, pa + kk * 8, d0 + o0, pa + kk * 8, d1 + o0, pa + 32 + kk * 8, d0 + o0,
-                        pa + (kk + 1) * 8, d0 + o1, pa + (kk + 1) * 8, d1 + o1, pa + 32 + (kk + 1) * 8, d0 + o1,
-                        id_pv, (m == 0 && kk == 0) ? 0u : 1u);
-        }
-        tc_commit_elect(sm.v_empty(gv % S));
-        tc_commit_elect(sm.pv_done());
-        if (m == it.N - 1) tc_commit_elect(sm.o_final());  // the item's last P.V
-      }
+    for (int n = 0; ok && n <= it.N; ++n) {
       if (n < it.N) {
         // S_{n%2} = Q K_n^T: q0k0 + q0k1 + q1k0 + q0k2 + q1k1 + q2k0
         const int gs = g0 + n;
-        if (!mbar_wait_warp(sm.k_full(gs % S), (gs / S) & 1, p.timeout_ns, p.status)) { ok = false; break; }
+        if (!mbar_wait_warp(sm.kv_full(gs % KS), (gs / KS) & 1, p.timeout_ns, p.status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kb = sm.sK + (gs % S) * C::kKTileBytes;
+        const uint32_t kb = sm.sK + (gs % KS) * C::kKTileBytes;
         uint64_t kd[kKPieces];
 #pragma unroll
         for (int pc = 0; pc < kKPieces; ++pc) kd[pc] = make_sdesc_sw128(kb + pc * C::kPieceBytes, 16, 1024);
@@ -332,9 +315,34 @@ __device__ __forceinline__ void f_mma(const F32TcParams& P, const FSmem<D>& sm, 
                         q1, kd[1] + off16, q2, kd[0] + off16, id_qk, kk > 0 ? 1u : 0u);
         }
         tc_commit_elect(sm.s_full(n & 1));
-        tc_commit_elect(sm.k_empty(gs % S));
+        tc_commit_elect(sm.k_empty(gs % KS));
         // the item's last QK^T products are issued: Q may be replaced once they finish
         if (n == it.N - 1) tc_commit_elect(sm.q_empty());
+      }
+      if (n >= 1) {
+        // O (+)= P_{n-1} V_{n-1}: p0 v0 + p0 v1 + p1 v0
+        const int m = n - 1;
+        const int gv = g0 + m;
+        if (!mbar_wait_warp(sm.p_full(m & 1), pb[m & 1] & 1, p.timeout_ns, p.status)) { ok = false; break; }
+        ++pb[m & 1];
+        tc_fence_after();
+        // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B apart,
+        // 64-column blocks kSubBytes apart
+        const uint32_t vb = sm.sV + (gv % VS) * C::kVTileBytes;
+        const uint64_t d0 = make_sdesc_sw128(vb, C::kSubBytes, 1024);
+        const uint64_t d1 = make_sdesc_sw128(vb + C::kPieceBytes, C::kSubBytes, 1024);
+        const uint32_t pa = tmem + kFColS + 64 * (m & 1);  // p0 in its first 32 columns, p1 in the next 32
+        // two K steps (16 keys each, 2048 bytes of V apart) per issue block
+#pragma unroll
+        for (int kk = 0; kk < FN / 16; kk += 2) {
+          const uint32_t o0 = (uint32_t)(kk * 2048) >> 4, o1 = (uint32_t)((kk + 1) * 2048) >> 4;
+          mma_ts6_elect(tmem + kFColO, pa + kk * 8, d0 + o0, pa + kk * 8, d1 + o0, pa + 32 + kk * 8, d0 + o0,
+                        pa + (kk + 1) * 8, d0 + o1, pa + (kk + 1) * 8, d1 + o1, pa + 32 + (kk + 1) * 8, d0 + o1,
+                        id_pv, (m == 0 && kk == 0) ? 0u : 1u);
+        }
+        tc_commit_elect(sm.v_empty(gv % VS));
+        tc_commit_elect(sm.pv_done());
+        if (m == it.N - 1) tc_commit_elect(sm.o_final());  // the item's last P.V
       }
     }
     if (!ok) break;
@@ -374,11 +382,15 @@ template <int D>
 __device__ __forceinline__ void store_q_row(const CommonParams& p, const float* q, const FItem& it, int64_t qi,
                                             uint32_t tlane) {
   const float4* src = reinterpret_cast<const float4*>(q + (((int64_t)it.b * p.Hq + it.h) * p.Sq + qi) * D);
+  // the whole row in flight at once (D / 4 independent 16-byte loads)
+  float4 row[D / 4];
+#pragma unroll
+  for (int i = 0; i < D / 4; ++i) row[i] = qi < p.Sq ? __ldg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int ch = 0; ch < D / 32; ++ch) {
     float4 v[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = qi < p.Sq ? __ldg(src + ch * 8 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < 8; ++i) v[i] = row[ch * 8 + i];
     uint32_t pcs[kKPieces][16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -668,7 +680,6 @@ __device__ __forceinline__ void f_softmax(const F32TcParams& P, const FSmem<D>& 
 template <int D, bool SOFTCAP, bool MASK>
 __global__ void __launch_bounds__(kFThreads, 1) attn_fwd_f32tc_kernel(const __grid_constant__ F32TcParams P) {
   using C = FCfg<D>;
-  constexpr int S = C::kStages;
   const CommonParams& p = P.c;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   FSmem<D> sm;
@@ -683,12 +694,11 @@ __global__ void __launch_bounds__(kFThreads, 1) attn_fwd_f32tc_kernel(const __gr
   const int n_items = ((p.Sq + FM - 1) / FM) * p.B * p.Hq;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(sm.k_full(s), 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(sm.kv_full(s), 1);
       mbar_init(sm.k_empty(s), 1);
-      mbar_init(sm.v_full(s), 1);
-      mbar_init(sm.v_empty(s), 1);
     }
+    for (int s = 0; s < C::kVStages; ++s) mbar_init(sm.v_empty(s), 1);
     mbar_init(sm.q_full(), 4);  // one arrival per softmax warp
     mbar_init(sm.q_empty(), 1);
     for (int b = 0; b < 2; ++b) {
