@@ -103,7 +103,8 @@ def test_invalid_arguments(lib, case):
 
 UNSUPPORTED = {
     "bf16_d96": dict(D=96),
-    "f16_d256": dict(D=256, dtype=1),
+    "f16_d320": dict(D=320, dtype=1),
+    "f32_d256": dict(D=256, dtype=0),
     "f32_d129": dict(D=129, dtype=0),
     "misaligned_q": dict(q=Q + 8),
     "misaligned_out": dict(out=OUT + 2),
@@ -138,6 +139,7 @@ def test_splitkv_validation(lib):
     assert call_splitkv(lib, 2, lse=0x7C000002) == attn.ATTN_ERR_UNSUPPORTED
     assert lib.attn_splitkv_workspace_bytes(2, 4, 200, 64, 1) == 0
     assert call_splitkv(lib, 4, B=0) == attn.ATTN_OK
+    assert call_splitkv(lib, 4, D=256) == attn.ATTN_ERR_UNSUPPORTED  # D 256: attn_fwd only
 
 
 def test_valid_plane_counts_pass_validation_order(lib):

@@ -79,7 +79,7 @@ FEATURES = {
 }
 
 DTYPE_D = [("f32", 64), ("f32", 128), ("f32", 40), ("f32", 96), ("bf16", 64), ("bf16", 128),
-           ("f16", 64), ("f16", 128)]
+           ("f16", 64), ("f16", 128), ("bf16", 256), ("f16", 256)]
 
 
 @pytest.mark.parametrize("feature", list(FEATURES))
@@ -103,7 +103,7 @@ EDGES = {
 
 
 @pytest.mark.parametrize("edge", list(EDGES))
-@pytest.mark.parametrize("dtype,D", [("f32", 64), ("bf16", 128), ("f16", 64)])
+@pytest.mark.parametrize("dtype,D", [("f32", 64), ("bf16", 128), ("f16", 64), ("bf16", 256)])
 def test_edge(dtype, D, edge):
     run_and_check(_base(dtype, D, **EDGES[edge]), what=f"{edge} {dtype} D={D}")
 
@@ -140,6 +140,21 @@ def test_empty_batch_is_noop():
     k = torch.zeros(0, 1, 8, 64, dtype=torch.bfloat16, device="cuda")
     out = attn.attn_fwd(q, k, k)
     assert out.shape == (0, 2, 8, 64)
+
+
+def test_head_dim_256_long_rows():
+    """D = 256 (single-lane kernel): several query tiles, dozens of key tiles,
+    GQA, causal with ragged tails; and the ragged cache with non-finite garbage."""
+    run_and_check(_base("bf16", 256, Hq=8, Hkv=2, Sq=700, Sk=1400, kv_capacity=1500, causal=True))
+    run_and_check(_base("f16", 256, ragged=True, Sq=90, Sk=900, kv_capacity=900, causal=True,
+                        garbage="nonfinite", mask="per_batch", mask_neg_inf_frac=0.1))
+
+
+def test_head_dim_256_splitkv_unsupported():
+    q = torch.zeros(1, 2, 8, 256, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(attn.AttnError) as e:
+        attn.attn_fwd_splitkv(q, q, q, num_splits=2)
+    assert e.value.status == attn.ATTN_ERR_UNSUPPORTED
 
 
 def test_unsupported_head_dim_raises():

@@ -241,7 +241,11 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
     if (lse && !aligned(lse, 4)) return ATTN_ERR_UNSUPPORTED;
     if (lse && overlaps(lse, splitkv_rows(B, Hq, Sq) * 4, out, qbytes)) return ATTN_ERR_INVALID_ARG;
   }
-  if (dtype != ATTN_F32 && D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  // 16-bit: D 64 / 128 on every entry, D 256 on attn_fwd (the single-lane kernel)
+  const bool wide16 = dtype != ATTN_F32 && D == 256 && !splitkv_api;
+  if (dtype != ATTN_F32 && D != 64 && D != 128 && !wide16) return ATTN_ERR_UNSUPPORTED;
+  if ((wide16 || f32split) && (int64_t)((Sq + 127) / 128) * BHq > INT32_MAX)
+    return ATTN_ERR_INVALID_ARG;  // work items of the single-lane kernel
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
     return ATTN_ERR_UNSUPPORTED;
   if (mask && !aligned(mask, 4)) return ATTN_ERR_UNSUPPORTED;
@@ -306,13 +310,25 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
 
   cudaError_t e;
   if (f32split) {
-    F32TcParams fp{};
-    fp.q = static_cast<const float*>(q);
-    fp.ws = workspace;
-    fp.c = c;
-    int rc = encode_map(&fp.tmap_ws, workspace, true, kF32TcPlanesPerKv * (int64_t)B * Hkv, kv_capacity, D, 64);
+    // K / V pieces in the workspace: k0, k1, k2 then v0, v1, B * Hkv planes each
+    LaneParams lp{};
+    lp.q = q;
+    lp.c = c;
+    lp.v_plane0 = 3 * B * Hkv;
+    int rc = encode_map(&lp.tmap_k, workspace, true, kF32TcPlanesPerKv * (int64_t)B * Hkv, kv_capacity, D, 64);
     if (rc != ATTN_OK) return rc;
-    e = launch_attn_f32tc(fp, static_cast<const float*>(k), static_cast<const float*>(v), st);
+    lp.tmap_v = lp.tmap_k;
+    e = launch_attn_f32tc(lp, static_cast<const float*>(k), static_cast<const float*>(v), workspace, st);
+  } else if (wide16) {
+    const bool bf16 = dtype == ATTN_BF16;
+    LaneParams lp{};
+    lp.q = q;
+    lp.c = c;
+    lp.v_plane0 = 0;
+    int rc = encode_map(&lp.tmap_k, k, bf16, (int64_t)B * Hkv, kv_capacity, D, 64);
+    if (rc == ATTN_OK) rc = encode_map(&lp.tmap_v, v, bf16, (int64_t)B * Hkv, kv_capacity, D, 64);
+    if (rc != ATTN_OK) return rc;
+    e = launch_attn_lane16(lp, bf16, st);
   } else if (dtype == ATTN_F32) {
     F32Params fp{};
     fp.q = static_cast<const float*>(q);

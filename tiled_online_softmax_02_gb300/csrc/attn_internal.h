@@ -65,14 +65,18 @@ struct F32Params {
   CommonParams c;
 };
 
-// fp32 on the tensor cores: K / V split into bf16 pieces in a workspace
-// (k0, k1, k2, v0, v1, each [B, Hkv, kv_capacity, D]) read through one TMA
-// map over [5 * B * Hkv planes, kv_capacity rows, D]; Q (fp32) is split in
-// the kernel.
-struct F32TcParams {
-  CUtensorMap tmap_ws;  // box {64, 64, 1}, 128B swizzle
-  const float* q;
-  void* ws;
+// Single-lane tensor-core kernel (one query tile per CTA, Q in tensor
+// memory): fp32 inputs as bf16 pieces (K / V split into a workspace by a
+// pre-pass: k0, k1, k2, v0, v1, each [B, Hkv, kv_capacity, D], read through
+// one TMA map over [5 * B * Hkv planes, kv_capacity rows, D]), or bf16 / f16
+// inputs with D = 256 (maps over the caller's k and v).  K piece t of kv
+// plane i is plane t * B * Hkv + i of tmap_k; V piece t is plane
+// v_plane0 + t * B * Hkv + i of tmap_v.
+struct LaneParams {
+  CUtensorMap tmap_k;  // box {64, 64, 1}, 128B swizzle
+  CUtensorMap tmap_v;
+  const void* q;       // [B, Hq, Sq, D] fp32 or 16-bit, split / stored to tensor memory in the kernel
+  int v_plane0;
   CommonParams c;
 };
 
@@ -83,7 +87,8 @@ constexpr int kF32BlockM = 64;  // query rows per fp32 CTA
 // Launchers.  They assume validated parameters.
 cudaError_t launch_attn_tc(const TcParams& p, bool bf16, cudaStream_t stream);
 cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream);
-cudaError_t launch_attn_f32tc(const F32TcParams& p, const float* k, const float* v, cudaStream_t stream);
+cudaError_t launch_attn_f32tc(const LaneParams& p, const float* k, const float* v, void* ws, cudaStream_t stream);
+cudaError_t launch_attn_lane16(const LaneParams& p, bool bf16, cudaStream_t stream);
 // workspace bytes of the fp32 tensor-core path for B * Hkv * kv_capacity * D elements of K (and of V)
 size_t f32tc_workspace_bytes(int64_t kv_elems);
 constexpr int kF32TcPlanesPerKv = 5;  // k0, k1, k2, v0, v1

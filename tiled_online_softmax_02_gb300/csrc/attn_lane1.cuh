@@ -1,0 +1,818 @@
+#pragma once
+// attn_lane1.cuh -- single-lane tensor-core attention forward for sm_103a:
+// one softmax warpgroup per CTA, Q in tensor memory, two S buffers.  Used
+// where the ping-pong tile kernel's tensor-memory layout does not fit:
+//   - fp32 inputs as error-compensated bf16 pieces (attn_f32tc.cu, D 64 /
+//     128): Q and K in three pieces, P and V in two, six products for QK^T
+//     and three for P.V;
+//   - bf16 / f16 inputs with D = 256 (attn_lane16.cu): one piece each.
+//
+// The method is the tiled online softmax of "onnx-runtime-ep-cuda
+// 0.1.0-dev.5, src/kernels/flash_attention.rs" (module doc and
+// `flash_attention_body`): scores of one key tile at a time, running row
+// max and denominator, O rescaled when the max moves.  Work item = one
+// 128-row query tile of one (b, h); its 64-key tiles run in order through
+// two S buffers.
+//   warps 0-3   softmax: thread = query row.  At each item start they write
+//               the item's Q rows (split into pieces for fp32) to tensor memory.
+//   warp 4      TMA producer: the K pieces of key tile g into K slot g % KS and
+//               the V pieces into V slot g % VS, one barrier per tile; it also
+//               prefetches each item's Q block into L2.
+//   warp 5      MMA issuer (converged warp, elect.sync) and owner of tensor
+//               memory.  Step n of an item: S_{n%2} = Q K_n^T, then
+//               O += P_{n-1} V_{n-1}.  S(n) overwrites the P of tile n - 2, whose
+//               P.V this warp issued one step earlier (tensor-core operations of
+//               one thread run in issue order).
+// Tensor memory (512 columns): Q pieces [0, KP D/2), S_0 / S_1 (64 columns
+// each) from kColS, O (D columns) from kColS + 128; P_b over S_b (as VP
+// bf16 / f16 pieces of 32 columns).  Every barrier wait is bounded; a timeout
+// sets ATTN_ERR_TIMEOUT in the device status word and the kernel drains and
+// exits.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "device_common.cuh"
+
+namespace gb300_attn {
+namespace lane1 {
+
+constexpr int FM = 128;          // query rows per item
+constexpr int FN = 64;           // keys per key tile
+constexpr int kThreads = 192;    // 4 softmax warps + producer + MMA
+constexpr int kTmaWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;  // keep the old max while it is within 2^8
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kMaskBufBytes = 32 * 32 * 4;  // per softmax warp: 32 rows x 32 keys of f32
+
+// Input kinds.
+constexpr int kInF32Split = 0;  // fp32 q / k / v, K / V pre-split in a workspace, fp32 out
+constexpr int kInF16 = 1;
+constexpr int kInBF16 = 2;
+
+template <int IN>
+struct In {
+  static constexpr int KP = IN == kInF32Split ? 3 : 1;   // pieces of Q and K
+  static constexpr int VP = IN == kInF32Split ? 2 : 1;   // pieces of P and V
+  static constexpr bool kBF16 = IN != kInF16;            // MMA operand type (pieces are bf16)
+};
+
+template <int D, int IN>
+struct Cfg {
+  static constexpr int KP = In<IN>::KP, VP = In<IN>::VP;
+  static constexpr int kSub = D / 64;                          // 128-byte column blocks per row
+  static constexpr uint32_t kSubBytes = FN * 128;              // [64 rows][64 cols] of 16-bit
+  static constexpr uint32_t kPieceBytes = kSub * kSubBytes;    // one piece of one tile
+  static constexpr uint32_t kKTileBytes = KP * kPieceBytes;
+  static constexpr uint32_t kVTileBytes = VP * kPieceBytes;
+  // K and V of a key tile arrive together (one barrier); a V slot is freed
+  // a key tile later than its K slot, so V has one stage more
+  static constexpr int kKStages = kKTileBytes <= 24576 ? 4 : 2;
+  static constexpr int kVStages = kKStages + 1;
+  static constexpr uint32_t kOffK = 0;
+  static constexpr uint32_t kOffV = kOffK + kKStages * kKTileBytes;
+  static constexpr uint32_t kOffMaskBuf = kOffV + kVStages * kVTileBytes;
+  static constexpr uint32_t kOffBar = kOffMaskBuf + 4 * kMaskBufBytes;
+  // kv_full[KS], k_empty[KS], v_empty[VS], q_full, q_empty, s_full[2],
+  // p_full[2], pv_done, o_final, drain
+  static constexpr int kNumBars = 2 * kKStages + kVStages + 2 + 2 + 2 + 3;
+  static constexpr uint32_t kOffSlot = kOffBar + kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  // tensor memory columns
+  static constexpr uint32_t kQPiece = D / 2;                       // columns per piece of Q
+  static constexpr uint32_t kColQ = 0;
+  static constexpr uint32_t kColS = (KP * kQPiece + 63) / 64 * 64;  // + buffer * 64
+  static constexpr uint32_t kColO = kColS + 128;
+  static_assert(kColO + D <= kTmemCols, "tensor memory columns");
+};
+
+template <int D, int IN>
+struct Smem {
+  using C = Cfg<D, IN>;
+  static constexpr int KS = C::kKStages, VS = C::kVStages;
+  static constexpr int kB = 2 * KS + VS;  // first barrier after the rings
+  uint8_t* base;
+  uint32_t sK, sV, bar0;
+  // K and V of key tile g, on ring index g % KS (V slot g % VS)
+  __device__ uint32_t kv_full(int s) const { return bar0 + 8u * s; }
+  __device__ uint32_t k_empty(int s) const { return bar0 + 8u * (KS + s); }
+  __device__ uint32_t v_empty(int s) const { return bar0 + 8u * (2 * KS + s); }
+  __device__ uint32_t q_full() const { return bar0 + 8u * kB; }
+  __device__ uint32_t q_empty() const { return bar0 + 8u * (kB + 1); }
+  // per S buffer b: the scores of its next tile are in (s_full), its P is
+  // written (p_full, 4 arrivals).  A buffer's next scores wait for the P.V of
+  // its previous P, so neither barrier can run two phases ahead of its waiter.
+  __device__ uint32_t s_full(int b) const { return bar0 + 8u * (kB + 2 + b); }
+  __device__ uint32_t p_full(int b) const { return bar0 + 8u * (kB + 4 + b); }
+  // one completion per P.V (the softmax waits on it only before rescaling O)
+  __device__ uint32_t pv_done() const { return bar0 + 8u * (kB + 6); }
+  __device__ uint32_t o_final() const { return bar0 + 8u * (kB + 7); }
+  __device__ uint32_t drain() const { return bar0 + 8u * (kB + 8); }
+  __device__ uint8_t* mask_buf(int warp) const { return base + C::kOffMaskBuf + warp * kMaskBufBytes; }
+};
+
+// ------------------------------------------------------------------ pieces
+// bf16 pieces of fp32 values; each subtraction is exact in fp32.
+__device__ __forceinline__ float bf16_lo(uint32_t pair) { return __uint_as_float(pair << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t pair) { return __uint_as_float(pair & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t bf16_pair(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// (a, b) -> n pieces, each a packed bf16 pair (first value in the low half,
+// as the MMA's K order wants).
+template <int N>
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t (&out)[N]) {
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    out[k] = bf16_pair(a, b);
+    if (k + 1 < N) {
+      // (a, b) - piece, two lanes in one packed FMA
+      f2_split(ffma2(f2(bf16_lo(out[k]), bf16_hi(out[k])), f2(-1.0f, -1.0f), f2(a, b)), a, b);
+    }
+  }
+}
+
+// A pair of fp32 values rounded to the 16-bit type, packed (first value low).
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+// ------------------------------------------------------------------ work items
+// One 128-row query tile of one (b, h) and the 64-key tiles [tb, tb + N) its
+// rows can see.
+struct FItem {
+  int b, h, kvh;
+  int64_t q0;
+  BatchLimits L;
+  TileRange T;
+  int tb, N;
+};
+
+// Latest query tiles (longest causal rows) first; the heads of one kv group
+// are consecutive items, so their K / V tiles come from L2.
+__device__ __forceinline__ FItem make_fitem(const CommonParams& p, int idx) {
+  const int bh = p.B * p.Hq;
+  const int nqt = (p.Sq + FM - 1) / FM;
+  FItem it;
+  const int qt = nqt - 1 - idx / bh;
+  const int rem = idx - (idx / bh) * bh;
+  it.b = rem / p.Hq;
+  it.h = rem - it.b * p.Hq;
+  it.kvh = it.h / p.group;
+  it.q0 = (int64_t)qt * FM;
+  it.L = batch_limits(p, it.b);
+  it.T = tile_range(p, it.L, it.q0, FM, FN);
+  it.tb = it.T.t_begin;
+  it.N = it.T.t_end - it.T.t_begin;
+  return it;
+}
+
+// Static snake schedule over the persistent CTAs.
+__device__ __forceinline__ int f_item_of_round(int r, int n_items) {
+  const int G = gridDim.x;
+  const int c = blockIdx.x;
+  const int idx = r * G + ((r & 1) ? (G - 1 - c) : c);
+  return idx < n_items ? idx : -1;
+}
+
+// ------------------------------------------------------------------ producer
+// One thread.  Per key tile g: the K pieces into K slot g % KS and the V
+// pieces into V slot g % VS, both completing kv_full(g % KS).  A K slot is
+// freed by its tile's QK^T products, a V slot by its P.V products.  At each
+// item start it also prefetches the item's Q rows into L2, so the softmax
+// warps' Q loads come from L2.
+template <int D, int IN>
+__device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN>& sm, int n_items) {
+  using C = Cfg<D, IN>;
+  constexpr int KP = C::KP, VP = C::VP;
+  constexpr int KS = C::kKStages, VS = C::kVStages;
+  const CommonParams& p = P.c;
+  const int kvp = p.B * p.Hkv;  // planes per piece
+  int g = 0;
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int idx = f_item_of_round(r, n_items);
+    if (idx < 0) break;
+    const FItem it = make_fitem(p, idx);
+    if (it.N == 0) continue;
+    {
+      const int64_t rows = (int64_t)p.Sq - it.q0 < FM ? (int64_t)p.Sq - it.q0 : FM;
+      constexpr int kQElem = IN == kInF32Split ? 4 : 2;  // bytes per Q element
+      const uint8_t* qsrc = static_cast<const uint8_t*>(P.q) + (((int64_t)it.b * p.Hq + it.h) * p.Sq + it.q0) * D * kQElem;
+      bulk_prefetch_l2(qsrc, (uint32_t)(rows * D * kQElem));
+    }
+    const int kv_plane = it.b * p.Hkv + it.kvh;
+    for (int n = 0; n < it.N; ++n, ++g) {
+      const int ks = g % KS, vs = g % VS;
+      const int key0 = (it.tb + n) * FN;
+      if (g >= KS && !mbar_wait(sm.k_empty(ks), ((g / KS) - 1) & 1, p.timeout_ns, p.status)) {
+        ok = false;
+        break;
+      }
+      if (g >= VS && !mbar_wait(sm.v_empty(vs), ((g / VS) - 1) & 1, p.timeout_ns, p.status)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(sm.kv_full(ks), C::kKTileBytes + C::kVTileBytes);
+      for (int pc = 0; pc < KP; ++pc)
+        for (int s = 0; s < C::kSub; ++s)
+          tma_load_3d(sm.sK + ks * C::kKTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_k,
+                      sm.kv_full(ks), s * 64, key0, pc * kvp + kv_plane);
+      for (int pc = 0; pc < VP; ++pc)
+        for (int s = 0; s < C::kSub; ++s)
+          tma_load_3d(sm.sV + vs * C::kVTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_v,
+                      sm.kv_full(ks), s * 64, key0, P.v_plane0 + pc * kvp + kv_plane);
+    }
+  }
+  // Let every copy this thread started land before the CTA can exit.
+  for (int n = (g > KS ? g - KS : 0); n < g; ++n) mbar_wait(sm.kv_full(n % KS), (n / KS) & 1, p.timeout_ns, p.status);
+}
+
+// ------------------------------------------------------------------ MMA issuer
+// The whole warp runs this; elect.sync picks the issuing lane.  Step n of an
+// item: the scores of tile n into S buffer n % 2 (once its K / V are in), then
+// the P.V products of tile n - 1 (once its P is written).  One barrier wait
+// sits between consecutive issue blocks.  For inputs read straight from the
+// caller's cache (16-bit), V rows at or past the valid length may hold any
+// bits (NaN / Inf included): P is 0 there but 0 * NaN is not, so those rows
+// are zeroed in shared memory before the P.V products read them.
+template <int D, int IN>
+__device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm, uint32_t tmem, int n_items,
+                                      int lane) {
+  using C = Cfg<D, IN>;
+  constexpr int KS = C::kKStages, VS = C::kVStages;
+  constexpr int KP = C::KP, VP = C::VP;
+  constexpr bool kBF16 = In<IN>::kBF16;
+  constexpr uint32_t id_qk = make_idesc_f16kind(kBF16, FM, FN, false);
+  constexpr uint32_t id_pv = make_idesc_f16kind(kBF16, FM, D, true);
+  const CommonParams& p = P.c;
+  int g0 = 0;          // ring position of the item's first key tile
+  int q_items = 0;     // items whose Q was consumed
+  int pb[2] = {0, 0};  // P tiles consumed per S buffer (all items)
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int idx = f_item_of_round(r, n_items);
+    if (idx < 0) break;
+    const FItem it = make_fitem(p, idx);
+    if (it.N == 0) continue;
+    if (!mbar_wait_warp(sm.q_full(), q_items & 1, p.timeout_ns, p.status)) break;
+    ++q_items;
+    tc_fence_after();
+    int64_t zero_from = it.L.lsk < (int64_t)p.Sk ? it.L.lsk : (int64_t)p.Sk;
+    if (zero_from < 0) zero_from = 0;
+    for (int n = 0; ok && n <= it.N; ++n) {
+      if (n < it.N) {
+        // S_{n%2} = Q K_n^T (pieces: q0k0 + q0k1 + q1k0 + q0k2 + q1k1 + q2k0)
+        const int gs = g0 + n;
+        if (!mbar_wait_warp(sm.kv_full(gs % KS), (gs / KS) & 1, p.timeout_ns, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kb = sm.sK + (gs % KS) * C::kKTileBytes;
+        const uint32_t sd = tmem + C::kColS + 64 * (n & 1);
+        if constexpr (KP == 3) {
+          uint64_t kd[3];
+#pragma unroll
+          for (int pc = 0; pc < 3; ++pc) kd[pc] = make_sdesc_sw128(kb + pc * C::kPieceBytes, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // K step kk: 32 bytes into a 128-byte row, 64-column blocks kSubBytes apart
+            const uint32_t off16 = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
+            const uint32_t q0 = tmem + C::kColQ + kk * 8, q1 = q0 + C::kQPiece, q2 = q0 + 2 * C::kQPiece;
+            mma_ts6_elect(sd, q0, kd[0] + off16, q0, kd[1] + off16, q1, kd[0] + off16, q0, kd[2] + off16,
+                          q1, kd[1] + off16, q2, kd[0] + off16, id_qk, kk > 0 ? 1u : 0u);
+          }
+        } else {
+          const uint64_t kd = make_sdesc_sw128(kb, 16, 1024);
+          // K steps 4s..4s+3 lie in 64-column block s
+#pragma unroll
+          for (int s = 0; s < D / 64; ++s) {
+            const uint32_t o = (s * C::kSubBytes) >> 4;
+            const uint32_t q = tmem + C::kColQ + s * 32;
+            mma_ts4_elect(sd, q, kd + o, q + 8, kd + o + 2, q + 16, kd + o + 4, q + 24, kd + o + 6, id_qk,
+                          s > 0 ? 1u : 0u);
+          }
+        }
+        tc_commit_elect(sm.s_full(n & 1));
+        tc_commit_elect(sm.k_empty(gs % KS));
+        // the item's last QK^T products are issued: Q may be replaced once they finish
+        if (n == it.N - 1) tc_commit_elect(sm.q_empty());
+      }
+      if (n >= 1) {
+        // O (+)= P_{n-1} V_{n-1} (pieces: p0 v0 + p0 v1 + p1 v0)
+        const int m = n - 1;
+        const int gv = g0 + m;
+        if (!mbar_wait_warp(sm.p_full(m & 1), pb[m & 1] & 1, p.timeout_ns, p.status)) { ok = false; break; }
+        ++pb[m & 1];
+        const uint32_t vb = sm.sV + (gv % VS) * C::kVTileBytes;
+        if constexpr (IN != kInF32Split) {
+          const int64_t key0 = (int64_t)(it.tb + m) * FN;
+          if (zero_from < key0 + FN && zero_from < (int64_t)p.kv_capacity) {
+            const int r0 = zero_from > key0 ? (int)(zero_from - key0) : 0;
+            const int chunks = (FN - r0) * 8;  // 16-byte chunks of whole 128-byte rows
+            for (int s = 0; s < C::kSub; ++s) {
+              uint8_t* blk = sm.base + C::kOffV + (gv % VS) * C::kVTileBytes + s * C::kSubBytes;
+              for (int c = lane; c < chunks; c += 32)
+                *reinterpret_cast<uint4*>(blk + (size_t)(r0 + (c >> 3)) * 128 + (c & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        tc_fence_after();
+        // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B apart,
+        // 64-column blocks kSubBytes apart
+        const uint64_t d0 = make_sdesc_sw128(vb, C::kSubBytes, 1024);
+        const uint32_t pa = tmem + C::kColS + 64 * (m & 1);  // P piece t over 32 columns from pa + 32 t
+        if constexpr (VP == 2) {
+          const uint64_t d1 = make_sdesc_sw128(vb + C::kPieceBytes, C::kSubBytes, 1024);
+          // two K steps (16 keys each, 2048 bytes of V apart) per issue block
+#pragma unroll
+          for (int kk = 0; kk < FN / 16; kk += 2) {
+            const uint32_t o0 = (uint32_t)(kk * 2048) >> 4, o1 = (uint32_t)((kk + 1) * 2048) >> 4;
+            mma_ts6_elect(tmem + C::kColO, pa + kk * 8, d0 + o0, pa + kk * 8, d1 + o0, pa + 32 + kk * 8, d0 + o0,
+                          pa + (kk + 1) * 8, d0 + o1, pa + (kk + 1) * 8, d1 + o1, pa + 32 + (kk + 1) * 8,
+                          d0 + o1, id_pv, (m == 0 && kk == 0) ? 0u : 1u);
+          }
+        } else {
+          mma_ts4_elect(tmem + C::kColO, pa, d0, pa + 8, d0 + 128, pa + 16, d0 + 256, pa + 24, d0 + 384, id_pv,
+                        m == 0 ? 0u : 1u);
+        }
+        tc_commit_elect(sm.v_empty(gv % VS));
+        tc_commit_elect(sm.pv_done());
+        if (m == it.N - 1) tc_commit_elect(sm.o_final());  // the item's last P.V
+      }
+    }
+    if (!ok) break;
+    g0 += it.N;
+  }
+  // Wait for every MMA this warp issued before tensor memory is freed.
+  tc_commit_elect(sm.drain());
+  mbar_wait_warp(sm.drain(), 0, p.timeout_ns, p.status);
+}
+
+// ------------------------------------------------------------------ softmax
+__device__ __forceinline__ float max64(const float (&x)[FN]) {
+  float m[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = fmaxf(x[k], x[k + 8]);
+#pragma unroll
+  for (int i = 16; i < FN; i += 16)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m[k] = fmax3(m[k], x[i + k], x[i + 8 + k]);
+  return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], fmax3(m[5], m[6], m[7])));
+}
+
+__device__ __forceinline__ float min64(const float (&x)[FN]) {
+  float m[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = fminf(x[k], x[k + 8]);
+#pragma unroll
+  for (int i = 16; i < FN; i += 16)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m[k] = fmin3(m[k], x[i + k], x[i + 8 + k]);
+  return fminf(fmin3(m[0], m[1], m[2]), fmin3(m[3], m[4], fmin3(m[5], m[6], m[7])));
+}
+
+// This thread's Q row in tensor memory: piece t over columns [t D/2,
+// (t+1) D/2), column c holding d = 2c, 2c + 1.  fp32 rows are split into KP
+// bf16 pieces; 16-bit rows are stored as they are.
+template <int D, int IN>
+__device__ __forceinline__ void store_q_row(const CommonParams& p, const void* q, const FItem& it, int64_t qi,
+                                            uint32_t tlane) {
+  using C = Cfg<D, IN>;
+  const int64_t row = ((int64_t)it.b * p.Hq + it.h) * p.Sq + qi;
+  if constexpr (IN == kInF32Split) {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(q) + row * D);
+    // the whole row in flight at once (D / 4 independent 16-byte loads)
+    float4 rowv[D / 4];
+#pragma unroll
+    for (int i = 0; i < D / 4; ++i) rowv[i] = qi < p.Sq ? __ldg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t pcs[C::KP][16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 v = rowv[ch * 8 + i];
+        uint32_t a[C::KP], b[C::KP];
+        split_pair<C::KP>(v.x, v.y, a);
+        split_pair<C::KP>(v.z, v.w, b);
+#pragma unroll
+        for (int t = 0; t < C::KP; ++t) {
+          pcs[t][2 * i] = a[t];
+          pcs[t][2 * i + 1] = b[t];
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < C::KP; ++t) tmem_st16(tlane + C::kColQ + t * C::kQPiece + ch * 16, pcs[t]);
+    }
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(q) + row * D);
+    uint4 rowv[D / 8];
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) rowv[i] = qi < p.Sq ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = rowv[ch * 4 + i];
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+      }
+      tmem_st16(tlane + C::kColQ + ch * 16, w);
+    }
+  }
+}
+
+// Mask block of one warp -- 32 rows by the 64 keys [key0, key0 + 64) -- into
+// x of the lane that owns each row (natural units; 0 outside).  Each
+// instruction loads 4 rows x 128 contiguous bytes; a 4 KB per-warp buffer
+// (16-byte chunks XOR-swizzled by row) turns rows into lanes.  vec4 needs
+// 16-byte aligned mask rows (Sk % 4 == 0).
+__device__ __forceinline__ void mask_rows64(float (&x)[FN], const float* mwarp, int nrows, int Sk, int key0,
+                                            bool vec4, uint8_t* buf, int lane) {
+  const int rsub = lane >> 3;
+  const int csub = lane & 7;
+#pragma unroll
+  for (int k = 0; k < FN / 32; ++k) {
+    float4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int row = 4 * i + rsub;
+      const int key = key0 + 32 * k + 4 * csub;
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float* src = mwarp + (int64_t)row * Sk + key;
+      if (vec4) {
+        if (row < nrows && key + 3 < Sk) t = __ldg(reinterpret_cast<const float4*>(src));
+      } else if (row < nrows) {
+        if (key + 0 < Sk) t.x = __ldg(src + 0);
+        if (key + 1 < Sk) t.y = __ldg(src + 1);
+        if (key + 2 < Sk) t.z = __ldg(src + 2);
+        if (key + 3 < Sk) t.w = __ldg(src + 3);
+      }
+      v[i] = t;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int row = 4 * i + rsub;
+      *reinterpret_cast<float4*>(buf + row * 128 + ((csub ^ (row & 7)) << 4)) = v[i];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float4 t = *reinterpret_cast<const float4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4));
+      x[32 * k + 4 * c + 0] = t.x;
+      x[32 * k + 4 * c + 1] = t.y;
+      x[32 * k + 4 * c + 2] = t.z;
+      x[32 * k + 4 * c + 3] = t.w;
+    }
+    __syncwarp();
+  }
+}
+
+// Warps 0-3: thread = one query row of the item.
+template <int D, int IN, bool SOFTCAP, bool MASK>
+__device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>& sm, uint32_t tmem, int n_items,
+                                          int warp, int lane) {
+  using C = Cfg<D, IN>;
+  constexpr bool kF32 = IN == kInF32Split;
+  const CommonParams& p = P.c;
+  const int row = warp * 32 + lane;
+  const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
+  const uint32_t o_addr = tlane + C::kColO;
+  int sb[2] = {0, 0};  // S tiles consumed per buffer (all items)
+  int tiles = 0;       // key tiles consumed (all items): P.V completions to wait for
+  int qn = 0;          // items whose Q was stored
+  int on = 0;          // o_final completions
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int idx = f_item_of_round(r, n_items);
+    if (idx < 0) break;
+    const FItem it = make_fitem(p, idx);
+    const int64_t qi = it.q0 + row;
+    const int64_t row_id = ((int64_t)it.b * p.Hq + it.h) * p.Sq + qi;
+    const int64_t obase = p.out_layout == 0 ? row_id * D : (((int64_t)it.b * p.Sq + qi) * p.Hq + it.h) * D;
+    // the output row as 16-byte units: 4 fp32 or 8 16-bit values each
+    uint4* orow = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + obase * (kF32 ? 4 : 2));
+    if (it.N == 0) {
+      // no visible key for any row of the tile: the rows are 0
+      if (qi < p.Sq) {
+#pragma unroll 4
+        for (int i = 0; i < D / (kF32 ? 4 : 8); ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      continue;
+    }
+    // Q of this item into tensor memory once the previous item's QK^T finished
+    if (qn > 0 && !mbar_wait_warp(sm.q_empty(), (qn - 1) & 1, p.timeout_ns, p.status)) { ok = false; break; }
+    ++qn;
+    store_q_row<D, IN>(p, P.q, it, qi, tlane);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.q_full());
+
+    const RowLimits R = row_limits(p, it.L, qi);
+    const float* mwarp = nullptr;
+    int mrows = 0;
+    if constexpr (MASK) {
+      int64_t plane = 0;
+      if (p.mask_planes == p.B) plane = it.b;
+      else if (p.mask_planes == p.B * p.Hq) plane = (int64_t)it.b * p.Hq + it.h;
+      const int64_t qw0 = qi - lane;
+      mwarp = p.mask + (plane * p.Sq + (qw0 < p.Sq ? qw0 : 0)) * (int64_t)p.Sk;
+      mrows = qw0 < p.Sq ? (int)min((int64_t)32, (int64_t)p.Sq - qw0) : 0;
+    }
+    const float xs = SOFTCAP ? p.sc_out : p.scale_log2;  // brings a raw x to log2 units
+    float m_run = -INFINITY;  // running max, log2 units
+    float l_run = 0.0f;
+    for (int n = 0; n < it.N; ++n, ++tiles) {
+      const int bsel = n & 1;
+      const uint32_t s_addr = tlane + C::kColS + 64 * bsel;
+      const int64_t key0 = (int64_t)(it.tb + n) * FN;
+      float x[FN];
+      if constexpr (MASK)
+        mask_rows64(x, mwarp, mrows, p.Sk, (int)key0, p.mask_vec4 != 0, sm.mask_buf(warp), lane);
+      if (!mbar_wait_warp(sm.s_full(bsel), sb[bsel] & 1, p.timeout_ns, p.status)) { ok = false; break; }
+      ++sb[bsel];
+      tc_fence_after();
+      const bool need_mask = !(key0 >= it.T.full_lo && key0 + FN <= it.T.full_hi);
+      bool scaled = false;
+      {
+        uint32_t sr[2][32];
+        tmem_ld32(s_addr, sr[0]);
+        tmem_ld32(s_addr + 32, sr[1]);
+        tmem_wait_ld();
+        if constexpr (MASK) {
+          const uint64_t le2 = f2(kLog2e, kLog2e);
+          if constexpr (SOFTCAP) {
+            const uint64_t in2 = f2(p.sc_in, p.sc_in), out2 = f2(p.sc_out, p.sc_out);
+#pragma unroll
+            for (int i = 0; i < FN; i += 2) {
+              float a0, a1;
+              f2_split(fmul2(f2(__uint_as_float(sr[i >> 5][i & 31]), __uint_as_float(sr[i >> 5][(i & 31) + 1])), in2),
+                       a0, a1);
+              f2_split(ffma2(f2(fast_tanh(a0), fast_tanh(a1)), out2, fmul2(f2(x[i], x[i + 1]), le2)), x[i], x[i + 1]);
+            }
+          } else {
+            const uint64_t sc2 = f2(p.scale_log2, p.scale_log2);
+#pragma unroll
+            for (int i = 0; i < FN; i += 2) {
+              const uint64_t sv =
+                  fmul2(f2(__uint_as_float(sr[i >> 5][i & 31]), __uint_as_float(sr[i >> 5][(i & 31) + 1])), sc2);
+              f2_split(ffma2(f2(x[i], x[i + 1]), le2, sv), x[i], x[i + 1]);
+            }
+          }
+          scaled = true;
+        } else if constexpr (SOFTCAP) {
+          const uint64_t in2 = f2(p.sc_in, p.sc_in);
+#pragma unroll
+          for (int i = 0; i < FN; i += 2) {
+            float a0, a1;
+            f2_split(fmul2(f2(__uint_as_float(sr[i >> 5][i & 31]), __uint_as_float(sr[i >> 5][(i & 31) + 1])), in2),
+                     a0, a1);
+            x[i] = fast_tanh(a0);
+            x[i + 1] = fast_tanh(a1);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < FN; ++i) x[i] = __uint_as_float(sr[i >> 5][i & 31]);
+        }
+      }
+      if (need_mask) {
+        // structural limits of this row: keys outside [lo, hi) become -inf
+        if (!scaled && !(xs > 0.0f)) {
+#pragma unroll
+          for (int i = 0; i < FN; ++i) x[i] *= xs;
+          scaled = true;
+        }
+        int lo = R.lo - (int)key0, hi = R.hi - (int)key0;
+        lo = lo < 0 ? 0 : (lo > FN ? FN : lo);
+        hi = hi < 0 ? 0 : (hi > FN ? FN : hi);
+        const uint32_t span = hi > lo ? (uint32_t)(hi - lo) : 0u;
+#pragma unroll
+        for (int i = 0; i < FN; ++i) x[i] = ((uint32_t)(i - lo) < span) ? x[i] : -INFINITY;
+      }
+      float m_tile;
+      if (scaled) {
+        m_tile = max64(x);
+      } else if (!need_mask) {
+        m_tile = (xs >= 0.0f ? max64(x) : min64(x)) * xs;
+      } else {
+        const float mr = max64(x);
+        m_tile = mr == -INFINITY ? -INFINITY : mr * xs;
+      }
+      // online update, keeping the old max unless it grew by more than 2^8
+      const float m_new = fmaxf(m_run, m_tile);
+      float alpha = 1.0f;
+      bool rescale = false;
+      float m_use = m_run;
+      if (m_run == -INFINITY) {
+        m_use = m_new;
+      } else if (m_new - m_run > kRescaleLog2) {
+        m_use = m_new;
+        alpha = fast_exp2(m_run - m_new);
+        rescale = true;
+      }
+      const float m_sub = (m_use == -INFINITY) ? 0.0f : m_use;
+      const float xmul = scaled ? 1.0f : xs;
+      const uint64_t mul2 = f2(xmul, xmul), sub2 = f2(-m_sub, -m_sub);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+      // P = 2^(x - m) over this row's S columns, 16 columns per store: for
+      // fp32 two bf16 pieces (p0 in columns [0, 32), p1 in [32, 64)), else
+      // rounded to the input type (columns [0, 32))
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t ph[16], pl[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float a0, a1;
+          f2_split(ffma2(f2(x[ch * 32 + 2 * i], x[ch * 32 + 2 * i + 1]), mul2, sub2), a0, a1);
+          const float e0 = fast_exp2(a0), e1 = fast_exp2(a1);
+          acc[i & 3] = fadd2(acc[i & 3], f2(e0, e1));
+          if constexpr (C::VP == 2) {
+            uint32_t pc[2];
+            split_pair<2>(e0, e1, pc);
+            ph[i] = pc[0];
+            pl[i] = pc[1];
+          } else {
+            ph[i] = pack16<In<IN>::kBF16>(e0, e1);
+          }
+        }
+        tmem_st16(s_addr + ch * 16, ph);
+        if constexpr (C::VP == 2) tmem_st16(s_addr + 32 + ch * 16, pl);
+      }
+      float sum, sum_hi;
+      f2_split(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), sum, sum_hi);
+      l_run = l_run * alpha + sum + sum_hi;
+      m_run = m_use;
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O must hold every earlier P.V of the item first: wait for the P.V of
+        // the previous key tile (the tiles - 1 -th completion of pv_done)
+        if (!mbar_wait_warp(sm.pv_done(), (tiles - 1) & 1, p.timeout_ns, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t a2 = f2(alpha, alpha);
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) {
+          uint32_t o[32];
+          tmem_ld32(o_addr + k * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float u0, u1;
+            f2_split(fmul2(f2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), u0, u1);
+            o[i] = __float_as_uint(u0);
+            o[i + 1] = __float_as_uint(u1);
+          }
+          tmem_st32(o_addr + k * 32, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.p_full(bsel));
+    }
+    if (!ok) break;
+
+    // ------------------------------------------------------------ epilogue
+    if (!mbar_wait_warp(sm.o_final(), on & 1, p.timeout_ns, p.status)) { ok = false; break; }
+    ++on;
+    tc_fence_after();
+    const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+    const uint64_t w2 = f2(inv_l, inv_l);
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) {
+      uint32_t o[32];
+      tmem_ld32(o_addr + k * 32, o);
+      tmem_wait_ld();
+      if (qi < p.Sq) {
+        float r[32];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2)
+          f2_split(fmul2(f2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), w2), r[i], r[i + 1]);
+        if constexpr (kF32) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            orow[k * 8 + i] = make_uint4(__float_as_uint(r[4 * i]), __float_as_uint(r[4 * i + 1]),
+                                         __float_as_uint(r[4 * i + 2]), __float_as_uint(r[4 * i + 3]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            orow[k * 4 + i] = make_uint4(pack16<In<IN>::kBF16>(r[8 * i], r[8 * i + 1]),
+                                         pack16<In<IN>::kBF16>(r[8 * i + 2], r[8 * i + 3]),
+                                         pack16<In<IN>::kBF16>(r[8 * i + 4], r[8 * i + 5]),
+                                         pack16<In<IN>::kBF16>(r[8 * i + 6], r[8 * i + 7]));
+        }
+      }
+    }
+    // The next item's first P.V (which overwrites O) waits for this
+    // warpgroup's next P, written after these reads (fence before arrive).
+    tc_fence_before();
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int D, int IN, bool SOFTCAP, bool MASK>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_lane1_kernel(const __grid_constant__ LaneParams P) {
+  using C = Cfg<D, IN>;
+  const CommonParams& p = P.c;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Smem<D, IN> sm;
+  sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm.base);
+  sm.sK = sbase + C::kOffK;
+  sm.sV = sbase + C::kOffV;
+  sm.bar0 = sbase + C::kOffBar;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm.base + C::kOffSlot);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_items = ((p.Sq + FM - 1) / FM) * p.B * p.Hq;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(sm.kv_full(s), 1);
+      mbar_init(sm.k_empty(s), 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) mbar_init(sm.v_empty(s), 1);
+    mbar_init(sm.q_full(), 4);  // one arrival per softmax warp
+    mbar_init(sm.q_empty(), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(sm.s_full(b), 1);
+      mbar_init(sm.p_full(b), 4);  // one arrival per softmax warp
+    }
+    mbar_init(sm.pv_done(), 1);
+    mbar_init(sm.o_final(), 1);
+    mbar_init(sm.drain(), 1);
+    mbar_init_fence();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&P.tmap_k);
+    tma_prefetch_desc(&P.tmap_v);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp == kTmaWarp) {
+    if (lane == 0) f_producer<D, IN>(P, sm, n_items);
+  } else if (warp == kMmaWarp) {
+    f_mma<D, IN>(P, sm, tmem, n_items, lane);
+  } else {
+    f_softmax<D, IN, SOFTCAP, MASK>(P, sm, tmem, n_items, warp, lane);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, int IN, bool SOFTCAP, bool MASK>
+cudaError_t launch_lane1_variant(const LaneParams& P, cudaStream_t stream) {
+  auto kernel = attn_fwd_lane1_kernel<D, IN, SOFTCAP, MASK>;
+  constexpr uint32_t smem = Cfg<D, IN>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int64_t n_items = (int64_t)((P.c.Sq + FM - 1) / FM) * P.c.B * P.c.Hq;
+  if (n_items > INT32_MAX) return cudaErrorInvalidConfiguration;
+  const int grid = (int)(n_items < sms ? n_items : sms);  // one persistent CTA per SM
+  kernel<<<grid, kThreads, smem, stream>>>(P);
+  return cudaGetLastError();
+}
+
+// One head dim and input kind: the four soft-cap / mask variants.
+template <int D, int IN>
+cudaError_t launch_lane1(const LaneParams& P, cudaStream_t stream) {
+  const bool sc = P.c.softcap > 0.0f;
+  const bool mk = P.c.mask != nullptr && P.c.mask_planes > 0;
+  if (sc && mk) return launch_lane1_variant<D, IN, true, true>(P, stream);
+  if (sc) return launch_lane1_variant<D, IN, true, false>(P, stream);
+  if (mk) return launch_lane1_variant<D, IN, false, true>(P, stream);
+  return launch_lane1_variant<D, IN, false, false>(P, stream);
+}
+
+}  // namespace lane1
+}  // namespace gb300_attn
