@@ -153,13 +153,16 @@ KERNEL_SOURCES = {
            "attn_tc_f16_d64.cu", "attn_tc_f16_d128.cu", "device_common.cuh", "attn_internal.h"),
     "f32": ("attn_f32.cu", "device_common.cuh", "attn_internal.h"),
     "decode": ("attn_decode.cu", "attn_decode.h", "device_common.cuh", "attn_internal.h"),
-    "f32tc": ("attn_f32tc.cu", "device_common.cuh", "attn_internal.h"),
+    "f32tc": ("attn_f32tc.cu", "attn_lane1.cuh", "device_common.cuh", "attn_internal.h"),
+    "lane16": ("attn_lane16.cu", "attn_lane1.cuh", "device_common.cuh", "attn_internal.h"),
 }
 
 
 def kernel_family(w: Workload, splitkv: bool = False, f32split: bool = False) -> str:
     if w.dtype == "f32":
         return "f32tc" if f32split else "f32"
+    if w.D == 256:
+        return "lane16"
     return "decode" if w.group * w.Sq <= 32 else "tc"
 
 

@@ -96,11 +96,15 @@ _add(4, Workload("ragged_kvcache_f16", B=8, Hq=32, Hkv=4, Sq=128, Sk=4096, kv_ca
 WORKLOAD_ORDER = list(WORKLOADS)
 
 # Shapes beyond the five: decode (one new token per sequence over a long
-# ragged cache), the case split-KV serves.
+# ragged cache), the case split-KV serves; and the GQA causal prefill with
+# head dim 256 (the wider head dim of the DiT page's kernel variants).
 EXTRA_WORKLOADS: dict[str, Workload] = {
     "decode_bf16": Workload("decode_bf16", B=8, Hq=32, Hkv=8, Sq=1, Sk=32768, kv_capacity=32768,
                             D=128, dtype="bf16", causal=True, ragged=True, garbage="finite",
                             seed=SEED_BASE + 10),
+    "gqa_causal_bf16_d256": Workload("gqa_causal_bf16_d256", B=2, Hq=32, Hkv=8, Sq=4096, Sk=4096,
+                                     kv_capacity=4096, D=256, dtype="bf16", causal=True,
+                                     seed=SEED_BASE + 11),
 }
 
 
