@@ -46,12 +46,14 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # attn_fwd_splitkv entry), with the hash of that kernel's sources at the time;
 # reported as null once those sources change.
 NCU_TRAFFIC = {
-    "gqa_causal_bf16": {"bytes_per_launch": 127573248, "source_hash": "edfb8aacc86b1fc1"},
-    "window_softcap_bf16": {"bytes_per_launch": 396639488, "source_hash": "edfb8aacc86b1fc1"},
-    "ragged_kvcache_f16": {"bytes_per_launch": 48539904, "source_hash": "edfb8aacc86b1fc1"},
-    "dit_f32": {"bytes_per_launch": 57720576, "source_hash": "0d1800f9038e6334"},
-    "decode_bf16": {"bytes_per_launch": 775716096, "source_hash": "12ff4660b69f949f"},
-    "decode_bf16+splitkv": {"bytes_per_launch": 776804352, "source_hash": "12ff4660b69f949f"},
+    "gqa_causal_bf16": {"bytes_per_launch": 127821824, "source_hash": "9e8ae31fdce6f12b"},
+    "window_softcap_bf16": {"bytes_per_launch": 396507648, "source_hash": "9e8ae31fdce6f12b"},
+    "ragged_kvcache_f16": {"bytes_per_launch": 48636160, "source_hash": "9e8ae31fdce6f12b"},
+    "dit_f32": {"bytes_per_launch": 57955840, "source_hash": "eae79b8b5b3f0a83"},
+    "dit_f32+f32split": {"bytes_per_launch": 76163072, "source_hash": "1734554f5cdad589"},
+    "decode_bf16": {"bytes_per_launch": 775665920, "source_hash": "aee60e800bf42d81"},
+    "decode_bf16+splitkv": {"bytes_per_launch": 777046272, "source_hash": "aee60e800bf42d81"},
+    "gqa_causal_bf16_d256": {"bytes_per_launch": 435266560, "source_hash": "6b4b5aabb41779d5"},
 }
 
 
