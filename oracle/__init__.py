@@ -10,7 +10,8 @@ module compiles it with gcc on first use and marshals numpy arrays into it.
 See that file's header for the definition it implements and the passages of
 "onnx-runtime-ep-cuda 0.1.0-dev.5, src/kernels/flash_attention.rs" and
 "pictor-kernels 0.1.0, src/gpu_backend/cuda_imagen_attn_kernels.rs" it
-follows.
+follows.  ``oracle.dsa`` is the oracle of the DSA indexer's index selection
+("onnx-runtime-ep-cuda 0.1.0-dev.6, src/kernels/dsa_index_select.rs").
 """
 from __future__ import annotations
 
@@ -46,6 +47,9 @@ def build(force: bool = False, extra_cflags: tuple[str, ...] = (), out_path: str
            *extra_cflags, "-o", tmp, _SRC, "-lm", "-lpthread"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, path)
+    if out_path is None and not extra_cflags:
+        from . import dsa  # the DSA indexer oracle, a library of its own
+        dsa.build(force=force)
     return path
 
 
