@@ -33,7 +33,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from tiled_online_softmax_02_gb300.inputs import (EXTRA_WORKLOADS, WORKLOADS, Workload,  # noqa: E402
+from tiled_online_softmax_02_gb300.inputs import (DSA_WORKLOADS, EXTRA_WORKLOADS,  # noqa: E402
+                                                  WORKLOADS, DsaWorkload, Workload, make_dsa_inputs,
                                                   make_inputs)
 
 ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}
@@ -157,6 +158,7 @@ KERNEL_SOURCES = {
     "decode": ("attn_decode.cu", "attn_decode.h", "device_common.cuh", "attn_internal.h"),
     "f32tc": ("attn_f32tc.cu", "attn_lane1.cuh", "device_common.cuh", "attn_internal.h"),
     "lane16": ("attn_lane16.cu", "attn_lane1.cuh", "device_common.cuh", "attn_internal.h"),
+    "dsa": ("dsa_select.cu", "attn_internal.h"),
 }
 
 
@@ -565,13 +567,230 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+# --------------------------------------------------- DSA indexer workloads
+DSA_METRIC = "DSA index select TFLOP/s (2*H*D per allowed cell)"
+
+
+def dsa_allowed_counts(x: dict) -> np.ndarray:
+    """Allowed keys per (b, s) row (bias above -1e30), [B, S]."""
+    return (x["bias"].numpy()[:, 0] > np.float32(-1e30)).sum(-1)
+
+
+def dsa_flops(w: DsaWorkload, cnt: np.ndarray) -> int:
+    return 2 * w.H * w.D * int(cnt.sum())
+
+
+def dsa_algorithmic_bytes(w: DsaWorkload) -> int:
+    es = 4 if w.dtype == "f32" else 2
+    rows = w.B * w.S
+    return (rows * w.H * w.D * es + w.B * w.T * w.D * es + rows * w.H * es   # query, key, weights
+            + rows * w.T * 4                                                # bias
+            + 2 * rows * w.T * 4                                            # scores written, read back
+            + rows * w.top_k * 8)                                           # indices
+
+
+def dsa_config(w: DsaWorkload, flops: int, n: int) -> dict:
+    return {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "D": w.D, "T": w.T, "top_k": w.top_k,
+            "bias": w.bias, "scale": w.softmax_scale, "weights_scale": w.weights_scale,
+            "seed": w.seed, "flops_per_step": flops, "parallelism": f"replicas x{n}",
+            "entry": "dsa_index_select",
+            "l2": "flushed between timed steps outside the timed events: a 256 MiB write, then a "
+                  "256 MiB read"}
+
+
+def dsa_oracle_sample(w: DsaWorkload, x: dict, budget_s: float, seed: int = 3):
+    """Times the fp32 oracle (oracle_dsa_rows, one thread) on seeded random
+    rows for about budget_s seconds.  Returns (flops, seconds, threads, rows)."""
+    from oracle import dsa
+    cnt = dsa_allowed_counts(x).reshape(-1)
+    arrs = [np.ascontiguousarray(x[n].float().numpy()) for n in ("query", "key", "weights", "bias")]
+    rng = np.random.default_rng(seed)
+    rows_total = w.B * w.S
+
+    def run(n):
+        rows = rng.integers(0, rows_total, n)
+        t = time.perf_counter()
+        dsa.rows(*arrs, rows, top_k=w.top_k, scale=w.softmax_scale, weights_scale=w.weights_scale)
+        return time.perf_counter() - t, 2 * w.H * w.D * int(cnt[rows].sum()), n
+
+    n, tot_s, tot_fl, tot_rows = 1, 0.0, 0, 0
+    while True:
+        dt, fl, r = run(n)
+        tot_s, tot_fl, tot_rows = tot_s + dt, tot_fl + fl, tot_rows + r
+        if dt >= 0.5 or tot_s + 4 * dt > budget_s:
+            break
+        n *= 4
+    left = budget_s - tot_s
+    per_row_s = tot_s / max(tot_rows, 1)
+    if left > 0.2 and per_row_s > 0:
+        dt, fl, r = run(int(max(1, min(1_000_000, left / per_row_s))))
+        tot_s, tot_fl, tot_rows = tot_s + dt, tot_fl + fl, tot_rows + r
+    return tot_fl, tot_s, 1, tot_rows
+
+
+def dsa_reference_arm(args, world, rank):
+    if rank != 0:
+        return 0
+    w = DSA_WORKLOADS[args.workload]
+    x = make_dsa_inputs(w)
+    flops = dsa_flops(w, dsa_allowed_counts(x))
+    per_step_budget = max(0.02, args.ref_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        dsa_oracle_sample(w, x, per_step_budget, seed=11)
+    tot_fl, tot_s, rows = 0, 0.0, 0
+    for i in range(args.steps):
+        fl, s, threads, r = dsa_oracle_sample(w, x, per_step_budget, seed=100 + i)
+        tot_fl, tot_s, rows = tot_fl + fl, tot_s + s, rows + r
+    value = tot_fl / tot_s / 1e12
+    sample = (f"{rows} seeded random (b, s) rows of {w.name}, oracle_dsa_rows, "
+              f"{args.steps} steps of ~{per_step_budget:.2f} s")
+    line = {"metric": DSA_METRIC, "impl": "reference", "value": value, "unit": "TFLOP/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_s * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded)", "config": dsa_config(w, flops, 1),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_dsa(args, world, rank, local):
+    import tiled_online_softmax_02_gb300 as attn
+    from tiled_online_softmax_02_gb300 import build as libbuild
+    if not libbuild.up_to_date() and rank == 0:
+        libbuild.build()
+    barrier(world)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = attn.load_library()
+    w = DSA_WORKLOADS[args.workload]
+    x = make_dsa_inputs(w)
+    flops = dsa_flops(w, dsa_allowed_counts(x))
+    abytes = dsa_algorithmic_bytes(w)
+    names = ("query", "key", "weights", "bias")
+    g = {n: x[n].to(dev) for n in names}
+    out = torch.empty((w.B, 1, w.S, w.top_k), dtype=torch.int64, device=dev)
+    ws = torch.empty(max(lib.dsa_index_select_workspace_bytes(w.B, w.S, w.T), 16), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def evict_l2():
+        flush.zero_()
+        flush_rd.max()
+
+    def step():
+        attn.dsa_index_select(g["query"], g["key"], g["weights"], g["bias"], top_k=w.top_k,
+                              scale=w.softmax_scale, weights_scale=w.weights_scale, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        evict_l2()
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local) if not args.no_clocks else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.6)
+    barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark(True)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        evict_l2()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    if clocks:
+        clocks.mark(False)
+    clock_info = clocks.stop() if clocks else None
+    kernel_s = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
+    max_s = max_over_ranks(kernel_s, world, dev)
+    value = replica_throughput(flops, args.steps, world, max_s)
+    avg_step_s = kernel_s / args.steps
+
+    # end to end through the public API with pinned host tensors
+    host = {n: x[n].pin_memory() for n in names}
+    host_out = torch.empty(out.shape, dtype=torch.int64, pin_memory=True)
+    h2d = sum(int(v.numel() * v.element_size()) for v in host.values())
+    d2h = int(host_out.numel() * host_out.element_size())
+
+    def e2e_step():
+        attn.dsa_index_select(host["query"], host["key"], host["weights"], host["bias"], top_k=w.top_k,
+                              scale=w.softmax_scale, weights_scale=w.weights_scale, out=host_out,
+                              workspace=ws)
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+    e2e_value = replica_throughput(flops, args.e2e_steps, world, e2e_s)
+    if rank != 0:
+        return 0
+
+    # The score kernel is bound by fp32 arithmetic on the CUDA cores: each
+    # multiply and add is its own instruction (the page fixes unfused fp32),
+    # so the ceiling is one FLOP per lane per clock.  The step time (both
+    # kernels of the call) is the denominator, so the fraction is a floor.
+    peaks, _ = read_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    peak = props.multi_processor_count * 128 * mhz * 1e6 / 1e12
+    achieved = flops / avg_step_s / 1e12
+    traffic = None
+    ent = NCU_TRAFFIC.get(w.name)
+    if ent and ent.get("source_hash") == kernel_source_hash("dsa"):
+        traffic = ent["bytes_per_launch"]
+    cpu = None
+    if not args.no_cpu_baseline:
+        fl, s, threads, rows = dsa_oracle_sample(w, x, args.cpu_seconds)
+        cpu = {"value": fl / s / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{rows} seeded random (b, s) rows of {w.name} ({fl / 1e9:.2f} GFLOP, {s:.1f} s), "
+                         f"fp32 oracle_dsa_rows"}
+    line = {
+        "metric": DSA_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_s * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded)", "config": dsa_config(w, flops, world),
+        "frac_of_peak": achieved / peak,
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": "derived: SMs x 128 fp32 lanes x 1 unfused op/clk x max SM clock",
+                     "kernel": "dsa_score_kernel + dsa_select_kernel (one call, timed together)",
+                     "algorithmic_bytes": abytes, "hbm_gbs": abytes / avg_step_s / 1e9},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": args.e2e_steps},
+        "cpu_baseline": cpu,
+        "gpu_launches": args.steps * 2,
+        "clocks": clock_info,
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(ALL_WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", choices=list(ALL_WORKLOADS) + list(DSA_WORKLOADS),
+                    default=DEFAULT_WORKLOAD)
     ap.add_argument("--splitkv", action="store_true",
                     help="time attn_fwd_splitkv (split count: --splits, else the library's choice)")
     ap.add_argument("--splits", type=int, default=0, help="split count for --splitkv (0: library)")
@@ -587,6 +806,10 @@ def main(argv=None):
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     world, rank, local = dist_setup()
     try:
+        if args.workload in DSA_WORKLOADS:
+            if args.impl == "reference":
+                return dsa_reference_arm(args, world, rank)
+            return run_dsa(args, world, rank, local)
         if args.impl == "reference":
             return reference_arm(args, world, rank)
         return run_ours(args, world, rank, local)

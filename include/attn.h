@@ -187,6 +187,50 @@ int attn_fwd_f32_split(const float *q, const float *k, const float *v, const flo
  * (three bf16 pieces of k, two of v); 0 for non-positive sizes. */
 size_t attn_f32_split_workspace_bytes(int B, int Hkv, int kv_capacity, int D);
 
+/*
+ * dsa_index_select -- sparse index selection of the DSA indexer.
+ *
+ * Defined by "onnx-runtime-ep-cuda 0.1.0-dev.6, src/kernels/dsa_index_select.rs"
+ * (module doc and score kernel).  For every batch b, query s and key t:
+ *   allowed = bias[b, 0, s, t] > -1e30
+ *   score   = sum over heads h = 0..H-1 of
+ *               max(scale * sum over d = 0..D-1 of q[b,s,h,d] * k[b,t,d], 0)
+ *               * (w[b,s,h] * weights_scale)
+ *             + bias[b, 0, s, t]
+ * computed in fp32, each multiply and add rounded separately, in exactly
+ * that order (d ascending, then h ascending); a NaN score becomes the
+ * positive quiet NaN.  out[b, 0, s, :] holds the min(#allowed, top_k)
+ * allowed keys with the largest scores (f32 total order: NaN above +inf,
+ * -0 below +0; ties to the lower index), in ascending order, then -1s.
+ * The scores run on the CUDA cores in that exact order: the result is an
+ * index set, and any other rounding could change it.
+ *
+ * Arguments (device pointers, caller-owned):
+ *   query    [B, S, H, D]   dtype;  key [B, T, D] dtype;  weights [B, S, H] dtype
+ *   bias     [B, 1, S, T]   f32
+ *   out      [B, 1, S, top_k] int64; must not overlap the inputs
+ *   B, S, T  >= 0 (B * S == 0: OK, nothing written; T == 0: every slot -1,
+ *            and key / bias may be NULL)
+ *   H        1..64 (more: ATTN_ERR_UNSUPPORTED);  D >= 1;  top_k >= 1
+ *   scale, weights_scale  finite and > 0
+ *   dtype    0 f32, 1 f16, 2 bf16 (query, key and weights share it)
+ *   workspace  at least dsa_index_select_workspace_bytes(B, S, T) bytes,
+ *            16-byte aligned, not overlapping any other argument (the fp32
+ *            scores); may be NULL when T == 0.  Calls that share a workspace
+ *            must not overlap on the GPU.
+ * Launches two kernels on `stream`; allocates and synchronises nothing.
+ * Errors: ATTN_ERR_INVALID_ARG (bad size, attribute, dtype, null or
+ * overlapping pointer, small workspace), ATTN_ERR_UNSUPPORTED (H > 64,
+ * misaligned pointers), ATTN_ERR_CUDA (launch failure).
+ */
+int dsa_index_select(const void *query, const void *key, const void *weights, const float *bias,
+                     int64_t *out, int B, int S, int H, int D, int T, int top_k, float scale,
+                     float weights_scale, int dtype, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/* Workspace bytes dsa_index_select needs: B * S * T * 4 (0 for non-positive sizes). */
+size_t dsa_index_select_workspace_bytes(int B, int S, int T);
+
 /* Size of the library-owned buffer attn_fwd_splitkv_noalloc uses (8 MiB). */
 #define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -24,7 +24,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(attn_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:attn|dsa)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
@@ -198,3 +198,67 @@ def test_f32_split_validation(lib):
     # B * Hkv beyond the TMA plane coordinates of the four pieces
     assert call_f32split(lib, ws=WS, ws_bytes=2**62, B=40000, Hq=40000, Hkv=40000, Sq=1, Sk=1,
                          cap=1) == attn.ATTN_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- dsa_index_select
+DQ, DK, DW, DB, DO, DWS = (0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000, 0x60000000)
+DSA_GOOD = dict(query=DQ, key=DK, weights=DW, bias=DB, out=DO, B=2, S=8, H=16, D=64, T=300, top_k=32,
+                scale=0.125, weights_scale=1.0, dtype=2, ws=DWS, ws_bytes=2 * 8 * 300 * 4)
+
+
+def call_dsa(lib, **kw):
+    a = dict(DSA_GOOD, **kw)
+    return lib.dsa_index_select(a["query"], a["key"], a["weights"], a["bias"], a["out"], a["B"], a["S"],
+                                a["H"], a["D"], a["T"], a["top_k"], a["scale"], a["weights_scale"],
+                                a["dtype"], a["ws"], a["ws_bytes"], None)
+
+
+def test_dsa_workspace_bytes(lib):
+    assert lib.dsa_index_select_workspace_bytes(2, 8, 300) == 2 * 8 * 300 * 4
+    assert lib.dsa_index_select_workspace_bytes(0, 8, 300) == 0
+    assert lib.dsa_index_select_workspace_bytes(2, 8, 0) == 0
+    assert lib.dsa_index_select_workspace_bytes(-1, 8, 300) == 0
+
+
+@pytest.mark.parametrize("case", [
+    dict(dtype=3), dict(dtype=-1), dict(B=-1), dict(S=-1), dict(T=-1), dict(H=0), dict(D=0), dict(top_k=0),
+    dict(scale=0.0), dict(scale=-1.0), dict(scale=math.inf), dict(scale=math.nan),
+    dict(weights_scale=0.0), dict(weights_scale=math.nan),
+    dict(query=None), dict(key=None), dict(weights=None), dict(bias=None), dict(out=None),
+    dict(T=0, key=None, bias=None, query=None),
+    dict(ws=None), dict(ws_bytes=2 * 8 * 300 * 4 - 1),
+    dict(out=DQ + 64), dict(out=DB), dict(ws=DK), dict(ws=DO - 16),
+    dict(B=2**20, S=2**20, T=2**20),
+])
+def test_dsa_invalid_arguments(lib, case):
+    assert call_dsa(lib, **case) == attn.ATTN_ERR_INVALID_ARG, case
+
+
+@pytest.mark.parametrize("case", [
+    dict(H=65), dict(query=DQ + 1), dict(key=DK + 2, dtype=0), dict(bias=DB + 2), dict(out=DO + 4),
+    dict(ws=DWS + 8),
+])
+def test_dsa_unsupported(lib, case):
+    assert call_dsa(lib, **case) == attn.ATTN_ERR_UNSUPPORTED, case
+
+
+def test_dsa_empty_problems_are_ok(lib):
+    assert call_dsa(lib, B=0) == attn.ATTN_OK
+    assert call_dsa(lib, S=0, query=None, out=None) == attn.ATTN_OK
+    assert call_dsa(lib, T=0, key=None, bias=None, ws=None, ws_bytes=0, H=65) == attn.ATTN_ERR_UNSUPPORTED
+
+
+def test_dsa_binding_rejects_bad_tensors():
+    import torch
+    q = torch.zeros(1, 2, 3, 8, dtype=torch.bfloat16)
+    k = torch.zeros(1, 5, 8, dtype=torch.bfloat16)
+    w = torch.zeros(1, 2, 3, dtype=torch.bfloat16)
+    b = torch.zeros(1, 1, 2, 5)
+    with pytest.raises(ValueError):
+        attn.dsa_index_select(q, k.float(), w, b, top_k=2, scale=1.0)       # mixed dtypes
+    with pytest.raises(ValueError):
+        attn.dsa_index_select(q, k, w, b.half(), top_k=2, scale=1.0)        # bias not f32
+    with pytest.raises(ValueError):
+        attn.dsa_index_select(q, k[:, :4], w, b, top_k=2, scale=1.0)        # T mismatch
+    with pytest.raises(ValueError):
+        attn.dsa_index_select(q[0], k, w, b, top_k=2, scale=1.0)            # rank

@@ -1,0 +1,264 @@
+"""GPU parity of the DSA indexer's sparse index selection (dsa_index_select)
+against the fp32 oracle: the selected indices must be identical (integer
+output) and the fp32 score of every allowed cell, read from the workspace,
+bit-identical (the page fixes the score arithmetic and order).  Cases: every
+input dtype, head counts on both sides of each register tier, head dims that
+are not a multiple of the 32-column chunk, ragged key tails, T = 0, top_k
+above / equal to / far above the allowed count, top_k = 1, fully masked rows,
+the -1e30 boundary, NaN / inf inputs, exact ties spanning threads, grid-stride
+loops, and the full-size prefill and decode workloads on sampled rows plus the
+selection of every row."""
+import numpy as np
+import pytest
+import torch
+
+import tiled_online_softmax_02_gb300 as attn
+from oracle import dsa
+from tiled_online_softmax_02_gb300.inputs import DSA_WORKLOADS, DsaWorkload, make_dsa_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    attn.load_library()
+    torch.cuda.set_device(0)
+
+
+def _w(**kw) -> DsaWorkload:
+    base = dict(name="case", B=2, S=37, H=16, D=64, T=700, top_k=64, dtype="bf16", bias="causal")
+    base.update(kw)
+    return DsaWorkload(**base)
+
+
+def run_gpu(w: DsaWorkload, x: dict, ws=None):
+    """Indices (numpy int64 [B, 1, S, top_k]) and the workspace tensor."""
+    dev = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
+    if ws is None:
+        ws = torch.empty(max(w.B * w.S * w.T * 4, 16), dtype=torch.uint8, device="cuda")
+    out = attn.dsa_index_select(dev["query"], dev["key"], dev["weights"], dev["bias"], top_k=w.top_k,
+                                scale=w.softmax_scale, weights_scale=w.weights_scale, workspace=ws)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), ws
+
+
+def gpu_score_bits(ws, w: DsaWorkload) -> np.ndarray:
+    n = w.B * w.S * w.T
+    return ws[: n * 4].view(torch.int32).cpu().numpy().view(np.uint32).reshape(w.B, w.S, w.T)
+
+
+def compare_indices(got: np.ndarray, exp: np.ndarray, what: str):
+    assert got.shape == exp.shape, (what, got.shape, exp.shape)
+    bad = np.argwhere((got != exp).reshape(-1, got.shape[-1]).any(-1)).reshape(-1)
+    if bad.size:
+        r = int(bad[0])
+        g, e = got.reshape(-1, got.shape[-1])[r], exp.reshape(-1, exp.shape[-1])[r]
+        diff = np.flatnonzero(g != e)
+        raise AssertionError(f"{what}: {bad.size} rows differ; row {r} first at slot {diff[0]}: "
+                             f"gpu {g[diff[:8]]} oracle {e[diff[:8]]}")
+
+
+def check(w: DsaWorkload, x: dict | None = None, scores: bool = True, what: str = ""):
+    x = make_dsa_inputs(w) if x is None else x
+    what = what or w.name
+    got, ws = run_gpu(w, x)
+    args = (x["query"], x["key"], x["weights"], x["bias"])
+    kw = dict(scale=w.softmax_scale, weights_scale=w.weights_scale)
+    if scores and w.T > 0:
+        sc, al = dsa.scores(*args, **kw)
+        gb, ob = gpu_score_bits(ws, w), sc.view(np.uint32)
+        bad = al.astype(bool) & (gb != ob)
+        if bad.any():
+            b, s, t = np.argwhere(bad)[0]
+            raise AssertionError(f"{what}: {int(bad.sum())} score cells differ; first (b={b}, s={s}, t={t}) "
+                                 f"gpu {gb[b, s, t]:#010x} oracle {ob[b, s, t]:#010x}")
+        exp = dsa.select(sc, al, w.top_k).reshape(w.B, 1, w.S, w.top_k)
+    else:
+        exp = dsa.index_select(*args, top_k=w.top_k, **kw)
+    compare_indices(got, exp, what)
+    return got, x
+
+
+# ---------------------------------------------------------------- dtype x heads x head dim
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("H", [1, 7, 16, 32, 33, 64])
+def test_heads_and_dtypes(dtype, H):
+    check(_w(dtype=dtype, H=H, D=72, S=19, T=600, top_k=96, seed=1000 + H), what=f"{dtype} H={H}")
+
+
+@pytest.mark.parametrize("D", [1, 31, 33, 100, 128, 192])
+def test_head_dims(D):
+    check(_w(D=D, H=20, S=23, T=530, seed=2000 + D), what=f"D={D}")
+
+
+@pytest.mark.parametrize("T", [1, 5, 255, 256, 257, 511, 1023])
+def test_key_tails(T):
+    check(_w(T=T, S=11, top_k=40, bias="random", seed=3000 + T), what=f"T={T}")
+
+
+@pytest.mark.parametrize("bias", ["causal", "causal_min", "ragged_causal", "random", "zeros"])
+def test_bias_modes(bias):
+    check(_w(bias=bias, B=3, S=29, T=777, seed=4000), what=bias)
+
+
+# ---------------------------------------------------------------- top_k edge cases
+@pytest.mark.parametrize("top_k", [1, 2, 63, 700, 701, 5000])
+def test_top_k(top_k):
+    check(_w(top_k=top_k, T=700, bias="random", seed=5000), what=f"top_k={top_k}")
+
+
+def test_empty_key_axis():
+    w = _w(T=0, top_k=9)
+    got, _ = check(w, scores=False)
+    assert (got == -1).all()
+
+
+def test_empty_rows():
+    w = _w(B=0)
+    got, _ = run_gpu(w, make_dsa_inputs(w))
+    assert got.shape == (0, 1, w.S, w.top_k)
+
+
+def test_fully_masked_rows():
+    w = _w(bias="random", seed=6000)
+    x = make_dsa_inputs(w)
+    x["bias"][0, 0, 3] = -np.inf
+    x["bias"][1, 0, 7] = -1e30
+    x["bias"][1, 0, 8] = float("nan")
+    got, _ = check(w, x, what="masked rows")
+    assert (got[0, 0, 3] == -1).all() and (got[1, 0, 7] == -1).all() and (got[1, 0, 8] == -1).all()
+
+
+def test_allow_boundary():
+    """bias == -1e30 (as f32) is not allowed; the next f32 above it is; the
+    most negative finite f32 and NaN are not; +inf is allowed."""
+    w = _w(bias="zeros", top_k=700, seed=6100)
+    x = make_dsa_inputs(w)
+    m30 = np.float32(-1e30)
+    above = np.nextafter(m30, np.float32(0))
+    b = x["bias"].numpy()
+    b[:, 0, :, 0::5] = m30
+    b[:, 0, :, 1::5] = above
+    b[:, 0, :, 2::5] = np.finfo(np.float32).min
+    b[:, 0, :, 3::5] = np.nan
+    b[:, 0, :, 4::10] = np.inf
+    got, _ = check(w, x, what="allow boundary")
+    sel = got[got >= 0]
+    assert set(np.unique(sel % 5)) <= {1, 4}
+
+
+# ---------------------------------------------------------------- special values and ties
+def test_nan_and_inf_inputs():
+    w = _w(dtype="f32", bias="random", S=17, T=600, seed=7000)
+    x = make_dsa_inputs(w)
+    x["weights"][0, 2, 5] = float("nan")          # a NaN weight: the whole row's scores are NaN
+    x["weights"][1, 4, 0] = float("inf")          # +inf weight: relu(dot) * inf (NaN where dot <= 0)
+    x["weights"][1, 5, 3] = float("-inf")
+    x["key"][0, 11] = float("inf")                # an inf key row: inf - inf inside some dots
+    x["key"][1, 40, 7] = float("nan")
+    x["query"][1, 9, 2, 0] = float("inf")
+    x["query"][0, 6, :, :] *= 3e37                # products overflow to inf
+    check(w, x, what="nan/inf")
+
+
+def test_exact_ties_across_threads():
+    """All weights zero: every allowed score equals its bias, so with a zero
+    bias the whole row ties and the lowest indices win; the tie block spans
+    many threads' key ranges."""
+    w = _w(bias="zeros", T=3000, top_k=1500, S=5, seed=7100)
+    x = make_dsa_inputs(w)
+    x["weights"].zero_()
+    got, _ = check(w, x, what="all tied")
+    assert (got[..., :1500] == np.arange(1500)).all()
+
+
+def test_duplicate_keys_tie():
+    check(_w(ties=True, bias="random", T=1200, top_k=333, seed=7200), what="duplicate keys")
+
+
+def test_quantised_values_tie():
+    """Integer-valued inputs give exactly representable scores with many
+    repeats; the radix threshold lands inside large tie groups."""
+    w = _w(dtype="f16", bias="zeros", T=2000, top_k=517, S=9, H=5, D=8, seed=7300)
+    x = make_dsa_inputs(w)
+    g = torch.Generator().manual_seed(7300)
+    x["query"] = torch.randint(-2, 3, x["query"].shape, generator=g).to(torch.float16)
+    x["key"] = torch.randint(-2, 3, x["key"].shape, generator=g).to(torch.float16)
+    x["weights"] = torch.randint(-1, 3, x["weights"].shape, generator=g).to(torch.float16)
+    check(w, x, what="quantised ties")
+
+
+def test_weights_scale_and_scale():
+    check(_w(scale=0.37, weights_scale=2.5, seed=7400), what="scales")
+
+
+# ---------------------------------------------------------------- grid-stride loops, reuse, streams
+def test_many_rows_grid_stride():
+    """More score units and rows than either kernel's grid holds."""
+    check(_w(B=4, S=700, H=2, D=8, T=300, top_k=17, bias="random", seed=8000), what="grid stride")
+
+
+def test_workspace_and_out_reuse_on_side_stream():
+    w = _w(bias="random", seed=8100)
+    x = make_dsa_inputs(w)
+    exp = dsa.index_select(x["query"], x["key"], x["weights"], x["bias"], top_k=w.top_k,
+                           scale=w.softmax_scale)
+    dev = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
+    ws = torch.full((w.B * w.S * w.T * 4 + 64,), 0xAB, dtype=torch.uint8, device="cuda")
+    out = torch.full((w.B, 1, w.S, w.top_k), 12345, dtype=torch.int64, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            attn.dsa_index_select(dev["query"], dev["key"], dev["weights"], dev["bias"], top_k=w.top_k,
+                                  scale=w.softmax_scale, out=out, workspace=ws)
+    side.synchronize()
+    compare_indices(out.cpu().numpy(), exp, "reuse")
+
+
+def test_host_tensors_end_to_end():
+    w = _w(bias="ragged_causal", seed=8200)
+    x = make_dsa_inputs(w)
+    got = attn.dsa_index_select(x["query"], x["key"], x["weights"], x["bias"], top_k=w.top_k,
+                                scale=w.softmax_scale)
+    assert got.device.type == "cpu"
+    exp = dsa.index_select(x["query"], x["key"], x["weights"], x["bias"], top_k=w.top_k,
+                           scale=w.softmax_scale)
+    compare_indices(got.numpy(), exp, "host path")
+
+
+def test_too_many_heads_unsupported():
+    w = _w(H=65, T=50, S=2)
+    x = make_dsa_inputs(w)
+    with pytest.raises(attn.AttnError) as e:
+        run_gpu(w, x)
+    assert e.value.status == attn.ATTN_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- full size
+@pytest.mark.parametrize("name", list(DSA_WORKLOADS))
+def test_full_size(name):
+    """The full workload in one call: the selection of every row against the
+    oracle's selection of the GPU's own scores (exact selection check at full
+    size), and for sampled rows the oracle's scores (bit-exact) and indices."""
+    w = DSA_WORKLOADS[name]
+    x = make_dsa_inputs(w)
+    got, ws = run_gpu(w, x)
+    bits = gpu_score_bits(ws, w)
+    allowed = (x["bias"].numpy()[:, 0] > np.float32(-1e30)).astype(np.uint8)
+    sel = dsa.select(bits.view(np.float32), allowed, w.top_k).reshape(got.shape)
+    compare_indices(got, sel, f"{name} selection of every row")
+    rng = np.random.default_rng(9)
+    rows = np.unique(np.concatenate([[0, w.B * w.S - 1], rng.integers(0, w.B * w.S, size=10)]))
+    exp = dsa.rows(x["query"], x["key"], x["weights"], x["bias"], rows, top_k=w.top_k,
+                   scale=w.softmax_scale, weights_scale=w.weights_scale)
+    compare_indices(got.reshape(-1, w.top_k)[rows], exp, f"{name} sampled rows")
+    for r in rows[:4]:
+        b, s = divmod(int(r), w.S)
+        sc, al = dsa.scores(x["query"][b:b + 1, s:s + 1], x["key"][b:b + 1], x["weights"][b:b + 1, s:s + 1],
+                            x["bias"][b:b + 1, :, s:s + 1], scale=w.softmax_scale,
+                            weights_scale=w.weights_scale)
+        ok = al[0, 0].astype(bool)
+        assert np.array_equal(bits[b, s][ok], sc.view(np.uint32)[0, 0][ok]), f"{name} row {r} scores"

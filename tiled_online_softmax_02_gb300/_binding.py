@@ -42,6 +42,9 @@ SIGNATURES = {
                                   _i32, _i32, ctypes.c_float, ctypes.c_float, _i32,
                                   _i32, _vp, ctypes.c_size_t, _vp]),
     "attn_f32_split_workspace_bytes": (ctypes.c_size_t, [_i32, _i32, _i32, _i32]),
+    "dsa_index_select": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                ctypes.c_float, ctypes.c_float, _i32, _vp, ctypes.c_size_t, _vp]),
+    "dsa_index_select_workspace_bytes": (ctypes.c_size_t, [_i32, _i32, _i32]),
     "attn_splitkv_num_splits": (_i32, [_i32, _i32, _i32, _i32, _i32]),
     "attn_splitkv_workspace_bytes": (ctypes.c_size_t, [_i32, _i32, _i32, _i32, _i32]),
     "attn_status_string": (ctypes.c_char_p, [_i32]),
@@ -244,6 +247,60 @@ def attn_fwd_splitkv(q, k, v, *, mask=None, total_lengths=None, past_lengths=Non
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_splitkv")
     return out, lse
+
+
+def dsa_index_select(query, key, weights, bias, *, top_k, scale, weights_scale=1.0, out=None,
+                     workspace=None):
+    """Sparse index selection of the DSA indexer (dsa_index_select in the C ABI).
+
+    query [B, S, H, D], key [B, T, D], weights [B, S, H] (one dtype among
+    float32 / float16 / bfloat16), bias float32 [B, 1, S, T].  Returns int64
+    [B, 1, S, top_k]: per (b, s) the allowed keys (bias > -1e30) with the
+    largest scores, ascending, then -1s.  CUDA tensors run on torch's current
+    stream; CPU tensors are copied in and the result copied back.  The fp32
+    score workspace is allocated with torch when not given."""
+    if query.dim() != 4 or key.dim() != 3 or weights.dim() != 3 or bias.dim() != 4:
+        raise ValueError("query [B,S,H,D], key [B,T,D], weights [B,S,H], bias [B,1,S,T]")
+    B, S, H, D = query.shape
+    T = key.shape[1]
+    if tuple(key.shape) != (B, T, D) or tuple(weights.shape) != (B, S, H) or \
+            tuple(bias.shape) != (B, 1, S, T):
+        raise ValueError(f"shape mismatch: query {tuple(query.shape)} key {tuple(key.shape)} "
+                         f"weights {tuple(weights.shape)} bias {tuple(bias.shape)}")
+    if query.dtype not in DTYPE_CODES or key.dtype != query.dtype or weights.dtype != query.dtype:
+        raise ValueError("query, key and weights must share one dtype among float32 / float16 / bfloat16")
+    if bias.dtype != torch.float32:
+        raise ValueError("bias must be float32")
+    for t in (query, key, weights, bias):
+        if not t.is_contiguous() or t.device != query.device:
+            raise ValueError("inputs must be contiguous and on one device")
+    host = not query.is_cuda
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        query, key, weights, bias = (t.to(dev, non_blocking=True) for t in (query, key, weights, bias))
+    shape = (B, 1, S, int(top_k))
+    dev_out = out if (out is not None and out.is_cuda and not host) else \
+        torch.empty(shape, dtype=torch.int64, device=query.device)
+    if tuple(dev_out.shape) != shape or dev_out.dtype != torch.int64 or not dev_out.is_contiguous():
+        raise ValueError(f"out must be a contiguous int64 tensor of shape {shape}")
+    lib = load_library()
+    with torch.cuda.device(query.device):
+        need = lib.dsa_index_select_workspace_bytes(B, S, T)
+        if workspace is None or not workspace.is_cuda:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=query.device)
+        ws_bytes = workspace.numel() * workspace.element_size()
+        rc = lib.dsa_index_select(_ptr(query), _ptr(key), _ptr(weights), _ptr(bias), _ptr(dev_out),
+                                  B, S, H, D, T, int(top_k), float(scale), float(weights_scale),
+                                  DTYPE_CODES[query.dtype], _ptr(workspace), ws_bytes,
+                                  _stream_handle(query.device))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "dsa_index_select")
+    if host:
+        res = out if out is not None else torch.empty(shape, dtype=torch.int64, pin_memory=True)
+        res.copy_(dev_out, non_blocking=True)
+        torch.cuda.current_stream(query.device).synchronize()
+        return res
+    return dev_out
 
 
 def get_device_status(device=None) -> int:

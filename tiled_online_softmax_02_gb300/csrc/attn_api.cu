@@ -413,6 +413,63 @@ extern "C" size_t attn_f32_split_workspace_bytes(int B, int Hkv, int kv_capacity
   return f32tc_workspace_bytes((int64_t)B * Hkv * kv_capacity * D);
 }
 
+// ---------------------------------------------------------------------------
+// DSA indexer index selection ("onnx-runtime-ep-cuda 0.1.0-dev.6,
+// src/kernels/dsa_index_select.rs"): validation, then the score and the
+// selection kernels on `stream`.
+extern "C" size_t dsa_index_select_workspace_bytes(int B, int S, int T) {
+  if (B <= 0 || S <= 0 || T <= 0) return 0;
+  return (size_t)B * (size_t)S * (size_t)T * 4;
+}
+
+extern "C" int dsa_index_select(const void* query, const void* key, const void* weights, const float* bias,
+                                int64_t* out, int B, int S, int H, int D, int T, int top_k, float scale,
+                                float weights_scale, int dtype, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  if (dtype != 0 && dtype != 1 && dtype != 2) return ATTN_ERR_INVALID_ARG;
+  if (B < 0 || S < 0 || H <= 0 || D <= 0 || T < 0 || top_k <= 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale <= 0.0f) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(weights_scale) || weights_scale <= 0.0f) return ATTN_ERR_INVALID_ARG;
+  const int64_t es = dtype == 0 ? 4 : 2;
+  int64_t rows, q_el, k_el, w_el, b_el, o_el, t;
+  if (!mul_ok(B, S, &rows) || !mul_ok(rows, H, &t) || !mul_ok(t, D, &q_el)) return ATTN_ERR_INVALID_ARG;
+  if (!mul_ok(B, T, &t) || !mul_ok(t, D, &k_el)) return ATTN_ERR_INVALID_ARG;
+  if (!mul_ok(rows, H, &w_el) || !mul_ok(rows, T, &b_el) || !mul_ok(rows, top_k, &o_el))
+    return ATTN_ERR_INVALID_ARG;
+  if (q_el > (INT64_C(1) << 60) / 4 || k_el > (INT64_C(1) << 60) / 4 || b_el > (INT64_C(1) << 60) / 4 ||
+      o_el > (INT64_C(1) << 60) / 8)
+    return ATTN_ERR_INVALID_ARG;
+  if (rows == 0) return ATTN_OK;  // empty problem: nothing to write
+  // key and bias hold no element when T == 0 and may then be NULL
+  if (!query || !weights || !out || (T > 0 && (!key || !bias))) return ATTN_ERR_INVALID_ARG;
+  if (H > 64) return ATTN_ERR_UNSUPPORTED;  // heads are held in registers, up to 64
+  const int64_t ws_need = b_el * 4;
+  if (T > 0 && (!workspace || workspace_bytes < (size_t)ws_need)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(query, es) || !aligned(key, es) || !aligned(weights, es) || !aligned(bias, 4) ||
+      !aligned(out, 8) || (T > 0 && !aligned(workspace, 16)))
+    return ATTN_ERR_UNSUPPORTED;
+  const int64_t ob = o_el * 8;
+  if (overlaps(out, ob, query, q_el * es) || overlaps(out, ob, key, k_el * es) ||
+      overlaps(out, ob, weights, w_el * es) || overlaps(out, ob, bias, b_el * 4))
+    return ATTN_ERR_INVALID_ARG;
+  if (T > 0 && (overlaps(workspace, ws_need, out, ob) || overlaps(workspace, ws_need, query, q_el * es) ||
+                overlaps(workspace, ws_need, key, k_el * es) || overlaps(workspace, ws_need, weights, w_el * es) ||
+                overlaps(workspace, ws_need, bias, b_el * 4)))
+    return ATTN_ERR_INVALID_ARG;
+  DsaParams dp{};
+  dp.query = query;
+  dp.key = key;
+  dp.weights = weights;
+  dp.bias = bias;
+  dp.scores = static_cast<float*>(workspace);
+  dp.out = out;
+  dp.B = B; dp.S = S; dp.H = H; dp.D = D; dp.T = T; dp.top_k = top_k; dp.dtype = dtype;
+  dp.scale = scale;
+  dp.weights_scale = weights_scale;
+  const cudaError_t e = launch_dsa_select(dp, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
 extern "C" int attn_splitkv_num_splits(int B, int Hq, int Hkv, int Sq, int Sk) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0) return 1;
   return auto_splits(B, Hq, Hkv, Sq, Sk);

@@ -181,3 +181,78 @@ def sample_rows(w: Workload, n: int, seed: int = 7) -> np.ndarray:
         picks.add((int(rng.integers(0, w.B)), int(rng.integers(0, w.Hq)),
                    int(rng.integers(0, w.Sq))))
     return np.array(sorted(picks), dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
+# DSA indexer index selection ("onnx-runtime-ep-cuda 0.1.0-dev.6,
+# src/kernels/dsa_index_select.rs"): query [B, S, H, D], key [B, T, D],
+# weights [B, S, H], bias f32 [B, 1, S, T].  The page gives no workload sizes;
+# the synthetic ones below follow its use -- an indexer over a prefill (causal
+# bias) and over decode steps with ragged cache lengths.
+@dataclass(frozen=True)
+class DsaWorkload:
+    name: str
+    B: int
+    S: int
+    H: int
+    D: int
+    T: int
+    top_k: int
+    dtype: str                      # "f32" | "bf16" | "f16"
+    bias: str = "causal"            # "causal" | "causal_min" | "ragged_causal" | "random" | "zeros"
+    weights_scale: float = 1.0
+    q_std: float = 1.0
+    k_std: float = 1.0
+    w_std: float = 1.0
+    ties: bool = False              # duplicate some key rows (exactly tied scores)
+    seed: int = SEED_BASE + 20
+    scale: float | None = None      # None -> 1/sqrt(D)
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale is not None else 1.0 / math.sqrt(self.D)
+
+    def replace(self, **kw) -> "DsaWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+DSA_WORKLOADS: dict[str, DsaWorkload] = {
+    "dsa_prefill_bf16": DsaWorkload("dsa_prefill_bf16", B=1, S=4096, H=32, D=128, T=4096,
+                                    top_k=2048, dtype="bf16", bias="causal", seed=SEED_BASE + 20),
+    "dsa_decode_bf16": DsaWorkload("dsa_decode_bf16", B=8, S=1, H=32, D=128, T=32768, top_k=2048,
+                                   dtype="bf16", bias="ragged_causal", seed=SEED_BASE + 21),
+}
+
+
+def make_dsa_inputs(w: DsaWorkload, seed: int | None = None) -> dict:
+    """Seeded inputs of a DSA workload on the CPU: query / key / weights in the
+    workload dtype, bias float32 [B, 1, S, T].  Bias modes: "causal" (0 on keys
+    t <= T - S + s, -inf above), "causal_min" (the same with the most negative
+    f32 as the fill), "ragged_causal" (per-batch valid length L_b ~ U{T/4..T},
+    causal against its end, -inf beyond), "random" (N(0, 1) with 10% -inf),
+    "zeros"."""
+    rng = np.random.Generator(np.random.PCG64(w.seed if seed is None else seed))
+    q = rng.standard_normal((w.B, w.S, w.H, w.D), dtype=np.float32) * np.float32(w.q_std)
+    k = rng.standard_normal((w.B, w.T, w.D), dtype=np.float32) * np.float32(w.k_std)
+    wt = rng.standard_normal((w.B, w.S, w.H), dtype=np.float32) * np.float32(w.w_std)
+    if w.ties and w.T >= 4:
+        # every fourth key repeats the key before it: those pairs tie exactly
+        k[:, 3::4, :] = k[:, 2:-1:4, :][:, : k[:, 3::4, :].shape[1], :]
+    s_idx = np.arange(w.S)[:, None]
+    t_idx = np.arange(w.T)[None, :]
+    bias = np.zeros((w.B, 1, w.S, w.T), dtype=np.float32)
+    lengths = None
+    if w.bias in ("causal", "causal_min"):
+        fill = -np.inf if w.bias == "causal" else np.finfo(np.float32).min
+        bias[:, 0] = np.where(t_idx <= (w.T - w.S) + s_idx, 0.0, fill)
+    elif w.bias == "ragged_causal":
+        lengths = rng.integers(max(1, w.T // 4), w.T + 1, size=w.B)
+        for b in range(w.B):
+            bias[b, 0] = np.where(t_idx <= (int(lengths[b]) - w.S) + s_idx, 0.0, -np.inf)
+    elif w.bias == "random":
+        bias[:] = rng.standard_normal(bias.shape, dtype=np.float32)
+        bias[rng.random(bias.shape) < 0.1] = -np.inf
+    elif w.bias != "zeros":
+        raise ValueError(f"unknown bias mode {w.bias!r}")
+    return dict(query=_round(q, w.dtype), key=_round(k, w.dtype), weights=_round(wt, w.dtype),
+                bias=torch.from_numpy(bias), lengths=lengths)
