@@ -82,15 +82,52 @@ def check(w: DsaWorkload, x: dict | None = None, scores: bool = True, what: str 
 
 
 # ---------------------------------------------------------------- dtype x heads x head dim
+# D = 64: the TMA-fed tile kernel; D = 72: the general score kernel
+@pytest.mark.parametrize("D", [64, 72])
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
-@pytest.mark.parametrize("H", [1, 7, 16, 32, 33, 64])
-def test_heads_and_dtypes(dtype, H):
-    check(_w(dtype=dtype, H=H, D=72, S=19, T=600, top_k=96, seed=1000 + H), what=f"{dtype} H={H}")
+@pytest.mark.parametrize("H", [1, 7, 16, 17, 32, 33, 64])
+def test_heads_and_dtypes(dtype, H, D):
+    check(_w(dtype=dtype, H=H, D=D, S=19, T=600, top_k=96, seed=1000 + H), what=f"{dtype} H={H} D={D}")
 
 
-@pytest.mark.parametrize("D", [1, 31, 33, 100, 128, 192])
-def test_head_dims(D):
-    check(_w(D=D, H=20, S=23, T=530, seed=2000 + D), what=f"D={D}")
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("H", [7, 17, 64])
+def test_tile_many_units(dtype, H):
+    """Enough (row, key block) units that the tile kernel takes 4 keys a
+    lane (small problems take 2); one, two and four head groups."""
+    check(_w(dtype=dtype, H=H, D=64, B=1, S=1300, T=600, top_k=50, bias="random", seed=1500 + H),
+          what=f"many units {dtype} H={H}")
+
+
+@pytest.mark.parametrize("D", [1, 16, 31, 32, 33, 48, 100, 128, 192, 256])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_head_dims(D, dtype):
+    check(_w(D=D, H=20, S=23, T=530, dtype=dtype, seed=2000 + D), what=f"{dtype} D={D}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_subnormal_products(dtype):
+    """Products and partial sums in the fp32 subnormal range: the paired
+    instructions must round them like scalar IEEE arithmetic (no flush)."""
+    w = _w(dtype=dtype, q_std=3e-20, k_std=2e-19, scale=1.0, weights_scale=1.0, bias="random", seed=2500)
+    x = make_dsa_inputs(w)
+    x["weights"] = x["weights"] * 1e20            # head terms back in the normal range
+    check(w, x, what=f"subnormal {dtype}")
+
+
+def test_unaligned_query_takes_the_general_path():
+    """A query that is not 16-byte aligned must give the same indices (the
+    general score kernel) as the aligned one (the tile kernel)."""
+    w = _w(D=64, H=8, bias="random", seed=2600)
+    x = make_dsa_inputs(w)
+    q = x["query"]
+    buf = torch.empty(q.numel() + 1, dtype=q.dtype)
+    buf[1:].copy_(q.reshape(-1))
+    x_off = dict(x, query=buf[1:].view(q.shape))
+    assert x_off["query"].data_ptr() % 16 != 0
+    got_a, _ = check(w, x, what="aligned")
+    got_b, _ = check(w, x_off, what="unaligned")
+    assert np.array_equal(got_a, got_b)
 
 
 @pytest.mark.parametrize("T", [1, 5, 255, 256, 257, 511, 1023])
@@ -195,9 +232,33 @@ def test_weights_scale_and_scale():
 
 
 # ---------------------------------------------------------------- grid-stride loops, reuse, streams
-def test_many_rows_grid_stride():
-    """More score units and rows than either kernel's grid holds."""
-    check(_w(B=4, S=700, H=2, D=8, T=300, top_k=17, bias="random", seed=8000), what="grid stride")
+@pytest.mark.parametrize("D", [8, 64])
+def test_many_rows_grid_stride(D):
+    """More score units and rows than either kernel's grid holds (D = 8: the
+    general score kernel, D = 64: the tile kernel)."""
+    check(_w(B=4, S=700, H=2, D=D, T=300, top_k=17, bias="random", seed=8000), what=f"grid stride D={D}")
+
+
+def test_cluster_ties_across_slices():
+    """Few rows: the selection splits each row over a cluster of CTAs; with
+    zero weights every allowed key ties, so the lowest-index ties must be
+    taken across slice boundaries."""
+    w = _w(B=2, S=3, T=3001, top_k=1700, bias="random", seed=8050)
+    x = make_dsa_inputs(w)
+    x["weights"].zero_()
+    x["bias"] = torch.where(torch.isinf(x["bias"]), x["bias"], torch.zeros_like(x["bias"]))
+    got, _ = check(w, x, what="cluster ties")
+    allowed = (x["bias"].numpy()[:, 0] > np.float32(-1e30))
+    for b in range(w.B):
+        for s_ in range(w.S):
+            exp = np.flatnonzero(allowed[b, s_])[: w.top_k]
+            assert np.array_equal(got[b, 0, s_, : exp.size], exp)
+
+
+def test_long_rows_stream_select():
+    """Rows longer than a cluster's shared memory: the streaming selection."""
+    check(_w(B=1, S=2, H=1, D=16, T=400_000, top_k=1000, dtype="f32", bias="random", seed=8060),
+          what="long rows")
 
 
 def test_workspace_and_out_reuse_on_side_stream():

@@ -18,6 +18,10 @@ LIB = os.path.join(PKG, "libattn.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
+# Per-file flags.  dsa_select.cu computes scores whose exact fp32 rounding
+# decides an index set: no multiply may be fused into an add there, including
+# the packed f32x2 pairs (which an explicit .rn does not keep apart).
+FILE_FLAGS = {"dsa_select.cu": ["-fmad=false"]}
 
 
 def _nvcc() -> str:
@@ -57,7 +61,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags: tuple[str, ..
     procs = []
     for src in sources():
         obj = os.path.join(objdir, os.path.basename(src) + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *FILE_FLAGS.get(os.path.basename(src), []), *extra_flags, "-c", src,
+               "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         procs.append((src, obj, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT,

@@ -82,6 +82,8 @@ struct LaneParams {
 
 // DSA indexer index selection (dsa_select.cu).
 struct DsaParams {
+  CUtensorMap tmap_key;  // key as {D, T, B}, box {64 bytes of dims, 256, 1}, 64B swizzle (tile path)
+  int tile_path;         // 1: the TMA-fed score kernel (tmap_key valid), 0: the general one
   const void* query;    // [B, S, H, D] of dtype
   const void* key;      // [B, T, D]
   const void* weights;  // [B, S, H]
@@ -90,7 +92,14 @@ struct DsaParams {
   int64_t* out;         // [B, 1, S, top_k]
   int B, S, H, D, T, top_k, dtype;  // dtype: 0 f32, 1 f16, 2 bf16
   float scale, weights_scale;
+  uint64_t timeout_ns;
+  int* status;          // device status word (timeouts)
+  uint64_t neg_zero2;   // (-0.0f, -0.0f) as a packed pair: the addend of the rounded products
 };
+
+// Whether the TMA-fed score kernel takes a problem: key / query rows of
+// whole 64-byte chunks, heads held in registers, q of a row in shared memory.
+bool dsa_tile_path_ok(int dtype, int H, int D);
 
 constexpr int kTcBlockM = 128;  // query rows per tcgen05 CTA
 constexpr int kTcBlockN = 128;  // keys per tcgen05 tile

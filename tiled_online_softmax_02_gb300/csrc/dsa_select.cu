@@ -11,28 +11,41 @@
 // positive quiet NaN; the top min(#allowed, top_k) allowed keys by (score desc
 // in f32 total order, index asc), emitted ascending and padded with -1.  The
 // page fixes the precision because the output is an index set: the score
-// kernel keeps that exact arithmetic (no fused multiply-add, no reordering),
-// so it runs on the CUDA cores -- a tensor-core product would round
+// kernels keep that exact arithmetic (no fused multiply-add, no reordering),
+// so they run on the CUDA cores -- a tensor-core product would round
 // differently and move near-tied selections.
 //
-//   dsa_score_kernel   one CTA per (row, 256-key block).  K arrives in
-//                      32-dim chunks, transposed into shared memory; each
-//                      thread keeps two keys' dot products for every head in
-//                      registers (heads padded with zeros to HP, which adds
-//                      exactly nothing), then takes the head sum in order.
-//                      Blocks whose keys are all masked write the "not
-//                      allowed" mark without computing (causal prefill skips
-//                      about half the grid).
-//   dsa_select_kernel  one CTA per row: 8-bit radix select over the
-//                      total-order keys (four histogram passes) finds the
-//                      top_k-th key, then an ordered block compaction keeps
-//                      the larger keys and the lowest-index ties.
+//   dsa_tile_kernel     the score kernel for rows of whole 64-byte chunks.
+//                       A producer warp streams K through a two-stage
+//                       shared-memory ring with TMA (64-byte swizzled rows);
+//                       four compute warps each own 32 * KPT keys and keep
+//                       their dot products for every head in registers as
+//                       packed pairs (two heads per fma.rn.f32x2 with a -0
+//                       addend / add.rn.f32x2: each element still rounded
+//                       on its own; a pair takes one issue slot, leaving
+//                       slots for the loads while the fp32 pipe, not issue,
+//                       bounds the loop).  q of the row
+//                       sits in shared memory as fp32 [d][h], one broadcast
+//                       128-bit load feeding two head pairs.  Units whose
+//                       keys are all masked are skipped by both sides.
+//   dsa_score_kernel    the general score kernel (any head dim / alignment):
+//                       K chunks transposed into shared memory by the CTA,
+//                       scalar rounded multiplies and adds.
+//   dsa_select_cluster  selection with the row's slice resident in shared
+//                       memory: a cluster of C CTAs splits a row (C > 1 when
+//                       rows are few), 8-bit radix select whose per-CTA
+//                       histograms (warp-aggregated atomics) are merged over
+//                       distributed shared memory, then an ordered tile
+//                       compaction.
+//   dsa_select_kernel   selection streaming the row from global memory
+//                       (rows too long for the cluster's shared memory).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <cstdint>
 
 #include "attn_internal.h"
+#include "device_common.cuh"
 
 namespace gb300_attn {
 namespace {
@@ -40,18 +53,52 @@ namespace {
 constexpr int kScoreThreads = 128;
 constexpr int kDChunk = 32;                  // head-dim columns per shared-memory chunk
 constexpr int kSelectThreads = 256;
+constexpr int kSelectWarps = kSelectThreads / 32;
 constexpr uint32_t kNotAllowed = 0xFFFFFFFFu;  // score bits of a cell that is not allowed
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-// -------------------------------------------------------------- scores
+// Packed fp32 pairs with IEEE round-to-nearest on each element and no flush
+// of subnormals: the same results as two scalar __fmul_rn / __fadd_rn.  The
+// rounded product is formed as fma(a, b, z) with z = (-0, -0) taken from the
+// launch parameters: q * k + (-0) is q * k rounded once, for zeros, infinities
+// and NaNs too, and an addend the assembler cannot see keeps it from fusing
+// the product into the following add (which it does for a packed mul.rn /
+// add.rn pair even when contraction is switched off).
+__device__ __forceinline__ uint64_t mul_rn2(uint64_t a, uint64_t b, uint64_t z) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(z));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_rn2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// Final score bits of a cell: the head sum plus the bias, NaN made the
+// positive quiet NaN; a cell that is not allowed gets the mark.
+__device__ __forceinline__ uint32_t score_bits(float wsum, float bias, bool ok) {
+  const float s = __fadd_rn(wsum, bias);
+  return ok ? (isnan(s) ? 0x7FC00000u : __float_as_uint(s)) : kNotAllowed;
+}
+
+// -------------------------------------------------------------- general scores
 // Unit u = (row, key block of KPT * 128 keys); thread tid takes keys
 // t0 + tid + 128 j, j < KPT.  HP = heads rounded up (16, 32 or 64); the
 // per-thread accumulators are KPT x HP.
 template <typename T, int HP, int KPT>
-__global__ void __launch_bounds__(kScoreThreads) dsa_score_kernel(const DsaParams p) {
+__global__ void __launch_bounds__(kScoreThreads) dsa_score_kernel(const __grid_constant__ DsaParams p) {
   constexpr int kKeys = KPT * kScoreThreads;
   constexpr int kStride = kKeys + 1;  // padded row of the transposed K chunk
   __shared__ float k_s[kDChunk * kStride];  // [d][key]
@@ -65,8 +112,8 @@ __global__ void __launch_bounds__(kScoreThreads) dsa_score_kernel(const DsaParam
   const int64_t kblocks = ((int64_t)p.T + kKeys - 1) / kKeys;
   const int64_t units = rows * kblocks;
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-    const int64_t row = u / kblocks;
-    const int64_t t0 = (u - row * kblocks) * kKeys;
+    const int64_t row = u % rows;  // row-fastest: a grid stride sees every key block
+    const int64_t t0 = (u / rows) * kKeys;
     const int64_t b = row / p.S;
     const float* brow = p.bias + row * (int64_t)p.T;
     uint32_t* out_bits = reinterpret_cast<uint32_t*>(p.scores) + row * (int64_t)p.T;
@@ -141,12 +188,330 @@ __global__ void __launch_bounds__(kScoreThreads) dsa_score_kernel(const DsaParam
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
       const int64_t t = t0 + tid + j * kScoreThreads;
-      if (t < p.T) {
-        const float s = __fadd_rn(wsum[j], bias_v[j]);
-        out_bits[t] = ok[j] ? (isnan(s) ? 0x7FC00000u : __float_as_uint(s)) : kNotAllowed;
-      }
+      if (t < p.T) out_bits[t] = score_bits(wsum[j], bias_v[j], ok[j]);
     }
     __syncthreads();  // w_s is rewritten by the next unit
+  }
+}
+
+// -------------------------------------------------------------- tile scores
+constexpr int kTileWarps = 4;                          // compute warps
+constexpr int kTileThreads = (kTileWarps + 1) * 32;    // + the TMA producer warp
+constexpr int kTileStages = 2;
+constexpr int kBoxRows = 128;                          // key rows per TMA box
+constexpr int kRowBytes = 64;                          // one swizzled shared-memory row of K
+constexpr int kGroupHeads = 16;                        // heads per pass over K
+constexpr int kMaxQFloats = 8192;                      // q of a row in shared memory: D * heads (padded)
+// KPT keys per lane: 4 for throughput (per dim a lane loads 16 broadcast q
+// values for 4 keys, so shared-memory delivery stays under the fp32 pipe),
+// 2 when rows are few and smaller units spread better over the SMs.
+template <int KPT>
+struct Tile {
+  static constexpr int kKeys = kTileWarps * 32 * KPT;  // keys per unit
+  static constexpr int kStageBytes = kKeys * kRowBytes;
+  static constexpr int kBoxes = kKeys / kBoxRows;
+};
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// Barrier `id` over the first n threads of the CTA; returns the OR of v.
+__device__ __forceinline__ bool bar_any(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void bar_sync_n(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Element e of a 16-byte group of K as fp32.
+template <typename T>
+__device__ __forceinline__ float group_elem(const uint4& g, int e);
+template <>
+__device__ __forceinline__ float group_elem<float>(const uint4& g, int e) {
+  const uint32_t w = e == 0 ? g.x : e == 1 ? g.y : e == 2 ? g.z : g.w;
+  return __uint_as_float(w);
+}
+template <>
+__device__ __forceinline__ float group_elem<__nv_bfloat16>(const uint4& g, int e) {
+  const int i = e >> 1;
+  const uint32_t w = i == 0 ? g.x : i == 1 ? g.y : i == 2 ? g.z : g.w;
+  return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+template <>
+__device__ __forceinline__ float group_elem<__half>(const uint4& g, int e) {
+  const int i = e >> 1;
+  const uint32_t w = i == 0 ? g.x : i == 1 ? g.y : i == 2 ? g.z : g.w;
+  return __half2float(__ushort_as_half((unsigned short)((e & 1) ? (w >> 16) : (w & 0xFFFFu))));
+}
+
+// One chunk of 64 bytes of dims for this lane's KPT keys and one group of
+// 16 heads: acc[j][hp] holds heads (2 hp, 2 hp + 1) of the group for key
+// r0 + 32 j.  q_c points at the chunk's first dim and the group's first head
+// in q_s ([d][hs], row stride hs); each accumulator takes its dims in
+// ascending order.
+template <typename T, int KPT>
+__device__ __forceinline__ void tile_chunk(uint64_t (&acc)[KPT][kGroupHeads / 2], uint32_t kst, const float* q_c,
+                                           int hs, int r0, uint64_t z) {
+  constexpr int kGroups = kRowBytes / 16;
+  constexpr int kVec = 16 / (int)sizeof(T);
+#pragma unroll 1
+  for (int g = 0; g < kGroups; ++g) {
+    uint4 raw[KPT];
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const uint32_t off = (uint32_t)(r0 + 32 * j) * kRowBytes + (uint32_t)g * 16u;
+      raw[j] = lds128(kst + (off ^ ((off >> 3) & 0x30u)));  // 64-byte swizzle
+    }
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+      uint64_t kd[KPT];
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) {
+        const float kv = group_elem<T>(raw[j], e);
+        kd[j] = pack2(kv, kv);
+      }
+      const float4* qd = reinterpret_cast<const float4*>(q_c + (g * kVec + e) * hs);
+#pragma unroll
+      for (int hq = 0; hq < kGroupHeads / 4; ++hq) {
+        const float4 qv = qd[hq];
+        const uint64_t q01 = pack2(qv.x, qv.y), q23 = pack2(qv.z, qv.w);
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) {
+          acc[j][2 * hq] = add_rn2(acc[j][2 * hq], mul_rn2(q01, kd[j], z));
+          acc[j][2 * hq + 1] = add_rn2(acc[j][2 * hq + 1], mul_rn2(q23, kd[j], z));
+        }
+      }
+    }
+  }
+}
+
+// q of one row as fp32 [d][h] over hs (padded) heads, zeros past H, and the
+// head weights times weights_scale, staged by the compute warps.
+template <typename T>
+__device__ __forceinline__ void stage_q(const DsaParams& p, int64_t row, int hs, float* q_s, float* w_s, int tid) {
+  constexpr int kVec = 16 / (int)sizeof(T);
+  const T* qrow = static_cast<const T*>(p.query) + row * (int64_t)p.H * p.D;
+  const int groups = p.D / kVec;
+  for (int i = tid; i < hs * groups; i += kTileWarps * 32) {
+    const int h = i % hs, g = i / hs;
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    if (h < p.H) raw = *reinterpret_cast<const uint4*>(qrow + (int64_t)h * p.D + g * kVec);
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) q_s[(g * kVec + e) * hs + h] = group_elem<T>(raw, e);
+  }
+  for (int h = tid; h < hs; h += kTileWarps * 32)
+    w_s[h] = h < p.H ? __fmul_rn(to_f32(static_cast<const T*>(p.weights)[row * p.H + h]), p.weights_scale) : 0.0f;
+}
+
+// Unit u = (row, kTileKeys keys); grid-stride over units.  Warps 0..3
+// compute (lane owns keys r0 + 32 j of the unit), warp 4 streams K: every
+// chunk of dims once per group of 16 heads, in (group, chunk) order.
+template <typename T, int KPT>
+__global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_constant__ DsaParams p) {
+  constexpr int kDims = kRowBytes / (int)sizeof(T);  // dims per chunk
+  constexpr int kTileKeys = Tile<KPT>::kKeys;
+  constexpr int kStageBytes = Tile<KPT>::kStageBytes;
+  constexpr int kTileBoxes = Tile<KPT>::kBoxes;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int abort_s;
+  const int groups = (p.H + kGroupHeads - 1) / kGroupHeads;
+  const int hs = groups * kGroupHeads;  // heads padded to whole groups
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_addr + 1023u) & ~1023u;  // stages on the swizzle period
+  uint8_t* gbase = smem_raw + (sbase - raw_addr);
+  float* q_s = reinterpret_cast<float*>(gbase + kTileStages * kStageBytes);  // [D][hs]
+  float* w_s = q_s + p.D * hs;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(w_s + hs);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kTileStages);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTileStages; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, kTileWarps);
+    }
+    mbar_init_fence();
+    abort_s = 0;
+  }
+  __syncthreads();
+  const int64_t rows = (int64_t)p.B * p.S;
+  const int64_t kblocks = ((int64_t)p.T + kTileKeys - 1) / kTileKeys;
+  const int64_t units = rows * kblocks;
+  const int nchunks = p.D / kDims;
+
+  if (warp == kTileWarps) {  // ---------------- producer: K chunks by TMA
+    if (lane == 0) tma_prefetch_desc(&p.tmap_key);
+    // whether unit v has an allowed key (the consumers skip it by the same
+    // rule): independent loads, one latency
+    auto active = [&](int64_t v) -> bool {
+      if (v >= units) return false;
+      const int64_t row = v % rows;
+      const int64_t t0 = (v / rows) * kTileKeys;
+      const float* brow = p.bias + row * (int64_t)p.T;
+      bool any = false;
+#pragma unroll
+      for (int i = 0; i < kTileKeys / 32; ++i) {
+        const int64_t t = t0 + lane + 32 * i;
+        any |= t < p.T && brow[t] > -1e30f;
+      }
+      return __any_sync(0xffffffffu, any);
+    };
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t last_phase[kTileStages] = {};
+    bool used[kTileStages] = {};
+    bool dead = false;
+    int64_t u = blockIdx.x;
+    bool cur = active(u);
+    while (u < units && !dead) {
+      const int64_t nu = u + gridDim.x;
+      if (!cur) {
+        u = nu;
+        cur = active(u);
+        continue;
+      }
+      const int64_t row = u % rows;
+      const int64_t t0 = (u / rows) * kTileKeys;
+      const int64_t b = row / p.S;
+      bool next = false;
+      for (int it = 0; it < groups * nchunks; ++it) {
+        const int c = it % nchunks;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(empty0 + 8u * stage, phase ^ 1u, p.timeout_ns, p.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          dead = true;
+          *reinterpret_cast<volatile int*>(&abort_s) = 1;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t fb = full0 + 8u * stage;
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          const uint32_t dst = sbase + (uint32_t)stage * kStageBytes;
+#pragma unroll
+          for (int x = 0; x < kTileBoxes; ++x)
+            tma_load_3d(dst + (uint32_t)x * kBoxRows * kRowBytes, &p.tmap_key, fb, c * kDims,
+                        (int)(t0 + x * kBoxRows), (int)b);
+        }
+        last_phase[stage] = phase;
+        used[stage] = true;
+        if (++stage == kTileStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (it == 0) next = active(nu);  // looked up while the consumers work on this unit
+      }
+      u = nu;
+      cur = next;
+    }
+    // every copy this CTA issued has landed before it can end
+    if (lane == 0)
+      for (int s = 0; s < kTileStages; ++s)
+        if (used[s]) mbar_wait(full0 + 8u * s, last_phase[s], p.timeout_ns, p.status);
+    return;
+  }
+
+  // ---------------- compute warps
+  const int tid = threadIdx.x;
+  const int r0 = warp * 32 * KPT + lane;
+  int stage = 0;
+  uint32_t phase = 0;
+  bool my_abort = false;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    bool warp_any;
+    {
+      const int64_t row = u % rows;
+      const int64_t t0 = (u / rows) * kTileKeys + r0;
+      const float* brow = p.bias + row * (int64_t)p.T;
+      bool mine = false;
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) mine = mine || (t0 + 32 * j < p.T && brow[t0 + 32 * j] > -1e30f);
+      warp_any = __any_sync(0xffffffffu, mine);
+    }
+    // every compute warp agrees on stopping (a timed-out wait anywhere) ...
+    my_abort = my_abort || *reinterpret_cast<volatile int*>(&abort_s) != 0;
+    if (bar_any(1, kTileWarps * 32, my_abort)) break;
+    // ... and on the unit having an allowed key; past this barrier every
+    // warp is done with the previous unit's q_s
+    if (!bar_any(1, kTileWarps * 32, warp_any)) {
+      const int64_t row = u % rows;
+      const int64_t t0 = (u / rows) * kTileKeys + r0;
+      uint32_t* out_bits = reinterpret_cast<uint32_t*>(p.scores) + row * (int64_t)p.T;
+#pragma unroll
+      for (int j = 0; j < KPT; ++j)
+        if (t0 + 32 * j < p.T) out_bits[t0 + 32 * j] = kNotAllowed;
+      continue;
+    }
+    stage_q<T>(p, u % rows, hs, q_s, w_s, tid);
+    bar_sync_n(1, kTileWarps * 32);
+    float wsum[KPT];
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) wsum[j] = 0.0f;
+    for (int grp = 0; grp < groups && !my_abort; ++grp) {
+      uint64_t acc[KPT][kGroupHeads / 2];
+#pragma unroll
+      for (int j = 0; j < KPT; ++j)
+#pragma unroll
+        for (int h = 0; h < kGroupHeads / 2; ++h) acc[j][h] = 0ull;
+      for (int c = 0; c < nchunks; ++c) {
+        if (!mbar_wait_warp(full0 + 8u * stage, phase, p.timeout_ns, p.status)) {
+          my_abort = true;
+          break;
+        }
+        if (warp_any)
+          tile_chunk<T, KPT>(acc, sbase + (uint32_t)stage * kStageBytes, q_s + c * kDims * hs + grp * kGroupHeads, hs,
+                        r0, p.neg_zero2);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8u * stage);
+        if (++stage == kTileStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      // this group's heads into the head sum, heads ascending
+      const float* wg = w_s + grp * kGroupHeads;
+#pragma unroll
+      for (int hp = 0; hp < kGroupHeads / 2; ++hp) {
+        const float w0 = wg[2 * hp], w1 = wg[2 * hp + 1];
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) {
+          float a0, a1;
+          unpack2(acc[j][hp], a0, a1);
+          float s0 = __fmul_rn(p.scale, a0);
+          s0 = s0 > 0.0f ? s0 : 0.0f;  // ReLU (a NaN dot gives 0)
+          wsum[j] = __fadd_rn(wsum[j], __fmul_rn(s0, w0));
+          float s1 = __fmul_rn(p.scale, a1);
+          s1 = s1 > 0.0f ? s1 : 0.0f;
+          wsum[j] = __fadd_rn(wsum[j], __fmul_rn(s1, w1));
+        }
+      }
+    }
+    if (my_abort) continue;  // the next unit's barrier stops every warp
+    const int64_t row = u % rows;
+    const int64_t t0 = (u / rows) * kTileKeys + r0;
+    const float* brow = p.bias + row * (int64_t)p.T;
+    uint32_t* out_bits = reinterpret_cast<uint32_t*>(p.scores) + row * (int64_t)p.T;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const int64_t t = t0 + 32 * j;
+      if (t < p.T) {
+        const float bv = brow[t];
+        out_bits[t] = score_bits(wsum[j], bv, bv > -1e30f);
+      }
+    }
   }
 }
 
@@ -158,7 +523,206 @@ __device__ __forceinline__ uint32_t order_key(uint32_t bits) {
   return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
 }
 
-// Exclusive prefix sum over the CTA (kSelectThreads); also returns the total.
+// Adds one to bin `bin` of h for every lane with `active`: one shared atomic
+// per distinct bin in the warp (scores of a row crowd into few top digits).
+// Warp-collective.
+__device__ __forceinline__ void hist_add(uint32_t* h, uint32_t bin, bool active) {
+  const uint32_t act = __ballot_sync(0xffffffffu, active);
+  if (active) {
+    const uint32_t peers = __match_any_sync(act, bin);
+    if (__ffs(peers) - 1 == (int)(threadIdx.x & 31)) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+  }
+}
+
+// Sum over the CTA; every thread gets it.  red: kSelectWarps words.
+__device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t* red) {
+  v = __reduce_add_sync(0xffffffffu, v);
+  __syncthreads();  // the previous use of red is over
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  uint32_t s = 0;
+#pragma unroll
+  for (int w = 0; w < kSelectWarps; ++w) s += red[w];
+  return s;
+}
+
+// Warp 0: the bin of histogram gh (counted from the top) holding the
+// rank-th largest element, and the rank within it.
+__device__ __forceinline__ void find_digit(const uint32_t* gh, uint32_t rank, uint32_t* digit_s, uint32_t* rank_s) {
+  const int lane = threadIdx.x & 31;
+  // lane l holds bins 255 - 8l ... 248 - 8l (descending)
+  uint32_t c[8], s = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    c[i] = gh[255 - 8 * lane - i];
+    s += c[i];
+  }
+  uint32_t incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t excl = incl - s;
+  if (excl < rank && rank <= incl) {  // exactly one lane
+    uint32_t acc = excl;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (acc < rank && rank <= acc + c[i]) {
+        *digit_s = 255u - 8u * lane - i;
+        *rank_s = rank - acc;
+      }
+      acc += c[i];
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Barrier over every thread of every CTA of the cluster, with release /
+// acquire ordering of shared memory (a hardware barrier: all CTAs of a
+// cluster are resident together).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Word `p` (a shared-memory variable of this CTA) in CTA `cta` of the cluster.
+__device__ __forceinline__ uint32_t ld_peer(const uint32_t* p, uint32_t cta) {
+  uint32_t remote, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(cta));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// A cluster of csize CTAs per row (grid-stride over rows by cluster); CTA c
+// holds keys [c * slice, (c + 1) * slice) of the row in shared memory.
+__global__ void __launch_bounds__(kSelectThreads) dsa_select_cluster(const __grid_constant__ DsaParams p, int csize,
+                                                                     int slice) {
+  extern __shared__ uint32_t keys_s[];  // this CTA's slice as order keys (0: not allowed)
+  __shared__ uint32_t hist[2][256];     // per pass, alternating (peers read the last one)
+  __shared__ uint32_t gh[256];          // the cluster's histogram
+  __shared__ uint32_t red[kSelectWarps];
+  __shared__ uint32_t tile_tot[2][kSelectWarps];
+  __shared__ uint32_t cnt[3];           // allowed / greater / equal in this slice, read by peers
+  __shared__ uint32_t digit_s, rank_s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t crank = cluster_rank();
+  const int64_t rows = (int64_t)p.B * p.S;
+  const int64_t T = p.T;
+  const int64_t base = (int64_t)crank * slice;
+  const int n = (int)(T - base < 0 ? 0 : (T - base < slice ? T - base : slice));
+  int hpar = 0;
+  for (int64_t row = cluster_index(); row < rows; row += cluster_count()) {
+    const uint32_t* bits = reinterpret_cast<const uint32_t*>(p.scores) + row * T + base;
+    int64_t* out = p.out + row * (int64_t)p.top_k;
+    uint32_t mine = 0;
+    for (int i = tid; i < n; i += kSelectThreads) {
+      const uint32_t k = order_key(bits[i]);
+      keys_s[i] = k;
+      mine += k != 0u;
+    }
+    mine = block_sum(mine, red);
+    if (tid == 0) cnt[0] = mine;
+    cluster_sync_all();  // slices and counts complete in every CTA
+    const uint32_t allowed = __reduce_add_sync(0xffffffffu, lane < csize ? ld_peer(&cnt[0], lane) : 0u);
+    const uint32_t keep = allowed < (uint32_t)p.top_k ? allowed : (uint32_t)p.top_k;
+    for (int64_t i = keep + (int64_t)crank * kSelectThreads + tid; i < p.top_k; i += (int64_t)csize * kSelectThreads)
+      out[i] = -1;
+    if (keep > 0) {  // the same in every CTA of the cluster
+      // radix select of the keep-th largest key, 8 bits at a time from the top
+      uint32_t prefix = 0, pmask = 0, rank = keep;
+      for (int shift = 24; shift >= 0; shift -= 8) {
+        uint32_t* h = hist[hpar];
+        h[tid] = 0u;  // kSelectThreads == 256 bins
+        __syncthreads();
+        for (int i0 = 0; i0 < n; i0 += kSelectThreads) {
+          const int i = i0 + tid;
+          const uint32_t k = i < n ? keys_s[i] : 0u;
+          // cells that are not allowed (key 0) sit below every allowed one
+          // and rank <= #allowed, so they never decide a digit
+          hist_add(h, (k >> shift) & 255u, k != 0u && (k & pmask) == prefix);
+        }
+        cluster_sync_all();  // every CTA's histogram is complete
+        uint32_t g = 0;
+        for (int c = 0; c < csize; ++c) g += ld_peer(&h[tid], (uint32_t)c);
+        gh[tid] = g;
+        __syncthreads();
+        if (warp == 0) find_digit(gh, rank, &digit_s, &rank_s);
+        __syncthreads();
+        prefix |= digit_s << shift;
+        pmask |= 255u << shift;
+        rank = rank_s;
+        hpar ^= 1;
+      }
+      const uint32_t thr = prefix;  // the keep-th largest key
+      uint32_t gt = 0, eq = 0;
+      for (int i = tid; i < n; i += kSelectThreads) {
+        const uint32_t k = keys_s[i];
+        gt += k > thr;
+        eq += k == thr;
+      }
+      gt = block_sum(gt, red);
+      eq = block_sum(eq, red);
+      if (tid == 0) {
+        cnt[1] = gt;
+        cnt[2] = eq;
+      }
+      cluster_sync_all();
+      const uint32_t pg = lane < csize ? ld_peer(&cnt[1], lane) : 0u;
+      const uint32_t pe = lane < csize ? ld_peer(&cnt[2], lane) : 0u;
+      const uint32_t gt_total = __reduce_add_sync(0xffffffffu, pg);
+      const uint32_t gt_before = __reduce_add_sync(0xffffffffu, (uint32_t)lane < crank ? pg : 0u);
+      const uint32_t eq_before = __reduce_add_sync(0xffffffffu, (uint32_t)lane < crank ? pe : 0u);
+      // keys equal to thr are taken lowest index first, slices in key order
+      const uint32_t ties = keep - gt_total;
+      const uint32_t budget = ties > eq_before ? (ties - eq_before < eq ? ties - eq_before : eq) : 0u;
+      const uint32_t slot0 = gt_before + (eq_before < ties ? eq_before : ties);
+      // ordered compaction, one tile of kSelectThreads keys at a time
+      const uint32_t lt = (1u << lane) - 1u;
+      uint32_t run_gt = 0, run_eq = 0;
+      int tpar = 0;
+      for (int i0 = 0; i0 < n; i0 += kSelectThreads) {
+        const int i = i0 + tid;
+        const uint32_t k = i < n ? keys_s[i] : 0u;
+        const bool kg = k > thr, ke = k == thr;
+        const uint32_t bg = __ballot_sync(0xffffffffu, kg), be = __ballot_sync(0xffffffffu, ke);
+        if (lane == 0) tile_tot[tpar][warp] = ((uint32_t)__popc(bg) << 16) | (uint32_t)__popc(be);
+        __syncthreads();
+        uint32_t before = 0, tot = 0;
+#pragma unroll
+        for (int w = 0; w < kSelectWarps; ++w) {
+          const uint32_t v = tile_tot[tpar][w];
+          tot += v;
+          before += w < warp ? v : 0u;
+        }
+        const uint32_t gb = run_gt + (before >> 16) + (uint32_t)__popc(bg & lt);
+        const uint32_t eb = run_eq + (before & 0xFFFFu) + (uint32_t)__popc(be & lt);
+        if (kg || (ke && eb < budget)) out[slot0 + gb + (eb < budget ? eb : budget)] = base + i;
+        run_gt += tot >> 16;
+        run_eq += tot & 0xFFFFu;
+        tpar ^= 1;
+      }
+    }
+    cluster_sync_all();  // peers are done with this row's counts
+  }
+}
+
+// One CTA per row (grid-stride), the row streamed from global memory: rows
+// too long for the cluster kernel's shared memory.
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
@@ -171,33 +735,32 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
   if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t s = lane < kSelectThreads / 32 ? warp_sums[lane] : 0u;
+    uint32_t s = lane < kSelectWarps ? warp_sums[lane] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
       if (lane >= o) s += y;
     }
-    if (lane < kSelectThreads / 32) warp_sums[lane] = s;  // inclusive over warps
+    if (lane < kSelectWarps) warp_sums[lane] = s;  // inclusive over warps
   }
   __syncthreads();
   const uint32_t before = (warp > 0 ? warp_sums[warp - 1] : 0u) + x - v;
-  *total = warp_sums[kSelectThreads / 32 - 1];
+  *total = warp_sums[kSelectWarps - 1];
   return before;
 }
 
-__global__ void __launch_bounds__(kSelectThreads) dsa_select_kernel(const DsaParams p) {
+__global__ void __launch_bounds__(kSelectThreads) dsa_select_kernel(const __grid_constant__ DsaParams p) {
   __shared__ uint32_t hist[256];
-  __shared__ uint32_t warp_sums[kSelectThreads / 32];
+  __shared__ uint32_t warp_sums[kSelectWarps];
   __shared__ uint32_t digit_s, rank_s;
   const int tid = threadIdx.x;
-  const int lane = tid & 31;
   const int64_t rows = (int64_t)p.B * p.S;
   const int64_t T = p.T;
   const int64_t chunk = (T + kSelectThreads - 1) / kSelectThreads;  // contiguous keys per thread
   const int64_t beg = tid * chunk < T ? tid * chunk : T;
   const int64_t end = beg + chunk < T ? beg + chunk : T;
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-    const uint32_t* bits = reinterpret_cast<const uint32_t*>(p.scores) + row * (int64_t)T;
+    const uint32_t* bits = reinterpret_cast<const uint32_t*>(p.scores) + row * T;
     int64_t* out = p.out + row * (int64_t)p.top_k;
     uint32_t n_ok = 0;
     for (int64_t t = beg; t < end; ++t) n_ok += bits[t] != kNotAllowed;
@@ -206,53 +769,24 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_kernel(const DsaPar
     const uint32_t keep = allowed < (uint32_t)p.top_k ? allowed : (uint32_t)p.top_k;
     for (int64_t i = keep + tid; i < p.top_k; i += kSelectThreads) out[i] = -1;
     if (keep == 0) continue;
-    // radix select of the keep-th largest key, 8 bits at a time from the top
     uint32_t prefix = 0, pmask = 0, rank = keep;
     for (int shift = 24; shift >= 0; shift -= 8) {
-      hist[tid] = 0u;  // kSelectThreads == 256 bins
+      hist[tid] = 0u;
       __syncthreads();
-      for (int64_t t = beg; t < end; ++t) {
-        const uint32_t k = order_key(bits[t]);
-        // cells that are not allowed (key 0) sit below every allowed one and
-        // rank <= #allowed, so they never decide a digit: leave them out
-        if (k != 0u && (k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+      for (int64_t m = 0; m < chunk; ++m) {  // the same trip count in every lane
+        const int64_t t = beg + m;
+        const uint32_t k = t < end ? order_key(bits[t]) : 0u;
+        hist_add(hist, (k >> shift) & 255u, k != 0u && (k & pmask) == prefix);
       }
       __syncthreads();
-      if (tid < 32) {
-        // lane l holds bins 255 - 8l ... 248 - 8l (descending); count from the top
-        uint32_t c[8], s = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          c[i] = hist[255 - 8 * lane - i];
-          s += c[i];
-        }
-        uint32_t incl = s;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const uint32_t excl = incl - s;
-        if (excl < rank && rank <= incl) {  // exactly one lane
-          uint32_t acc = excl;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (acc < rank && rank <= acc + c[i]) {
-              digit_s = 255u - 8u * lane - i;
-              rank_s = rank - acc;
-            }
-            acc += c[i];
-          }
-        }
-      }
+      if (tid < 32) find_digit(hist, rank, &digit_s, &rank_s);
       __syncthreads();
       prefix |= digit_s << shift;
       pmask |= 255u << shift;
       rank = rank_s;
       __syncthreads();
     }
-    const uint32_t thr = prefix;  // the keep-th largest key
-    // ordered compaction: keys above thr, and the lowest-index keys equal to it
+    const uint32_t thr = prefix;
     uint32_t n_gt = 0, n_eq = 0;
     for (int64_t t = beg; t < end; ++t) {
       const uint32_t k = order_key(bits[t]);
@@ -262,7 +796,7 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_kernel(const DsaPar
     uint32_t total_gt, total_eq;
     block_exclusive_scan(n_gt, warp_sums, &total_gt);
     const uint32_t eq_before = block_exclusive_scan(n_eq, warp_sums, &total_eq);
-    const uint32_t ties = keep - total_gt;  // equal keys to take, lowest indices first
+    const uint32_t ties = keep - total_gt;
     const uint32_t my_ties = eq_before >= ties ? 0u : (n_eq < ties - eq_before ? n_eq : ties - eq_before);
     uint32_t n_sel_total;
     uint32_t slot = block_exclusive_scan(n_gt + my_ties, warp_sums, &n_sel_total);
@@ -277,6 +811,39 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_kernel(const DsaPar
   }
 }
 
+// -------------------------------------------------------------- launchers
+
+template <typename T, int KPT>
+cudaError_t launch_tile(const DsaParams& p, int sms, cudaStream_t stream) {
+  const int hs = (p.H + kGroupHeads - 1) / kGroupHeads * kGroupHeads;
+  const size_t fixed = 1024 + (size_t)kTileStages * Tile<KPT>::kStageBytes + 2 * kTileStages * 8;
+  const size_t smem = fixed + (size_t)(p.D + 1) * hs * 4;
+  static bool attr_set = false;  // the same value from every caller
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(dsa_tile_kernel<T, KPT>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)(fixed + (size_t)kMaxQFloats * 4 + 64 * 4));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int64_t rows = (int64_t)p.B * p.S;
+  const int64_t units = rows * (((int64_t)p.T + Tile<KPT>::kKeys - 1) / Tile<KPT>::kKeys);
+  const int64_t cap = (int64_t)sms * 2;
+  const int grid = (int)(units < cap ? units : cap);
+  dsa_tile_kernel<T, KPT><<<grid, kTileThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// 4 keys per lane when that still gives every resident CTA four units or
+// more, else 2.
+template <typename T>
+cudaError_t launch_tile_any(const DsaParams& p, int sms, cudaStream_t stream) {
+  const int64_t rows = (int64_t)p.B * p.S;
+  const int64_t units4 = rows * (((int64_t)p.T + Tile<4>::kKeys - 1) / Tile<4>::kKeys);
+  if (units4 >= (int64_t)sms * 2 * 4) return launch_tile<T, 4>(p, sms, stream);
+  return launch_tile<T, 2>(p, sms, stream);
+}
+
 template <typename T, int HP, int KPT>
 void launch_score_v(const DsaParams& p, int sms, cudaStream_t stream) {
   const int64_t rows = (int64_t)p.B * p.S;
@@ -289,30 +856,83 @@ void launch_score_v(const DsaParams& p, int sms, cudaStream_t stream) {
 
 template <typename T>
 cudaError_t launch_score_t(const DsaParams& p, int sms, cudaStream_t stream) {
+  if (p.tile_path) return launch_tile_any<T>(p, sms, stream);
   if (p.H <= 16) launch_score_v<T, 16, 2>(p, sms, stream);
   else if (p.H <= 32) launch_score_v<T, 32, 2>(p, sms, stream);
   else launch_score_v<T, 64, 1>(p, sms, stream);
   return cudaGetLastError();
 }
 
+constexpr int64_t kSliceMaxBytes = 160 * 1024;  // a CTA's slice of a row in shared memory
+
+// Cluster size for the resident selection (0: stream from global memory):
+// the smallest of 1, 2, 4, 8 that gives every SM a CTA, else 8, as long as
+// the slice fits.
+int select_cluster_size(int64_t rows, int64_t T, int sms, int* slice) {
+  for (int c = 1; c <= 8; c *= 2) {
+    const int64_t L = (T + c - 1) / c;
+    if (L * 4 <= kSliceMaxBytes && (rows * c >= sms || c == 8)) {
+      *slice = (int)L;
+      return c;
+    }
+  }
+  return 0;
+}
+
+cudaError_t launch_select(const DsaParams& p, int sms, cudaStream_t stream) {
+  const int64_t rows = (int64_t)p.B * p.S;
+  int slice = 0;
+  const int c = select_cluster_size(rows, p.T, sms, &slice);
+  if (c == 0) {
+    const int64_t cap = (int64_t)sms * 8;
+    dsa_select_kernel<<<(int)(rows < cap ? rows : cap), kSelectThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(dsa_select_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kSliceMaxBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int64_t max_clusters = (int64_t)sms * 8 / c;
+  const int64_t clusters = rows < max_clusters ? rows : max_clusters;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(clusters * c), 1, 1);
+  cfg.blockDim = dim3(kSelectThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)slice * 4;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)c;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, dsa_select_cluster, p, c, slice);
+}
+
 }  // namespace
+
+bool dsa_tile_path_ok(int dtype, int H, int D) {
+  if (H < 1 || H > 64 || D < 1) return false;
+  const int dims = dtype == 0 ? 16 : 32;  // dims in one 64-byte row of K
+  const int64_t hs = (H + kGroupHeads - 1) / kGroupHeads * kGroupHeads;
+  return D % dims == 0 && (int64_t)D * hs <= kMaxQFloats;
+}
 
 cudaError_t launch_dsa_select(const DsaParams& p, cudaStream_t stream) {
   int dev = 0, sms = 0;
   cudaError_t e;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const int64_t rows = (int64_t)p.B * p.S;
   if (p.T > 0) {
     if (p.dtype == 0) e = launch_score_t<float>(p, sms, stream);
     else if (p.dtype == 1) e = launch_score_t<__half>(p, sms, stream);
     else e = launch_score_t<__nv_bfloat16>(p, sms, stream);
     if (e != cudaSuccess) return e;
   }
-  const int64_t cap = (int64_t)sms * 8;
-  const int grid = (int)(rows < cap ? rows : cap);
-  dsa_select_kernel<<<grid, kSelectThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_select(p, sms, stream);
 }
 
 }  // namespace gb300_attn
