@@ -99,26 +99,6 @@ int encode_map(CUtensorMap* map, const void* base, bool bf16, int64_t planes, in
   return ATTN_OK;
 }
 
-// key [B, T, D] of the DSA indexer as a 3-D TMA map {D, T, B}: a box of
-// 64 bytes of dims by 128 keys, 64-byte swizzle; keys past T read as zero.
-int encode_dsa_key_map(CUtensorMap* map, const void* key, int dtype, int B, int T, int D) {
-  int err = ATTN_OK;
-  auto fn = encode_fn(&err);
-  if (!fn) return err;
-  const int es = dtype == 0 ? 4 : 2;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)B};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)T * (cuuint64_t)D * es};
-  const cuuint32_t box[3] = {(cuuint32_t)(64 / es), 128, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapDataType ty = dtype == 0   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                 : dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  CUresult r = fn(map, ty, 3, const_cast<void*>(key), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
-  return ATTN_OK;
-}
-
 bool mul_ok(int64_t a, int64_t b, int64_t* out) {
   if (a < 0 || b < 0) return false;
   if (a != 0 && b > (INT64_C(1) << 62) / a) return false;
@@ -496,7 +476,11 @@ extern "C" int dsa_index_select(const void* query, const void* key, const void* 
   dp.tile_path = T > 0 && T <= (1 << 30) && dsa_tile_path_ok(dtype, H, D) && aligned(key, 16) &&
                  aligned(query, 16);
   if (dp.tile_path) {
-    const int rc = encode_dsa_key_map(&dp.tmap_key, key, dtype, B, T, D);
+    int rc = ATTN_OK;
+    auto fn = encode_fn(&rc);
+    if (!fn) return rc;
+    if (dsa_encode_key_map(&dp.tmap_key, reinterpret_cast<void*>(fn), key, dtype, B, T, D) != 0)
+      return cuda_fail(cudaErrorInvalidValue);
     if (rc != ATTN_OK) return rc;
   }
   const cudaError_t e = launch_dsa_select(dp, static_cast<cudaStream_t>(stream));

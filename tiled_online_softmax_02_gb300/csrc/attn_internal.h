@@ -82,7 +82,7 @@ struct LaneParams {
 
 // DSA indexer index selection (dsa_select.cu).
 struct DsaParams {
-  CUtensorMap tmap_key;  // key as {D, T, B}, box {64 bytes of dims, 256, 1}, 64B swizzle (tile path)
+  CUtensorMap tmap_key;  // key as {D, T, B}, box {32 bytes of dims, 128, 1}, 32B swizzle (tile path)
   int tile_path;         // 1: the TMA-fed score kernel (tmap_key valid), 0: the general one
   const void* query;    // [B, S, H, D] of dtype
   const void* key;      // [B, T, D]
@@ -98,8 +98,11 @@ struct DsaParams {
 };
 
 // Whether the TMA-fed score kernel takes a problem: key / query rows of
-// whole 64-byte chunks, heads held in registers, q of a row in shared memory.
+// whole chunks of its K rows, q of a row in shared memory.
 bool dsa_tile_path_ok(int dtype, int H, int D);
+// The key tensor map the TMA-fed score kernel reads (its box and swizzle
+// follow the kernel's K rows); encoder = cuTensorMapEncodeTiled.  0 on success.
+int dsa_encode_key_map(CUtensorMap* map, void* encoder, const void* key, int dtype, int B, int T, int D);
 
 constexpr int kTcBlockM = 128;  // query rows per tcgen05 CTA
 constexpr int kTcBlockN = 128;  // keys per tcgen05 tile

@@ -15,9 +15,9 @@
 // so they run on the CUDA cores -- a tensor-core product would round
 // differently and move near-tied selections.
 //
-//   dsa_tile_kernel     the score kernel for rows of whole 64-byte chunks.
-//                       A producer warp streams K through a two-stage
-//                       shared-memory ring with TMA (64-byte swizzled rows);
+//   dsa_tile_kernel     the score kernel for rows of whole 32-byte chunks.
+//                       A producer warp streams K through a four-stage
+//                       shared-memory ring with TMA (32-byte swizzled rows);
 //                       four compute warps each own 32 * KPT keys and keep
 //                       their dot products for every head in registers as
 //                       packed pairs (two heads per fma.rn.f32x2 with a -0
@@ -39,6 +39,8 @@
 //                       compaction.
 //   dsa_select_kernel   selection streaming the row from global memory
 //                       (rows too long for the cluster's shared memory).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -196,9 +198,9 @@ __global__ void __launch_bounds__(kScoreThreads) dsa_score_kernel(const __grid_c
 
 // -------------------------------------------------------------- tile scores
 constexpr int kTileWarps = 4;                          // compute warps
-constexpr int kTileThreads = (kTileWarps + 1) * 32;    // + the TMA producer warp
-constexpr int kTileStages = 2;
-constexpr int kBoxRows = 128;                          // key rows per TMA box
+constexpr int kTileThreads = (kTileWarps + 1) * 32;    // + the staging warp
+constexpr int kTileStages = 2;                         // K ring depth of each compute warp
+constexpr int kBoxRows = 64;                           // key rows per TMA box
 constexpr int kRowBytes = 64;                          // one swizzled shared-memory row of K
 constexpr int kGroupHeads = 16;                        // heads per pass over K
 constexpr int kMaxQFloats = 8192;                      // q of a row in shared memory: D * heads (padded)
@@ -207,9 +209,10 @@ constexpr int kMaxQFloats = 8192;                      // q of a row in shared m
 // 2 when rows are few and smaller units spread better over the SMs.
 template <int KPT>
 struct Tile {
-  static constexpr int kKeys = kTileWarps * 32 * KPT;  // keys per unit
-  static constexpr int kStageBytes = kKeys * kRowBytes;
-  static constexpr int kBoxes = kKeys / kBoxRows;
+  static constexpr int kWarpKeys = 32 * KPT;                // keys of one compute warp in a unit
+  static constexpr int kKeys = kTileWarps * kWarpKeys;      // keys per unit
+  static constexpr int kStageBytes = kWarpKeys * kRowBytes; // one stage of one warp's ring
+  static constexpr int kBoxes = kWarpKeys / kBoxRows;
 };
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -258,7 +261,7 @@ __device__ __forceinline__ float group_elem<__half>(const uint4& g, int e) {
   return __half2float(__ushort_as_half((unsigned short)((e & 1) ? (w >> 16) : (w & 0xFFFFu))));
 }
 
-// One chunk of 64 bytes of dims for this lane's KPT keys and one group of
+// One chunk of 32 bytes of dims for this lane's KPT keys and one group of
 // 16 heads: acc[j][hp] holds heads (2 hp, 2 hp + 1) of the group for key
 // r0 + 32 j.  q_c points at the chunk's first dim and the group's first head
 // in q_s ([d][hs], row stride hs); each accumulator takes its dims in
@@ -300,218 +303,248 @@ __device__ __forceinline__ void tile_chunk(uint64_t (&acc)[KPT][kGroupHeads / 2]
 }
 
 // q of one row as fp32 [d][h] over hs (padded) heads, zeros past H, and the
-// head weights times weights_scale, staged by the compute warps.
+// head weights times weights_scale, staged by one warp.
 template <typename T>
-__device__ __forceinline__ void stage_q(const DsaParams& p, int64_t row, int hs, float* q_s, float* w_s, int tid) {
+__device__ __forceinline__ void stage_q_warp(const DsaParams& p, int64_t row, int hs, float* q_s, float* w_s,
+                                             int lane) {
   constexpr int kVec = 16 / (int)sizeof(T);
   const T* qrow = static_cast<const T*>(p.query) + row * (int64_t)p.H * p.D;
-  const int groups = p.D / kVec;
-  for (int i = tid; i < hs * groups; i += kTileWarps * 32) {
-    const int h = i % hs, g = i / hs;
-    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-    if (h < p.H) raw = *reinterpret_cast<const uint4*>(qrow + (int64_t)h * p.D + g * kVec);
+  // lanes over heads (hs is a multiple of 16: whole half-warps), dims in
+  // 16-byte groups
+  const int gstep = hs >= 32 ? 1 : 2;  // hs == 16: two dim groups a pass
+  const int h0 = hs >= 32 ? lane : lane & 15;
+  const int g0 = hs >= 32 ? 0 : lane >> 4;
+  for (int hb = 0; hb < hs; hb += 32) {
+    const int h = hb + h0;
+    if (h >= hs) break;
+    const T* src = qrow + (int64_t)h * p.D;
+#pragma unroll 4
+    for (int g = g0; g < p.D / kVec; g += gstep) {
+      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+      if (h < p.H) raw = __ldg(reinterpret_cast<const uint4*>(src + g * kVec));
+      float* dst = q_s + g * kVec * hs + h;
 #pragma unroll
-    for (int e = 0; e < kVec; ++e) q_s[(g * kVec + e) * hs + h] = group_elem<T>(raw, e);
+      for (int e = 0; e < kVec; ++e) dst[e * hs] = group_elem<T>(raw, e);
+    }
   }
-  for (int h = tid; h < hs; h += kTileWarps * 32)
+  for (int h = lane; h < hs; h += 32)
     w_s[h] = h < p.H ? __fmul_rn(to_f32(static_cast<const T*>(p.weights)[row * p.H + h]), p.weights_scale) : 0.0f;
 }
 
-// Unit u = (row, kTileKeys keys); grid-stride over units.  Warps 0..3
-// compute (lane owns keys r0 + 32 j of the unit), warp 4 streams K: every
-// chunk of dims once per group of 16 heads, in (group, chunk) order.
+// Shared-memory plan of the tile kernel: the compute warps' K rings, then
+// two unit slots (q [D][hs], head weights [hs], the unit's bias [keys]), the
+// slots' unit indices and the mbarriers.
+template <int KPT>
+struct TileSmem {
+  static constexpr int kSlots = 2;
+  static constexpr int kBars = kTileWarps * kTileStages + 2 * kSlots;
+  __host__ __device__ static size_t slot_floats(int D, int hs) { return (size_t)D * hs + hs + Tile<KPT>::kKeys; }
+  __host__ __device__ static size_t bytes(int D, int hs) {
+    return 1024 + (size_t)kTileWarps * kTileStages * Tile<KPT>::kStageBytes + kSlots * slot_floats(D, hs) * 4 +
+           kSlots * 8 + kBars * 8;
+  }
+};
+
+// The producer's look at unit v: whether a key is allowed, with this lane's
+// bias values (keys t0 + lane + 32 i) kept for the unit's slot.
+template <int KPT>
+__device__ __forceinline__ bool unit_bias(const DsaParams& p, int64_t rows, int64_t v, int lane,
+                                          float (&bv)[Tile<KPT>::kKeys / 32]) {
+  const int64_t row = v % rows, t0 = (v / rows) * Tile<KPT>::kKeys;
+  const float* brow = p.bias + row * (int64_t)p.T;
+  bool any = false;
+#pragma unroll
+  for (int i = 0; i < Tile<KPT>::kKeys / 32; ++i) {
+    const int64_t t = t0 + lane + 32 * i;
+    bv[i] = t < p.T ? brow[t] : -INFINITY;
+    any = any || bv[i] > -1e30f;
+  }
+  return __any_sync(0xffffffffu, any);
+}
+
+// Unit u = (row, kTileKeys keys), rows fastest (a grid stride then sees every
+// key block); grid-stride over units.  Warp 4 looks at each unit's bias
+// first: a unit without an allowed key gets the "not allowed" mark from it
+// and nothing else; every other unit it stages into a slot (q, head weights,
+// bias) ahead of the compute warps.  Warps 0..3 take the posted units in
+// order; in the n-th unit warp w owns key block (w + n) mod 4 (lane: keys
+// r0 + 32 j), so masked blocks fall on every warp alike, and streams that
+// block's K through its own TMA ring -- every chunk of dims once per group of
+// 16 heads -- so no warp waits for another within a unit.  A warp whose keys
+// are all masked loads and computes nothing.
 template <typename T, int KPT>
 __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_constant__ DsaParams p) {
   constexpr int kDims = kRowBytes / (int)sizeof(T);  // dims per chunk
   constexpr int kTileKeys = Tile<KPT>::kKeys;
+  constexpr int kWarpKeys = Tile<KPT>::kWarpKeys;
   constexpr int kStageBytes = Tile<KPT>::kStageBytes;
-  constexpr int kTileBoxes = Tile<KPT>::kBoxes;
+  constexpr int kSlots = TileSmem<KPT>::kSlots;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ int abort_s;
   const int groups = (p.H + kGroupHeads - 1) / kGroupHeads;
   const int hs = groups * kGroupHeads;  // heads padded to whole groups
+  const int slot_floats = (int)TileSmem<KPT>::slot_floats(p.D, hs);
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;  // stages on the swizzle period
   uint8_t* gbase = smem_raw + (sbase - raw_addr);
-  float* q_s = reinterpret_cast<float*>(gbase + kTileStages * kStageBytes);  // [D][hs]
-  float* w_s = q_s + p.D * hs;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(w_s + hs);
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kTileStages);
+  float* slots = reinterpret_cast<float*>(gbase + kTileWarps * kTileStages * kStageBytes);
+  int64_t* unit_s = reinterpret_cast<int64_t*>(slots + kSlots * slot_floats);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(unit_s + kSlots);
+  const uint32_t full0 = smem_u32(bars);                           // [warp][stage]
+  const uint32_t ufull0 = full0 + 8u * kTileWarps * kTileStages, uempty0 = ufull0 + 8u * kSlots;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kTileStages; ++s) {
-      mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, kTileWarps);
+    for (int i = 0; i < kTileWarps * kTileStages; ++i) mbar_init(full0 + 8u * i, 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(ufull0 + 8u * s, 1);
+      mbar_init(uempty0 + 8u * s, kTileWarps);
     }
     mbar_init_fence();
-    abort_s = 0;
   }
   __syncthreads();
   const int64_t rows = (int64_t)p.B * p.S;
   const int64_t kblocks = ((int64_t)p.T + kTileKeys - 1) / kTileKeys;
   const int64_t units = rows * kblocks;
   const int nchunks = p.D / kDims;
+  const int per_unit = groups * nchunks;
 
-  if (warp == kTileWarps) {  // ---------------- producer: K chunks by TMA
-    if (lane == 0) tma_prefetch_desc(&p.tmap_key);
-    // whether unit v has an allowed key (the consumers skip it by the same
-    // rule): independent loads, one latency
-    auto active = [&](int64_t v) -> bool {
-      if (v >= units) return false;
-      const int64_t row = v % rows;
-      const int64_t t0 = (v / rows) * kTileKeys;
-      const float* brow = p.bias + row * (int64_t)p.T;
-      bool any = false;
+  if (warp == kTileWarps) {  // ---------------- staging warp
+    int slot = 0;
+    uint32_t uphase[kSlots] = {};
+    float bv[kTileKeys / 32];
+    // the next unit from v on with an allowed key (units passed over get the
+    // mark); bv then holds its bias
+    auto next_active = [&](int64_t v) -> int64_t {
+      for (; v < units; v += gridDim.x) {
+        if (unit_bias<KPT>(p, rows, v, lane, bv)) return v;
+        const int64_t row = v % rows, t0 = (v / rows) * kTileKeys;
+        uint32_t* ob = reinterpret_cast<uint32_t*>(p.scores) + row * (int64_t)p.T;
 #pragma unroll
-      for (int i = 0; i < kTileKeys / 32; ++i) {
-        const int64_t t = t0 + lane + 32 * i;
-        any |= t < p.T && brow[t] > -1e30f;
+        for (int i = 0; i < kTileKeys / 32; ++i) {
+          const int64_t t = t0 + lane + 32 * i;
+          if (t < p.T) ob[t] = kNotAllowed;
+        }
       }
-      return __any_sync(0xffffffffu, any);
+      return units;
     };
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t last_phase[kTileStages] = {};
-    bool used[kTileStages] = {};
-    bool dead = false;
-    int64_t u = blockIdx.x;
-    bool cur = active(u);
-    while (u < units && !dead) {
-      const int64_t nu = u + gridDim.x;
-      if (!cur) {
-        u = nu;
-        cur = active(u);
-        continue;
-      }
-      const int64_t row = u % rows;
-      const int64_t t0 = (u / rows) * kTileKeys;
-      const int64_t b = row / p.S;
-      bool next = false;
-      for (int it = 0; it < groups * nchunks; ++it) {
-        const int c = it % nchunks;
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(empty0 + 8u * stage, phase ^ 1u, p.timeout_ns, p.status);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          dead = true;
-          *reinterpret_cast<volatile int*>(&abort_s) = 1;
-          break;
-        }
-        if (lane == 0) {
-          const uint32_t fb = full0 + 8u * stage;
-          mbar_arrive_expect_tx(fb, kStageBytes);
-          const uint32_t dst = sbase + (uint32_t)stage * kStageBytes;
+    for (int64_t v = blockIdx.x;;) {
+      v = next_active(v);
+      // unit v (v == units: the end mark) into the next slot
+      bool w = true;
+      if (lane == 0) w = mbar_wait(uempty0 + 8u * slot, uphase[slot] ^ 1u, p.timeout_ns, p.status);
+      if (!__shfl_sync(0xffffffffu, w, 0)) return;  // timed out (recorded)
+      float* sl = slots + slot * slot_floats;
+      if (v < units) {
+        stage_q_warp<T>(p, v % rows, hs, sl, sl + p.D * hs, lane);
+        float* bs = sl + p.D * hs + hs;
 #pragma unroll
-          for (int x = 0; x < kTileBoxes; ++x)
-            tma_load_3d(dst + (uint32_t)x * kBoxRows * kRowBytes, &p.tmap_key, fb, c * kDims,
-                        (int)(t0 + x * kBoxRows), (int)b);
-        }
-        last_phase[stage] = phase;
-        used[stage] = true;
-        if (++stage == kTileStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        if (it == 0) next = active(nu);  // looked up while the consumers work on this unit
+        for (int i = 0; i < kTileKeys / 32; ++i) bs[lane + 32 * i] = bv[i];
       }
-      u = nu;
-      cur = next;
+      if (lane == 0) unit_s[slot] = v < units ? v : -1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ufull0 + 8u * slot);  // release: the slot's contents
+      uphase[slot] ^= 1u;
+      slot ^= 1;
+      if (v >= units) return;
+      v += gridDim.x;
     }
-    // every copy this CTA issued has landed before it can end
-    if (lane == 0)
-      for (int s = 0; s < kTileStages; ++s)
-        if (used[s]) mbar_wait(full0 + 8u * s, last_phase[s], p.timeout_ns, p.status);
-    return;
   }
 
   // ---------------- compute warps
-  const int tid = threadIdx.x;
-  const int r0 = warp * 32 * KPT + lane;
-  int stage = 0;
-  uint32_t phase = 0;
-  bool my_abort = false;
-  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-    bool warp_any;
-    {
-      const int64_t row = u % rows;
-      const int64_t t0 = (u / rows) * kTileKeys + r0;
-      const float* brow = p.bias + row * (int64_t)p.T;
-      bool mine = false;
+  const uint32_t my_full = full0 + 8u * warp * kTileStages;
+  const uint32_t my_ring = sbase + (uint32_t)warp * kTileStages * kStageBytes;
+  uint32_t n_issued = 0, n_used = 0;  // chunks through this warp's ring
+  int slot = 0;
+  uint32_t uphase[kSlots] = {};
+  for (uint32_t seq = 0;; ++seq) {
+    if (!mbar_wait_warp(ufull0 + 8u * slot, uphase[slot], p.timeout_ns, p.status)) return;
+    const int64_t u = unit_s[slot];
+    if (u < 0) return;  // the end mark (every chunk issued has been waited on)
+    const float* q_s = slots + slot * slot_floats;
+    const float* w_s = q_s + p.D * hs;
+    const float* b_s = w_s + hs;
+    const int rw = (int)((warp + seq) % kTileWarps) * kWarpKeys;  // this warp's key block in the unit
+    const int64_t row = u % rows;
+    const int64_t t0 = (u / rows) * kTileKeys + rw;
+    bool mine = false;
 #pragma unroll
-      for (int j = 0; j < KPT; ++j) mine = mine || (t0 + 32 * j < p.T && brow[t0 + 32 * j] > -1e30f);
-      warp_any = __any_sync(0xffffffffu, mine);
-    }
-    // every compute warp agrees on stopping (a timed-out wait anywhere) ...
-    my_abort = my_abort || *reinterpret_cast<volatile int*>(&abort_s) != 0;
-    if (bar_any(1, kTileWarps * 32, my_abort)) break;
-    // ... and on the unit having an allowed key; past this barrier every
-    // warp is done with the previous unit's q_s
-    if (!bar_any(1, kTileWarps * 32, warp_any)) {
-      const int64_t row = u % rows;
-      const int64_t t0 = (u / rows) * kTileKeys + r0;
-      uint32_t* out_bits = reinterpret_cast<uint32_t*>(p.scores) + row * (int64_t)p.T;
-#pragma unroll
-      for (int j = 0; j < KPT; ++j)
-        if (t0 + 32 * j < p.T) out_bits[t0 + 32 * j] = kNotAllowed;
-      continue;
-    }
-    stage_q<T>(p, u % rows, hs, q_s, w_s, tid);
-    bar_sync_n(1, kTileWarps * 32);
+    for (int j = 0; j < KPT; ++j) mine = mine || b_s[rw + lane + 32 * j] > -1e30f;
     float wsum[KPT];
 #pragma unroll
     for (int j = 0; j < KPT; ++j) wsum[j] = 0.0f;
-    for (int grp = 0; grp < groups && !my_abort; ++grp) {
+    if (__any_sync(0xffffffffu, mine)) {
+      const int64_t b = row / p.S;
+      // chunk `it` of the unit ((head group, chunk of dims) order) into the ring
+      auto issue = [&](int it) {
+        const uint32_t st = n_issued % kTileStages;
+        if (lane == 0) {
+          fence_proxy_async_smem();  // this warp's reads of the stage come first
+          mbar_arrive_expect_tx(my_full + 8u * st, kStageBytes);
+#pragma unroll
+          for (int x = 0; x < Tile<KPT>::kBoxes; ++x)
+            tma_load_3d(my_ring + st * kStageBytes + (uint32_t)x * kBoxRows * kRowBytes, &p.tmap_key,
+                        my_full + 8u * st, (it % nchunks) * kDims, (int)(t0 + x * kBoxRows), (int)b);
+        }
+        ++n_issued;
+      };
+      const int head = per_unit < kTileStages ? per_unit : kTileStages;
+      for (int it = 0; it < head; ++it) issue(it);
       uint64_t acc[KPT][kGroupHeads / 2];
+      for (int it = 0; it < per_unit; ++it) {
+        const int grp = it / nchunks, c = it - grp * nchunks;
+        if (c == 0) {
 #pragma unroll
-      for (int j = 0; j < KPT; ++j)
+          for (int j = 0; j < KPT; ++j)
 #pragma unroll
-        for (int h = 0; h < kGroupHeads / 2; ++h) acc[j][h] = 0ull;
-      for (int c = 0; c < nchunks; ++c) {
-        if (!mbar_wait_warp(full0 + 8u * stage, phase, p.timeout_ns, p.status)) {
-          my_abort = true;
-          break;
+            for (int h = 0; h < kGroupHeads / 2; ++h) acc[j][h] = 0ull;
         }
-        if (warp_any)
-          tile_chunk<T, KPT>(acc, sbase + (uint32_t)stage * kStageBytes, q_s + c * kDims * hs + grp * kGroupHeads, hs,
-                        r0, p.neg_zero2);
+        const uint32_t st = n_used % kTileStages;
+        if (!mbar_wait_warp(my_full + 8u * st, (n_used / kTileStages) & 1u, p.timeout_ns, p.status)) {
+          // timed out (recorded): let the other copy in flight land first
+          if (lane == 0 && n_issued > n_used + 1) {
+            const uint32_t o = (n_used + 1) % kTileStages;
+            mbar_wait(my_full + 8u * o, ((n_used + 1) / kTileStages) & 1u, p.timeout_ns, p.status);
+          }
+          return;
+        }
+        ++n_used;
+        tile_chunk<T, KPT>(acc, my_ring + st * kStageBytes, q_s + c * kDims * hs + grp * kGroupHeads, hs, lane,
+                           p.neg_zero2);
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8u * stage);
-        if (++stage == kTileStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-      // this group's heads into the head sum, heads ascending
-      const float* wg = w_s + grp * kGroupHeads;
+        if (it + kTileStages < per_unit) issue(it + kTileStages);
+        if (c == nchunks - 1) {
+          // this group's heads into the head sum, heads ascending
+          const float* wg = w_s + grp * kGroupHeads;
 #pragma unroll
-      for (int hp = 0; hp < kGroupHeads / 2; ++hp) {
-        const float w0 = wg[2 * hp], w1 = wg[2 * hp + 1];
+          for (int hp = 0; hp < kGroupHeads / 2; ++hp) {
+            const float w0 = wg[2 * hp], w1 = wg[2 * hp + 1];
 #pragma unroll
-        for (int j = 0; j < KPT; ++j) {
-          float a0, a1;
-          unpack2(acc[j][hp], a0, a1);
-          float s0 = __fmul_rn(p.scale, a0);
-          s0 = s0 > 0.0f ? s0 : 0.0f;  // ReLU (a NaN dot gives 0)
-          wsum[j] = __fadd_rn(wsum[j], __fmul_rn(s0, w0));
-          float s1 = __fmul_rn(p.scale, a1);
-          s1 = s1 > 0.0f ? s1 : 0.0f;
-          wsum[j] = __fadd_rn(wsum[j], __fmul_rn(s1, w1));
+            for (int j = 0; j < KPT; ++j) {
+              float a0, a1;
+              unpack2(acc[j][hp], a0, a1);
+              float s0 = __fmul_rn(p.scale, a0);
+              s0 = s0 > 0.0f ? s0 : 0.0f;  // ReLU (a NaN dot gives 0)
+              wsum[j] = __fadd_rn(wsum[j], __fmul_rn(s0, w0));
+              float s1 = __fmul_rn(p.scale, a1);
+              s1 = s1 > 0.0f ? s1 : 0.0f;
+              wsum[j] = __fadd_rn(wsum[j], __fmul_rn(s1, w1));
+            }
+          }
         }
       }
     }
-    if (my_abort) continue;  // the next unit's barrier stops every warp
-    const int64_t row = u % rows;
-    const int64_t t0 = (u / rows) * kTileKeys + r0;
-    const float* brow = p.bias + row * (int64_t)p.T;
     uint32_t* out_bits = reinterpret_cast<uint32_t*>(p.scores) + row * (int64_t)p.T;
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
-      const int64_t t = t0 + 32 * j;
+      const int64_t t = t0 + lane + 32 * j;
       if (t < p.T) {
-        const float bv = brow[t];
+        const float bv = b_s[rw + lane + 32 * j];
         out_bits[t] = score_bits(wsum[j], bv, bv > -1e30f);
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(uempty0 + 8u * slot);  // this warp is done with the slot
+    uphase[slot] ^= 1u;
+    slot ^= 1;
   }
 }
 
@@ -816,13 +849,13 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_kernel(const __grid
 template <typename T, int KPT>
 cudaError_t launch_tile(const DsaParams& p, int sms, cudaStream_t stream) {
   const int hs = (p.H + kGroupHeads - 1) / kGroupHeads * kGroupHeads;
-  const size_t fixed = 1024 + (size_t)kTileStages * Tile<KPT>::kStageBytes + 2 * kTileStages * 8;
-  const size_t smem = fixed + (size_t)(p.D + 1) * hs * 4;
+  const size_t smem = TileSmem<KPT>::bytes(p.D, hs);
   static bool attr_set = false;  // the same value from every caller
   if (!attr_set) {
+    // the largest plan: D * hs at its cap, hs = 64
     const cudaError_t e = cudaFuncSetAttribute(dsa_tile_kernel<T, KPT>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)(fixed + (size_t)kMaxQFloats * 4 + 64 * 4));
+                                               (int)TileSmem<KPT>::bytes(kMaxQFloats / 64, 64));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -916,9 +949,27 @@ cudaError_t launch_select(const DsaParams& p, int sms, cudaStream_t stream) {
 
 bool dsa_tile_path_ok(int dtype, int H, int D) {
   if (H < 1 || H > 64 || D < 1) return false;
-  const int dims = dtype == 0 ? 16 : 32;  // dims in one 64-byte row of K
+  const int dims = kRowBytes / (dtype == 0 ? 4 : 2);  // dims in one row of K
   const int64_t hs = (H + kGroupHeads - 1) / kGroupHeads * kGroupHeads;
   return D % dims == 0 && (int64_t)D * hs <= kMaxQFloats;
+}
+
+// key [B, T, D] as a 3-D TMA map {D, T, B}: a box of one K row of dims by
+// 128 keys with the matching swizzle; keys past T read as zero.
+int dsa_encode_key_map(CUtensorMap* map, void* encoder, const void* key, int dtype, int B, int T, int D) {
+  auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(encoder);
+  const int es = dtype == 0 ? 4 : 2;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)B};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)T * (cuuint64_t)D * es};
+  const cuuint32_t box[3] = {(cuuint32_t)(kRowBytes / es), (cuuint32_t)kBoxRows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType ty = dtype == 0   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_64B;  // kRowBytes
+  const CUresult r = fn(map, ty, 3, const_cast<void*>(key), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : 1;
 }
 
 cudaError_t launch_dsa_select(const DsaParams& p, cudaStream_t stream) {
