@@ -55,6 +55,9 @@ NCU_TRAFFIC = {
     "decode_bf16": {"bytes_per_launch": 775665920, "source_hash": "aee60e800bf42d81"},
     "decode_bf16+splitkv": {"bytes_per_launch": 777046272, "source_hash": "aee60e800bf42d81"},
     "gqa_causal_bf16_d256": {"bytes_per_launch": 435266560, "source_hash": "6b4b5aabb41779d5"},
+    # the DSA indexer: the tile score kernel (the selection kernel's traffic is in its profile)
+    "dsa_prefill_bf16": {"bytes_per_launch": 142317312, "source_hash": "4118fcf4a0dfe7c0"},
+    "dsa_decode_bf16": {"bytes_per_launch": 34628864, "source_hash": "4118fcf4a0dfe7c0"},
 }
 
 
@@ -158,7 +161,7 @@ KERNEL_SOURCES = {
     "decode": ("attn_decode.cu", "attn_decode.h", "device_common.cuh", "attn_internal.h"),
     "f32tc": ("attn_f32tc.cu", "attn_lane1.cuh", "device_common.cuh", "attn_internal.h"),
     "lane16": ("attn_lane16.cu", "attn_lane1.cuh", "device_common.cuh", "attn_internal.h"),
-    "dsa": ("dsa_select.cu", "attn_internal.h"),
+    "dsa": ("dsa_select.cu", "dsa_internal.h", "device_common.cuh"),
 }
 
 

@@ -22,6 +22,7 @@
 #include "../../include/attn.h"
 #include "attn_decode.h"
 #include "attn_internal.h"
+#include "dsa_internal.h"
 #include "device_common.cuh"
 
 namespace gb300_attn {

@@ -80,30 +80,6 @@ struct LaneParams {
   CommonParams c;
 };
 
-// DSA indexer index selection (dsa_select.cu).
-struct DsaParams {
-  CUtensorMap tmap_key;  // key as {D, T, B}, box {32 bytes of dims, 128, 1}, 32B swizzle (tile path)
-  int tile_path;         // 1: the TMA-fed score kernel (tmap_key valid), 0: the general one
-  const void* query;    // [B, S, H, D] of dtype
-  const void* key;      // [B, T, D]
-  const void* weights;  // [B, S, H]
-  const float* bias;    // [B, 1, S, T]
-  float* scores;        // workspace [B * S, T]: fp32 scores, 0xFFFFFFFF where not allowed
-  int64_t* out;         // [B, 1, S, top_k]
-  int B, S, H, D, T, top_k, dtype;  // dtype: 0 f32, 1 f16, 2 bf16
-  float scale, weights_scale;
-  uint64_t timeout_ns;
-  int* status;          // device status word (timeouts)
-  uint64_t neg_zero2;   // (-0.0f, -0.0f) as a packed pair: the addend of the rounded products
-};
-
-// Whether the TMA-fed score kernel takes a problem: key / query rows of
-// whole chunks of its K rows, q of a row in shared memory.
-bool dsa_tile_path_ok(int dtype, int H, int D);
-// The key tensor map the TMA-fed score kernel reads (its box and swizzle
-// follow the kernel's K rows); encoder = cuTensorMapEncodeTiled.  0 on success.
-int dsa_encode_key_map(CUtensorMap* map, void* encoder, const void* key, int dtype, int B, int T, int D);
-
 constexpr int kTcBlockM = 128;  // query rows per tcgen05 CTA
 constexpr int kTcBlockN = 128;  // keys per tcgen05 tile
 constexpr int kF32BlockM = 64;  // query rows per fp32 CTA
@@ -113,7 +89,6 @@ cudaError_t launch_attn_tc(const TcParams& p, bool bf16, cudaStream_t stream);
 cudaError_t launch_attn_f32(const F32Params& p, cudaStream_t stream);
 cudaError_t launch_attn_f32tc(const LaneParams& p, const float* k, const float* v, void* ws, cudaStream_t stream);
 cudaError_t launch_attn_lane16(const LaneParams& p, bool bf16, cudaStream_t stream);
-cudaError_t launch_dsa_select(const DsaParams& p, cudaStream_t stream);
 // workspace bytes of the fp32 tensor-core path for B * Hkv * kv_capacity * D elements of K (and of V)
 size_t f32tc_workspace_bytes(int64_t kv_elems);
 constexpr int kF32TcPlanesPerKv = 5;  // k0, k1, k2, v0, v1

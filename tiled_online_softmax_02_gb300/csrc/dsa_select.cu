@@ -47,6 +47,7 @@
 #include <cstdint>
 
 #include "attn_internal.h"
+#include "dsa_internal.h"
 #include "device_common.cuh"
 
 namespace gb300_attn {
