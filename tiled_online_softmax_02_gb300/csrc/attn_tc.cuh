@@ -288,8 +288,10 @@ __device__ __forceinline__ void producer_role(const TcParams& P, const Smem<D>& 
     if (q_items > 0 && !mbar_wait(sm.q_empty(), (q_items - 1) & 1, p.timeout_ns, p.status)) break;
     const int q_plane = it.b * p.Hq + it.h;
     const int kv_plane = it.b * p.Hkv + it.kvh;
-    mbar_arrive_expect_tx(sm.q_full(), kQTiles * Cfg::kTileBytes);
-    for (int t = 0; t < kQTiles; ++t)
+    // a lane-split item's two lanes share query tile 0's rows: one Q tile
+    const int nq = it.lanesplit ? 1 : kQTiles;
+    mbar_arrive_expect_tx(sm.q_full(), nq * Cfg::kTileBytes);
+    for (int t = 0; t < nq; ++t)
       for (int s = 0; s < Cfg::kSub; ++s)
         tma_load_3d(sm.sQ + t * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_q, sm.q_full(), s * 64,
                     (int)it.row0(t), q_plane);
@@ -326,13 +328,14 @@ __device__ __forceinline__ void producer_role(const TcParams& P, const Smem<D>& 
   if (q_items > 0) mbar_wait(sm.q_full(), (q_items - 1) & 1, p.timeout_ns, p.status);
 }
 
-// S_t = Q_t K^T for one key tile (K tile at kaddr), then commit s_full(t).
+// S_t = Q K^T for one key tile (K tile at kaddr, Q from query tile slot qt:
+// t, or 0 for both lanes of a lane-split item), then commit s_full(t).
 // Warp-collective: the whole MMA warp calls it, one elected lane issues.
 template <int D, bool BF16>
-__device__ __forceinline__ void issue_qk(const Smem<D>& sm, uint32_t tmem, int t, uint32_t kaddr) {
+__device__ __forceinline__ void issue_qk(const Smem<D>& sm, uint32_t tmem, int t, int qt, uint32_t kaddr) {
   using Cfg = TcConfig<D>;
   constexpr uint32_t idesc_qk = make_idesc_f16kind(BF16, BM, BN, false);
-  const uint64_t adesc0 = make_sdesc_sw128(sm.sQ + t * Cfg::kTileBytes, 16, 1024);
+  const uint64_t adesc0 = make_sdesc_sw128(sm.sQ + qt * Cfg::kTileBytes, 16, 1024);
   const uint64_t bdesc0 = make_sdesc_sw128(kaddr, 16, 1024);
   // K steps kk = 4s..4s+3 lie in 64-column block s (kSubBytes apart), 32
   // bytes into each 128-byte row; the start address field counts 16 bytes
@@ -447,7 +450,7 @@ __device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, u
         }
         if (s0) {
           if (!wait_k()) { ok = false; break; }
-          issue_qk<D, BF16>(sm, tmem, 0, kaddr);
+          issue_qk<D, BF16>(sm, tmem, 0, 0, kaddr);
         }
         __syncwarp();
         if (pv1) {
@@ -460,17 +463,17 @@ __device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, u
         }
         if (s1) {
           if (!wait_k()) { ok = false; break; }
-          issue_qk<D, BF16>(sm, tmem, 1, kaddr);
+          issue_qk<D, BF16>(sm, tmem, 1, it.lanesplit ? 0 : 1, kaddr);
         }
         __syncwarp();
       } else {
       if (s0 && !pv0) {
         if (!wait_k()) { ok = false; break; }
-        issue_qk<D, BF16>(sm, tmem, 0, kaddr);
+        issue_qk<D, BF16>(sm, tmem, 0, 0, kaddr);
       }
       if (s1 && !pv1) {
         if (!wait_k()) { ok = false; break; }
-        issue_qk<D, BF16>(sm, tmem, 1, kaddr);
+        issue_qk<D, BF16>(sm, tmem, 1, it.lanesplit ? 0 : 1, kaddr);
       }
       if (pv0) {
         if (!mbar_wait_warp(sm.p_full(0), pc[0] & 1, p.timeout_ns, p.status)) { ok = false; break; }
@@ -481,7 +484,7 @@ __device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, u
         ++pc[0];
         if (s0) {
           if (!wait_k()) { ok = false; break; }
-          issue_qk<D, BF16>(sm, tmem, 0, kaddr);
+          issue_qk<D, BF16>(sm, tmem, 0, 0, kaddr);
         }
       }
       if (pv1) {
@@ -493,7 +496,7 @@ __device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, u
         ++pc[1];
         if (s1) {
           if (!wait_k()) { ok = false; break; }
-          issue_qk<D, BF16>(sm, tmem, 1, kaddr);
+          issue_qk<D, BF16>(sm, tmem, 1, it.lanesplit ? 0 : 1, kaddr);
         }
       }
       }  // KSPLIT
@@ -570,11 +573,52 @@ __device__ __forceinline__ void mask_rows_coalesced(float (&x)[BN], const float*
   }
 }
 
+// The asynchronous form of the same staging, for rows of whole 16-byte
+// chunks (vec4) when a second 4 KB buffer per warp is free (key-split
+// kernels whose items all share one query tile leave query tile 1's shared
+// memory unused): chunk k of 32 keys goes to buffer k & 1 by cp.async
+// (zero-filled outside the mask), so two chunks are in flight and no
+// registers hold them, and the next key tile's first two chunks are
+// requested as soon as their buffers are read, to land during this tile's
+// softmax.
+__device__ __forceinline__ void mask_chunk_async(uint8_t* buf, const float* mwarp, int nrows, int Sk, int key0,
+                                                 int k, int lane) {
+  const int rsub = lane >> 3, csub = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = 4 * i + rsub;
+    const int key = key0 + 32 * k + 4 * csub;
+    const bool valid = row < nrows && key + 3 < Sk;
+    const float* src = valid ? mwarp + (int64_t)row * Sk + key : mwarp;
+    const uint32_t dst = smem_u32(buf + row * 128 + ((csub ^ (row & 7)) << 4));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void mask_chunk_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+  __syncwarp();  // every lane's copies of the chunk have landed
+}
+__device__ __forceinline__ void mask_chunk_read(float (&x)[BN], const uint8_t* buf, int k, int lane) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float4 t = *reinterpret_cast<const float4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4));
+    x[32 * k + 4 * c + 0] = t.x;
+    x[32 * k + 4 * c + 1] = t.y;
+    x[32 * k + 4 * c + 2] = t.z;
+    x[32 * k + 4 * c + 3] = t.w;
+  }
+  __syncwarp();  // every lane has read the buffer before it is refilled
+}
+
 // ------------------------------------------------------------------ softmax
 // Warpgroup t (warps 4t..4t+3); thread = one query row of query tile t.
 template <int D, bool BF16, bool SOFTCAP, bool MASK, bool KSPLIT, bool SPLITKV>
 __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& sm, uint32_t tmem,
                                              int n_items, int warp, int lane) {
+  using Cfg = TcConfig<D>;
   const CommonParams& p = P.c;
   const int t = warp >> 2;  // query tile of this warpgroup
   const int wq = warp & 3;  // TMEM lane quarter
@@ -612,14 +656,44 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
 
     float m_run = -INFINITY;  // running max, log2 units
     float l_run = 0.0f;       // running denominator
+    // asynchronous mask staging: key-split kernel, every item one query tile
+    // (query tile 1's shared memory is then never used), 16-byte mask rows
+    const bool mpipe = MASK && KSPLIT && D == 128 && p.Sq <= BM && p.mask_vec4 != 0;
+    uint8_t* mb0 = sm.mask_buf(warp);
+    uint8_t* mb1 = sm.base + Cfg::kOffQ + Cfg::kTileBytes + warp * kMaskBufBytes;
+    const int kstep = (KSPLIT ? it.stride : 1) * BN;
+    if (mpipe && nt > 0) {
+      mask_chunk_async(mb0, mwarp, mrows, p.Sk, T.t_begin * BN, 0, lane);
+      mask_chunk_async(mb1, mwarp, mrows, p.Sk, T.t_begin * BN, 1, lane);
+    }
     for (int c = 0; c < nt; ++c, ++sc) {
       const int64_t key0 = (int64_t)(T.t_begin + c * (KSPLIT ? it.stride : 1)) * BN;
       float x[BN];
       if constexpr (MASK) {
         // this tile's mask rows into x (natural units), before the S wait:
         // the loads overlap the tensor core's work
-        mask_rows_coalesced(x, mwarp, mrows, p.Sk, (int)key0, p.mask_vec4 != 0, sm.mask_buf(warp),
-                            lane);
+        if (mpipe) {
+          const bool more = c + 1 < nt;
+          const int kn = (int)key0 + kstep;
+          mask_chunk_wait<1>();
+          mask_chunk_read(x, mb0, 0, lane);
+          mask_chunk_async(mb0, mwarp, mrows, p.Sk, (int)key0, 2, lane);
+          mask_chunk_wait<1>();
+          mask_chunk_read(x, mb1, 1, lane);
+          mask_chunk_async(mb1, mwarp, mrows, p.Sk, (int)key0, 3, lane);
+          mask_chunk_wait<1>();
+          mask_chunk_read(x, mb0, 2, lane);
+          if (more) {
+            mask_chunk_async(mb0, mwarp, mrows, p.Sk, kn, 0, lane);
+            mask_chunk_wait<1>();
+          } else {
+            mask_chunk_wait<0>();
+          }
+          mask_chunk_read(x, mb1, 3, lane);
+          if (more) mask_chunk_async(mb1, mwarp, mrows, p.Sk, kn, 1, lane);
+        } else {
+          mask_rows_coalesced(x, mwarp, mrows, p.Sk, (int)key0, p.mask_vec4 != 0, sm.mask_buf(warp), lane);
+        }
       }
       if (!mbar_wait_warp(sm.s_full(t), sc & 1, p.timeout_ns, p.status)) { ok = false; break; }
       tc_fence_after();
@@ -877,6 +951,8 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
     // The next item's first P.V into O_t waits for this warpgroup's next
     // p_full arrival, which comes after these reads (fence before arrive).
   }
+  // mask copies still in flight after an early stop land before the exit
+  if (MASK) asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 template <int D, bool BF16, bool SOFTCAP, bool MASK, bool KSPLIT, bool SPLITKV>
