@@ -47,9 +47,9 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # attn_fwd_splitkv entry), with the hash of that kernel's sources at the time;
 # reported as null once those sources change.
 NCU_TRAFFIC = {
-    "gqa_causal_bf16": {"bytes_per_launch": 127821824, "source_hash": "9e8ae31fdce6f12b"},
-    "window_softcap_bf16": {"bytes_per_launch": 396507648, "source_hash": "9e8ae31fdce6f12b"},
-    "ragged_kvcache_f16": {"bytes_per_launch": 48636160, "source_hash": "9e8ae31fdce6f12b"},
+    "gqa_causal_bf16": {"bytes_per_launch": 127524096, "source_hash": "026bc7d58294bb1a"},
+    "window_softcap_bf16": {"bytes_per_launch": 396008704, "source_hash": "026bc7d58294bb1a"},
+    "ragged_kvcache_f16": {"bytes_per_launch": 48547584, "source_hash": "026bc7d58294bb1a"},
     "dit_f32": {"bytes_per_launch": 57955840, "source_hash": "eae79b8b5b3f0a83"},
     "dit_f32+f32split": {"bytes_per_launch": 76163072, "source_hash": "1734554f5cdad589"},
     "decode_bf16": {"bytes_per_launch": 775665920, "source_hash": "aee60e800bf42d81"},
