@@ -216,9 +216,11 @@ size_t attn_f32_split_workspace_bytes(int B, int Hkv, int kv_capacity, int D);
  *   dtype    0 f32, 1 f16, 2 bf16 (query, key and weights share it)
  *   workspace  at least dsa_index_select_workspace_bytes(B, S, T) bytes,
  *            16-byte aligned, not overlapping any other argument (the fp32
- *            scores); may be NULL when T == 0.  Calls that share a workspace
- *            must not overlap on the GPU.
- * Launches two kernels on `stream`; allocates and synchronises nothing.
+ *            scores, then a work counter the call zeroes on `stream`); may be
+ *            NULL when T == 0.  Calls that share a workspace must not overlap
+ *            on the GPU.
+ * Enqueues an 8-byte memset (for the counter) and two kernels on
+ * `stream`; allocates and synchronises nothing.
  * Errors: ATTN_ERR_INVALID_ARG (bad size, attribute, dtype, null or
  * overlapping pointer, small workspace), ATTN_ERR_UNSUPPORTED (H > 64,
  * misaligned pointers), ATTN_ERR_CUDA (launch failure).
@@ -228,7 +230,7 @@ int dsa_index_select(const void *query, const void *key, const void *weights, co
                      float weights_scale, int dtype, void *workspace, size_t workspace_bytes,
                      void *stream);
 
-/* Workspace bytes dsa_index_select needs: B * S * T * 4 (0 for non-positive sizes). */
+/* Workspace bytes dsa_index_select needs: B * S * T * 4 + 256 (0 for non-positive sizes). */
 size_t dsa_index_select_workspace_bytes(int B, int S, int T);
 
 /* Size of the library-owned buffer attn_fwd_splitkv_noalloc uses (8 MiB). */

@@ -203,7 +203,7 @@ def test_f32_split_validation(lib):
 # ---------------------------------------------------------------- dsa_index_select
 DQ, DK, DW, DB, DO, DWS = (0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000, 0x60000000)
 DSA_GOOD = dict(query=DQ, key=DK, weights=DW, bias=DB, out=DO, B=2, S=8, H=16, D=64, T=300, top_k=32,
-                scale=0.125, weights_scale=1.0, dtype=2, ws=DWS, ws_bytes=2 * 8 * 300 * 4)
+                scale=0.125, weights_scale=1.0, dtype=2, ws=DWS, ws_bytes=2 * 8 * 300 * 4 + 256)
 
 
 def call_dsa(lib, **kw):
@@ -214,7 +214,7 @@ def call_dsa(lib, **kw):
 
 
 def test_dsa_workspace_bytes(lib):
-    assert lib.dsa_index_select_workspace_bytes(2, 8, 300) == 2 * 8 * 300 * 4
+    assert lib.dsa_index_select_workspace_bytes(2, 8, 300) == 2 * 8 * 300 * 4 + 256  # scores, counter
     assert lib.dsa_index_select_workspace_bytes(0, 8, 300) == 0
     assert lib.dsa_index_select_workspace_bytes(2, 8, 0) == 0
     assert lib.dsa_index_select_workspace_bytes(-1, 8, 300) == 0
@@ -226,7 +226,7 @@ def test_dsa_workspace_bytes(lib):
     dict(weights_scale=0.0), dict(weights_scale=math.nan),
     dict(query=None), dict(key=None), dict(weights=None), dict(bias=None), dict(out=None),
     dict(T=0, key=None, bias=None, query=None),
-    dict(ws=None), dict(ws_bytes=2 * 8 * 300 * 4 - 1),
+    dict(ws=None), dict(ws_bytes=2 * 8 * 300 * 4 + 255),
     dict(out=DQ + 64), dict(out=DB), dict(ws=DK), dict(ws=DO - 16),
     dict(B=2**20, S=2**20, T=2**20),
 ])

@@ -37,7 +37,8 @@ def run_gpu(w: DsaWorkload, x: dict, ws=None):
     """Indices (numpy int64 [B, 1, S, top_k]) and the workspace tensor."""
     dev = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
     if ws is None:
-        ws = torch.empty(max(w.B * w.S * w.T * 4, 16), dtype=torch.uint8, device="cuda")
+        need = attn.load_library().dsa_index_select_workspace_bytes(w.B, w.S, w.T)
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
     out = attn.dsa_index_select(dev["query"], dev["key"], dev["weights"], dev["bias"], top_k=w.top_k,
                                 scale=w.softmax_scale, weights_scale=w.weights_scale, workspace=ws)
     torch.cuda.synchronize()
@@ -267,7 +268,8 @@ def test_workspace_and_out_reuse_on_side_stream():
     exp = dsa.index_select(x["query"], x["key"], x["weights"], x["bias"], top_k=w.top_k,
                            scale=w.softmax_scale)
     dev = {k: v.cuda() for k, v in x.items() if isinstance(v, torch.Tensor)}
-    ws = torch.full((w.B * w.S * w.T * 4 + 64,), 0xAB, dtype=torch.uint8, device="cuda")
+    need = attn.load_library().dsa_index_select_workspace_bytes(w.B, w.S, w.T)
+    ws = torch.full((need + 64,), 0xAB, dtype=torch.uint8, device="cuda")  # stale counter bytes too
     out = torch.full((w.B, 1, w.S, w.top_k), 12345, dtype=torch.int64, device="cuda")
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())

@@ -420,7 +420,7 @@ extern "C" size_t attn_f32_split_workspace_bytes(int B, int Hkv, int kv_capacity
 // selection kernels on `stream`.
 extern "C" size_t dsa_index_select_workspace_bytes(int B, int S, int T) {
   if (B <= 0 || S <= 0 || T <= 0) return 0;
-  return (size_t)B * (size_t)S * (size_t)T * 4;
+  return (size_t)B * (size_t)S * (size_t)T * 4 + kDsaCounterBytes;
 }
 
 extern "C" int dsa_index_select(const void* query, const void* key, const void* weights, const float* bias,
@@ -444,7 +444,7 @@ extern "C" int dsa_index_select(const void* query, const void* key, const void* 
   // key and bias hold no element when T == 0 and may then be NULL
   if (!query || !weights || !out || (T > 0 && (!key || !bias))) return ATTN_ERR_INVALID_ARG;
   if (H > 64) return ATTN_ERR_UNSUPPORTED;  // heads are held in registers, up to 64
-  const int64_t ws_need = b_el * 4;
+  const int64_t ws_need = b_el * 4 + (int64_t)kDsaCounterBytes;  // scores, then the unit counter
   if (T > 0 && (!workspace || workspace_bytes < (size_t)ws_need)) return ATTN_ERR_INVALID_ARG;
   if (!aligned(query, es) || !aligned(key, es) || !aligned(weights, es) || !aligned(bias, 4) ||
       !aligned(out, 8) || (T > 0 && !aligned(workspace, 16)))
@@ -477,6 +477,12 @@ extern "C" int dsa_index_select(const void* query, const void* key, const void* 
   dp.tile_path = T > 0 && T <= (1 << 30) && dsa_tile_path_ok(dtype, H, D) && aligned(key, 16) &&
                  aligned(query, 16);
   if (dp.tile_path) {
+    // the counter sits 16-byte aligned after the scores; zeroed on the stream
+    const size_t off = ((size_t)b_el * 4 + 15) & ~(size_t)15;
+    dp.unit_counter = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + off);
+    const cudaError_t me = cudaMemsetAsync(dp.unit_counter, 0, sizeof(unsigned long long),
+                                           static_cast<cudaStream_t>(stream));
+    if (me != cudaSuccess) return cuda_fail(me);
     int rc = ATTN_OK;
     auto fn = encode_fn(&rc);
     if (!fn) return rc;

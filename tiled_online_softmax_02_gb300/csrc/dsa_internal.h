@@ -24,6 +24,7 @@ struct DsaParams {
   uint64_t timeout_ns;
   int* status;          // device status word (timeouts)
   uint64_t neg_zero2;   // (-0.0f, -0.0f) as a packed pair: the addend of the rounded products
+  unsigned long long* unit_counter;  // tile path: next unit to take, zero at launch (in the workspace)
 };
 
 // Whether the TMA-fed score kernel takes a problem: key / query rows of
@@ -33,6 +34,8 @@ bool dsa_tile_path_ok(int dtype, int H, int D);
 // follow the kernel's K rows); encoder = cuTensorMapEncodeTiled.  0 on success.
 int dsa_encode_key_map(CUtensorMap* map, void* encoder, const void* key, int dtype, int B, int T, int D);
 
+// Bytes of the workspace after the scores: the tile kernel's unit counter.
+constexpr size_t kDsaCounterBytes = 256;
 cudaError_t launch_dsa_select(const DsaParams& p, cudaStream_t stream);
 
 }  // namespace gb300_attn

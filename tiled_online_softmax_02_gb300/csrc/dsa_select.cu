@@ -363,8 +363,9 @@ __device__ __forceinline__ bool unit_bias(const DsaParams& p, int64_t rows, int6
   return __any_sync(0xffffffffu, any);
 }
 
-// Unit u = (row, kTileKeys keys), rows fastest (a grid stride then sees every
-// key block); grid-stride over units.  Warp 4 looks at each unit's bias
+// Unit u = (row, kTileKeys keys), rows fastest (CTAs working at the same time
+// then share key blocks in L2); CTAs take units from a counter in the
+// workspace, zeroed before the launch.  Warp 4 looks at each unit's bias
 // first: a unit without an allowed key gets the "not allowed" mark from it
 // and nothing else; every other unit it stages into a slot (q, head weights,
 // bias) ahead of the compute warps.  Warps 0..3 take the posted units in
@@ -412,10 +413,16 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
     int slot = 0;
     uint32_t uphase[kSlots] = {};
     float bv[kTileKeys / 32];
-    // the next unit from v on with an allowed key (units passed over get the
-    // mark); bv then holds its bias
-    auto next_active = [&](int64_t v) -> int64_t {
-      for (; v < units; v += gridDim.x) {
+    // the next unit this CTA takes from the shared counter (units in
+    // increasing order over all CTAs, so an SM that finishes early takes
+    // more) that has an allowed key; units passed over get the mark; bv then
+    // holds its bias
+    auto next_active = [&]() -> int64_t {
+      for (;;) {
+        unsigned long long w = 0;
+        if (lane == 0) w = atomicAdd(p.unit_counter, 1ull);
+        const int64_t v = (int64_t)__shfl_sync(0xffffffffu, w, 0);
+        if (v >= units) return units;
         if (unit_bias<KPT>(p, rows, v, lane, bv)) return v;
         const int64_t row = v % rows, t0 = (v / rows) * kTileKeys;
         uint32_t* ob = reinterpret_cast<uint32_t*>(p.scores) + row * (int64_t)p.T;
@@ -425,10 +432,9 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
           if (t < p.T) ob[t] = kNotAllowed;
         }
       }
-      return units;
     };
-    for (int64_t v = blockIdx.x;;) {
-      v = next_active(v);
+    for (;;) {
+      const int64_t v = next_active();
       // unit v (v == units: the end mark) into the next slot
       bool w = true;
       if (lane == 0) w = mbar_wait(uempty0 + 8u * slot, uphase[slot] ^ 1u, p.timeout_ns, p.status);
@@ -446,7 +452,6 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
       uphase[slot] ^= 1u;
       slot ^= 1;
       if (v >= units) return;
-      v += gridDim.x;
     }
   }
 
