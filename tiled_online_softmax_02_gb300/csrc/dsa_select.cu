@@ -224,22 +224,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-// Barrier `id` over the first n threads of the CTA; returns the OR of v.
-__device__ __forceinline__ bool bar_any(int id, int n, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ void bar_sync_n(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 // Element e of a 16-byte group of K as fp32.
 template <typename T>
@@ -573,17 +557,6 @@ __device__ __forceinline__ void hist_add(uint32_t* h, uint32_t bin, bool active)
   }
 }
 
-// Sum over the CTA; every thread gets it.  red: kSelectWarps words.
-__device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t* red) {
-  v = __reduce_add_sync(0xffffffffu, v);
-  __syncthreads();  // the previous use of red is over
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  uint32_t s = 0;
-#pragma unroll
-  for (int w = 0; w < kSelectWarps; ++w) s += red[w];
-  return s;
-}
 
 // Warp 0: the bin of histogram gh (counted from the top) holding the
 // rank-th largest element, and the rank within it.
@@ -639,32 +612,72 @@ __device__ __forceinline__ void cluster_sync_all() {
       "barrier.cluster.arrive.release.aligned;\n\t"
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Word `p` (a shared-memory variable of this CTA) in CTA `cta` of the cluster.
-__device__ __forceinline__ uint32_t ld_peer(const uint32_t* p, uint32_t cta) {
-  uint32_t remote, v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(cta));
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
-  return v;
+
+// Shared word `a` summed over the cluster's csize (<= 8) CTAs: the eight
+// remote loads go out in one block (ranks past csize read the last CTA and
+// are not added), so they cost one latency.
+__device__ __forceinline__ uint32_t cluster_sum8(const uint32_t* a, int csize) {
+  uint32_t r[8], v[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) r[c] = (uint32_t)(c < csize ? c : csize - 1);
+  asm volatile(
+      "{\n\t.reg .u32 a<8>;\n\t"
+      "mapa.shared::cluster.u32 a0, %8, %9;\n\tmapa.shared::cluster.u32 a1, %8, %10;\n\t"
+      "mapa.shared::cluster.u32 a2, %8, %11;\n\tmapa.shared::cluster.u32 a3, %8, %12;\n\t"
+      "mapa.shared::cluster.u32 a4, %8, %13;\n\tmapa.shared::cluster.u32 a5, %8, %14;\n\t"
+      "mapa.shared::cluster.u32 a6, %8, %15;\n\tmapa.shared::cluster.u32 a7, %8, %16;\n\t"
+      "ld.shared::cluster.u32 %0, [a0];\n\tld.shared::cluster.u32 %1, [a1];\n\t"
+      "ld.shared::cluster.u32 %2, [a2];\n\tld.shared::cluster.u32 %3, [a3];\n\t"
+      "ld.shared::cluster.u32 %4, [a4];\n\tld.shared::cluster.u32 %5, [a5];\n\t"
+      "ld.shared::cluster.u32 %6, [a6];\n\tld.shared::cluster.u32 %7, [a7];\n\t}"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+      : "r"(smem_u32(a)), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+  uint32_t sum = 0;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) sum += c < csize ? v[c] : 0u;
+  return sum;
+}
+
+// Words a[0..7] of CTA `cta`'s copy, summed (eight loads in one block).
+__device__ __forceinline__ uint32_t peer_sum8(const uint32_t* a, uint32_t cta) {
+  uint32_t v[8];
+  asm volatile(
+      "{\n\t.reg .u32 b;\n\t"
+      "mapa.shared::cluster.u32 b, %8, %9;\n\t"
+      "ld.shared::cluster.u32 %0, [b];\n\tld.shared::cluster.u32 %1, [b+4];\n\t"
+      "ld.shared::cluster.u32 %2, [b+8];\n\tld.shared::cluster.u32 %3, [b+12];\n\t"
+      "ld.shared::cluster.u32 %4, [b+16];\n\tld.shared::cluster.u32 %5, [b+20];\n\t"
+      "ld.shared::cluster.u32 %6, [b+24];\n\tld.shared::cluster.u32 %7, [b+28];\n\t}"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+      : "r"(smem_u32(a)), "r"(cta)
+      : "memory");
+  return v[0] + v[1] + v[2] + v[3] + v[4] + v[5] + v[6] + v[7];
 }
 
 // A cluster of csize CTAs per row (grid-stride over rows by cluster); CTA c
-// holds keys [c * slice, (c + 1) * slice) of the row in shared memory.
+// holds keys [c * slice, (c + 1) * slice) of the row in shared memory, and
+// warp w of it the contiguous segment [w * seg, (w + 1) * seg) of that slice
+// for the ordered compaction.  Per row: 7 cluster barriers and no other.
 __global__ void __launch_bounds__(kSelectThreads) dsa_select_cluster(const __grid_constant__ DsaParams p, int csize,
                                                                      int slice) {
   extern __shared__ uint32_t keys_s[];  // this CTA's slice as order keys (0: not allowed)
-  __shared__ uint32_t hist[2][256];     // per pass, alternating (peers read the last one)
-  __shared__ uint32_t gh[256];          // the cluster's histogram
-  __shared__ uint32_t red[kSelectWarps];
-  __shared__ uint32_t tile_tot[2][kSelectWarps];
-  __shared__ uint32_t cnt[3];           // allowed / greater / equal in this slice, read by peers
-  __shared__ uint32_t digit_s, rank_s;
+  __shared__ uint32_t hist[3][256];     // per radix pass, three in rotation (peers read them)
+  __shared__ uint32_t gh[256];          // the cluster's histogram of a pass (clusters of 2 or more)
+  __shared__ __align__(16) uint32_t w_ok[kSelectWarps];  // per-warp counts, read by peers
+  __shared__ __align__(16) uint32_t w_gt[kSelectWarps];
+  __shared__ __align__(16) uint32_t w_eq[kSelectWarps];
+  static_assert(kSelectWarps == 8, "peer_sum8 reads eight per-warp counts");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t crank = cluster_rank();
   const int64_t rows = (int64_t)p.B * p.S;
   const int64_t T = p.T;
   const int64_t base = (int64_t)crank * slice;
   const int n = (int)(T - base < 0 ? 0 : (T - base < slice ? T - base : slice));
-  int hpar = 0;
+  const int seg = ((n + kSelectWarps - 1) / kSelectWarps + 31) & ~31;
+  const int s0 = warp * seg < n ? warp * seg : n;
+  const int s1 = s0 + seg < n ? s0 + seg : n;
+  const uint32_t lt = (1u << lane) - 1u;
   for (int64_t row = cluster_index(); row < rows; row += cluster_count()) {
     const uint32_t* bits = reinterpret_cast<const uint32_t*>(p.scores) + row * T + base;
     int64_t* out = p.out + row * (int64_t)p.top_k;
@@ -674,20 +687,31 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_cluster(const __gri
       keys_s[i] = k;
       mine += k != 0u;
     }
-    mine = block_sum(mine, red);
-    if (tid == 0) cnt[0] = mine;
-    cluster_sync_all();  // slices and counts complete in every CTA
-    const uint32_t allowed = __reduce_add_sync(0xffffffffu, lane < csize ? ld_peer(&cnt[0], lane) : 0u);
+    mine = __reduce_add_sync(0xffffffffu, mine);
+    if (lane == 0) w_ok[warp] = mine;
+    hist[0][tid] = 0u;  // the first two passes' histograms (kSelectThreads == 256 bins)
+    hist[1][tid] = 0u;
+    cluster_sync_all();  // slices, counts and zeroed histograms, cluster-wide
+    uint32_t a = 0;
+    if (lane < csize) {
+      if (csize == 1)
+        for (int w = 0; w < kSelectWarps; ++w) a += w_ok[w];
+      else
+        a = peer_sum8(w_ok, (uint32_t)lane);
+    }
+    const uint32_t allowed = __reduce_add_sync(0xffffffffu, a);
     const uint32_t keep = allowed < (uint32_t)p.top_k ? allowed : (uint32_t)p.top_k;
     for (int64_t i = keep + (int64_t)crank * kSelectThreads + tid; i < p.top_k; i += (int64_t)csize * kSelectThreads)
       out[i] = -1;
     if (keep > 0) {  // the same in every CTA of the cluster
       // radix select of the keep-th largest key, 8 bits at a time from the top
       uint32_t prefix = 0, pmask = 0, rank = keep;
-      for (int shift = 24; shift >= 0; shift -= 8) {
-        uint32_t* h = hist[hpar];
-        h[tid] = 0u;  // kSelectThreads == 256 bins
-        __syncthreads();
+#pragma unroll 1
+      for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        uint32_t* h = hist[pass % 3];
+        // the next pass's buffer, last read by the peers two passes ago
+        if (pass == 1 || pass == 2) hist[(pass + 1) % 3][tid] = 0u;
         for (int i0 = 0; i0 < n; i0 += kSelectThreads) {
           const int i = i0 + tid;
           const uint32_t k = i < n ? keys_s[i] : 0u;
@@ -695,68 +719,95 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_cluster(const __gri
           // and rank <= #allowed, so they never decide a digit
           hist_add(h, (k >> shift) & 255u, k != 0u && (k & pmask) == prefix);
         }
-        cluster_sync_all();  // every CTA's histogram is complete
-        uint32_t g = 0;
-        for (int c = 0; c < csize; ++c) g += ld_peer(&h[tid], (uint32_t)c);
-        gh[tid] = g;
-        __syncthreads();
-        if (warp == 0) find_digit(gh, rank, &digit_s, &rank_s);
-        __syncthreads();
-        prefix |= digit_s << shift;
+        cluster_sync_all();  // every CTA's histogram of this pass is complete
+        const uint32_t* hc = h;
+        if (csize > 1) {
+          // the cluster's histogram, one bin a thread (gh is rewritten only
+          // after the next pass's cluster barrier, when every warp has read it)
+          gh[tid] = cluster_sum8(&h[tid], csize);
+          __syncthreads();
+          hc = gh;
+        }
+        // every warp: bins 255 - 8 lane .. 248 - 8 lane, counted from the top
+        uint32_t c[8], sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          c[i] = hc[255 - 8 * lane - i];
+          sum += c[i];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t excl = incl - sum;
+        const int owner = __ffs(__ballot_sync(0xffffffffu, excl < rank && rank <= incl)) - 1;
+        uint32_t digit = 0, rin = 0, acc = excl;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (acc < rank && rank <= acc + c[i]) {
+            digit = 255u - 8u * lane - i;
+            rin = rank - acc;
+          }
+          acc += c[i];
+        }
+        digit = __shfl_sync(0xffffffffu, digit, owner);
+        rank = __shfl_sync(0xffffffffu, rin, owner);
+        prefix |= digit << shift;
         pmask |= 255u << shift;
-        rank = rank_s;
-        hpar ^= 1;
       }
       const uint32_t thr = prefix;  // the keep-th largest key
-      uint32_t gt = 0, eq = 0;
-      for (int i = tid; i < n; i += kSelectThreads) {
+      uint32_t g = 0, e = 0;
+      for (int i = s0 + lane; i < s1; i += 32) {
         const uint32_t k = keys_s[i];
-        gt += k > thr;
-        eq += k == thr;
+        g += k > thr;
+        e += k == thr;
       }
-      gt = block_sum(gt, red);
-      eq = block_sum(eq, red);
-      if (tid == 0) {
-        cnt[1] = gt;
-        cnt[2] = eq;
+      g = __reduce_add_sync(0xffffffffu, g);
+      e = __reduce_add_sync(0xffffffffu, e);
+      if (lane == 0) {
+        w_gt[warp] = g;
+        w_eq[warp] = e;
       }
       cluster_sync_all();
-      const uint32_t pg = lane < csize ? ld_peer(&cnt[1], lane) : 0u;
-      const uint32_t pe = lane < csize ? ld_peer(&cnt[2], lane) : 0u;
+      // keys above / at thr in the CTAs before this one (slices in key order),
+      // over the cluster, and in this CTA's warps before this one
+      uint32_t pg = 0, pe = 0;
+      if (lane < csize) {
+        if (csize == 1) {
+          for (int w = 0; w < kSelectWarps; ++w) {
+            pg += w_gt[w];
+            pe += w_eq[w];
+          }
+        } else {
+          pg = peer_sum8(w_gt, (uint32_t)lane);
+          pe = peer_sum8(w_eq, (uint32_t)lane);
+        }
+      }
       const uint32_t gt_total = __reduce_add_sync(0xffffffffu, pg);
-      const uint32_t gt_before = __reduce_add_sync(0xffffffffu, (uint32_t)lane < crank ? pg : 0u);
-      const uint32_t eq_before = __reduce_add_sync(0xffffffffu, (uint32_t)lane < crank ? pe : 0u);
-      // keys equal to thr are taken lowest index first, slices in key order
+      uint32_t gt_before = __reduce_add_sync(0xffffffffu, (uint32_t)lane < crank ? pg : 0u);
+      uint32_t eq_before = __reduce_add_sync(0xffffffffu, (uint32_t)lane < crank ? pe : 0u);
+      for (int w = 0; w < warp; ++w) {
+        gt_before += w_gt[w];
+        eq_before += w_eq[w];
+      }
+      // keys equal to thr are taken lowest index first
       const uint32_t ties = keep - gt_total;
-      const uint32_t budget = ties > eq_before ? (ties - eq_before < eq ? ties - eq_before : eq) : 0u;
-      const uint32_t slot0 = gt_before + (eq_before < ties ? eq_before : ties);
-      // ordered compaction, one tile of kSelectThreads keys at a time
-      const uint32_t lt = (1u << lane) - 1u;
-      uint32_t run_gt = 0, run_eq = 0;
-      int tpar = 0;
-      for (int i0 = 0; i0 < n; i0 += kSelectThreads) {
-        const int i = i0 + tid;
-        const uint32_t k = i < n ? keys_s[i] : 0u;
+      // ordered compaction of this warp's segment, 32 keys a step
+      for (int i0 = s0; i0 < s1; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t k = i < s1 ? keys_s[i] : 0u;
         const bool kg = k > thr, ke = k == thr;
         const uint32_t bg = __ballot_sync(0xffffffffu, kg), be = __ballot_sync(0xffffffffu, ke);
-        if (lane == 0) tile_tot[tpar][warp] = ((uint32_t)__popc(bg) << 16) | (uint32_t)__popc(be);
-        __syncthreads();
-        uint32_t before = 0, tot = 0;
-#pragma unroll
-        for (int w = 0; w < kSelectWarps; ++w) {
-          const uint32_t v = tile_tot[tpar][w];
-          tot += v;
-          before += w < warp ? v : 0u;
-        }
-        const uint32_t gb = run_gt + (before >> 16) + (uint32_t)__popc(bg & lt);
-        const uint32_t eb = run_eq + (before & 0xFFFFu) + (uint32_t)__popc(be & lt);
-        if (kg || (ke && eb < budget)) out[slot0 + gb + (eb < budget ? eb : budget)] = base + i;
-        run_gt += tot >> 16;
-        run_eq += tot & 0xFFFFu;
-        tpar ^= 1;
+        const uint32_t eb = eq_before + (uint32_t)__popc(be & lt);  // equal keys before this one
+        if (kg || (ke && eb < ties))
+          out[gt_before + (uint32_t)__popc(bg & lt) + (eb < ties ? eb : ties)] = base + i;
+        gt_before += (uint32_t)__popc(bg);
+        eq_before += (uint32_t)__popc(be);
       }
     }
-    cluster_sync_all();  // peers are done with this row's counts
+    cluster_sync_all();  // peers are done with this row's counts and histograms
   }
 }
 
