@@ -316,48 +316,74 @@ __device__ __forceinline__ void stage_q_warp(const DsaParams& p, int64_t row, in
     w_s[h] = h < p.H ? __fmul_rn(to_f32(static_cast<const T*>(p.weights)[row * p.H + h]), p.weights_scale) : 0.0f;
 }
 
+// How a unit is split over the four compute warps.  G groups of 16 heads;
+// Gs warps share one key block (each takes G / Gs groups) and a unit holds
+// 4 / Gs key blocks.  With 2 keys a lane (small problems) and G = 2 or 4,
+// the heads are split over warps so a unit holds fewer keys and the units
+// spread over more SMs; otherwise every warp takes all groups (Gs = 1).
+struct TileShape {
+  int G, Gs, KB, gpw, unit_keys, term_floats;
+};
+__host__ __device__ inline TileShape tile_shape(int H, int kpt) {
+  TileShape t;
+  t.G = (H + kGroupHeads - 1) / kGroupHeads;
+  t.Gs = (kpt == 2 && (t.G == 2 || t.G == 4)) ? t.G : 1;
+  t.KB = kTileWarps / t.Gs;
+  t.gpw = t.G / t.Gs;
+  t.unit_keys = t.KB * 32 * kpt;
+  // per slot: the terms the other warps of a key block hand to its first
+  t.term_floats = t.KB * (t.Gs - 1) * t.gpw * kGroupHeads * 32 * kpt;
+  return t;
+}
+
 // Shared-memory plan of the tile kernel: the compute warps' K rings, then
-// two unit slots (q [D][hs], head weights [hs], the unit's bias [keys]), the
-// slots' unit indices and the mbarriers.
+// two unit slots (q [D][hs], head weights [hs], the unit's bias [keys],
+// handed-over terms), the slots' unit indices and the mbarriers.
 template <int KPT>
 struct TileSmem {
   static constexpr int kSlots = 2;
-  static constexpr int kBars = kTileWarps * kTileStages + 2 * kSlots;
-  __host__ __device__ static size_t slot_floats(int D, int hs) { return (size_t)D * hs + hs + Tile<KPT>::kKeys; }
-  __host__ __device__ static size_t bytes(int D, int hs) {
-    return 1024 + (size_t)kTileWarps * kTileStages * Tile<KPT>::kStageBytes + kSlots * slot_floats(D, hs) * 4 +
+  static constexpr int kBars = kTileWarps * kTileStages + 2 * kSlots + kSlots * kTileWarps;
+  __host__ __device__ static size_t slot_floats(int D, int hs, int terms) {
+    return (size_t)D * hs + hs + Tile<KPT>::kKeys + terms;
+  }
+  __host__ __device__ static size_t bytes(int D, int hs, int terms) {
+    return 1024 + (size_t)kTileWarps * kTileStages * Tile<KPT>::kStageBytes + kSlots * slot_floats(D, hs, terms) * 4 +
            kSlots * 8 + kBars * 8;
   }
 };
 
-// The producer's look at unit v: whether a key is allowed, with this lane's
-// bias values (keys t0 + lane + 32 i) kept for the unit's slot.
+// The staging warp's look at unit v of `ukeys` keys: whether a key is
+// allowed, with this lane's bias values (keys t0 + lane + 32 i) kept for the
+// unit's slot.
 template <int KPT>
-__device__ __forceinline__ bool unit_bias(const DsaParams& p, int64_t rows, int64_t v, int lane,
+__device__ __forceinline__ bool unit_bias(const DsaParams& p, int64_t rows, int64_t v, int ukeys, int lane,
                                           float (&bv)[Tile<KPT>::kKeys / 32]) {
-  const int64_t row = v % rows, t0 = (v / rows) * Tile<KPT>::kKeys;
+  const int64_t row = v % rows, t0 = (v / rows) * ukeys;
   const float* brow = p.bias + row * (int64_t)p.T;
   bool any = false;
 #pragma unroll
   for (int i = 0; i < Tile<KPT>::kKeys / 32; ++i) {
     const int64_t t = t0 + lane + 32 * i;
-    bv[i] = t < p.T ? brow[t] : -INFINITY;
+    bv[i] = (32 * i < ukeys && t < p.T) ? brow[t] : -INFINITY;
     any = any || bv[i] > -1e30f;
   }
   return __any_sync(0xffffffffu, any);
 }
 
-// Unit u = (row, kTileKeys keys), rows fastest (CTAs working at the same time
-// then share key blocks in L2); CTAs take units from a counter in the
+// Unit u = (row, unit_keys keys), rows fastest (CTAs working at the same
+// time then share key blocks in L2); CTAs take units from a counter in the
 // workspace, zeroed before the launch.  Warp 4 looks at each unit's bias
 // first: a unit without an allowed key gets the "not allowed" mark from it
 // and nothing else; every other unit it stages into a slot (q, head weights,
 // bias) ahead of the compute warps.  Warps 0..3 take the posted units in
-// order; in the n-th unit warp w owns key block (w + n) mod 4 (lane: keys
-// r0 + 32 j), so masked blocks fall on every warp alike, and streams that
-// block's K through its own TMA ring -- every chunk of dims once per group of
-// 16 heads -- so no warp waits for another within a unit.  A warp whose keys
-// are all masked loads and computes nothing.
+// order.  Compute warp w works on key block (w / Gs + n) mod KB of the n-th
+// unit (lane: keys r0 + 32 j), so masked blocks fall on every warp alike,
+// and on head groups [(w % Gs) gpw, + gpw).  Each streams its block's K
+// through its own TMA ring -- every chunk of dims once per group -- so no
+// warp waits for another's stage.  The first warp of a key block sums the
+// heads in order: its own groups, then the relu-weighted terms the other
+// warps of the block left in the slot.  A warp whose keys are all masked
+// loads and computes nothing.
 template <typename T, int KPT>
 __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_constant__ DsaParams p) {
   constexpr int kDims = kRowBytes / (int)sizeof(T);  // dims per chunk
@@ -366,32 +392,33 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
   constexpr int kStageBytes = Tile<KPT>::kStageBytes;
   constexpr int kSlots = TileSmem<KPT>::kSlots;
   extern __shared__ uint8_t smem_raw[];
-  const int groups = (p.H + kGroupHeads - 1) / kGroupHeads;
-  const int hs = groups * kGroupHeads;  // heads padded to whole groups
-  const int slot_floats = (int)TileSmem<KPT>::slot_floats(p.D, hs);
+  const TileShape sh = tile_shape(p.H, KPT);
+  const int hs = sh.G * kGroupHeads;  // heads padded to whole groups
+  const int slot_floats = (int)TileSmem<KPT>::slot_floats(p.D, hs, sh.term_floats);
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;  // stages on the swizzle period
   uint8_t* gbase = smem_raw + (sbase - raw_addr);
   float* slots = reinterpret_cast<float*>(gbase + kTileWarps * kTileStages * kStageBytes);
   int64_t* unit_s = reinterpret_cast<int64_t*>(slots + kSlots * slot_floats);
   uint64_t* bars = reinterpret_cast<uint64_t*>(unit_s + kSlots);
-  const uint32_t full0 = smem_u32(bars);                           // [warp][stage]
+  const uint32_t full0 = smem_u32(bars);  // [warp][stage]
   const uint32_t ufull0 = full0 + 8u * kTileWarps * kTileStages, uempty0 = ufull0 + 8u * kSlots;
+  const uint32_t tfull0 = uempty0 + 8u * kSlots;  // [slot][key block]: the other warps' terms
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTileWarps * kTileStages; ++i) mbar_init(full0 + 8u * i, 1);
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(ufull0 + 8u * s, 1);
       mbar_init(uempty0 + 8u * s, kTileWarps);
+      for (int k = 0; k < kTileWarps; ++k) mbar_init(tfull0 + 8u * (s * kTileWarps + k), sh.Gs > 1 ? sh.Gs - 1 : 1);
     }
     mbar_init_fence();
   }
   __syncthreads();
   const int64_t rows = (int64_t)p.B * p.S;
-  const int64_t kblocks = ((int64_t)p.T + kTileKeys - 1) / kTileKeys;
+  const int64_t kblocks = ((int64_t)p.T + sh.unit_keys - 1) / sh.unit_keys;
   const int64_t units = rows * kblocks;
   const int nchunks = p.D / kDims;
-  const int per_unit = groups * nchunks;
 
   if (warp == kTileWarps) {  // ---------------- staging warp
     int slot = 0;
@@ -407,13 +434,13 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
         if (lane == 0) w = atomicAdd(p.unit_counter, 1ull);
         const int64_t v = (int64_t)__shfl_sync(0xffffffffu, w, 0);
         if (v >= units) return units;
-        if (unit_bias<KPT>(p, rows, v, lane, bv)) return v;
-        const int64_t row = v % rows, t0 = (v / rows) * kTileKeys;
+        if (unit_bias<KPT>(p, rows, v, sh.unit_keys, lane, bv)) return v;
+        const int64_t row = v % rows, t0 = (v / rows) * sh.unit_keys;
         uint32_t* ob = reinterpret_cast<uint32_t*>(p.scores) + row * (int64_t)p.T;
 #pragma unroll
         for (int i = 0; i < kTileKeys / 32; ++i) {
           const int64_t t = t0 + lane + 32 * i;
-          if (t < p.T) ob[t] = kNotAllowed;
+          if (32 * i < sh.unit_keys && t < p.T) ob[t] = kNotAllowed;
         }
       }
     };
@@ -428,7 +455,8 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
         stage_q_warp<T>(p, v % rows, hs, sl, sl + p.D * hs, lane);
         float* bs = sl + p.D * hs + hs;
 #pragma unroll
-        for (int i = 0; i < kTileKeys / 32; ++i) bs[lane + 32 * i] = bv[i];
+        for (int i = 0; i < kTileKeys / 32; ++i)
+          if (32 * i < sh.unit_keys) bs[lane + 32 * i] = bv[i];
       }
       if (lane == 0) unit_s[slot] = v < units ? v : -1;
       __syncwarp();
@@ -442,6 +470,10 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
   // ---------------- compute warps
   const uint32_t my_full = full0 + 8u * warp * kTileStages;
   const uint32_t my_ring = sbase + (uint32_t)warp * kTileStages * kStageBytes;
+  const int kb0 = warp / sh.Gs, gw = warp - kb0 * sh.Gs;  // key block share and group share
+  const int g_first = gw * sh.gpw;
+  const int per_unit = sh.gpw * nchunks;
+  const int term_block = (sh.Gs - 1) * sh.gpw * kGroupHeads * kWarpKeys;  // floats per key block
   uint32_t n_issued = 0, n_used = 0;  // chunks through this warp's ring
   int slot = 0;
   uint32_t uphase[kSlots] = {};
@@ -452,18 +484,21 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
     const float* q_s = slots + slot * slot_floats;
     const float* w_s = q_s + p.D * hs;
     const float* b_s = w_s + hs;
-    const int rw = (int)((warp + seq) % kTileWarps) * kWarpKeys;  // this warp's key block in the unit
+    const int kb = (int)((kb0 + seq) % sh.KB);  // this warp's key block in the unit
+    float* terms = const_cast<float*>(b_s) + kTileKeys + kb * term_block;
+    const int rw = kb * kWarpKeys;
     const int64_t row = u % rows;
-    const int64_t t0 = (u / rows) * kTileKeys + rw;
+    const int64_t t0 = (u / rows) * sh.unit_keys + rw;
     bool mine = false;
 #pragma unroll
     for (int j = 0; j < KPT; ++j) mine = mine || b_s[rw + lane + 32 * j] > -1e30f;
+    const bool warp_any = __any_sync(0xffffffffu, mine);
     float wsum[KPT];
 #pragma unroll
     for (int j = 0; j < KPT; ++j) wsum[j] = 0.0f;
-    if (__any_sync(0xffffffffu, mine)) {
+    if (warp_any) {
       const int64_t b = row / p.S;
-      // chunk `it` of the unit ((head group, chunk of dims) order) into the ring
+      // chunk `it` of this warp's groups ((group, chunk of dims) order) into the ring
       auto issue = [&](int it) {
         const uint32_t st = n_issued % kTileStages;
         if (lane == 0) {
@@ -480,7 +515,8 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
       for (int it = 0; it < head; ++it) issue(it);
       uint64_t acc[KPT][kGroupHeads / 2];
       for (int it = 0; it < per_unit; ++it) {
-        const int grp = it / nchunks, c = it - grp * nchunks;
+        const int gl = it / nchunks, c = it - gl * nchunks;
+        const int grp = g_first + gl;
         if (c == 0) {
 #pragma unroll
           for (int j = 0; j < KPT; ++j)
@@ -502,8 +538,10 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
         __syncwarp();
         if (it + kTileStages < per_unit) issue(it + kTileStages);
         if (c == nchunks - 1) {
-          // this group's heads into the head sum, heads ascending
+          // this group's heads, heads ascending: into the head sum (the
+          // block's first warp) or handed over as terms (the others)
           const float* wg = w_s + grp * kGroupHeads;
+          float* tg = terms + ((gw - 1) * sh.gpw + gl) * kGroupHeads * kWarpKeys;
 #pragma unroll
           for (int hp = 0; hp < kGroupHeads / 2; ++hp) {
             const float w0 = wg[2 * hp], w1 = wg[2 * hp + 1];
@@ -513,22 +551,41 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
               unpack2(acc[j][hp], a0, a1);
               float s0 = __fmul_rn(p.scale, a0);
               s0 = s0 > 0.0f ? s0 : 0.0f;  // ReLU (a NaN dot gives 0)
-              wsum[j] = __fadd_rn(wsum[j], __fmul_rn(s0, w0));
               float s1 = __fmul_rn(p.scale, a1);
               s1 = s1 > 0.0f ? s1 : 0.0f;
-              wsum[j] = __fadd_rn(wsum[j], __fmul_rn(s1, w1));
+              const float e0 = __fmul_rn(s0, w0), e1 = __fmul_rn(s1, w1);
+              if (gw == 0) {
+                wsum[j] = __fadd_rn(wsum[j], e0);
+                wsum[j] = __fadd_rn(wsum[j], e1);
+              } else {
+                tg[(2 * hp) * kWarpKeys + lane + 32 * j] = e0;
+                tg[(2 * hp + 1) * kWarpKeys + lane + 32 * j] = e1;
+              }
             }
           }
         }
       }
     }
-    uint32_t* out_bits = reinterpret_cast<uint32_t*>(p.scores) + row * (int64_t)p.T;
+    if (gw > 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tfull0 + 8u * (slot * kTileWarps + kb));  // release: the terms (every unit)
+    } else {
+      if (warp_any && sh.Gs > 1) {
+        // the other warps' heads, in order, after this warp's own
+        if (!mbar_wait_warp(tfull0 + 8u * (slot * kTileWarps + kb), uphase[slot], p.timeout_ns, p.status)) return;
+        const int nt = (sh.Gs - 1) * sh.gpw * kGroupHeads;
+        for (int h = 0; h < nt; ++h)
 #pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-      const int64_t t = t0 + lane + 32 * j;
-      if (t < p.T) {
-        const float bv = b_s[rw + lane + 32 * j];
-        out_bits[t] = score_bits(wsum[j], bv, bv > -1e30f);
+          for (int j = 0; j < KPT; ++j) wsum[j] = __fadd_rn(wsum[j], terms[h * kWarpKeys + lane + 32 * j]);
+      }
+      uint32_t* out_bits = reinterpret_cast<uint32_t*>(p.scores) + row * (int64_t)p.T;
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) {
+        const int64_t t = t0 + lane + 32 * j;
+        if (t < p.T) {
+          const float bv = b_s[rw + lane + 32 * j];
+          out_bits[t] = score_bits(wsum[j], bv, bv > -1e30f);
+        }
       }
     }
     __syncwarp();
@@ -905,19 +962,20 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_kernel(const __grid
 
 template <typename T, int KPT>
 cudaError_t launch_tile(const DsaParams& p, int sms, cudaStream_t stream) {
-  const int hs = (p.H + kGroupHeads - 1) / kGroupHeads * kGroupHeads;
-  const size_t smem = TileSmem<KPT>::bytes(p.D, hs);
+  const TileShape sh = tile_shape(p.H, KPT);
+  const size_t smem = TileSmem<KPT>::bytes(p.D, sh.G * kGroupHeads, sh.term_floats);
   static bool attr_set = false;  // the same value from every caller
   if (!attr_set) {
-    // the largest plan: D * hs at its cap, hs = 64
+    // the largest plan: D * hs at its cap, hs = 64, the most terms
     const cudaError_t e = cudaFuncSetAttribute(dsa_tile_kernel<T, KPT>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)TileSmem<KPT>::bytes(kMaxQFloats / 64, 64));
+                                               (int)TileSmem<KPT>::bytes(kMaxQFloats / 64, 64,
+                                                                         tile_shape(64, KPT).term_floats));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int64_t rows = (int64_t)p.B * p.S;
-  const int64_t units = rows * (((int64_t)p.T + Tile<KPT>::kKeys - 1) / Tile<KPT>::kKeys);
+  const int64_t units = rows * (((int64_t)p.T + sh.unit_keys - 1) / sh.unit_keys);
   const int64_t cap = (int64_t)sms * 2;
   const int grid = (int)(units < cap ? units : cap);
   dsa_tile_kernel<T, KPT><<<grid, kTileThreads, smem, stream>>>(p);
