@@ -57,6 +57,7 @@ constexpr int kScoreThreads = 128;
 constexpr int kDChunk = 32;                  // head-dim columns per shared-memory chunk
 constexpr int kSelectThreads = 256;
 constexpr int kSelectWarps = kSelectThreads / 32;
+constexpr int kMaxCluster = 8;  // CTAs splitting one row in the selection (16, non-portable, measured slower)
 constexpr uint32_t kNotAllowed = 0xFFFFFFFFu;  // score bits of a cell that is not allowed
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
@@ -670,13 +671,13 @@ __device__ __forceinline__ void cluster_sync_all() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Shared word `a` summed over the cluster's csize (<= 8) CTAs: the eight
-// remote loads go out in one block (ranks past csize read the last CTA and
-// are not added), so they cost one latency.
-__device__ __forceinline__ uint32_t cluster_sum8(const uint32_t* a, int csize) {
+// Shared word `a` summed over CTAs r0 .. r0 + 7 of the cluster's csize: the
+// eight remote loads go out in one block (ranks past csize read the last CTA
+// and are not added), so they cost one latency.
+__device__ __forceinline__ uint32_t cluster_sum8(const uint32_t* a, int r0, int csize) {
   uint32_t r[8], v[8];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) r[c] = (uint32_t)(c < csize ? c : csize - 1);
+  for (int c = 0; c < 8; ++c) r[c] = (uint32_t)(r0 + c < csize ? r0 + c : csize - 1);
   asm volatile(
       "{\n\t.reg .u32 a<8>;\n\t"
       "mapa.shared::cluster.u32 a0, %8, %9;\n\tmapa.shared::cluster.u32 a1, %8, %10;\n\t"
@@ -692,7 +693,7 @@ __device__ __forceinline__ uint32_t cluster_sum8(const uint32_t* a, int csize) {
       : "memory");
   uint32_t sum = 0;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) sum += c < csize ? v[c] : 0u;
+  for (int c = 0; c < 8; ++c) sum += r0 + c < csize ? v[c] : 0u;
   return sum;
 }
 
@@ -725,6 +726,7 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_cluster(const __gri
   __shared__ __align__(16) uint32_t w_gt[kSelectWarps];
   __shared__ __align__(16) uint32_t w_eq[kSelectWarps];
   static_assert(kSelectWarps == 8, "peer_sum8 reads eight per-warp counts");
+  static_assert(kMaxCluster <= 8, "cluster_sum8 sums eight CTAs");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t crank = cluster_rank();
   const int64_t rows = (int64_t)p.B * p.S;
@@ -761,10 +763,12 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_cluster(const __gri
     for (int64_t i = keep + (int64_t)crank * kSelectThreads + tid; i < p.top_k; i += (int64_t)csize * kSelectThreads)
       out[i] = -1;
     if (keep > 0) {  // the same in every CTA of the cluster
-      // radix select of the keep-th largest key, 8 bits at a time from the top
+      // radix select of the keep-th largest key, 8 bits at a time from the
+      // top; when every allowed key is kept the threshold is simply 0 (the
+      // "not allowed" key), and the passes are skipped
       uint32_t prefix = 0, pmask = 0, rank = keep;
 #pragma unroll 1
-      for (int pass = 0; pass < 4; ++pass) {
+      for (int pass = 0; pass < (keep < allowed ? 4 : 0); ++pass) {
         const int shift = 24 - 8 * pass;
         uint32_t* h = hist[pass % 3];
         // the next pass's buffer, last read by the peers two passes ago
@@ -781,7 +785,7 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_cluster(const __gri
         if (csize > 1) {
           // the cluster's histogram, one bin a thread (gh is rewritten only
           // after the next pass's cluster barrier, when every warp has read it)
-          gh[tid] = cluster_sum8(&h[tid], csize);
+          gh[tid] = cluster_sum8(&h[tid], 0, csize);  // csize <= kMaxCluster == 8
           __syncthreads();
           hc = gh;
         }
@@ -1014,12 +1018,12 @@ cudaError_t launch_score_t(const DsaParams& p, int sms, cudaStream_t stream) {
 constexpr int64_t kSliceMaxBytes = 160 * 1024;  // a CTA's slice of a row in shared memory
 
 // Cluster size for the resident selection (0: stream from global memory):
-// the smallest of 1, 2, 4, 8 that gives every SM a CTA, else 8, as long as
-// the slice fits.
+// the smallest of 1, 2, 4, ... kMaxCluster that gives every SM a CTA, else
+// kMaxCluster, as long as the slice fits.
 int select_cluster_size(int64_t rows, int64_t T, int sms, int* slice) {
-  for (int c = 1; c <= 8; c *= 2) {
+  for (int c = 1; c <= kMaxCluster; c *= 2) {
     const int64_t L = (T + c - 1) / c;
-    if (L * 4 <= kSliceMaxBytes && (rows * c >= sms || c == 8)) {
+    if (L * 4 <= kSliceMaxBytes && (rows * c >= sms || c == kMaxCluster)) {
       *slice = (int)L;
       return c;
     }
