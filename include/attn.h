@@ -21,7 +21,7 @@ extern "C" {
 enum attn_status {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1, /* a bad size, flag, null pointer or overlapping output      */
-    ATTN_ERR_UNSUPPORTED = 2, /* a valid request this build has no kernel for              */
+    ATTN_ERR_UNSUPPORTED = 2, /* a valid request the library has no kernel for             */
     ATTN_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed (see attn_last_cuda_error) */
     ATTN_ERR_TIMEOUT = 4      /* a kernel gave up on a bounded wait (see attn_get_device_status) */
 };
