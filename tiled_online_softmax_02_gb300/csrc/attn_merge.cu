@@ -19,7 +19,12 @@ namespace {
 // unconditionally (a range without keys holds -inf and weight 0, and its
 // partial row is never multiplied in), so they overlap instead of forming a
 // chain of dependent branches.
+//
+// Launched as a programmatic dependent of the split kernel: its CTAs may be
+// scheduled as that grid drains, and every thread waits for the whole grid
+// (and its writes to the workspace) before reading.
 __global__ void attn_merge_kernel(const MergeParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t groups = p.D / 2;
   const int64_t rows = (int64_t)p.B * p.Hq * p.Sq;
   const int64_t plane = rows * p.D;  // floats per split in ws_o
@@ -73,8 +78,16 @@ cudaError_t launch_attn_merge(const MergeParams& p, cudaStream_t stream) {
   const int64_t work = (int64_t)p.B * p.Hq * p.Sq * (p.D / 2);
   const int threads = 128;
   const int64_t blocks = (work + threads - 1) / threads;
-  attn_merge_kernel<<<(unsigned)(blocks < 65535 * 8 ? blocks : 65535 * 8), threads, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(blocks < 65535 * 8 ? blocks : 65535 * 8), 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_merge_kernel, p);
 }
 
 cudaError_t launch_fill_f32(float* dst, int64_t n, float value, cudaStream_t stream) {

@@ -15,19 +15,20 @@
 // so they run on the CUDA cores -- a tensor-core product would round
 // differently and move near-tied selections.
 //
-//   dsa_tile_kernel     the score kernel for rows of whole 32-byte chunks.
-//                       A producer warp streams K through a four-stage
-//                       shared-memory ring with TMA (32-byte swizzled rows);
-//                       four compute warps each own 32 * KPT keys and keep
-//                       their dot products for every head in registers as
-//                       packed pairs (two heads per fma.rn.f32x2 with a -0
-//                       addend / add.rn.f32x2: each element still rounded
-//                       on its own; a pair takes one issue slot, leaving
-//                       slots for the loads while the fp32 pipe, not issue,
-//                       bounds the loop).  q of the row
-//                       sits in shared memory as fp32 [d][h], one broadcast
-//                       128-bit load feeding two head pairs.  Units whose
-//                       keys are all masked are skipped by both sides.
+//   dsa_tile_kernel     the score kernel for rows of whole 64-byte chunks.
+//                       CTAs take (row, key block) units from a counter; a
+//                       staging warp posts each unit's q (fp32 [d][h] in
+//                       shared memory, one broadcast 128-bit load feeding
+//                       two head pairs), head weights and bias into one of
+//                       two slots, and four compute warps each stream their
+//                       own keys of K through a private two-stage TMA ring
+//                       (64-byte swizzled rows).  Dot products sit in
+//                       registers as packed pairs (two heads per
+//                       fma.rn.f32x2 with a -0 addend / add.rn.f32x2: each
+//                       element still rounded on its own; a pair takes one
+//                       issue slot, leaving slots for the loads while the
+//                       fp32 pipe, not issue, bounds the loop).  Units whose
+//                       keys are all masked are marked and skipped.
 //   dsa_score_kernel    the general score kernel (any head dim / alignment):
 //                       K chunks transposed into shared memory by the CTA,
 //                       scalar rounded multiplies and adds.
@@ -39,6 +40,11 @@
 //                       compaction.
 //   dsa_select_kernel   selection streaming the row from global memory
 //                       (rows too long for the cluster's shared memory).
+//
+// The selection kernels are launched as programmatic dependents of the score
+// kernel: their CTAs may become resident while its last units run, and each
+// thread waits (griddepcontrol.wait, a hardware dependency on the whole score
+// grid and its memory) before it reads anything.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -59,6 +65,12 @@ constexpr int kSelectThreads = 256;
 constexpr int kSelectWarps = kSelectThreads / 32;
 constexpr int kMaxCluster = 8;  // CTAs splitting one row in the selection (16, non-portable, measured slower)
 constexpr uint32_t kNotAllowed = 0xFFFFFFFFu;  // score bits of a cell that is not allowed
+
+// Programmatic dependent launch.  The dependents may launch once every CTA
+// of this grid has signalled (or exited); they still see this grid's writes
+// only after their own wait, which returns once the whole grid is complete.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
@@ -406,6 +418,7 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
   const uint32_t ufull0 = full0 + 8u * kTileWarps * kTileStages, uempty0 = ufull0 + 8u * kSlots;
   const uint32_t tfull0 = uempty0 + 8u * kSlots;  // [slot][key block]: the other warps' terms
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();  // the selection may take SMs this grid leaves idle
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTileWarps * kTileStages; ++i) mbar_init(full0 + 8u * i, 1);
     for (int s = 0; s < kSlots; ++s) {
@@ -429,11 +442,15 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
     // increasing order over all CTAs, so an SM that finishes early takes
     // more) that has an allowed key; units passed over get the mark; bv then
     // holds its bias
+    // (a CTA's first unit is its own index: the grid is never larger than
+    // the unit count, and the counter hands out units from gridDim.x on)
+    bool first = true;
     auto next_active = [&]() -> int64_t {
       for (;;) {
         unsigned long long w = 0;
-        if (lane == 0) w = atomicAdd(p.unit_counter, 1ull);
-        const int64_t v = (int64_t)__shfl_sync(0xffffffffu, w, 0);
+        if (lane == 0 && !first) w = atomicAdd(p.unit_counter, 1ull);
+        const int64_t v = first ? (int64_t)blockIdx.x : (int64_t)gridDim.x + (int64_t)__shfl_sync(0xffffffffu, w, 0);
+        first = false;
         if (v >= units) return units;
         if (unit_bias<KPT>(p, rows, v, sh.unit_keys, lane, bv)) return v;
         const int64_t row = v % rows, t0 = (v / rows) * sh.unit_keys;
@@ -727,6 +744,7 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_cluster(const __gri
   __shared__ __align__(16) uint32_t w_eq[kSelectWarps];
   static_assert(kSelectWarps == 8, "peer_sum8 reads eight per-warp counts");
   static_assert(kMaxCluster <= 8, "cluster_sum8 sums eight CTAs");
+  pdl_wait();  // the score grid is complete and its scores visible
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t crank = cluster_rank();
   const int64_t rows = (int64_t)p.B * p.S;
@@ -904,6 +922,7 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_kernel(const __grid
   __shared__ uint32_t hist[256];
   __shared__ uint32_t warp_sums[kSelectWarps];
   __shared__ uint32_t digit_s, rank_s;
+  pdl_wait();  // the score grid is complete and its scores visible
   const int tid = threadIdx.x;
   const int64_t rows = (int64_t)p.B * p.S;
   const int64_t T = p.T;
@@ -1035,10 +1054,22 @@ cudaError_t launch_select(const DsaParams& p, int sms, cudaStream_t stream) {
   const int64_t rows = (int64_t)p.B * p.S;
   int slice = 0;
   const int c = select_cluster_size(rows, p.T, sms, &slice);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kSelectThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (p.T > 0) {  // a programmatic dependent of the score kernel just enqueued
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   if (c == 0) {
     const int64_t cap = (int64_t)sms * 8;
-    dsa_select_kernel<<<(int)(rows < cap ? rows : cap), kSelectThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    cfg.gridDim = dim3((unsigned)(rows < cap ? rows : cap), 1, 1);
+    cfg.attrs = attr;
+    cfg.numAttrs = (unsigned)na;
+    return cudaLaunchKernelEx(&cfg, dsa_select_kernel, p);
   }
   static bool attr_set = false;
   if (!attr_set) {
@@ -1049,18 +1080,15 @@ cudaError_t launch_select(const DsaParams& p, int sms, cudaStream_t stream) {
   }
   const int64_t max_clusters = (int64_t)sms * 8 / c;
   const int64_t clusters = rows < max_clusters ? rows : max_clusters;
-  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(clusters * c), 1, 1);
-  cfg.blockDim = dim3(kSelectThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)slice * 4;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)c;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = (unsigned)c;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = (unsigned)na;
   return cudaLaunchKernelEx(&cfg, dsa_select_cluster, p, c, slice);
 }
 
