@@ -98,6 +98,11 @@ __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
   asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
   return d;
 }
+__device__ __forceinline__ uint64_t pack2u(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
 __device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
 }
@@ -213,7 +218,6 @@ __global__ void __launch_bounds__(kScoreThreads) dsa_score_kernel(const __grid_c
 // -------------------------------------------------------------- tile scores
 constexpr int kTileWarps = 4;                          // compute warps
 constexpr int kTileThreads = (kTileWarps + 1) * 32;    // + the staging warp
-constexpr int kTileStages = 2;                         // K ring depth of each compute warp
 constexpr int kBoxRows = 64;                           // key rows per TMA box
 constexpr int kRowBytes = 64;                          // one swizzled shared-memory row of K
 constexpr int kGroupHeads = 16;                        // heads per pass over K
@@ -227,6 +231,10 @@ struct Tile {
   static constexpr int kKeys = kTileWarps * kWarpKeys;      // keys per unit
   static constexpr int kStageBytes = kWarpKeys * kRowBytes; // one stage of one warp's ring
   static constexpr int kBoxes = kWarpKeys / kBoxRows;
+  // K ring depth of each compute warp: with 2 keys a lane a chunk's compute
+  // is short against an HBM round trip, and the smaller stages leave room
+  // for a third at two CTAs per SM
+  static constexpr int kStages = KPT == 2 ? 3 : 2;
 };
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -261,11 +269,11 @@ __device__ __forceinline__ float group_elem<__half>(const uint4& g, int e) {
 
 // One chunk of 32 bytes of dims for this lane's KPT keys and one group of
 // 16 heads: acc[j][hp] holds heads (2 hp, 2 hp + 1) of the group for key
-// r0 + 32 j.  q_c points at the chunk's first dim and the group's first head
-// in q_s ([d][hs], row stride hs); each accumulator takes its dims in
-// ascending order.
+// r0 + 32 j.  q_c is the shared-memory address of the chunk's first dim and
+// the group's first head in q_s ([d][hs], row stride hs); each accumulator
+// takes its dims in ascending order.
 template <typename T, int KPT>
-__device__ __forceinline__ void tile_chunk(uint64_t (&acc)[KPT][kGroupHeads / 2], uint32_t kst, const float* q_c,
+__device__ __forceinline__ void tile_chunk(uint64_t (&acc)[KPT][kGroupHeads / 2], uint32_t kst, uint32_t q_c,
                                            int hs, int r0, uint64_t z) {
   constexpr int kGroups = kRowBytes / 16;
   constexpr int kVec = 16 / (int)sizeof(T);
@@ -285,11 +293,11 @@ __device__ __forceinline__ void tile_chunk(uint64_t (&acc)[KPT][kGroupHeads / 2]
         const float kv = group_elem<T>(raw[j], e);
         kd[j] = pack2(kv, kv);
       }
-      const float4* qd = reinterpret_cast<const float4*>(q_c + (g * kVec + e) * hs);
+      const uint32_t qd = q_c + (uint32_t)((g * kVec + e) * hs) * 4u;
 #pragma unroll
       for (int hq = 0; hq < kGroupHeads / 4; ++hq) {
-        const float4 qv = qd[hq];
-        const uint64_t q01 = pack2(qv.x, qv.y), q23 = pack2(qv.z, qv.w);
+        const uint4 qv = lds128(qd + 16u * hq);  // broadcast: every lane the same heads
+        const uint64_t q01 = pack2u(qv.x, qv.y), q23 = pack2u(qv.z, qv.w);
 #pragma unroll
         for (int j = 0; j < KPT; ++j) {
           acc[j][2 * hq] = add_rn2(acc[j][2 * hq], mul_rn2(q01, kd[j], z));
@@ -355,12 +363,12 @@ __host__ __device__ inline TileShape tile_shape(int H, int kpt) {
 template <int KPT>
 struct TileSmem {
   static constexpr int kSlots = 2;
-  static constexpr int kBars = kTileWarps * kTileStages + 2 * kSlots + kSlots * kTileWarps;
+  static constexpr int kBars = kTileWarps * Tile<KPT>::kStages + 2 * kSlots + kSlots * kTileWarps;
   __host__ __device__ static size_t slot_floats(int D, int hs, int terms) {
     return (size_t)D * hs + hs + Tile<KPT>::kKeys + terms;
   }
   __host__ __device__ static size_t bytes(int D, int hs, int terms) {
-    return 1024 + (size_t)kTileWarps * kTileStages * Tile<KPT>::kStageBytes + kSlots * slot_floats(D, hs, terms) * 4 +
+    return 1024 + (size_t)kTileWarps * Tile<KPT>::kStages * Tile<KPT>::kStageBytes + kSlots * slot_floats(D, hs, terms) * 4 +
            kSlots * 8 + kBars * 8;
   }
 };
@@ -403,6 +411,7 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
   constexpr int kTileKeys = Tile<KPT>::kKeys;
   constexpr int kWarpKeys = Tile<KPT>::kWarpKeys;
   constexpr int kStageBytes = Tile<KPT>::kStageBytes;
+  constexpr int kTileStages = Tile<KPT>::kStages;
   constexpr int kSlots = TileSmem<KPT>::kSlots;
   extern __shared__ uint8_t smem_raw[];
   const TileShape sh = tile_shape(p.H, KPT);
@@ -543,16 +552,15 @@ __global__ void __launch_bounds__(kTileThreads, 2) dsa_tile_kernel(const __grid_
         }
         const uint32_t st = n_used % kTileStages;
         if (!mbar_wait_warp(my_full + 8u * st, (n_used / kTileStages) & 1u, p.timeout_ns, p.status)) {
-          // timed out (recorded): let the other copy in flight land first
-          if (lane == 0 && n_issued > n_used + 1) {
-            const uint32_t o = (n_used + 1) % kTileStages;
-            mbar_wait(my_full + 8u * o, ((n_used + 1) / kTileStages) & 1u, p.timeout_ns, p.status);
-          }
+          // timed out (recorded): let the other copies in flight land first
+          if (lane == 0)
+            for (uint32_t o = n_used + 1; o < n_issued; ++o)
+              mbar_wait(my_full + 8u * (o % kTileStages), (o / kTileStages) & 1u, p.timeout_ns, p.status);
           return;
         }
         ++n_used;
-        tile_chunk<T, KPT>(acc, my_ring + st * kStageBytes, q_s + c * kDims * hs + grp * kGroupHeads, hs, lane,
-                           p.neg_zero2);
+        const uint32_t q_c = smem_u32(q_s + c * kDims * hs + grp * kGroupHeads);
+        tile_chunk<T, KPT>(acc, my_ring + st * kStageBytes, q_c, hs, lane, p.neg_zero2);
         __syncwarp();
         if (it + kTileStages < per_unit) issue(it + kTileStages);
         if (c == nchunks - 1) {
