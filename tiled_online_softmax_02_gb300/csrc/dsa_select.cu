@@ -748,8 +748,10 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_cluster(const __gri
   __shared__ uint32_t hist[3][256];     // per radix pass, three in rotation (peers read them)
   __shared__ uint32_t gh[256];          // the cluster's histogram of a pass (clusters of 2 or more)
   __shared__ __align__(16) uint32_t w_ok[kSelectWarps];  // per-warp counts, read by peers
-  __shared__ __align__(16) uint32_t w_gt[kSelectWarps];
-  __shared__ __align__(16) uint32_t w_eq[kSelectWarps];
+  // per-warp counts of keys above / at the threshold, packed (above) | (at << 16):
+  // a slice holds at most kSliceMaxBytes / 4 < 65536 keys, so the sums of
+  // eight warps never carry across the halves
+  __shared__ __align__(16) uint32_t w_ge[kSelectWarps];
   static_assert(kSelectWarps == 8, "peer_sum8 reads eight per-warp counts");
   static_assert(kMaxCluster <= 8, "cluster_sum8 sums eight CTAs");
   pdl_wait();  // the score grid is complete and its scores visible
@@ -767,7 +769,20 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_cluster(const __gri
     const uint32_t* bits = reinterpret_cast<const uint32_t*>(p.scores) + row * T + base;
     int64_t* out = p.out + row * (int64_t)p.top_k;
     uint32_t mine = 0;
-    for (int i = tid; i < n; i += kSelectThreads) {
+    int i0 = 0;
+    if ((reinterpret_cast<uintptr_t>(bits) & 15u) == 0) {  // 16-byte loads and stores for whole quads
+      const int n4 = n >> 2;
+      const uint4* b4 = reinterpret_cast<const uint4*>(bits);
+      uint4* k4 = reinterpret_cast<uint4*>(keys_s);
+      for (int v = tid; v < n4; v += kSelectThreads) {
+        const uint4 x = b4[v];
+        const uint4 k = make_uint4(order_key(x.x), order_key(x.y), order_key(x.z), order_key(x.w));
+        k4[v] = k;
+        mine += (k.x != 0u) + (k.y != 0u) + (k.z != 0u) + (k.w != 0u);
+      }
+      i0 = n4 << 2;
+    }
+    for (int i = i0 + tid; i < n; i += kSelectThreads) {
       const uint32_t k = order_key(bits[i]);
       keys_s[i] = k;
       mine += k != 0u;
@@ -830,19 +845,26 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_cluster(const __gri
         }
         const uint32_t excl = incl - sum;
         const int owner = __ffs(__ballot_sync(0xffffffffu, excl < rank && rank <= incl)) - 1;
-        uint32_t digit = 0, rin = 0, acc = excl;
+        uint32_t digit = 0, rin = 0, cnt = 0, acc = excl;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if (acc < rank && rank <= acc + c[i]) {
             digit = 255u - 8u * lane - i;
             rin = rank - acc;
+            cnt = c[i];
           }
           acc += c[i];
         }
         digit = __shfl_sync(0xffffffffu, digit, owner);
         rank = __shfl_sync(0xffffffffu, rin, owner);
+        cnt = __shfl_sync(0xffffffffu, cnt, owner);
         prefix |= digit << shift;
         pmask |= 255u << shift;
+        // the whole bin is kept: its lowest key (lower bits 0) serves as the
+        // threshold -- every key of the bin is >= it, those equal to it are
+        // all taken as ties -- and the remaining passes are not needed (the
+        // same decision in every CTA: they share the cluster's histogram)
+        if (rank == cnt) break;
       }
       const uint32_t thr = prefix;  // the keep-th largest key
       uint32_t g = 0, e = 0;
@@ -853,31 +875,24 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_cluster(const __gri
       }
       g = __reduce_add_sync(0xffffffffu, g);
       e = __reduce_add_sync(0xffffffffu, e);
-      if (lane == 0) {
-        w_gt[warp] = g;
-        w_eq[warp] = e;
-      }
+      if (lane == 0) w_ge[warp] = g | (e << 16);
       cluster_sync_all();
       // keys above / at thr in the CTAs before this one (slices in key order),
       // over the cluster, and in this CTA's warps before this one
-      uint32_t pg = 0, pe = 0;
+      uint32_t pge = 0;  // CTA `lane`'s packed counts
       if (lane < csize) {
-        if (csize == 1) {
-          for (int w = 0; w < kSelectWarps; ++w) {
-            pg += w_gt[w];
-            pe += w_eq[w];
-          }
-        } else {
-          pg = peer_sum8(w_gt, (uint32_t)lane);
-          pe = peer_sum8(w_eq, (uint32_t)lane);
-        }
+        if (csize == 1)
+          for (int w = 0; w < kSelectWarps; ++w) pge += w_ge[w];
+        else
+          pge = peer_sum8(w_ge, (uint32_t)lane);
       }
+      const uint32_t pg = pge & 0xFFFFu, pe = pge >> 16;
       const uint32_t gt_total = __reduce_add_sync(0xffffffffu, pg);
       uint32_t gt_before = __reduce_add_sync(0xffffffffu, (uint32_t)lane < crank ? pg : 0u);
       uint32_t eq_before = __reduce_add_sync(0xffffffffu, (uint32_t)lane < crank ? pe : 0u);
       for (int w = 0; w < warp; ++w) {
-        gt_before += w_gt[w];
-        eq_before += w_eq[w];
+        gt_before += w_ge[w] & 0xFFFFu;
+        eq_before += w_ge[w] >> 16;
       }
       // keys equal to thr are taken lowest index first
       const uint32_t ties = keep - gt_total;
@@ -1043,6 +1058,7 @@ cudaError_t launch_score_t(const DsaParams& p, int sms, cudaStream_t stream) {
 }
 
 constexpr int64_t kSliceMaxBytes = 160 * 1024;  // a CTA's slice of a row in shared memory
+static_assert(kSliceMaxBytes / 4 < 65536, "dsa_select_cluster packs per-CTA key counts in 16 bits");
 
 // Cluster size for the resident selection (0: stream from global memory):
 // the smallest of 1, 2, 4, ... kMaxCluster that gives every SM a CTA, else
