@@ -631,13 +631,11 @@ __device__ __forceinline__ uint32_t order_key(uint32_t bits) {
 
 // Adds one to bin `bin` of h for every lane with `active`: one shared atomic
 // per distinct bin in the warp (scores of a row crowd into few top digits).
-// Warp-collective.
+// Warp-collective and branch-free (inactive lanes match among themselves on
+// a key no bin has), so the updates of several keys can overlap.
 __device__ __forceinline__ void hist_add(uint32_t* h, uint32_t bin, bool active) {
-  const uint32_t act = __ballot_sync(0xffffffffu, active);
-  if (active) {
-    const uint32_t peers = __match_any_sync(act, bin);
-    if (__ffs(peers) - 1 == (int)(threadIdx.x & 31)) atomicAdd(&h[bin], (uint32_t)__popc(peers));
-  }
+  const uint32_t peers = __match_any_sync(0xffffffffu, active ? bin : 0xFFFFFFFFu);
+  if (active && __ffs(peers) - 1 == (int)(threadIdx.x & 31)) atomicAdd(&h[bin], (uint32_t)__popc(peers));
 }
 
 
@@ -814,12 +812,18 @@ __global__ void __launch_bounds__(kSelectThreads) dsa_select_cluster(const __gri
         uint32_t* h = hist[pass % 3];
         // the next pass's buffer, last read by the peers two passes ago
         if (pass == 1 || pass == 2) hist[(pass + 1) % 3][tid] = 0u;
-        for (int i0 = 0; i0 < n; i0 += kSelectThreads) {
-          const int i = i0 + tid;
-          const uint32_t k = i < n ? keys_s[i] : 0u;
+        // four keys a thread per step, loaded first (independent updates)
+        for (int i0 = 0; i0 < n; i0 += 4 * kSelectThreads) {
+          uint32_t k[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kSelectThreads + tid;
+            k[u] = i < n ? keys_s[i] : 0u;
+          }
           // cells that are not allowed (key 0) sit below every allowed one
           // and rank <= #allowed, so they never decide a digit
-          hist_add(h, (k >> shift) & 255u, k != 0u && (k & pmask) == prefix);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) hist_add(h, (k[u] >> shift) & 255u, k[u] != 0u && (k[u] & pmask) == prefix);
         }
         cluster_sync_all();  // every CTA's histogram of this pass is complete
         const uint32_t* hc = h;
