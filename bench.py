@@ -56,8 +56,8 @@ NCU_TRAFFIC = {
     "decode_bf16+splitkv": {"bytes_per_launch": 777046272, "source_hash": "aee60e800bf42d81"},
     "gqa_causal_bf16_d256": {"bytes_per_launch": 435266560, "source_hash": "6b4b5aabb41779d5"},
     # the DSA indexer: the tile score kernel (the selection kernel's traffic is in its profile)
-    "dsa_prefill_bf16": {"bytes_per_launch": 139407616, "source_hash": "03b129022f01c07b"},
-    "dsa_decode_bf16": {"bytes_per_launch": 34638080, "source_hash": "03b129022f01c07b"},
+    "dsa_prefill_bf16": {"bytes_per_launch": 139407616, "source_hash": "9717cc89f81595d7"},
+    "dsa_decode_bf16": {"bytes_per_launch": 34638080, "source_hash": "9717cc89f81595d7"},
 }
 
 

@@ -24,7 +24,7 @@ struct DsaParams {
   uint64_t timeout_ns;
   int* status;          // device status word (timeouts)
   uint64_t neg_zero2;   // (-0.0f, -0.0f) as a packed pair: the addend of the rounded products
-  unsigned long long* unit_counter;  // tile path: next unit to take, zero at launch (in the workspace)
+  unsigned long long* unit_counter;  // tile path: units handed out past the grid size, zero at launch (in the workspace)
 };
 
 // Whether the TMA-fed score kernel takes a problem: key / query rows of
