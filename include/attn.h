@@ -123,7 +123,10 @@ int attn_fwd(const void *q, const void *k, const void *v, const float *mask,
  *                   when the split count is 1.  Calls that share a workspace
  *                   must not overlap on the GPU.
  * Launches the attention kernel and, when split, one merge kernel, on
- * `stream`; allocates and synchronises nothing.  Errors as attn_fwd;
+ * `stream`; allocates and synchronises nothing.  The merge kernel is a
+ * programmatic dependent of the attention kernel (it may be scheduled while
+ * that kernel drains and waits for it in hardware; under stream capture the
+ * two are joined by a programmatic graph edge).  Errors as attn_fwd;
  * ATTN_ERR_INVALID_ARG also for a split count outside 0..64 or a missing /
  * too small workspace.
  */
@@ -220,7 +223,12 @@ size_t attn_f32_split_workspace_bytes(int B, int Hkv, int kv_capacity, int D);
  *            NULL when T == 0.  Calls that share a workspace must not overlap
  *            on the GPU.
  * Enqueues an 8-byte memset (for the counter) and two kernels on
- * `stream`; allocates and synchronises nothing.
+ * `stream`; allocates and synchronises nothing, so it may be captured into
+ * a CUDA graph (make one call on the device before capturing: the first call
+ * sets kernel attributes and looks up the tensor-map encoder).  The second
+ * kernel (the selection) is a programmatic dependent of the first (the
+ * scores): it may be scheduled while the first drains and waits for it in
+ * hardware before reading a score.
  * Errors: ATTN_ERR_INVALID_ARG (bad size, attribute, dtype, null or
  * overlapping pointer, small workspace), ATTN_ERR_UNSUPPORTED (H > 64,
  * misaligned pointers), ATTN_ERR_CUDA (launch failure).
