@@ -295,6 +295,10 @@ int attn_get_device_status(void *stream);
  * which a kernel stops waiting on an internal barrier, records
  * ATTN_ERR_TIMEOUT and exits.  Applies to launches made after the call.
  * 0 restores the default (2 s).  Returns ATTN_OK.
+ * After a timeout the outputs of the launches involved are not valid: rows a
+ * kernel could not finish keep what the buffer held before, except rows
+ * merged across a thread-block cluster from an unfinished part, which are
+ * written as 0 (log-sum-exp -inf) rather than from stale partial results.
  */
 int attn_set_wait_timeout_ns(uint64_t timeout_ns);
 

@@ -216,4 +216,23 @@ def pin_rows_equal_full(lib):
     assert full[0, 0, 3, :].tolist().count(5) == 0  # at the threshold: never listed
 
 
+def pin_threaded_calls_equal_one_thread(lib):
+    """Splitting rows over threads changes nothing: bit-identical scores and
+    identical indices, for row chunks that cross batch boundaries."""
+    rng = np.random.default_rng(15)
+    B, S, H, D, T = 3, 7, 5, 24, 50
+    q = rng.standard_normal((B, S, H, D)).astype(F32)
+    k = rng.standard_normal((B, T, D)).astype(F32)
+    w = rng.standard_normal((B, S, H)).astype(F32)
+    bias = np.where(rng.random((B, 1, S, T)) < 0.3, -np.inf, rng.standard_normal((B, 1, S, T))).astype(F32)
+    sc1, al1 = dsa.scores(q, k, w, bias, scale=0.2, lib=lib)
+    for nt in (2, 4, 0):
+        scn, aln = dsa.scores(q, k, w, bias, scale=0.2, nthreads=nt, lib=lib)
+        assert np.array_equal(sc1.view(np.uint32), scn.view(np.uint32)) and np.array_equal(al1, aln)
+        rows = np.arange(B * S)[::-1].copy()
+        r1 = dsa.rows(q, k, w, bias, rows, top_k=9, scale=0.2, lib=lib)
+        rn = dsa.rows(q, k, w, bias, rows, top_k=9, scale=0.2, nthreads=nt, lib=lib)
+        assert np.array_equal(r1, rn)
+
+
 PINS = [v for name, v in sorted(globals().items()) if name.startswith("pin_") and callable(v)]

@@ -91,6 +91,8 @@ INVALID = {
     "out_overlaps_q": dict(out=Q + 64),
     "out_overlaps_k": dict(out=K),
     "out_overlaps_mask": dict(mask=MASK, planes=2, out=MASK + 16),
+    "out_overlaps_total_lengths": dict(total=TOT, out=TOT - 64),
+    "out_overlaps_past_lengths": dict(past=PAST, out=PAST),
     "grid_z_too_large": dict(B=70000, Hq=2, Hkv=2, Sq=1, D=64),
     "size_overflow": dict(B=65535, Hq=65535, Hkv=65535, Sq=2**31 - 1, Sk=1, cap=2**31 - 1),
 }
@@ -137,6 +139,16 @@ def test_splitkv_validation(lib):
     assert call_splitkv(lib, 4, ws=0x78000008, ws_bytes=need) == attn.ATTN_ERR_UNSUPPORTED
     assert call_splitkv(lib, 4, ws=Q, ws_bytes=need) == attn.ATTN_ERR_INVALID_ARG  # overlaps q
     assert call_splitkv(lib, 2, lse=0x7C000002) == attn.ATTN_ERR_UNSUPPORTED
+    # the workspace and the log-sum-exp are written: they may overlap nothing the call reads
+    WS, LSE = 0x78000000, 0x7C000000
+    mask_kw = dict(mask=MASK, planes=2)
+    assert call_splitkv(lib, 4, ws=MASK, ws_bytes=need, **mask_kw) == attn.ATTN_ERR_INVALID_ARG
+    assert call_splitkv(lib, 4, ws=TOT - 16, ws_bytes=need, total=TOT) == attn.ATTN_ERR_INVALID_ARG
+    assert call_splitkv(lib, 4, ws=PAST, ws_bytes=need, past=PAST) == attn.ATTN_ERR_INVALID_ARG
+    assert call_splitkv(lib, 4, ws=WS, ws_bytes=need, lse=WS + need - 4) == attn.ATTN_ERR_INVALID_ARG
+    for where in (Q, K + 4096, V, MASK + 64, TOT, PAST):
+        assert call_splitkv(lib, 2, ws=WS, ws_bytes=need, lse=where, total=TOT, past=PAST,
+                            **mask_kw) == attn.ATTN_ERR_INVALID_ARG, hex(where)
     assert lib.attn_splitkv_workspace_bytes(2, 4, 200, 64, 1) == 0
     assert call_splitkv(lib, 4, B=0) == attn.ATTN_OK
     assert call_splitkv(lib, 4, D=256) == attn.ATTN_ERR_UNSUPPORTED  # D 256: attn_fwd only
@@ -190,6 +202,7 @@ def test_f32_split_validation(lib):
     assert call_f32split(lib, ws=WS, ws_bytes=need - 1) == attn.ATTN_ERR_INVALID_ARG  # too small
     assert call_f32split(lib, ws=WS + 8, ws_bytes=need) == attn.ATTN_ERR_UNSUPPORTED  # misaligned
     assert call_f32split(lib, ws=K, ws_bytes=need) == attn.ATTN_ERR_INVALID_ARG       # overlaps k
+    assert call_f32split(lib, ws=TOT, ws_bytes=need, total=TOT) == attn.ATTN_ERR_INVALID_ARG
     assert call_f32split(lib, ws=WS, ws_bytes=need, D=96) == attn.ATTN_ERR_UNSUPPORTED
     assert call_f32split(lib, ws=WS, ws_bytes=need, D=256) == attn.ATTN_ERR_UNSUPPORTED
     assert call_f32split(lib, ws=WS, ws_bytes=need, Hq=5) == attn.ATTN_ERR_INVALID_ARG

@@ -4,15 +4,14 @@ on the same seeded inputs -- every row count around the 16 / 32 variants,
 both head dims and 16-bit types, causal rows with different limits, window,
 soft-cap, the three mask broadcasts, token-major output, NaN / Inf garbage
 past the valid length, rows without keys, a running maximum that keeps
-growing, and the full-size decode workload on sampled rows."""
+growing, and every row of the full-size decode workload."""
 import numpy as np
 import pytest
 import torch
 
-from parity import (check, check_lse, gather_rows, oracle_rows, run_gpu, run_gpu_splitkv,
-                    run_oracle, run_oracle_lse)
-from tiled_online_softmax_02_gb300.inputs import (EXTRA_WORKLOADS, Workload, make_inputs,
-                                                  sample_rows)
+from parity import (check, check_lse, lse_tolerance, run_gpu, run_gpu_splitkv, run_oracle,
+                    run_oracle_lse)
+from tiled_online_softmax_02_gb300.inputs import EXTRA_WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -66,7 +65,7 @@ def test_row_counts_splitkv(shape, splits):
     out, lse = run_gpu_splitkv(w, x, splits)
     ref, ref_lse = run_oracle_lse(w, x)
     check(w, out.double().cpu().numpy(), ref, f"{shape} splits={splits}")
-    check_lse(lse.cpu().numpy(), ref_lse, f"{shape} splits={splits} lse")
+    check_lse(lse.cpu().numpy(), ref_lse, f"{shape} splits={splits} lse", tol=lse_tolerance(w, x))
 
 
 FEATURES = {
@@ -99,7 +98,7 @@ def test_features(feature, splits):
         out, lse = run_gpu_splitkv(w, x, splits)
         ref, ref_lse = run_oracle_lse(w, x)
         check(w, out.double().cpu().numpy(), ref, f"{feature} splits={splits}")
-        check_lse(lse.cpu().numpy(), ref_lse, f"{feature} splits={splits} lse")
+        check_lse(lse.cpu().numpy(), ref_lse, f"{feature} splits={splits} lse", tol=lse_tolerance(w, x))
 
 
 def test_rows_without_keys():
@@ -112,7 +111,7 @@ def test_rows_without_keys():
     ref, ref_lse = run_oracle_lse(w, x)
     assert np.isneginf(ref_lse[1, :, :2]).all()
     check(w, out.double().cpu().numpy(), ref, "rows without keys")
-    check_lse(lse.cpu().numpy(), ref_lse, "rows without keys lse")
+    check_lse(lse.cpu().numpy(), ref_lse, "rows without keys lse", tol=lse_tolerance(w, x))
     check(w, run_gpu(w, x).double().cpu().numpy(), ref, "rows without keys attn_fwd")
 
 
@@ -128,7 +127,7 @@ def test_growing_maximum():
     out, lse = run_gpu_splitkv(w, x, 4)
     ref, ref_lse = run_oracle_lse(w, x)
     check(w, out.double().cpu().numpy(), ref, "growing maximum split")
-    check_lse(lse.cpu().numpy(), ref_lse, "growing maximum lse")
+    check_lse(lse.cpu().numpy(), ref_lse, "growing maximum lse", tol=lse_tolerance(w, x))
 
 
 def test_above_32_rows_uses_the_tile_kernel_correctly():
@@ -147,13 +146,13 @@ def test_deterministic():
 
 
 @pytest.mark.parametrize("splits", [0, 1])
-def test_full_size_decode_sampled_rows(splits):
+def test_full_size_decode_every_row(splits):
     w = EXTRA_WORKLOADS["decode_bf16"]
     x = make_inputs(w)
+    ref, ref_lse = run_oracle_lse(w, x)
     if splits == 1:
         out = run_gpu(w, x)
     else:
-        out, _ = run_gpu_splitkv(w, x, splits)
-    assert bool(torch.isfinite(out).all())
-    rows = sample_rows(w, 96)
-    check(w, gather_rows(w, out, rows), oracle_rows(w, x, rows), f"decode_bf16 splits={splits}")
+        out, lse = run_gpu_splitkv(w, x, splits)
+        check_lse(lse.cpu().numpy(), ref_lse, "decode_bf16 lse", tol=lse_tolerance(w, x))
+    check(w, out.double().cpu().numpy(), ref, f"decode_bf16 splits={splits}, every row")

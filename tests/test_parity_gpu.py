@@ -1,7 +1,7 @@
 """GPU parity: the CUDA library (through its C ABI) against the fp64 oracle on
-the same seeded inputs.  Small cases compare every output element; the five
-full-size workloads compare a sample of rows the oracle computes one by one,
-plus properties that hold at any size."""
+the same seeded inputs.  Every case compares every output element, the five
+full-size workloads (and the head-dim-256 one) included; cases with more work
+items than CTAs run the persistent kernels' item-to-item carry-over."""
 import math
 
 import numpy as np
@@ -9,8 +9,8 @@ import pytest
 import torch
 
 import tiled_online_softmax_02_gb300 as attn
-from parity import check, gather_rows, oracle_rows, run_and_check, run_gpu, run_oracle, to_dev
-from tiled_online_softmax_02_gb300.inputs import WORKLOADS, Workload, make_inputs, sample_rows
+from parity import check, run_and_check, run_gpu, run_oracle, to_dev
+from tiled_online_softmax_02_gb300.inputs import EXTRA_WORKLOADS, WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -256,14 +256,45 @@ def test_bounded_wait_times_out_and_reports():
     run_and_check(SMALL["tiny_f32"])  # the context still works
 
 
-# --- full-size workloads, sampled rows + properties
-@pytest.mark.parametrize("name", list(WORKLOADS))
-def test_workload_full_size_sampled(name):
-    w = WORKLOADS[name]
+# --- more work items than the persistent kernels have CTAs (one per SM): a
+# --- CTA runs several items in turn, so the K/V ring, the barrier phases, the
+# --- snake order, the cost-ranked batches and tensor memory carry over from
+# --- item to item -- here under a check of every output element
+MULTI_ITEM = {
+    # tile kernel, two query tiles per item: 2 * 48 * ceil(400 / 256) = 192 items
+    # (single-lane kernels: 2 * 48 * ceil(400 / 128) = 384)
+    "two_tile_causal": dict(B=2, Hq=48, Hkv=8, Sq=400, Sk=400, kv_capacity=400, causal=True),
+    # key-split lanes (Sq <= 128): 4 * 48 = 192 items, ragged lengths ranked by
+    # cost, a per-batch mask (staged asynchronously at D = 128), NaN / Inf
+    # garbage past each valid length
+    "keysplit_ragged_mask": dict(B=4, Hq=48, Hkv=8, Sq=100, Sk=900, kv_capacity=900, causal=True,
+                                 ragged=True, mask="per_batch", mask_neg_inf_frac=0.1,
+                                 garbage="nonfinite"),
+    # both item kinds in one launch (the last query pair holds one tile):
+    # 2 * 40 * 3 = 240 items, window and soft-cap, token-major output
+    "mixed_window_softcap": dict(B=2, Hq=40, Hkv=8, Sq=520, Sk=520, kv_capacity=520, causal=True,
+                                 local_window=200, softcap=20.0, out_layout=1),
+}
+MULTI_DTYPE_D = [("bf16", 64), ("bf16", 128), ("f16", 64), ("f16", 128), ("bf16", 256),
+                 ("f16", 256), ("f32", 128)]
+
+
+@pytest.mark.parametrize("case", list(MULTI_ITEM))
+@pytest.mark.parametrize("dtype,D", MULTI_DTYPE_D, ids=[f"{a}-d{b}" for a, b in MULTI_DTYPE_D])
+def test_more_items_than_ctas(dtype, D, case):
+    run_and_check(_base(dtype, D, **MULTI_ITEM[case]), what=f"multi-item {case} {dtype} D={D}")
+
+
+# --- full-size workloads: every output element against the oracle (the
+# --- oracle's threaded fp64 path; the largest take seconds on the host)
+FULL_SIZE = dict(WORKLOADS, gqa_causal_bf16_d256=EXTRA_WORKLOADS["gqa_causal_bf16_d256"])
+
+
+@pytest.mark.parametrize("name", list(FULL_SIZE))
+def test_workload_full_size_every_row(name):
+    w = FULL_SIZE[name]
     x = make_inputs(w)
     out = run_gpu(w, x)
-    assert bool(torch.isfinite(out).all()), "non-finite output"
-    rows = sample_rows(w, 160)
-    got = gather_rows(w, out, rows)
-    ref = oracle_rows(w, x, rows)
-    check(w, got, ref, f"{name} sampled rows")
+    got = out.double().cpu().numpy()
+    del out
+    check(w, got, run_oracle(w, x), f"{name} full size, every row")

@@ -192,8 +192,9 @@ def attn_fwd_f32_split(q, k, v, *, mask=None, total_lengths=None, past_lengths=N
                        causal=False, local_window=0, scale=None, softcap=0.0, out_layout="head",
                        seq_k=None, out=None, workspace=None):
     """fp32 attention forward on the tensor cores (attn_fwd_f32_split in the C
-    ABI): q, k, v float32 with D = 64 or 128, each product taken as three bf16
-    MMAs over two-piece operands.  Arguments and result as attn_fwd (CUDA or,
+    ABI): q, k, v float32 with D = 64 or 128, carried as bf16 pieces: Q K^T as
+    six bf16 products of three-piece operands, P V as three products of
+    two-piece operands.  Arguments and result as attn_fwd (CUDA or,
     end to end, CPU tensors).  The bf16 workspace for the split K / V
     (attn_f32_split_workspace_bytes) is allocated with torch when not given."""
     if q.dtype != torch.float32:

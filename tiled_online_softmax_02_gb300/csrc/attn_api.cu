@@ -218,9 +218,15 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
   if ((int64_t)((Sq + 2 * kTcBlockM - 1) / (2 * kTcBlockM)) * BHq > INT32_MAX)
     return ATTN_ERR_INVALID_ARG;  // work items of the persistent tensor-core kernel
   const int64_t qbytes = q_elems * esize, kvbytes = kv_elems * esize, mbytes = mask_elems * 4;
-  if (overlaps(out, qbytes, q, qbytes) || overlaps(out, qbytes, k, kvbytes) ||
-      overlaps(out, qbytes, v, kvbytes) || overlaps(out, qbytes, mask, mbytes))
-    return ATTN_ERR_INVALID_ARG;
+  const int64_t lenbytes = (int64_t)B * 4;
+  // every buffer the call writes (out, and below the log-sum-exp and the
+  // workspace) must be disjoint from every buffer it reads
+  auto hits_inputs = [&](const void* p, int64_t bytes) {
+    return overlaps(p, bytes, q, qbytes) || overlaps(p, bytes, k, kvbytes) || overlaps(p, bytes, v, kvbytes) ||
+           overlaps(p, bytes, mask, mbytes) || overlaps(p, bytes, total_lengths, lenbytes) ||
+           overlaps(p, bytes, past_lengths, lenbytes);
+  };
+  if (hits_inputs(out, qbytes)) return ATTN_ERR_INVALID_ARG;
 
   // capability gate: no kernel, no launch
   if (dtype == ATTN_F32 && D > 128) return ATTN_ERR_UNSUPPORTED;
@@ -231,16 +237,16 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
     const size_t need = f32tc_workspace_bytes(kv_elems);
     if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
     if (!aligned(workspace, 16)) return ATTN_ERR_UNSUPPORTED;
-    if (overlaps(workspace, (int64_t)need, out, qbytes) || overlaps(workspace, (int64_t)need, q, qbytes) ||
-        overlaps(workspace, (int64_t)need, k, kvbytes) || overlaps(workspace, (int64_t)need, v, kvbytes) ||
-        overlaps(workspace, (int64_t)need, mask, mbytes))
+    if (overlaps(workspace, (int64_t)need, out, qbytes) || hits_inputs(workspace, (int64_t)need))
       return ATTN_ERR_INVALID_ARG;
   }
   if (splitkv_api) {
     if (num_splits < 0 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
     if (dtype == ATTN_F32) return ATTN_ERR_UNSUPPORTED;  // split-KV is a tensor-core path
     if (lse && !aligned(lse, 4)) return ATTN_ERR_UNSUPPORTED;
-    if (lse && overlaps(lse, splitkv_rows(B, Hq, Sq) * 4, out, qbytes)) return ATTN_ERR_INVALID_ARG;
+    if (lse && (overlaps(lse, splitkv_rows(B, Hq, Sq) * 4, out, qbytes) ||
+                hits_inputs(lse, splitkv_rows(B, Hq, Sq) * 4)))
+      return ATTN_ERR_INVALID_ARG;
   }
   // 16-bit: D 64 / 128 on every entry, D 256 on attn_fwd (the single-lane kernel)
   const bool wide16 = dtype != ATTN_F32 && D == 256 && !splitkv_api;
@@ -266,8 +272,8 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
       const size_t need = (size_t)splits * (size_t)splitkv_rows(B, Hq, Sq) * (size_t)(D + 1) * 4;
       if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
       if (!aligned(workspace, 16)) return ATTN_ERR_UNSUPPORTED;
-      if (overlaps(workspace, (int64_t)need, out, qbytes) || overlaps(workspace, (int64_t)need, q, qbytes) ||
-          overlaps(workspace, (int64_t)need, k, kvbytes) || overlaps(workspace, (int64_t)need, v, kvbytes))
+      if (overlaps(workspace, (int64_t)need, out, qbytes) || hits_inputs(workspace, (int64_t)need) ||
+          (lse && overlaps(workspace, (int64_t)need, lse, splitkv_rows(B, Hq, Sq) * 4)))
         return ATTN_ERR_INVALID_ARG;
     }
   }

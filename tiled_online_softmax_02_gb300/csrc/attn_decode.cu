@@ -107,6 +107,9 @@ struct DecLayout {
   __device__ uint32_t pv_done(int i) const { return s + C::kOffBar + (2 * C::kSK + 2 * C::kSV + 4 + i) * 8; }
   __device__ uint32_t red_bar() const { return s + C::kOffBar + (2 * C::kSK + 2 * C::kSV + 6) * 8; }
   __device__ uint32_t* slot() const { return reinterpret_cast<uint32_t*>(base + C::kOffSlot); }
+  // softmax warps that finished their partial rows (4 when the CTA's part is
+  // complete; fewer after a timed-out wait)
+  __device__ int* done_warps() const { return reinterpret_cast<int*>(base + C::kOffSlot + 8); }
   // cluster exchange, over the K ring once every S^T product is done:
   // normalised partial rows [NR][D] and their log-sum-exps (log2 units) [NR]
   __device__ float* xo() const { return reinterpret_cast<float*>(base + C::kOffK); }
@@ -509,6 +512,18 @@ __device__ __forceinline__ void dec_softmax(const CommonParams& p, const DecLayo
       dec_store_row<D, BF16>(p, u, r, tid, o[r] * inv, lse2);
     }
   }
+  if (cluster > 1) {
+    __syncwarp();
+    if (lane == 0) atomicAdd(sm.done_warps(), 1);  // this warp's share of the part is written
+  }
+}
+
+__device__ __forceinline__ int ld_dsmem_s32(uint32_t saddr, int rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr), "r"(rank));
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
 }
 
 // Cluster merge, by the softmax threads of the cluster's first CTA: row r of
@@ -518,6 +533,15 @@ template <int D, int NR, bool BF16>
 __device__ __forceinline__ void dec_cluster_merge(const CommonParams& p, const DecLayout<D, NR>& sm,
                                                   const DecUnit& u, int cluster, int tid) {
   const uint32_t xo = smem_u32(sm.xo()), xl = smem_u32(sm.xl());
+  // A CTA whose wait timed out left its part unwritten (the status word has
+  // the timeout): its rows are then written as 0 with log-sum-exp -inf rather
+  // than merged from stale shared memory.
+  bool complete = true;
+  for (int k = 0; k < cluster; ++k) complete &= ld_dsmem_s32(smem_u32(sm.done_warps()), k) == 4;
+  if (!complete) {
+    for (int r = 0; r < u.R; ++r) dec_store_row<D, BF16>(p, u, r, tid, 0.0f, -INFINITY);
+    return;
+  }
   for (int r = 0; r < u.R; ++r) {
     float lk[8];
     float mx = -INFINITY;
@@ -565,6 +589,7 @@ __global__ void __launch_bounds__(kDecThreads, NR == 16 ? GB300_DEC_MIN_BLOCKS :
       mbar_init(sm.pv_done(i), 1);
     }
     mbar_init(sm.red_bar(), 4);
+    *sm.done_warps() = 0;
     mbar_init_fence();
   }
   if (threadIdx.x < NR) {  // visible keys and mask row of every query row
