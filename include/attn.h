@@ -77,10 +77,13 @@ enum attn_out_layout {
  *   out_layout    enum attn_out_layout
  *   mask_planes   0 (mask must be NULL), 1, B or B*Hq (mask must be non-NULL)
  *   dtype         enum attn_dtype.  ATTN_F32 runs the fp32-exact CUDA-core
- *                 kernel (1 <= D <= 128).  ATTN_F16 / ATTN_BF16 run the
- *                 tensor-core (tcgen05) kernels: D must be 64, 128 or 256
- *                 (256 on attn_fwd only), fp32 accumulation, P rounded to
- *                 the input type before P.V, output rounded to nearest even.
+ *                 kernel, any 1 <= D <= 384 (the DiT page's kernel is
+ *                 compiled up to head dim 384 for its VAE variant, "Kernel
+ *                 structure").  ATTN_F16 / ATTN_BF16 run the
+ *                 tensor-core (tcgen05) kernels: D must be 64, 128, 256 or
+ *                 384 (256 and 384 on attn_fwd only), fp32 accumulation, P
+ *                 rounded to the input type before P.V, output rounded to
+ *                 nearest even.
  *   stream        a cudaStream_t (NULL = the legacy default stream)
  *
  * Behaviour: validates everything it can see on the host first; on any error
@@ -113,7 +116,7 @@ int attn_fwd(const void *q, const void *k, const void *v, const float *mask,
  *
  * Arguments as attn_fwd, plus:
  *   dtype           ATTN_F16 or ATTN_BF16 only (ATTN_F32: ATTN_ERR_UNSUPPORTED),
- *                   with D 64 or 128 (256: ATTN_ERR_UNSUPPORTED)
+ *                   with D 64 or 128 (256, 384: ATTN_ERR_UNSUPPORTED)
  *   num_splits      0 = chosen by the library (attn_splitkv_num_splits), else 1..64
  *   lse             NULL or f32 [B, Hq, Sq] device: log sum_j exp(s_j) per row,
  *                   natural log, -inf for rows without a finite score

@@ -106,8 +106,9 @@ def test_invalid_arguments(lib, case):
 UNSUPPORTED = {
     "bf16_d96": dict(D=96),
     "f16_d320": dict(D=320, dtype=1),
-    "f32_d256": dict(D=256, dtype=0),
-    "f32_d129": dict(D=129, dtype=0),
+    "f32_d385": dict(D=385, dtype=0),
+    "f32_d448": dict(D=448, dtype=0),
+    "bf16_d512": dict(D=512),
     "misaligned_q": dict(q=Q + 8),
     "misaligned_out": dict(out=OUT + 2),
     "misaligned_mask": dict(mask=MASK + 2, planes=2),
@@ -152,6 +153,7 @@ def test_splitkv_validation(lib):
     assert lib.attn_splitkv_workspace_bytes(2, 4, 200, 64, 1) == 0
     assert call_splitkv(lib, 4, B=0) == attn.ATTN_OK
     assert call_splitkv(lib, 4, D=256) == attn.ATTN_ERR_UNSUPPORTED  # D 256: attn_fwd only
+    assert call_splitkv(lib, 4, D=384) == attn.ATTN_ERR_UNSUPPORTED  # D 384: attn_fwd only
 
 
 def test_valid_plane_counts_pass_validation_order(lib):

@@ -78,8 +78,9 @@ FEATURES = {
     "large_scores": {"q_std": 4.0, "k_std": 4.0, "causal": True},
 }
 
-DTYPE_D = [("f32", 64), ("f32", 128), ("f32", 40), ("f32", 96), ("bf16", 64), ("bf16", 128),
-           ("f16", 64), ("f16", 128), ("bf16", 256), ("f16", 256)]
+DTYPE_D = [("f32", 64), ("f32", 128), ("f32", 40), ("f32", 96), ("f32", 200), ("f32", 256),
+           ("f32", 330), ("f32", 384), ("bf16", 64), ("bf16", 128), ("f16", 64), ("f16", 128),
+           ("bf16", 256), ("f16", 256), ("bf16", 384), ("f16", 384)]
 
 
 @pytest.mark.parametrize("feature", list(FEATURES))
@@ -102,8 +103,11 @@ EDGES = {
 }
 
 
+EDGE_DTYPE_D = [("f32", 64), ("f32", 384), ("bf16", 128), ("f16", 64), ("bf16", 256), ("f16", 384)]
+
+
 @pytest.mark.parametrize("edge", list(EDGES))
-@pytest.mark.parametrize("dtype,D", [("f32", 64), ("bf16", 128), ("f16", 64), ("bf16", 256)])
+@pytest.mark.parametrize("dtype,D", EDGE_DTYPE_D, ids=[f"{a}-d{b}" for a, b in EDGE_DTYPE_D])
 def test_edge(dtype, D, edge):
     run_and_check(_base(dtype, D, **EDGES[edge]), what=f"{edge} {dtype} D={D}")
 
@@ -150,8 +154,22 @@ def test_head_dim_256_long_rows():
                         garbage="nonfinite", mask="per_batch", mask_neg_inf_frac=0.1))
 
 
-def test_head_dim_256_splitkv_unsupported():
-    q = torch.zeros(1, 2, 8, 256, dtype=torch.bfloat16, device="cuda")
+def test_head_dim_384_long_rows():
+    """D = 384 (single-lane kernel, Q in shared memory, 32-key tiles): many key
+    tiles, GQA, causal with ragged tails; the ragged cache with non-finite
+    garbage and a mask; soft-cap with a window; the fp32 CUDA-core kernel."""
+    run_and_check(_base("bf16", 384, Hq=8, Hkv=2, Sq=700, Sk=1400, kv_capacity=1500, causal=True))
+    run_and_check(_base("f16", 384, ragged=True, Sq=90, Sk=900, kv_capacity=900, causal=True,
+                        garbage="nonfinite", mask="per_batch", mask_neg_inf_frac=0.1))
+    run_and_check(_base("bf16", 384, Sq=333, Sk=700, kv_capacity=700, causal=True, local_window=150,
+                        softcap=10.0, out_layout=1))
+    run_and_check(_base("f32", 384, Hq=8, Hkv=2, Sq=300, Sk=700, kv_capacity=700, causal=True,
+                        mask="per_head", mask_neg_inf_frac=0.1))
+
+
+@pytest.mark.parametrize("D", [256, 384])
+def test_wide_head_dim_splitkv_unsupported(D):
+    q = torch.zeros(1, 2, 8, D, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(attn.AttnError) as e:
         attn.attn_fwd_splitkv(q, q, q, num_splits=2)
     assert e.value.status == attn.ATTN_ERR_UNSUPPORTED
@@ -276,7 +294,7 @@ MULTI_ITEM = {
                                  local_window=200, softcap=20.0, out_layout=1),
 }
 MULTI_DTYPE_D = [("bf16", 64), ("bf16", 128), ("f16", 64), ("f16", 128), ("bf16", 256),
-                 ("f16", 256), ("f32", 128)]
+                 ("f16", 256), ("bf16", 384), ("f16", 384), ("f32", 128), ("f32", 384)]
 
 
 @pytest.mark.parametrize("case", list(MULTI_ITEM))
@@ -287,7 +305,8 @@ def test_more_items_than_ctas(dtype, D, case):
 
 # --- full-size workloads: every output element against the oracle (the
 # --- oracle's threaded fp64 path; the largest take seconds on the host)
-FULL_SIZE = dict(WORKLOADS, gqa_causal_bf16_d256=EXTRA_WORKLOADS["gqa_causal_bf16_d256"])
+FULL_SIZE = dict(WORKLOADS, **{n: EXTRA_WORKLOADS[n] for n in
+                                ("gqa_causal_bf16_d256", "gqa_causal_bf16_d384", "vae_f32_d384")})
 
 
 @pytest.mark.parametrize("name", list(FULL_SIZE))

@@ -229,7 +229,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
   if (hits_inputs(out, qbytes)) return ATTN_ERR_INVALID_ARG;
 
   // capability gate: no kernel, no launch
-  if (dtype == ATTN_F32 && D > 128) return ATTN_ERR_UNSUPPORTED;
+  if (dtype == ATTN_F32 && D > kF32MaxHeadDim) return ATTN_ERR_UNSUPPORTED;
   if (f32split) {
     if (dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
@@ -248,8 +248,8 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
                 hits_inputs(lse, splitkv_rows(B, Hq, Sq) * 4)))
       return ATTN_ERR_INVALID_ARG;
   }
-  // 16-bit: D 64 / 128 on every entry, D 256 on attn_fwd (the single-lane kernel)
-  const bool wide16 = dtype != ATTN_F32 && D == 256 && !splitkv_api;
+  // 16-bit: D 64 / 128 on every entry, D 256 / 384 on attn_fwd (the single-lane kernel)
+  const bool wide16 = dtype != ATTN_F32 && (D == 256 || D == 384) && !splitkv_api;
   if (dtype != ATTN_F32 && D != 64 && D != 128 && !wide16) return ATTN_ERR_UNSUPPORTED;
   if ((wide16 || f32split) && (int64_t)((Sq + 127) / 128) * BHq > INT32_MAX)
     return ATTN_ERR_INVALID_ARG;  // work items of the single-lane kernel
@@ -332,8 +332,10 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
     lp.q = q;
     lp.c = c;
     lp.v_plane0 = 0;
-    int rc = encode_map(&lp.tmap_k, k, bf16, (int64_t)B * Hkv, kv_capacity, D, 64);
-    if (rc == ATTN_OK) rc = encode_map(&lp.tmap_v, v, bf16, (int64_t)B * Hkv, kv_capacity, D, 64);
+    const int key_box = D == 384 ? 32 : 64;  // keys per tile of the single-lane kernel
+    int rc = encode_map(&lp.tmap_k, k, bf16, (int64_t)B * Hkv, kv_capacity, D, key_box);
+    if (rc == ATTN_OK) rc = encode_map(&lp.tmap_v, v, bf16, (int64_t)B * Hkv, kv_capacity, D, key_box);
+    if (rc == ATTN_OK && D == 384) rc = encode_map(&lp.tmap_q, q, bf16, BHq, Sq, D);  // Q by TMA
     if (rc != ATTN_OK) return rc;
     e = launch_attn_lane16(lp, bf16, st);
   } else if (dtype == ATTN_F32) {

@@ -8,23 +8,30 @@
 // src/gpu_backend/cuda_imagen_attn_kernels.rs" (module doc "Parity-first
 // design") asks.  The pages' scalar kernels give each warp one query row and
 // re-read Q per key; here a 256-thread CTA owns 64 query rows and walks the
-// keys in tiles of 64, with both products register-tiled:
-//   S tile (64 x 64): thread (ty, tx) owns rows ty + 16 i and keys tx + 16 j
-//                     (i, j < 4), 16 FFMA per 8 shared-memory vector loads;
+// keys in tiles of BN, with both products register-tiled:
+//   S tile (64 x BN): thread (ty, tx) owns rows ty + 16 i and keys tx + 16 j
+//                     (i < 4, j < BN / 16), 16 FFMA per 8 shared-memory
+//                     vector loads at BN = 64;
 //   O tile (64 x D):  thread owns rows ty + 16 i and columns 4 tx + 64 g.
 // Row max / sum reductions run over the 16 lanes that share a row.
+// Head dims are padded to DP = 64, 128, 256 or 384 (the page's wider VAE
+// variant compiles the same kernel for head dims up to 384, "Kernel
+// structure"); columns past D are zero in shared memory and never stored.
+// Q, a K tile, a V tile and P must fit in shared memory: BN = 64 keys up to
+// DP = 256 (211 KB), 32 keys at DP = 384 (203 KB).
 #include "device_common.cuh"
 
 namespace gb300_attn {
 namespace {
 
 constexpr int BM = kF32BlockM;  // 64 query rows
-constexpr int BN = 64;          // keys per tile
 constexpr int kThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int DP>
 struct F32Config {
+  static constexpr int BN = DP <= 256 ? 64 : 32;  // keys per tile
+  static constexpr int kKeysPerThread = BN / 16;
   static constexpr int kQStride = DP + 4;  // padded rows: conflict-free float4 reads
   static constexpr int kKStride = DP + 4;
   static constexpr int kVStride = DP;
@@ -33,6 +40,7 @@ struct F32Config {
   static constexpr size_t kSmemFloats =
       (size_t)BM * kQStride + (size_t)BN * kKStride + (size_t)BN * kVStride + (size_t)BM * kPStride;
   static constexpr size_t kSmemBytes = kSmemFloats * sizeof(float);
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 // Loads rows [row0, row0 + nrows) of a [rows, D] fp32 matrix into shared memory
@@ -64,6 +72,8 @@ __device__ __forceinline__ void load_rows(float* dst, int sstride, const float* 
 template <int DP, bool SOFTCAP, bool MASK>
 __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_constant__ F32Params P) {
   using Cfg = F32Config<DP>;
+  constexpr int BN = Cfg::BN;
+  constexpr int KJ = Cfg::kKeysPerThread;
   const CommonParams& p = P.c;
   extern __shared__ __align__(16) float fsm[];
   float* Qs = fsm;
@@ -126,25 +136,25 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
     load_rows<DP>(Vs, Cfg::kVStride, vplane, key0, BN, zero_from, D, vec4);
     __syncthreads();
 
-    // S = Q K^T for this thread's 4 x 4 block
-    float s[4][4];
+    // S = Q K^T for this thread's 4 x KJ block
+    float s[4][KJ];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+      for (int j = 0; j < KJ; ++j) s[i][j] = 0.f;
 #pragma unroll 4
     for (int d0 = 0; d0 < DP; d0 += 4) {
-      float4 qa[4], kb[4];
+      float4 qa[4], kb[KJ];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         qa[i] = *reinterpret_cast<const float4*>(Qs + (ty + 16 * i) * Cfg::kQStride + d0);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < KJ; ++j)
         kb[j] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * j) * Cfg::kKStride + d0);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < KJ; ++j) {
           s[i][j] = fmaf(qa[i].x, kb[j].x, s[i][j]);
           s[i][j] = fmaf(qa[i].y, kb[j].y, s[i][j]);
           s[i][j] = fmaf(qa[i].z, kb[j].z, s[i][j]);
@@ -157,7 +167,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < KJ; ++j) {
         const int64_t kj = key0 + tx + 16 * j;
         float v;
         if (SOFTCAP || MASK) {
@@ -178,7 +188,9 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
     // online softmax update per row (the tile update of the page's kernel)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      float mt = fmaxf(fmaxf(s[i][0], s[i][1]), fmaxf(s[i][2], s[i][3]));
+      float mt = s[i][0];
+#pragma unroll
+      for (int j = 1; j < KJ; ++j) mt = fmaxf(mt, s[i][j]);
 #pragma unroll
       for (int off = 1; off < 16; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
       const float m_new = fmaxf(m[i], mt);
@@ -186,7 +198,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
       const float alpha = (m[i] == -INFINITY) ? 0.f : fast_exp2(m[i] - m_new);
       float rs = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < KJ; ++j) {
         const float e = fast_exp2(s[i][j] - m_sub);
         s[i][j] = e;
         rs += e;
@@ -200,7 +212,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
 #pragma unroll
         for (int u = 0; u < 4; ++u) o[i][g][u] *= alpha;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) Ps[(ty + 16 * i) * Cfg::kPStride + tx + 16 * j] = s[i][j];
+      for (int j = 0; j < KJ; ++j) Ps[(ty + 16 * i) * Cfg::kPStride + tx + 16 * j] = s[i][j];
     }
     __syncthreads();
 
@@ -282,7 +294,10 @@ cudaError_t launch_dp(const F32Params& P, cudaStream_t stream) {
 
 cudaError_t launch_attn_f32(const F32Params& P, cudaStream_t stream) {
   if (P.c.D <= 64) return launch_dp<64>(P, stream);
-  return launch_dp<128>(P, stream);
+  if (P.c.D <= 128) return launch_dp<128>(P, stream);
+  if (P.c.D <= 256) return launch_dp<256>(P, stream);
+  if (P.c.D <= kF32MaxHeadDim) return launch_dp<384>(P, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace gb300_attn

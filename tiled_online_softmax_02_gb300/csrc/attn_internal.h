@@ -69,11 +69,13 @@ struct F32Params {
 // memory): fp32 inputs as bf16 pieces (K / V split into a workspace by a
 // pre-pass: k0, k1, k2, v0, v1, each [B, Hkv, kv_capacity, D], read through
 // one TMA map over [5 * B * Hkv planes, kv_capacity rows, D]), or bf16 / f16
-// inputs with D = 256 (maps over the caller's k and v).  K piece t of kv
+// inputs with D = 256 or 384 (maps over the caller's k and v; at D = 384 Q
+// goes to shared memory by TMA as well).  K piece t of kv
 // plane i is plane t * B * Hkv + i of tmap_k; V piece t is plane
 // v_plane0 + t * B * Hkv + i of tmap_v.
 struct LaneParams {
-  CUtensorMap tmap_k;  // box {64, 64, 1}, 128B swizzle
+  CUtensorMap tmap_q;  // 16-bit D = 384 only: Q [B*Hq planes, Sq rows, D], box {64, 128, 1}
+  CUtensorMap tmap_k;  // box {64, key tile (64, or 32 at D = 384), 1}, 128B swizzle
   CUtensorMap tmap_v;
   const void* q;       // [B, Hq, Sq, D] fp32 or 16-bit, split / stored to tensor memory in the kernel
   int v_plane0;
@@ -83,6 +85,7 @@ struct LaneParams {
 constexpr int kTcBlockM = 128;  // query rows per tcgen05 CTA
 constexpr int kTcBlockN = 128;  // keys per tcgen05 tile
 constexpr int kF32BlockM = 64;  // query rows per fp32 CTA
+constexpr int kF32MaxHeadDim = 384;  // fp32-exact kernel: any head dim up to this
 
 // Launchers.  They assume validated parameters.
 cudaError_t launch_attn_tc(const TcParams& p, bool bf16, cudaStream_t stream);

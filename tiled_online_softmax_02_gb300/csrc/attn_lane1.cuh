@@ -5,29 +5,35 @@
 //   - fp32 inputs as error-compensated bf16 pieces (attn_f32tc.cu, D 64 /
 //     128): Q and K in three pieces, P and V in two, six products for QK^T
 //     and three for P.V;
-//   - bf16 / f16 inputs with D = 256 (attn_lane16.cu): one piece each.
+//   - bf16 / f16 inputs with D = 256 or 384 (attn_lane16.cu): one piece
+//     each.  At D = 384, O alone takes 384 of the 512 tensor-memory columns,
+//     so Q goes to shared memory by TMA instead (QK^T as an SS-MMA) and key
+//     tiles hold 32 keys, which keeps Q, the K / V rings and the mask
+//     buffers within the 227 KB of shared memory a CTA may use.
 //
 // The method is the tiled online softmax of "onnx-runtime-ep-cuda
 // 0.1.0-dev.5, src/kernels/flash_attention.rs" (module doc and
 // `flash_attention_body`): scores of one key tile at a time, running row
 // max and denominator, O rescaled when the max moves.  Work item = one
-// 128-row query tile of one (b, h); its 64-key tiles run in order through
-// two S buffers.
+// 128-row query tile of one (b, h); its key tiles (64 keys, 32 at D = 384)
+// run in order through two S buffers.
 //   warps 0-3   softmax: thread = query row.  At each item start they write
-//               the item's Q rows (split into pieces for fp32) to tensor memory.
+//               the item's Q rows (split into pieces for fp32) to tensor
+//               memory (except at D = 384).
 //   warp 4      TMA producer: the K pieces of key tile g into K slot g % KS and
 //               the V pieces into V slot g % VS, one barrier per tile; it also
-//               prefetches each item's Q block into L2.
+//               prefetches each item's Q block into L2 (at D = 384: loads it
+//               into shared memory).
 //   warp 5      MMA issuer (converged warp, elect.sync) and owner of tensor
 //               memory.  Step n of an item: S_{n%2} = Q K_n^T, then
 //               O += P_{n-1} V_{n-1}.  S(n) overwrites the P of tile n - 2, whose
 //               P.V this warp issued one step earlier (tensor-core operations of
 //               one thread run in issue order).
 // Tensor memory (512 columns): Q pieces [0, KP D/2), S_0 / S_1 (64 columns
-// each) from kColS, O (D columns) from kColS + 128; P_b over S_b (as VP
-// bf16 / f16 pieces of 32 columns).  Every barrier wait is bounded; a timeout
-// sets ATTN_ERR_TIMEOUT in the device status word and the kernel drains and
-// exits.
+// apart; a 32-key tile uses half) from kColS, O (D columns) from kColS + 128;
+// P_b over S_b (as VP bf16 / f16 pieces of FN / 2 columns).  Every barrier
+// wait is bounded; a timeout sets ATTN_ERR_TIMEOUT in the device status word
+// and the kernel drains and exits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -37,14 +43,12 @@ namespace gb300_attn {
 namespace lane1 {
 
 constexpr int FM = 128;          // query rows per item
-constexpr int FN = 64;           // keys per key tile
 constexpr int kThreads = 192;    // 4 softmax warps + producer + MMA
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;  // keep the old max while it is within 2^8
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kMaskBufBytes = 32 * 32 * 4;  // per softmax warp: 32 rows x 32 keys of f32
 
 // Input kinds.
 constexpr int kInF32Split = 0;  // fp32 q / k / v, K / V pre-split in a workspace, fp32 out
@@ -61,16 +65,25 @@ struct In {
 template <int D, int IN>
 struct Cfg {
   static constexpr int KP = In<IN>::KP, VP = In<IN>::VP;
+  // Q in shared memory (SS-MMA) when O leaves no tensor-memory room for it
+  static constexpr bool kQSmem = IN != kInF32Split && D > 256;
+  static constexpr int FN = kQSmem ? 32 : 64;                  // keys per key tile
   static constexpr int kSub = D / 64;                          // 128-byte column blocks per row
-  static constexpr uint32_t kSubBytes = FN * 128;              // [64 rows][64 cols] of 16-bit
+  static constexpr uint32_t kSubBytes = FN * 128;              // [FN rows][64 cols] of 16-bit
   static constexpr uint32_t kPieceBytes = kSub * kSubBytes;    // one piece of one tile
   static constexpr uint32_t kKTileBytes = KP * kPieceBytes;
   static constexpr uint32_t kVTileBytes = VP * kPieceBytes;
+  static constexpr uint32_t kQSubBytes = FM * 128;             // [128 rows][64 cols] of 16-bit
+  static constexpr uint32_t kQBytes = kQSmem ? kSub * kQSubBytes : 0;
   // K and V of a key tile arrive together (one barrier); a V slot is freed
   // a key tile later than its K slot, so V has one stage more
-  static constexpr int kKStages = kKTileBytes <= 24576 ? 4 : 2;
+  static constexpr int kKStages = (kKTileBytes <= 24576 && !kQSmem) ? 4 : 2;
   static constexpr int kVStages = kKStages + 1;
-  static constexpr uint32_t kOffK = 0;
+  // mask staging per softmax warp: 32 rows x kMaskKeys keys of f32
+  static constexpr int kMaskKeys = kQSmem ? 16 : 32;
+  static constexpr uint32_t kMaskBufBytes = 32 * kMaskKeys * 4;
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = kOffQ + kQBytes;
   static constexpr uint32_t kOffV = kOffK + kKStages * kKTileBytes;
   static constexpr uint32_t kOffMaskBuf = kOffV + kVStages * kVTileBytes;
   static constexpr uint32_t kOffBar = kOffMaskBuf + 4 * kMaskBufBytes;
@@ -83,7 +96,7 @@ struct Cfg {
   // tensor memory columns
   static constexpr uint32_t kQPiece = D / 2;                       // columns per piece of Q
   static constexpr uint32_t kColQ = 0;
-  static constexpr uint32_t kColS = (KP * kQPiece + 63) / 64 * 64;  // + buffer * 64
+  static constexpr uint32_t kColS = kQSmem ? 0 : (KP * kQPiece + 63) / 64 * 64;  // + buffer * 64
   static constexpr uint32_t kColO = kColS + 128;
   static_assert(kColO + D <= kTmemCols, "tensor memory columns");
 };
@@ -94,7 +107,7 @@ struct Smem {
   static constexpr int KS = C::kKStages, VS = C::kVStages;
   static constexpr int kB = 2 * KS + VS;  // first barrier after the rings
   uint8_t* base;
-  uint32_t sK, sV, bar0;
+  uint32_t sQ, sK, sV, bar0;
   // K and V of key tile g, on ring index g % KS (V slot g % VS)
   __device__ uint32_t kv_full(int s) const { return bar0 + 8u * s; }
   __device__ uint32_t k_empty(int s) const { return bar0 + 8u * (KS + s); }
@@ -110,7 +123,7 @@ struct Smem {
   __device__ uint32_t pv_done() const { return bar0 + 8u * (kB + 6); }
   __device__ uint32_t o_final() const { return bar0 + 8u * (kB + 7); }
   __device__ uint32_t drain() const { return bar0 + 8u * (kB + 8); }
-  __device__ uint8_t* mask_buf(int warp) const { return base + C::kOffMaskBuf + warp * kMaskBufBytes; }
+  __device__ uint8_t* mask_buf(int warp) const { return base + C::kOffMaskBuf + warp * C::kMaskBufBytes; }
 };
 
 // ------------------------------------------------------------------ pieces
@@ -161,7 +174,8 @@ struct FItem {
 };
 
 // Latest query tiles (longest causal rows) first; the heads of one kv group
-// are consecutive items, so their K / V tiles come from L2.
+// are consecutive items, so their K / V tiles come from L2.  FN: keys per tile.
+template <int FN>
 __device__ __forceinline__ FItem make_fitem(const CommonParams& p, int idx) {
   const int bh = p.B * p.Hq;
   const int nqt = (p.Sq + FM - 1) / FM;
@@ -198,16 +212,25 @@ __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN
   using C = Cfg<D, IN>;
   constexpr int KP = C::KP, VP = C::VP;
   constexpr int KS = C::kKStages, VS = C::kVStages;
+  constexpr int FN = C::FN;
   const CommonParams& p = P.c;
   const int kvp = p.B * p.Hkv;  // planes per piece
   int g = 0;
+  int q_items = 0;  // items whose Q was loaded into shared memory (kQSmem)
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int idx = f_item_of_round(r, n_items);
     if (idx < 0) break;
-    const FItem it = make_fitem(p, idx);
+    const FItem it = make_fitem<C::FN>(p, idx);
     if (it.N == 0) continue;
-    {
+    if constexpr (C::kQSmem) {
+      // Q into shared memory once the previous item's QK^T products are done
+      if (q_items > 0 && !mbar_wait(sm.q_empty(), (q_items - 1) & 1, p.timeout_ns, p.status)) break;
+      mbar_arrive_expect_tx(sm.q_full(), C::kQBytes);
+      for (int s = 0; s < C::kSub; ++s)
+        tma_load_3d(sm.sQ + s * C::kQSubBytes, &P.tmap_q, sm.q_full(), s * 64, (int)it.q0, it.b * p.Hq + it.h);
+      ++q_items;
+    } else {
       const int64_t rows = (int64_t)p.Sq - it.q0 < FM ? (int64_t)p.Sq - it.q0 : FM;
       constexpr int kQElem = IN == kInF32Split ? 4 : 2;  // bytes per Q element
       const uint8_t* qsrc = static_cast<const uint8_t*>(P.q) + (((int64_t)it.b * p.Hq + it.h) * p.Sq + it.q0) * D * kQElem;
@@ -238,6 +261,7 @@ __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN
   }
   // Let every copy this thread started land before the CTA can exit.
   for (int n = (g > KS ? g - KS : 0); n < g; ++n) mbar_wait(sm.kv_full(n % KS), (n / KS) & 1, p.timeout_ns, p.status);
+  if (C::kQSmem && q_items > 0) mbar_wait(sm.q_full(), (q_items - 1) & 1, p.timeout_ns, p.status);
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -255,8 +279,12 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
   constexpr int KS = C::kKStages, VS = C::kVStages;
   constexpr int KP = C::KP, VP = C::VP;
   constexpr bool kBF16 = In<IN>::kBF16;
+  constexpr int FN = C::FN;
   constexpr uint32_t id_qk = make_idesc_f16kind(kBF16, FM, FN, false);
-  constexpr uint32_t id_pv = make_idesc_f16kind(kBF16, FM, D, true);
+  // one MMA's N is at most 256: D = 384 runs as N = 256 and N = 128 parts
+  constexpr int kN0 = D > 256 ? 256 : D;
+  constexpr uint32_t id_pv = make_idesc_f16kind(kBF16, FM, kN0, true);
+  constexpr uint32_t id_pv1 = make_idesc_f16kind(kBF16, FM, D > 256 ? D - 256 : 64, true);
   const CommonParams& p = P.c;
   int g0 = 0;          // ring position of the item's first key tile
   int q_items = 0;     // items whose Q was consumed
@@ -265,7 +293,7 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
   for (int r = 0; ok; ++r) {
     const int idx = f_item_of_round(r, n_items);
     if (idx < 0) break;
-    const FItem it = make_fitem(p, idx);
+    const FItem it = make_fitem<C::FN>(p, idx);
     if (it.N == 0) continue;
     if (!mbar_wait_warp(sm.q_full(), q_items & 1, p.timeout_ns, p.status)) break;
     ++q_items;
@@ -291,6 +319,17 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
             const uint32_t q0 = tmem + C::kColQ + kk * 8, q1 = q0 + C::kQPiece, q2 = q0 + 2 * C::kQPiece;
             mma_ts6_elect(sd, q0, kd[0] + off16, q0, kd[1] + off16, q1, kd[0] + off16, q0, kd[2] + off16,
                           q1, kd[1] + off16, q2, kd[0] + off16, id_qk, kk > 0 ? 1u : 0u);
+          }
+        } else if constexpr (C::kQSmem) {
+          // Q and K both K-major in shared memory; K steps 4s..4s+3 lie in
+          // 64-column block s of each (blocks kQSubBytes / kSubBytes apart)
+          const uint64_t qd = make_sdesc_sw128(sm.sQ, 16, 1024);
+          const uint64_t kd = make_sdesc_sw128(kb, 16, 1024);
+#pragma unroll
+          for (int s = 0; s < D / 64; ++s) {
+            const uint32_t oq = (s * C::kQSubBytes) >> 4, okk = (s * C::kSubBytes) >> 4;
+            mma_ss4_elect(sd, qd + oq, kd + okk, qd + oq + 2, kd + okk + 2, qd + oq + 4, kd + okk + 4,
+                          qd + oq + 6, kd + okk + 6, id_qk, s > 0 ? 1u : 0u);
           }
         } else {
           const uint64_t kd = make_sdesc_sw128(kb, 16, 1024);
@@ -345,7 +384,15 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
                           pa + (kk + 1) * 8, d0 + o1, pa + (kk + 1) * 8, d1 + o1, pa + 32 + (kk + 1) * 8,
                           d0 + o1, id_pv, (m == 0 && kk == 0) ? 0u : 1u);
           }
+        } else if constexpr (D > 256) {
+          // 32 keys = two K steps (2048 bytes of V apart); columns [0, 256)
+          // from V blocks 0-3, [256, D) from blocks 4.. into O + 256
+          const uint64_t d1 = make_sdesc_sw128(vb + 4 * C::kSubBytes, C::kSubBytes, 1024);
+          static_assert(FN == 32, "two K steps per key tile");
+          mma_ts2x2_elect(tmem + C::kColO, tmem + C::kColO + 256, pa, pa + 8, d0, d0 + 128, d1, d1 + 128, id_pv,
+                          id_pv1, m == 0 ? 0u : 1u);
         } else {
+          static_assert(FN == 64, "four K steps per key tile");
           mma_ts4_elect(tmem + C::kColO, pa, d0, pa + 8, d0 + 128, pa + 16, d0 + 256, pa + 24, d0 + 384, id_pv,
                         m == 0 ? 0u : 1u);
         }
@@ -363,23 +410,26 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
 }
 
 // ------------------------------------------------------------------ softmax
-__device__ __forceinline__ float max64(const float (&x)[FN]) {
+// Maximum / minimum of N values (N a multiple of 16) in eight chains.
+template <int N>
+__device__ __forceinline__ float maxn(const float (&x)[N]) {
   float m[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) m[k] = fmaxf(x[k], x[k + 8]);
 #pragma unroll
-  for (int i = 16; i < FN; i += 16)
+  for (int i = 16; i < N; i += 16)
 #pragma unroll
     for (int k = 0; k < 8; ++k) m[k] = fmax3(m[k], x[i + k], x[i + 8 + k]);
   return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], fmax3(m[5], m[6], m[7])));
 }
 
-__device__ __forceinline__ float min64(const float (&x)[FN]) {
+template <int N>
+__device__ __forceinline__ float minn(const float (&x)[N]) {
   float m[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) m[k] = fminf(x[k], x[k + 8]);
 #pragma unroll
-  for (int i = 16; i < FN; i += 16)
+  for (int i = 16; i < N; i += 16)
 #pragma unroll
     for (int k = 0; k < 8; ++k) m[k] = fmin3(m[k], x[i + k], x[i + 8 + k]);
   return fminf(fmin3(m[0], m[1], m[2]), fmin3(m[3], m[4], fmin3(m[5], m[6], m[7])));
@@ -438,22 +488,30 @@ __device__ __forceinline__ void store_q_row(const CommonParams& p, const void* q
   }
 }
 
-// Mask block of one warp -- 32 rows by the 64 keys [key0, key0 + 64) -- into
-// x of the lane that owns each row (natural units; 0 outside).  Each
-// instruction loads 4 rows x 128 contiguous bytes; a 4 KB per-warp buffer
-// (16-byte chunks XOR-swizzled by row) turns rows into lanes.  vec4 needs
-// 16-byte aligned mask rows (Sk % 4 == 0).
-__device__ __forceinline__ void mask_rows64(float (&x)[FN], const float* mwarp, int nrows, int Sk, int key0,
-                                            bool vec4, uint8_t* buf, int lane) {
-  const int rsub = lane >> 3;
-  const int csub = lane & 7;
+// Mask block of one warp -- 32 rows by the N keys [key0, key0 + N) -- into
+// x of the lane that owns each row (natural units; 0 outside), KC keys (32
+// or 16) at a time.  Each instruction loads rows of KC * 4 contiguous bytes
+// (4 rows x 128 bytes, or 8 rows x 64 bytes); a per-warp
+// buffer of 32 rows x KC keys (16-byte chunks XOR-swizzled by row so that
+// both the row-wise stores and the lane-per-row reads are conflict-free)
+// turns rows into lanes.  vec4 needs 16-byte aligned mask rows (Sk % 4 == 0).
+template <int N, int KC>
+__device__ __forceinline__ void mask_rows(float (&x)[N], const float* mwarp, int nrows, int Sk, int key0,
+                                          bool vec4, uint8_t* buf, int lane) {
+  static_assert(KC == 32 || KC == 16, "chunk of 32 or 16 keys");
+  constexpr int kCpr = KC / 4;     // 16-byte chunks per buffered row
+  constexpr int kRpi = 32 / kCpr;  // rows per load instruction
+  constexpr int kRowBytes = KC * 4;
+  const int rsub = lane / kCpr;
+  const int csub = lane % kCpr;
+  auto swz = [](int row) { return KC == 32 ? (row & 7) : ((row >> 1) & 3); };
 #pragma unroll
-  for (int k = 0; k < FN / 32; ++k) {
-    float4 v[8];
+  for (int k = 0; k < N / KC; ++k) {
+    float4 v[32 / kRpi];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int row = 4 * i + rsub;
-      const int key = key0 + 32 * k + 4 * csub;
+    for (int i = 0; i < 32 / kRpi; ++i) {
+      const int row = kRpi * i + rsub;
+      const int key = key0 + KC * k + 4 * csub;
       float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
       const float* src = mwarp + (int64_t)row * Sk + key;
       if (vec4) {
@@ -467,18 +525,18 @@ __device__ __forceinline__ void mask_rows64(float (&x)[FN], const float* mwarp, 
       v[i] = t;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int row = 4 * i + rsub;
-      *reinterpret_cast<float4*>(buf + row * 128 + ((csub ^ (row & 7)) << 4)) = v[i];
+    for (int i = 0; i < 32 / kRpi; ++i) {
+      const int row = kRpi * i + rsub;
+      *reinterpret_cast<float4*>(buf + row * kRowBytes + ((csub ^ swz(row)) << 4)) = v[i];
     }
     __syncwarp();
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const float4 t = *reinterpret_cast<const float4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4));
-      x[32 * k + 4 * c + 0] = t.x;
-      x[32 * k + 4 * c + 1] = t.y;
-      x[32 * k + 4 * c + 2] = t.z;
-      x[32 * k + 4 * c + 3] = t.w;
+    for (int c = 0; c < kCpr; ++c) {
+      const float4 t = *reinterpret_cast<const float4*>(buf + lane * kRowBytes + ((c ^ swz(lane)) << 4));
+      x[KC * k + 4 * c + 0] = t.x;
+      x[KC * k + 4 * c + 1] = t.y;
+      x[KC * k + 4 * c + 2] = t.z;
+      x[KC * k + 4 * c + 3] = t.w;
     }
     __syncwarp();
   }
@@ -490,6 +548,7 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
                                           int warp, int lane) {
   using C = Cfg<D, IN>;
   constexpr bool kF32 = IN == kInF32Split;
+  constexpr int FN = C::FN;
   const CommonParams& p = P.c;
   const int row = warp * 32 + lane;
   const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
@@ -502,7 +561,7 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
   for (int r = 0; ok; ++r) {
     const int idx = f_item_of_round(r, n_items);
     if (idx < 0) break;
-    const FItem it = make_fitem(p, idx);
+    const FItem it = make_fitem<C::FN>(p, idx);
     const int64_t qi = it.q0 + row;
     const int64_t row_id = ((int64_t)it.b * p.Hq + it.h) * p.Sq + qi;
     const int64_t obase = p.out_layout == 0 ? row_id * D : (((int64_t)it.b * p.Sq + qi) * p.Hq + it.h) * D;
@@ -516,14 +575,16 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
       }
       continue;
     }
-    // Q of this item into tensor memory once the previous item's QK^T finished
-    if (qn > 0 && !mbar_wait_warp(sm.q_empty(), (qn - 1) & 1, p.timeout_ns, p.status)) { ok = false; break; }
-    ++qn;
-    store_q_row<D, IN>(p, P.q, it, qi, tlane);
-    tmem_wait_st();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sm.q_full());
+    if constexpr (!C::kQSmem) {
+      // Q of this item into tensor memory once the previous item's QK^T finished
+      if (qn > 0 && !mbar_wait_warp(sm.q_empty(), (qn - 1) & 1, p.timeout_ns, p.status)) { ok = false; break; }
+      ++qn;
+      store_q_row<D, IN>(p, P.q, it, qi, tlane);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.q_full());
+    }
 
     const RowLimits R = row_limits(p, it.L, qi);
     const float* mwarp = nullptr;
@@ -545,16 +606,16 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
       const int64_t key0 = (int64_t)(it.tb + n) * FN;
       float x[FN];
       if constexpr (MASK)
-        mask_rows64(x, mwarp, mrows, p.Sk, (int)key0, p.mask_vec4 != 0, sm.mask_buf(warp), lane);
+        mask_rows<FN, C::kMaskKeys>(x, mwarp, mrows, p.Sk, (int)key0, p.mask_vec4 != 0, sm.mask_buf(warp), lane);
       if (!mbar_wait_warp(sm.s_full(bsel), sb[bsel] & 1, p.timeout_ns, p.status)) { ok = false; break; }
       ++sb[bsel];
       tc_fence_after();
       const bool need_mask = !(key0 >= it.T.full_lo && key0 + FN <= it.T.full_hi);
       bool scaled = false;
       {
-        uint32_t sr[2][32];
-        tmem_ld32(s_addr, sr[0]);
-        tmem_ld32(s_addr + 32, sr[1]);
+        uint32_t sr[FN / 32][32];
+#pragma unroll
+        for (int k = 0; k < FN / 32; ++k) tmem_ld32(s_addr + 32 * k, sr[k]);
         tmem_wait_ld();
         if constexpr (MASK) {
           const uint64_t le2 = f2(kLog2e, kLog2e);
@@ -608,11 +669,11 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
       }
       float m_tile;
       if (scaled) {
-        m_tile = max64(x);
+        m_tile = maxn<FN>(x);
       } else if (!need_mask) {
-        m_tile = (xs >= 0.0f ? max64(x) : min64(x)) * xs;
+        m_tile = (xs >= 0.0f ? maxn<FN>(x) : minn<FN>(x)) * xs;
       } else {
-        const float mr = max64(x);
+        const float mr = maxn<FN>(x);
         m_tile = mr == -INFINITY ? -INFINITY : mr * xs;
       }
       // online update, keeping the old max unless it grew by more than 2^8
@@ -635,7 +696,7 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
       // fp32 two bf16 pieces (p0 in columns [0, 32), p1 in [32, 64)), else
       // rounded to the input type (columns [0, 32))
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
+      for (int ch = 0; ch < FN / 32; ++ch) {
         uint32_t ph[16], pl[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -733,6 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_lane1_kernel(const __gri
   Smem<D, IN> sm;
   sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm.base);
+  sm.sQ = sbase + C::kOffQ;
   sm.sK = sbase + C::kOffK;
   sm.sV = sbase + C::kOffV;
   sm.bar0 = sbase + C::kOffBar;
@@ -747,7 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_lane1_kernel(const __gri
       mbar_init(sm.k_empty(s), 1);
     }
     for (int s = 0; s < C::kVStages; ++s) mbar_init(sm.v_empty(s), 1);
-    mbar_init(sm.q_full(), 4);  // one arrival per softmax warp
+    mbar_init(sm.q_full(), C::kQSmem ? 1 : 4);  // the producer's TMA, or one arrival per softmax warp
     mbar_init(sm.q_empty(), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(sm.s_full(b), 1);
@@ -759,6 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_lane1_kernel(const __gri
     mbar_init_fence();
   }
   if (warp == kTmaWarp && lane == 0) {
+    if (C::kQSmem) tma_prefetch_desc(&P.tmap_q);
     tma_prefetch_desc(&P.tmap_k);
     tma_prefetch_desc(&P.tmap_v);
   }

@@ -1,6 +1,6 @@
-// attn_lane16.cu -- bf16 / f16 attention forward with head dim 256 on the
-// tensor cores (sm_103a): the 16-bit instance of the single-lane kernel in
-// attn_lane1.cuh.
+// attn_lane16.cu -- bf16 / f16 attention forward with head dim 256 or 384 on
+// the tensor cores (sm_103a): the 16-bit instances of the single-lane kernel
+// in attn_lane1.cuh.
 //
 // "pictor-kernels 0.1.0, src/gpu_backend/cuda_imagen_attn_kernels.rs"
 // ("Kernel structure") compiles a wider head-dim variant of its attention
@@ -10,11 +10,18 @@
 // tensor memory (128 columns), two 64-key S buffers and O (256 columns).
 // K and V tiles come straight from the caller's tensors by TMA; V rows past
 // the valid length are zeroed in shared memory before the P.V products.
+// For D = 384 (the page's widest variant) O takes 384 columns, so Q moves to
+// shared memory (by TMA, read by an SS-MMA), two 32-column S buffers sit
+// below O, key tiles hold 32 keys, and the P.V product runs as N = 256 and
+// N = 128 parts.
 #include "attn_lane1.cuh"
 
 namespace gb300_attn {
 
 cudaError_t launch_attn_lane16(const LaneParams& P, bool bf16, cudaStream_t stream) {
+  if (P.c.D == 384)
+    return bf16 ? lane1::launch_lane1<384, lane1::kInBF16>(P, stream)
+                : lane1::launch_lane1<384, lane1::kInF16>(P, stream);
   return bf16 ? lane1::launch_lane1<256, lane1::kInBF16>(P, stream)
               : lane1::launch_lane1<256, lane1::kInF16>(P, stream);
 }

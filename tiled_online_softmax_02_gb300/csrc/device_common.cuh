@@ -347,6 +347,24 @@ __device__ __forceinline__ void mma_ts6_elect(uint32_t d, uint32_t a0, uint64_t 
       : "memory");
 }
 
+// Two K steps of a product whose N is split in two parts (N = 384 as 256 +
+// 128: one MMA's N is at most 256), A in tensor memory: part j of step k is
+// D_j (+)= A_k B_jk with instruction descriptor id_j.
+__device__ __forceinline__ void mma_ts2x2_elect(uint32_t d0, uint32_t d1, uint32_t a0, uint32_t a1,
+                                                uint64_t b00, uint64_t b01, uint64_t b10, uint64_t b11,
+                                                uint32_t id0, uint32_t id1, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "setp.ne.b32 q, %10, 0;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %4, %8, q;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %6, %9, q;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %5, %8, 1;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [%3], %7, %9, 1;\n\t}" ::"r"(d0),
+      "r"(d1), "r"(a0), "r"(a1), "l"(b00), "l"(b01), "l"(b10), "l"(b11), "r"(id0), "r"(id1), "r"(acc0)
+      : "memory");
+}
+
 // tc_commit by the elected lane (the lane that issued the warp's MMAs).
 __device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
   asm volatile(

@@ -96,8 +96,8 @@ _add(4, Workload("ragged_kvcache_f16", B=8, Hq=32, Hkv=4, Sq=128, Sk=4096, kv_ca
 WORKLOAD_ORDER = list(WORKLOADS)
 
 # Shapes beyond the five: decode (one new token per sequence over a long
-# ragged cache), the case split-KV serves; and the GQA causal prefill with
-# head dim 256 (the wider head dim of the DiT page's kernel variants).
+# ragged cache), the case split-KV serves; and the wider head dims of the DiT
+# page's kernel variants (256 and 384).
 EXTRA_WORKLOADS: dict[str, Workload] = {
     "decode_bf16": Workload("decode_bf16", B=8, Hq=32, Hkv=8, Sq=1, Sk=32768, kv_capacity=32768,
                             D=128, dtype="bf16", causal=True, ragged=True, garbage="finite",
@@ -105,6 +105,15 @@ EXTRA_WORKLOADS: dict[str, Workload] = {
     "gqa_causal_bf16_d256": Workload("gqa_causal_bf16_d256", B=2, Hq=32, Hkv=8, Sq=4096, Sk=4096,
                                      kv_capacity=4096, D=256, dtype="bf16", causal=True,
                                      seed=SEED_BASE + 11),
+    # the widest head dim of the DiT page's kernel variants (384, its VAE
+    # variant): the same GQA causal prefill in bf16, and an fp32 VAE-style
+    # attention (non-causal, token-major output, as the page's op) over a
+    # 32 x 32 latent grid
+    "gqa_causal_bf16_d384": Workload("gqa_causal_bf16_d384", B=2, Hq=32, Hkv=8, Sq=4096, Sk=4096,
+                                     kv_capacity=4096, D=384, dtype="bf16", causal=True,
+                                     seed=SEED_BASE + 12),
+    "vae_f32_d384": Workload("vae_f32_d384", B=1, Hq=4, Hkv=4, Sq=1024, Sk=1024, kv_capacity=1024,
+                             D=384, dtype="f32", causal=False, out_layout=1, seed=SEED_BASE + 13),
 }
 
 
