@@ -168,7 +168,7 @@ KERNEL_SOURCES = {
 def kernel_family(w: Workload, splitkv: bool = False, f32split: bool = False) -> str:
     if w.dtype == "f32":
         return "f32tc" if f32split else "f32"
-    if w.D == 256:
+    if w.D in (256, 384):
         return "lane16"
     return "decode" if w.group * w.Sq <= 32 else "tc"
 

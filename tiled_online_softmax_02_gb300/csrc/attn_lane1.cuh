@@ -206,7 +206,12 @@ __device__ __forceinline__ int f_item_of_round(int r, int n_items) {
 // pieces into V slot g % VS, both completing kv_full(g % KS).  A K slot is
 // freed by its tile's QK^T products, a V slot by its P.V products.  At each
 // item start it also prefetches the item's Q rows into L2, so the softmax
-// warps' Q loads come from L2.
+// warps' Q loads come from L2.  K / V tiles are read by every query tile of
+// their kv head, Q and O once: K / V are loaded as L2 evict_last, and the
+// softmax warps read Q and write O as evict_first, so a Q / O stream larger
+// than L2 does not push K / V out between the query tiles that share them
+// (the prefetch keeps the default policy: an evict_first prefetch measured a
+// few MB more DRAM reads).
 template <int D, int IN>
 __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN>& sm, int n_items) {
   using C = Cfg<D, IN>;
@@ -217,6 +222,7 @@ __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN
   const int kvp = p.B * p.Hkv;  // planes per piece
   int g = 0;
   int q_items = 0;  // items whose Q was loaded into shared memory (kQSmem)
+  const uint64_t keep = l2_evict_last_policy(), stream = l2_evict_first_policy();
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int idx = f_item_of_round(r, n_items);
@@ -228,7 +234,8 @@ __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN
       if (q_items > 0 && !mbar_wait(sm.q_empty(), (q_items - 1) & 1, p.timeout_ns, p.status)) break;
       mbar_arrive_expect_tx(sm.q_full(), C::kQBytes);
       for (int s = 0; s < C::kSub; ++s)
-        tma_load_3d(sm.sQ + s * C::kQSubBytes, &P.tmap_q, sm.q_full(), s * 64, (int)it.q0, it.b * p.Hq + it.h);
+        tma_load_3d_hint(sm.sQ + s * C::kQSubBytes, &P.tmap_q, sm.q_full(), s * 64, (int)it.q0,
+                         it.b * p.Hq + it.h, stream);
       ++q_items;
     } else {
       const int64_t rows = (int64_t)p.Sq - it.q0 < FM ? (int64_t)p.Sq - it.q0 : FM;
@@ -251,12 +258,12 @@ __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN
       mbar_arrive_expect_tx(sm.kv_full(ks), C::kKTileBytes + C::kVTileBytes);
       for (int pc = 0; pc < KP; ++pc)
         for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d(sm.sK + ks * C::kKTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_k,
-                      sm.kv_full(ks), s * 64, key0, pc * kvp + kv_plane);
+          tma_load_3d_hint(sm.sK + ks * C::kKTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_k,
+                           sm.kv_full(ks), s * 64, key0, pc * kvp + kv_plane, keep);
       for (int pc = 0; pc < VP; ++pc)
         for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d(sm.sV + vs * C::kVTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_v,
-                      sm.kv_full(ks), s * 64, key0, P.v_plane0 + pc * kvp + kv_plane);
+          tma_load_3d_hint(sm.sV + vs * C::kVTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_v,
+                           sm.kv_full(ks), s * 64, key0, P.v_plane0 + pc * kvp + kv_plane, keep);
     }
   }
   // Let every copy this thread started land before the CTA can exit.
@@ -447,8 +454,12 @@ __device__ __forceinline__ void store_q_row(const CommonParams& p, const void* q
     const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(q) + row * D);
     // the whole row in flight at once (D / 4 independent 16-byte loads)
     float4 rowv[D / 4];
+    const uint64_t stream = l2_evict_first_policy();
 #pragma unroll
-    for (int i = 0; i < D / 4; ++i) rowv[i] = qi < p.Sq ? __ldg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < D / 4; ++i) {
+      const uint4 u = qi < p.Sq ? ld_nc_hint(src + i, stream) : make_uint4(0u, 0u, 0u, 0u);
+      rowv[i] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+    }
 #pragma unroll
     for (int ch = 0; ch < D / 32; ++ch) {
       uint32_t pcs[C::KP][16];
@@ -470,8 +481,9 @@ __device__ __forceinline__ void store_q_row(const CommonParams& p, const void* q
   } else {
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(q) + row * D);
     uint4 rowv[D / 8];
+    const uint64_t stream = l2_evict_first_policy();
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) rowv[i] = qi < p.Sq ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+    for (int i = 0; i < D / 8; ++i) rowv[i] = qi < p.Sq ? ld_nc_hint(src + i, stream) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int ch = 0; ch < D / 32; ++ch) {
       uint32_t w[16];
@@ -753,6 +765,7 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
     ++on;
     tc_fence_after();
     const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+    const uint64_t o_policy = l2_evict_first_policy();
     const uint64_t w2 = f2(inv_l, inv_l);
 #pragma unroll
     for (int k = 0; k < D / 32; ++k) {
@@ -764,18 +777,23 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
 #pragma unroll
         for (int i = 0; i < 32; i += 2)
           f2_split(fmul2(f2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), w2), r[i], r[i + 1]);
+        // O is written once: evict_first, so it does not displace K / V in L2
         if constexpr (kF32) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            orow[k * 8 + i] = make_uint4(__float_as_uint(r[4 * i]), __float_as_uint(r[4 * i + 1]),
-                                         __float_as_uint(r[4 * i + 2]), __float_as_uint(r[4 * i + 3]));
+            st_hint(orow + k * 8 + i,
+                    make_uint4(__float_as_uint(r[4 * i]), __float_as_uint(r[4 * i + 1]),
+                               __float_as_uint(r[4 * i + 2]), __float_as_uint(r[4 * i + 3])),
+                    o_policy);
         } else {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            orow[k * 4 + i] = make_uint4(pack16<In<IN>::kBF16>(r[8 * i], r[8 * i + 1]),
-                                         pack16<In<IN>::kBF16>(r[8 * i + 2], r[8 * i + 3]),
-                                         pack16<In<IN>::kBF16>(r[8 * i + 4], r[8 * i + 5]),
-                                         pack16<In<IN>::kBF16>(r[8 * i + 6], r[8 * i + 7]));
+            st_hint(orow + k * 4 + i,
+                    make_uint4(pack16<In<IN>::kBF16>(r[8 * i], r[8 * i + 1]),
+                               pack16<In<IN>::kBF16>(r[8 * i + 2], r[8 * i + 3]),
+                               pack16<In<IN>::kBF16>(r[8 * i + 4], r[8 * i + 5]),
+                               pack16<In<IN>::kBF16>(r[8 * i + 6], r[8 * i + 7])),
+                    o_policy);
         }
       }
     }
