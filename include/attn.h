@@ -102,6 +102,47 @@ int attn_fwd(const void *q, const void *k, const void *v, const float *mask,
              int mask_planes, int dtype, void *stream);
 
 /*
+ * attn_fwd_host -- attn_fwd end to end from host memory: uploads the inputs,
+ * runs the attention and downloads the output, with the copies of one piece
+ * overlapped with the kernels of its neighbours.  Same operation as attn_fwd
+ * (every output element is bit-identical to attn_fwd on the same inputs).
+ *
+ * The problem is cut into pieces: one per batch, and for ATTN_OUT_HEAD_MAJOR
+ * each batch further into whole kv-head groups, about eight pieces in all.
+ * For each piece, in order: its q / k / v slices (and mask planes) are
+ * copied up on `copy_in_stream`; `stream` waits for them and runs attn_fwd on
+ * the piece; `copy_out_stream` waits for that and copies the piece's output
+ * down.  Lengths and a shared mask plane go up first.
+ *
+ * Arguments as attn_fwd, except:
+ *   q, k, v, mask, total_lengths, past_lengths, out
+ *                 HOST buffers with attn_fwd's shapes (page-locked memory is
+ *                 needed for the copies to overlap; pageable memory works,
+ *                 serialised).  mask / lengths NULL exactly when their device
+ *                 counterparts are NULL.
+ *   dq, dk, dv, dmask, dtotal, dpast, dout
+ *                 caller-owned DEVICE buffers of the same sizes, the device
+ *                 arguments of attn_fwd (alignment and overlap rules as there).
+ *   stream, copy_in_stream, copy_out_stream
+ *                 cudaStream_t; NULL copy streams fall back to `stream` (no
+ *                 overlap).  Work already on `stream` finishes before the
+ *                 device buffers are written.
+ * Behaviour: validates the whole problem as attn_fwd would before touching
+ * anything.  BLOCKS until the output is in `out` (and on any error, until
+ * nothing it enqueued still runs), so the host buffers may be reused as
+ * soon as it returns.  Creates and destroys its own events; allocates no
+ * device memory.  Errors as attn_fwd; ATTN_ERR_UNSUPPORTED for more than
+ * 4096 pieces (B > 4096).
+ */
+int attn_fwd_host(const void *q, const void *k, const void *v, const float *mask,
+                  const int32_t *total_lengths, const int32_t *past_lengths, void *out,
+                  void *dq, void *dk, void *dv, float *dmask, int32_t *dtotal, int32_t *dpast,
+                  void *dout, int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D,
+                  int causal, int local_window, float scale, float softcap, int out_layout,
+                  int mask_planes, int dtype, void *stream, void *copy_in_stream,
+                  void *copy_out_stream);
+
+/*
  * attn_fwd_splitkv -- attn_fwd with each query tile's keys split into
  * `num_splits` contiguous ranges computed by different CTAs, then merged
  * (the flash-decoding arrangement: for decode-like shapes with few query rows

@@ -41,6 +41,11 @@ SIGNATURES = {
                                   _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                   _i32, _i32, ctypes.c_float, ctypes.c_float, _i32,
                                   _i32, _vp, ctypes.c_size_t, _vp]),
+    "attn_fwd_host": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                             _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                             _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                             _i32, _i32, ctypes.c_float, ctypes.c_float, _i32,
+                             _i32, _i32, _vp, _vp, _vp]),
     "attn_f32_split_workspace_bytes": (ctypes.c_size_t, [_i32, _i32, _i32, _i32]),
     "dsa_index_select": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                 ctypes.c_float, ctypes.c_float, _i32, _vp, ctypes.c_size_t, _vp]),
@@ -145,47 +150,153 @@ def attn_fwd(q, k, v, *, mask=None, total_lengths=None, past_lengths=None, causa
             raise ValueError("all tensors must be contiguous")
         if t is not None and t.device != q.device:
             raise ValueError("all tensors must be on the same device")
-    host = not q.is_cuda
-    host_out = None
-    if host:
-        dev = torch.device("cuda", torch.cuda.current_device())
-
-        def up(t):
-            return None if t is None else t.to(dev, non_blocking=True)
-        q, k, v, mask, total_lengths, past_lengths = map(up, (q, k, v, mask, total_lengths,
-                                                               past_lengths))
-        host_out, out = out, None
-    shape = (B, Hq, Sq, D) if layout == 0 else (B, Sq, Hq * D)
-    if out is None:
-        out = torch.empty(shape, dtype=q.dtype, device=q.device)
-    elif tuple(out.shape) != shape or out.dtype != q.dtype or not out.is_contiguous():
-        raise ValueError(f"out must be a contiguous {q.dtype} tensor of shape {shape}")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
+    shape = (B, Hq, Sq, D) if layout == 0 else (B, Sq, Hq * D)
+    if out is not None and (tuple(out.shape) != shape or out.dtype != q.dtype or not out.is_contiguous()):
+        raise ValueError(f"out must be a contiguous {q.dtype} tensor of shape {shape}")
     lib = load_library()
+    what = "attn_fwd_f32_split" if _f32_split else "attn_fwd"
+
+    def launch(dq, dk, dv, dmask, dtot, dpast, dout, b_, hq_, hkv_, planes, ws, stream):
+        args = (_ptr(dq), _ptr(dk), _ptr(dv), _ptr(dmask), _ptr(dtot), _ptr(dpast), _ptr(dout), b_, hq_, hkv_,
+                Sq, Sk, kv_capacity, D, int(bool(causal)), int(local_window), float(scale), float(softcap),
+                layout, planes)
+        if _f32_split:
+            ws_bytes = ws.numel() * ws.element_size()
+            return lib.attn_fwd_f32_split(*args, _ptr(ws), ws_bytes, stream)
+        return lib.attn_fwd(*args, DTYPE_CODES[q.dtype], stream)
+
+    if not q.is_cuda:
+        return _host_pipeline(q, k, v, mask, total_lengths, past_lengths, out, shape, layout, mask_planes,
+                              launch, lib, _f32_split, what,
+                              (Sk, int(bool(causal)), int(local_window), float(scale), float(softcap)))
+    if out is None:
+        out = torch.empty(shape, dtype=q.dtype, device=q.device)
     with torch.cuda.device(q.device):
-        args = (_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(total_lengths), _ptr(past_lengths),
-                _ptr(out), B, Hq, Hkv, Sq, Sk, kv_capacity, D, int(bool(causal)),
-                int(local_window), float(scale), float(softcap), layout, mask_planes)
+        ws = None
         if _f32_split:
             need = lib.attn_f32_split_workspace_bytes(B, Hkv, kv_capacity, D)
-            if workspace is None or not workspace.is_cuda:
-                workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-            ws_bytes = workspace.numel() * workspace.element_size()
-            rc = lib.attn_fwd_f32_split(*args, _ptr(workspace), ws_bytes, _stream_handle(q.device))
-            what = "attn_fwd_f32_split"
-        else:
-            rc = lib.attn_fwd(*args, DTYPE_CODES[q.dtype], _stream_handle(q.device))
-            what = "attn_fwd"
+            ws = workspace if (workspace is not None and workspace.is_cuda) else \
+                torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        rc = launch(q, k, v, mask, total_lengths, past_lengths, out, B, Hq, Hkv, mask_planes, ws,
+                    _stream_handle(q.device))
     if rc != ATTN_OK:
         raise AttnError(rc, what)
-    if host:
-        if host_out is None:
-            host_out = torch.empty(shape, dtype=q.dtype, pin_memory=True)
-        host_out.copy_(out, non_blocking=True)
-        torch.cuda.current_stream(q.device).synchronize()
-        return host_out
     return out
+
+
+def _host_pieces(B, Hq, Hkv, layout):
+    """The host path's pieces of a problem, (b0, b1, h0, h1, kv0, kv1): runs
+    of whole batches, at most 64 pieces, and -- for head-major output, whose
+    head slices are contiguous -- with fewer than eight batches each batch
+    cut further by whole kv-head groups, so that about eight pieces exist to
+    overlap with one another.  attn_fwd_host cuts by the same rule."""
+    group = Hq // Hkv
+    pieces = []
+    if layout == 0 and B < 8:
+        per_batch = min(Hkv, -(-8 // max(B, 1)))
+        for b in range(B):
+            for i in range(per_batch):
+                kv0, kv1 = Hkv * i // per_batch, Hkv * (i + 1) // per_batch
+                if kv1 > kv0:
+                    pieces.append((b, b + 1, kv0 * group, kv1 * group, kv0, kv1))
+        return pieces
+    chunks = min(B, 64)
+    for i in range(chunks):
+        b0, b1 = B * i // chunks, B * (i + 1) // chunks
+        if b1 > b0:
+            pieces.append((b0, b1, 0, Hq, 0, Hkv))
+    return pieces
+
+
+def _host_pipeline(q, k, v, mask, total_lengths, past_lengths, host_out, shape, layout, mask_planes, launch,
+                   lib, f32_split, what, params):
+    """The end-to-end path for host (ideally pinned) tensors.  The problem is
+    cut into contiguous pieces (_host_pieces), each an ordinary call on its
+    slices, and three streams overlap piece i + 1's upload, piece i's kernel
+    and piece i - 1's download.  Every piece computes exactly what the whole
+    call would for its rows, so the result is the same bit for bit.  For
+    attn_fwd the library issues the pipeline itself (attn_fwd_host); the fp32
+    split path issues it from here."""
+    B, Hq, Sq, D = q.shape
+    Hkv, kv_capacity = k.shape[1], k.shape[2]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if host_out is None:
+        host_out = torch.empty(shape, dtype=q.dtype, pin_memory=True)
+    with torch.cuda.device(dev):
+        compute = torch.cuda.current_stream(dev)
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        s_in.wait_stream(compute)  # device buffers may be reused from earlier work on this stream
+        dq, dk, dv = (torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (q, k, v))
+        dout = torch.empty(shape, dtype=q.dtype, device=dev)
+        dtot = None if total_lengths is None else torch.empty_like(total_lengths, device=dev)
+        dpast = None if past_lengths is None else torch.empty_like(past_lengths, device=dev)
+        dmask = None if mask is None else torch.empty(mask.shape, dtype=mask.dtype, device=dev)
+        if not f32_split:
+            # the same pipeline, issued natively: one blocking call
+            rc = lib.attn_fwd_host(
+                _ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(total_lengths), _ptr(past_lengths), _ptr(host_out),
+                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dmask), _ptr(dtot), _ptr(dpast), _ptr(dout),
+                B, Hq, Hkv, Sq, params[0], kv_capacity, D, *params[1:], layout, mask_planes, DTYPE_CODES[q.dtype],
+                ctypes.c_void_p(compute.cuda_stream), ctypes.c_void_p(s_in.cuda_stream),
+                ctypes.c_void_p(s_out.cuda_stream))
+            if rc != ATTN_OK:
+                raise AttnError(rc, "attn_fwd_host")
+            return host_out
+        pieces = _host_pieces(B, Hq, Hkv, layout) if B > 0 and Sq > 0 else []
+        ws = None
+        if f32_split and pieces:
+            need = max(lib.attn_f32_split_workspace_bytes(b1 - b0, kv1 - kv0, kv_capacity, D)
+                       for b0, b1, _, _, kv0, kv1 in pieces)
+            ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(s_in):
+            for src, dst in ((total_lengths, dtot), (past_lengths, dpast)):
+                if src is not None:
+                    dst.copy_(src, non_blocking=True)
+            if mask is not None and mask_planes == 1:
+                dmask.copy_(mask, non_blocking=True)  # one plane shared by every piece
+        mask_batch = -1  # batch whose plane was last uploaded (per-batch planes)
+        for b0, b1, h0, h1, kv0, kv1 in pieces:
+            nb, hq_, hkv_ = b1 - b0, h1 - h0, kv1 - kv0
+            planes = 0
+            m_host = m_dev = None
+            if mask is not None:
+                if mask_planes == 1:
+                    m_dev, planes = dmask, 1
+                elif mask_planes == B and not (mask_planes == B * Hq and Hq > 1):
+                    m_dev, planes = dmask[b0:b1], nb
+                    if b0 != mask_batch:  # a batch's plane goes up once, with its first piece
+                        m_host, mask_batch = mask[b0:b1], b0
+                else:  # a plane per (batch, head); the piece's planes are contiguous
+                    p0, p1 = b0 * Hq + h0, (b1 - 1) * Hq + h1
+                    m_host, m_dev, planes = mask[p0:p1], dmask[p0:p1], p1 - p0
+            slices_h = (q[b0:b1, h0:h1], k[b0:b1, kv0:kv1], v[b0:b1, kv0:kv1])
+            slices_d = (dq[b0:b1, h0:h1], dk[b0:b1, kv0:kv1], dv[b0:b1, kv0:kv1])
+            o_d = dout[b0:b1, h0:h1] if layout == 0 else dout[b0:b1]
+            o_h = host_out[b0:b1, h0:h1] if layout == 0 else host_out[b0:b1]
+            with torch.cuda.stream(s_in):
+                for src, dst in zip(slices_h, slices_d):
+                    dst.copy_(src, non_blocking=True)
+                if m_host is not None:
+                    m_dev.copy_(m_host, non_blocking=True)
+                uploaded = torch.cuda.Event()
+                uploaded.record(s_in)
+            compute.wait_event(uploaded)
+            rc = launch(*slices_d, m_dev, None if dtot is None else dtot[b0:b1],
+                        None if dpast is None else dpast[b0:b1], o_d, nb, hq_, hkv_, planes, ws,
+                        ctypes.c_void_p(compute.cuda_stream))
+            if rc != ATTN_OK:
+                compute.synchronize()
+                raise AttnError(rc, what)
+            computed = torch.cuda.Event()
+            computed.record(compute)
+            s_out.wait_event(computed)
+            with torch.cuda.stream(s_out):
+                o_h.copy_(o_d, non_blocking=True)
+        s_out.synchronize()
+        compute.wait_stream(s_out)
+    return host_out
 
 
 def attn_fwd_f32_split(q, k, v, *, mask=None, total_lengths=None, past_lengths=None,

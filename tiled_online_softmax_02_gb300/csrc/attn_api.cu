@@ -9,6 +9,7 @@
 // the call is asynchronous (no synchronisation after the launch) and an
 // empty key range (Sk == 0) writes zeros instead of leaving the output
 // untouched.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -188,7 +189,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
              int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D,
              int causal, int local_window, float scale, float softcap, int out_layout,
              int mask_planes, int dtype, void* stream, bool splitkv_api, int num_splits, float* lse,
-             void* workspace, size_t workspace_bytes, bool f32split = false) {
+             void* workspace, size_t workspace_bytes, bool f32split = false, bool validate_only = false) {
   // ---------------------------------------------------------------- validation
   if (dtype != ATTN_F32 && dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   if (B < 0 || Sq < 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
@@ -259,6 +260,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
   if ((total_lengths && !aligned(total_lengths, 4)) || (past_lengths && !aligned(past_lengths, 4)))
     return ATTN_ERR_UNSUPPORTED;
 
+  if (validate_only) return ATTN_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (Sk == 0) {  // no key at all: every row is 0 (and its log-sum-exp -inf)
     cudaError_t e = cudaMemsetAsync(out, 0, (size_t)qbytes, st);
@@ -393,6 +395,155 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, const float
   return fwd_impl(q, k, v, mask, total_lengths, past_lengths, out, B, Hq, Hkv, Sq, Sk, kv_capacity,
                   D, causal, local_window, scale, softcap, out_layout, mask_planes, dtype, stream,
                   false, 1, nullptr, nullptr, 0);
+}
+
+// ---------------------------------------------------------------------------
+// End-to-end call on host buffers (attn_fwd_host): the problem is cut into
+// pieces -- runs of whole batches, at most 64 pieces, and for head-major
+// output, with fewer than eight batches, each batch cut further by whole
+// kv-head groups -- and three streams overlap piece i + 1's upload, piece i's
+// kernel and piece i - 1's download.  Each piece is an ordinary attn_fwd call
+// on its slices, so the result is the whole call's bit for bit.  Issuing this
+// natively keeps the host's cost per piece to a few microseconds, well under
+// a piece's copy time.
+namespace {
+
+struct HostPiece {
+  int b0, b1, h0, h1, kv0, kv1;
+};
+
+constexpr int kMaxHostPieces = 64;
+
+int host_pieces(int B, int Hq, int Hkv, int out_layout, HostPiece* pieces) {
+  const int group = Hq / Hkv;
+  int n = 0;
+  if (out_layout == ATTN_OUT_HEAD_MAJOR && B < 8) {
+    const int per_batch = std::min(Hkv, (8 + B - 1) / B);
+    for (int b = 0; b < B; ++b)
+      for (int i = 0; i < per_batch; ++i) {
+        const int kv0 = (int)((int64_t)Hkv * i / per_batch), kv1 = (int)((int64_t)Hkv * (i + 1) / per_batch);
+        if (kv1 > kv0) pieces[n++] = HostPiece{b, b + 1, kv0 * group, kv1 * group, kv0, kv1};
+      }
+    return n;
+  }
+  const int chunks = std::min(B, kMaxHostPieces);
+  for (int i = 0; i < chunks; ++i) {
+    const int b0 = (int)((int64_t)B * i / chunks), b1 = (int)((int64_t)B * (i + 1) / chunks);
+    if (b1 > b0) pieces[n++] = HostPiece{b0, b1, 0, Hq, 0, Hkv};
+  }
+  return n;
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_host(const void* q, const void* k, const void* v, const float* mask,
+                             const int32_t* total_lengths, const int32_t* past_lengths, void* out, void* dq,
+                             void* dk, void* dv, float* dmask, int32_t* dtotal, int32_t* dpast, void* dout, int B,
+                             int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D, int causal,
+                             int local_window, float scale, float softcap, int out_layout, int mask_planes,
+                             int dtype, void* stream, void* copy_in_stream, void* copy_out_stream) {
+  if ((mask == nullptr) != (dmask == nullptr) || (total_lengths == nullptr) != (dtotal == nullptr) ||
+      (past_lengths == nullptr) != (dpast == nullptr))
+    return ATTN_ERR_INVALID_ARG;
+  // the whole problem, as attn_fwd would see it on the device buffers
+  int rc = fwd_impl(dq, dk, dv, dmask, dtotal, dpast, dout, B, Hq, Hkv, Sq, Sk, kv_capacity, D, causal,
+                    local_window, scale, softcap, out_layout, mask_planes, dtype, stream, false, 1, nullptr,
+                    nullptr, 0, false, /*validate_only=*/true);
+  if (rc != ATTN_OK) return rc;
+  if (B == 0 || Sq == 0) return ATTN_OK;
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
+
+  const size_t es = dtype == ATTN_F32 ? 4 : 2;
+  const size_t q_head = (size_t)Sq * D * es, kv_head = (size_t)kv_capacity * D * es;
+  const size_t m_plane = (size_t)Sq * Sk * 4;
+  const size_t o_batch = (size_t)Sq * Hq * D * es;
+  HostPiece pieces[kMaxHostPieces];
+  int n;
+  if (q_head % 16 == 0 && kv_head % 16 == 0) {
+    n = host_pieces(B, Hq, Hkv, out_layout, pieces);
+  } else {  // a piece would start off the 16-byte alignment the kernels need: one piece
+    pieces[0] = HostPiece{0, B, 0, Hq, 0, Hkv};
+    n = 1;
+  }
+  const bool per_head_mask = mask != nullptr && (int64_t)mask_planes == (int64_t)B * Hq && Hq > 1;
+  const bool per_batch_mask = mask != nullptr && !per_head_mask && mask_planes == B && B > 1;
+
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaStream_t si = copy_in_stream ? static_cast<cudaStream_t>(copy_in_stream) : cs;
+  cudaStream_t so = copy_out_stream ? static_cast<cudaStream_t>(copy_out_stream) : cs;
+  auto h2d = [&](void* d, const void* h, size_t off, size_t bytes) {
+    return bytes ? cudaMemcpyAsync(static_cast<uint8_t*>(d) + off, static_cast<const uint8_t*>(h) + off, bytes,
+                                   cudaMemcpyHostToDevice, si)
+                 : cudaSuccess;
+  };
+  cudaEvent_t events[2 * kMaxHostPieces + 1];
+  int n_events = 0;
+  auto new_event = [&](cudaEvent_t* e) {
+    cudaError_t err = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
+    if (err == cudaSuccess) events[n_events++] = *e;
+    return err;
+  };
+  auto finish = [&](int status) {
+    // nothing of this call may still use the caller's buffers when it returns
+    cudaStreamSynchronize(si);
+    cudaStreamSynchronize(cs);
+    cudaStreamSynchronize(so);
+    for (int i = 0; i < n_events; ++i) cudaEventDestroy(events[i]);
+    return status;
+  };
+  cudaError_t e;
+  cudaEvent_t start;
+  // the device buffers may still be in use by earlier work on the compute stream
+  if ((e = new_event(&start)) != cudaSuccess) return finish(cuda_fail(e));
+  if ((e = cudaEventRecord(start, cs)) != cudaSuccess || (e = cudaStreamWaitEvent(si, start, 0)) != cudaSuccess)
+    return finish(cuda_fail(e));
+  if ((total_lengths && (e = h2d(dtotal, total_lengths, 0, (size_t)B * 4)) != cudaSuccess) ||
+      (past_lengths && (e = h2d(dpast, past_lengths, 0, (size_t)B * 4)) != cudaSuccess) ||
+      (mask && !per_head_mask && !per_batch_mask && (e = h2d(dmask, mask, 0, m_plane)) != cudaSuccess))
+    return finish(cuda_fail(e));  // lengths, and a mask plane shared by every piece
+  int mask_batch = -1;  // batch whose plane went up last (one plane per batch)
+  for (int i = 0; i < n; ++i) {
+    const HostPiece& pc = pieces[i];
+    const int nb = pc.b1 - pc.b0, hq = pc.h1 - pc.h0, hkv = pc.kv1 - pc.kv0;
+    const size_t qo = ((size_t)pc.b0 * Hq + pc.h0) * q_head, ko = ((size_t)pc.b0 * Hkv + pc.kv0) * kv_head;
+    const size_t qb = (size_t)nb * hq * q_head, kb = (size_t)nb * hkv * kv_head;
+    float* m_dev = dmask;
+    int planes = mask ? 1 : 0;
+    size_t mo = 0;
+    if (per_head_mask) {
+      mo = ((size_t)pc.b0 * Hq + pc.h0) * m_plane;
+      planes = nb * hq;
+      if ((e = h2d(dmask, mask, mo, (size_t)planes * m_plane)) != cudaSuccess) return finish(cuda_fail(e));
+    } else if (per_batch_mask) {
+      mo = (size_t)pc.b0 * m_plane;
+      planes = nb;
+      if (pc.b0 != mask_batch) {  // a batch's plane goes up once, with its first piece
+        if ((e = h2d(dmask, mask, mo, (size_t)nb * m_plane)) != cudaSuccess) return finish(cuda_fail(e));
+        mask_batch = pc.b0;
+      }
+    }
+    if (mask) m_dev = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dmask) + mo);
+    if ((e = h2d(dq, q, qo, qb)) != cudaSuccess || (e = h2d(dk, k, ko, kb)) != cudaSuccess ||
+        (e = h2d(dv, v, ko, kb)) != cudaSuccess)
+      return finish(cuda_fail(e));
+    cudaEvent_t up, done;
+    if ((e = new_event(&up)) != cudaSuccess || (e = new_event(&done)) != cudaSuccess) return finish(cuda_fail(e));
+    if ((e = cudaEventRecord(up, si)) != cudaSuccess || (e = cudaStreamWaitEvent(cs, up, 0)) != cudaSuccess)
+      return finish(cuda_fail(e));
+    const bool head_major = out_layout == ATTN_OUT_HEAD_MAJOR;
+    const size_t oo = head_major ? qo : (size_t)pc.b0 * o_batch, ob = head_major ? qb : (size_t)nb * o_batch;
+    rc = fwd_impl(static_cast<uint8_t*>(dq) + qo, static_cast<uint8_t*>(dk) + ko, static_cast<uint8_t*>(dv) + ko,
+                  m_dev, dtotal ? dtotal + pc.b0 : nullptr, dpast ? dpast + pc.b0 : nullptr,
+                  static_cast<uint8_t*>(dout) + oo, nb, hq, hkv, Sq, Sk, kv_capacity, D, causal, local_window,
+                  scale, softcap, out_layout, planes, dtype, cs, false, 1, nullptr, nullptr, 0);
+    if (rc != ATTN_OK) return finish(rc);
+    if ((e = cudaEventRecord(done, cs)) != cudaSuccess || (e = cudaStreamWaitEvent(so, done, 0)) != cudaSuccess)
+      return finish(cuda_fail(e));
+    if ((e = cudaMemcpyAsync(static_cast<uint8_t*>(out) + oo, static_cast<const uint8_t*>(dout) + oo, ob,
+                             cudaMemcpyDeviceToHost, so)) != cudaSuccess)
+      return finish(cuda_fail(e));
+  }
+  return finish(ATTN_OK);
 }
 
 extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, const float* mask,
