@@ -107,12 +107,21 @@ int attn_fwd(const void *q, const void *k, const void *v, const float *mask,
  * overlapped with the kernels of its neighbours.  Same operation as attn_fwd
  * (every output element is bit-identical to attn_fwd on the same inputs).
  *
- * The problem is cut into pieces: one per batch, and for ATTN_OUT_HEAD_MAJOR
- * each batch further into whole kv-head groups, about eight pieces in all.
+ * The problem is cut into pieces: runs of whole batches, at most 64 pieces,
+ * and for ATTN_OUT_HEAD_MAJOR with fewer than eight batches each batch cut
+ * further by whole kv-head groups, about eight pieces in all.  When a
+ * piece's slices would not start on a 16-byte boundary (fp32 with Sq * D or
+ * kv_capacity * D not a multiple of 4) the whole problem is one piece.
  * For each piece, in order: its q / k / v slices (and mask planes) are
- * copied up on `copy_in_stream`; `stream` waits for them and runs attn_fwd on
- * the piece; `copy_out_stream` waits for that and copies the piece's output
- * down.  Lengths and a shared mask plane go up first.
+ * copied up on an upload stream; one of a few compute streams waits for them
+ * and runs attn_fwd on the piece (so the kernels of small pieces can run
+ * side by side); a download stream waits for that and copies the piece's
+ * output down.  These streams are the library's own (created once per
+ * device, kept for the process), forked from and joined back into `stream`.
+ * Lengths and a shared mask plane go up first.  Only what can reach the
+ * output is uploaded: of each batch's cache rows and mask columns, those
+ * j < min(total_lengths[b], Sk) (all Sk when total_lengths is NULL); the
+ * other slots of dk / dv / dmask are left as they were.
  *
  * Arguments as attn_fwd, except:
  *   q, k, v, mask, total_lengths, past_lengths, out
@@ -123,24 +132,23 @@ int attn_fwd(const void *q, const void *k, const void *v, const float *mask,
  *   dq, dk, dv, dmask, dtotal, dpast, dout
  *                 caller-owned DEVICE buffers of the same sizes, the device
  *                 arguments of attn_fwd (alignment and overlap rules as there).
- *   stream, copy_in_stream, copy_out_stream
- *                 cudaStream_t; NULL copy streams fall back to `stream` (no
- *                 overlap).  Work already on `stream` finishes before the
- *                 device buffers are written.
+ *   stream        a cudaStream_t: work already on it finishes before the
+ *                 device buffers are written, and work queued on it after
+ *                 the call is ordered after all of the call's work.
+ *   copied_bytes  NULL or uint64_t[2]: on success receives the bytes copied
+ *                 host to device and device to host.
  * Behaviour: validates the whole problem as attn_fwd would before touching
  * anything.  BLOCKS until the output is in `out` (and on any error, until
  * nothing it enqueued still runs), so the host buffers may be reused as
  * soon as it returns.  Creates and destroys its own events; allocates no
- * device memory.  Errors as attn_fwd; ATTN_ERR_UNSUPPORTED for more than
- * 4096 pieces (B > 4096).
+ * device memory.  Errors as attn_fwd.
  */
 int attn_fwd_host(const void *q, const void *k, const void *v, const float *mask,
                   const int32_t *total_lengths, const int32_t *past_lengths, void *out,
                   void *dq, void *dk, void *dv, float *dmask, int32_t *dtotal, int32_t *dpast,
                   void *dout, int B, int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D,
                   int causal, int local_window, float scale, float softcap, int out_layout,
-                  int mask_planes, int dtype, void *stream, void *copy_in_stream,
-                  void *copy_out_stream);
+                  int mask_planes, int dtype, void *stream, uint64_t *copied_bytes);
 
 /*
  * attn_fwd_splitkv -- attn_fwd with each query tile's keys split into

@@ -8,6 +8,7 @@ import pytest
 import torch
 
 import tiled_online_softmax_02_gb300 as attn
+from tiled_online_softmax_02_gb300 import _binding
 from tiled_online_softmax_02_gb300.inputs import Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -83,3 +84,66 @@ def test_host_call_rejects_bad_arguments_before_copying():
     with pytest.raises(attn.AttnError):
         attn.attn_fwd(pin["q"], pin["k"], pin["v"], local_window=0, scale=float("nan"), out=out)
     assert bool((out == 7.0).all())  # nothing was written
+
+
+NAN_CASES = {
+    "ragged_per_batch_mask": dict(B=3, Hq=8, Hkv=2, Sq=100, Sk=700, kv_capacity=720, causal=True, ragged=True,
+                                  mask="per_batch", mask_neg_inf_frac=0.1),
+    "ragged_per_head_mask": dict(B=2, Hq=4, Hkv=4, Sq=64, Sk=300, kv_capacity=300, causal=True, ragged=True,
+                                 mask="per_head", mask_neg_inf_frac=0.1),
+    "ragged_shared_mask_window": dict(B=4, Hq=4, Hkv=2, Sq=40, Sk=500, kv_capacity=512, ragged=True,
+                                      mask="shared", local_window=64, out_layout=1),
+    "seq_k_below_capacity": dict(B=2, Hq=4, Hkv=1, Sq=90, Sk=200, kv_capacity=256, causal=True),
+}
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("case", list(NAN_CASES))
+def test_slots_past_the_valid_keys_are_not_uploaded(case, dtype):
+    """attn_fwd_host uploads only cache rows and mask columns j < min(lsk, Sk):
+    with every device buffer first filled with NaN, the output still equals
+    the device call on fully uploaded inputs, and the bytes it reports are
+    exactly those rows and columns plus q and the lengths."""
+    import ctypes
+    w = Workload("host", D=128 if dtype == "bf16" else 64, dtype=dtype, seed=324,
+                 **{"causal": False, **NAN_CASES[case]})
+    x = make_inputs(w)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    want = _call(attn.attn_fwd, w, dev).cpu()
+    pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    d = {}
+    for name in ("q", "k", "v", "mask"):
+        t = x[name]
+        d[name] = None if t is None else torch.full(t.shape, float("nan"), dtype=t.dtype, device="cuda")
+    for name in ("total_lengths", "past_lengths"):
+        t = x[name]
+        d[name] = None if t is None else torch.full(t.shape, -7, dtype=torch.int32, device="cuda")
+    dout = torch.full(want.shape, float("nan"), dtype=want.dtype, device="cuda")
+    host_out = torch.empty(want.shape, dtype=want.dtype).pin_memory()
+    lib = attn.load_library()
+    copied = (ctypes.c_uint64 * 2)()
+    ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    torch.cuda.synchronize()
+    rc = lib.attn_fwd_host(ptr(pin["q"]), ptr(pin["k"]), ptr(pin["v"]), ptr(pin["mask"]),
+                           ptr(pin["total_lengths"]), ptr(pin["past_lengths"]), ptr(host_out),
+                           ptr(d["q"]), ptr(d["k"]), ptr(d["v"]), ptr(d["mask"]), ptr(d["total_lengths"]),
+                           ptr(d["past_lengths"]), ptr(dout), w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.kv_capacity, w.D,
+                           int(w.causal), w.local_window, w.softmax_scale, w.softcap, w.out_layout,
+                           0 if x["mask"] is None else x["mask"].shape[0], _binding.DTYPE_CODES[x["q"].dtype],
+                           ctypes.c_void_p(torch.cuda.current_stream().cuda_stream), copied)
+    assert rc == attn.ATTN_OK, attn.status_string(rc)
+    assert torch.equal(host_out, want)
+    # the bytes the header's rule gives
+    es = x["q"].element_size()
+    tot = x["total_lengths"]
+    rows = [min(max(int(tot[b]), 0), w.Sk) if tot is not None else w.Sk for b in range(w.B)]
+    up = x["q"].numel() * es + 2 * sum(rows) * w.Hkv * w.D * es
+    up += sum(4 * t.numel() for t in (x["total_lengths"], x["past_lengths"]) if t is not None)
+    if w.mask == "per_batch":
+        up += sum(rows) * w.Sq * 4
+    elif w.mask == "per_head":
+        up += sum(rows) * w.Hq * w.Sq * 4
+    elif w.mask == "shared":
+        up += max(rows) * w.Sq * 4
+    assert (copied[0], copied[1]) == (up, want.numel() * es)
+    assert sum(rows) < w.B * w.kv_capacity  # the case leaves slots out

@@ -45,7 +45,7 @@ SIGNATURES = {
                              _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                              _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                              _i32, _i32, ctypes.c_float, ctypes.c_float, _i32,
-                             _i32, _i32, _vp, _vp, _vp]),
+                             _i32, _i32, _vp, _vp]),
     "attn_f32_split_workspace_bytes": (ctypes.c_size_t, [_i32, _i32, _i32, _i32]),
     "dsa_index_select": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                 ctypes.c_float, ctypes.c_float, _i32, _vp, ctypes.c_size_t, _vp]),
@@ -62,6 +62,7 @@ SIGNATURES = {
 
 _lock = threading.Lock()
 _lib = None
+_host_copies = threading.local()  # (h2d, d2h) bytes of this thread's last host-tensor call
 
 
 class AttnError(RuntimeError):
@@ -186,6 +187,12 @@ def attn_fwd(q, k, v, *, mask=None, total_lengths=None, past_lengths=None, causa
     return out
 
 
+def host_copy_bytes():
+    """(host-to-device, device-to-host) bytes the calling thread's last
+    attention call on host tensors copied; (0, 0) before the first."""
+    return getattr(_host_copies, "value", (0, 0))
+
+
 def _host_pieces(B, Hq, Hkv, layout):
     """The host path's pieces of a problem, (b0, b1, h0, h1, kv0, kv1): runs
     of whole batches, at most 64 pieces, and -- for head-major output, whose
@@ -217,13 +224,16 @@ def _host_pipeline(q, k, v, mask, total_lengths, past_lengths, host_out, shape, 
     slices, and three streams overlap piece i + 1's upload, piece i's kernel
     and piece i - 1's download.  Every piece computes exactly what the whole
     call would for its rows, so the result is the same bit for bit.  For
-    attn_fwd the library issues the pipeline itself (attn_fwd_host); the fp32
+    attn_fwd the library issues the pipeline itself (_host_native); the fp32
     split path issues it from here."""
     B, Hq, Sq, D = q.shape
     Hkv, kv_capacity = k.shape[1], k.shape[2]
     dev = torch.device("cuda", torch.cuda.current_device())
     if host_out is None:
         host_out = torch.empty(shape, dtype=q.dtype, pin_memory=True)
+    if not f32_split:
+        return _host_native(q, k, v, mask, total_lengths, past_lengths, host_out, layout, mask_planes, lib, dev,
+                            params)
     with torch.cuda.device(dev):
         compute = torch.cuda.current_stream(dev)
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -233,28 +243,20 @@ def _host_pipeline(q, k, v, mask, total_lengths, past_lengths, host_out, shape, 
         dtot = None if total_lengths is None else torch.empty_like(total_lengths, device=dev)
         dpast = None if past_lengths is None else torch.empty_like(past_lengths, device=dev)
         dmask = None if mask is None else torch.empty(mask.shape, dtype=mask.dtype, device=dev)
-        if not f32_split:
-            # the same pipeline, issued natively: one blocking call
-            rc = lib.attn_fwd_host(
-                _ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(total_lengths), _ptr(past_lengths), _ptr(host_out),
-                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dmask), _ptr(dtot), _ptr(dpast), _ptr(dout),
-                B, Hq, Hkv, Sq, params[0], kv_capacity, D, *params[1:], layout, mask_planes, DTYPE_CODES[q.dtype],
-                ctypes.c_void_p(compute.cuda_stream), ctypes.c_void_p(s_in.cuda_stream),
-                ctypes.c_void_p(s_out.cuda_stream))
-            if rc != ATTN_OK:
-                raise AttnError(rc, "attn_fwd_host")
-            return host_out
         pieces = _host_pieces(B, Hq, Hkv, layout) if B > 0 and Sq > 0 else []
         ws = None
         if f32_split and pieces:
             need = max(lib.attn_f32_split_workspace_bytes(b1 - b0, kv1 - kv0, kv_capacity, D)
                        for b0, b1, _, _, kv0, kv1 in pieces)
             ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        up = down = 0
         with torch.cuda.stream(s_in):
             for src, dst in ((total_lengths, dtot), (past_lengths, dpast)):
                 if src is not None:
                     dst.copy_(src, non_blocking=True)
+                    up += src.numel() * 4
             if mask is not None and mask_planes == 1:
+                up += mask.numel() * 4
                 dmask.copy_(mask, non_blocking=True)  # one plane shared by every piece
         mask_batch = -1  # batch whose plane was last uploaded (per-batch planes)
         for b0, b1, h0, h1, kv0, kv1 in pieces:
@@ -278,8 +280,10 @@ def _host_pipeline(q, k, v, mask, total_lengths, past_lengths, host_out, shape, 
             with torch.cuda.stream(s_in):
                 for src, dst in zip(slices_h, slices_d):
                     dst.copy_(src, non_blocking=True)
+                    up += src.numel() * src.element_size()
                 if m_host is not None:
                     m_dev.copy_(m_host, non_blocking=True)
+                    up += m_host.numel() * 4
                 uploaded = torch.cuda.Event()
                 uploaded.record(s_in)
             compute.wait_event(uploaded)
@@ -294,8 +298,35 @@ def _host_pipeline(q, k, v, mask, total_lengths, past_lengths, host_out, shape, 
             s_out.wait_event(computed)
             with torch.cuda.stream(s_out):
                 o_h.copy_(o_d, non_blocking=True)
+                down += o_h.numel() * o_h.element_size()
         s_out.synchronize()
         compute.wait_stream(s_out)
+    _host_copies.value = (up, down)
+    return host_out
+
+
+def _host_native(q, k, v, mask, total_lengths, past_lengths, host_out, layout, mask_planes, lib, dev, params):
+    """attn_fwd on host tensors through attn_fwd_host: one blocking library
+    call that pipelines the pieces on the library's own streams.  The device
+    copies of every argument are carved from one allocation."""
+    B, Hq, Sq, D = q.shape
+    Hkv, kv_capacity = k.shape[1], k.shape[2]
+    args = (q, k, v, mask, total_lengths, past_lengths, host_out)
+    sizes = [0 if t is None else t.numel() * t.element_size() for t in args]
+    offsets, total = [], 0
+    for n in sizes:
+        offsets.append(total)
+        total += -(-n // 256) * 256
+    copied = (ctypes.c_uint64 * 2)()
+    with torch.cuda.device(dev):
+        buf = torch.empty(max(total, 256), dtype=torch.uint8, device=dev)
+        base = buf.data_ptr()
+        dptr = [None if t is None else ctypes.c_void_p(base + o) for t, o in zip(args, offsets)]
+        rc = lib.attn_fwd_host(*(_ptr(t) for t in args), *dptr, B, Hq, Hkv, Sq, params[0], kv_capacity, D,
+                               *params[1:], layout, mask_planes, DTYPE_CODES[q.dtype], _stream_handle(dev), copied)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_host")
+    _host_copies.value = (int(copied[0]), int(copied[1]))
     return host_out
 
 

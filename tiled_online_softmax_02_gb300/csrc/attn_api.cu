@@ -401,8 +401,8 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, const float
 // End-to-end call on host buffers (attn_fwd_host): the problem is cut into
 // pieces -- runs of whole batches, at most 64 pieces, and for head-major
 // output, with fewer than eight batches, each batch cut further by whole
-// kv-head groups -- and three streams overlap piece i + 1's upload, piece i's
-// kernel and piece i - 1's download.  Each piece is an ordinary attn_fwd call
+// kv-head groups -- and the library's own streams overlap piece i + 1's
+// upload, piece i's kernel and piece i - 1's download.  Each piece is an ordinary attn_fwd call
 // on its slices, so the result is the whole call's bit for bit.  Issuing this
 // natively keeps the host's cost per piece to a few microseconds, well under
 // a piece's copy time.
@@ -413,6 +413,39 @@ struct HostPiece {
 };
 
 constexpr int kMaxHostPieces = 64;
+constexpr int kHostComputeStreams = 4;
+
+// The host path's own streams on one device: uploads, downloads, and a few
+// compute streams so that the kernels of small pieces (fewer work items than
+// SMs) run side by side.  Created on first use, kept for the process.
+struct HostStreams {
+  cudaStream_t in, out, compute[kHostComputeStreams];
+};
+
+HostStreams* host_streams(int* err) {
+  static std::mutex mu;
+  static HostStreams* cache[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 128) {
+    *err = cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice);
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    HostStreams hs{};
+    cudaStream_t* all[2 + kHostComputeStreams] = {&hs.in, &hs.out};
+    for (int i = 0; i < kHostComputeStreams; ++i) all[2 + i] = &hs.compute[i];
+    for (int i = 0; i < 2 + kHostComputeStreams; ++i)
+      if ((e = cudaStreamCreateWithFlags(all[i], cudaStreamNonBlocking)) != cudaSuccess) {
+        for (int j = 0; j < i; ++j) cudaStreamDestroy(*all[j]);
+        *err = cuda_fail(e);
+        return nullptr;
+      }
+    cache[dev] = new HostStreams(hs);
+  }
+  return cache[dev];
+}
 
 int host_pieces(int B, int Hq, int Hkv, int out_layout, HostPiece* pieces) {
   const int group = Hq / Hkv;
@@ -441,7 +474,8 @@ extern "C" int attn_fwd_host(const void* q, const void* k, const void* v, const 
                              void* dk, void* dv, float* dmask, int32_t* dtotal, int32_t* dpast, void* dout, int B,
                              int Hq, int Hkv, int Sq, int Sk, int kv_capacity, int D, int causal,
                              int local_window, float scale, float softcap, int out_layout, int mask_planes,
-                             int dtype, void* stream, void* copy_in_stream, void* copy_out_stream) {
+                             int dtype, void* stream, uint64_t* copied_bytes) {
+  if (copied_bytes) copied_bytes[0] = copied_bytes[1] = 0;
   if ((mask == nullptr) != (dmask == nullptr) || (total_lengths == nullptr) != (dtotal == nullptr) ||
       (past_lengths == nullptr) != (dpast == nullptr))
     return ATTN_ERR_INVALID_ARG;
@@ -468,80 +502,131 @@ extern "C" int attn_fwd_host(const void* q, const void* k, const void* v, const 
   const bool per_head_mask = mask != nullptr && (int64_t)mask_planes == (int64_t)B * Hq && Hq > 1;
   const bool per_batch_mask = mask != nullptr && !per_head_mask && mask_planes == B && B > 1;
 
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  cudaStream_t si = copy_in_stream ? static_cast<cudaStream_t>(copy_in_stream) : cs;
-  cudaStream_t so = copy_out_stream ? static_cast<cudaStream_t>(copy_out_stream) : cs;
-  auto h2d = [&](void* d, const void* h, size_t off, size_t bytes) {
-    return bytes ? cudaMemcpyAsync(static_cast<uint8_t*>(d) + off, static_cast<const uint8_t*>(h) + off, bytes,
-                                   cudaMemcpyHostToDevice, si)
-                 : cudaSuccess;
+  HostStreams* hs = host_streams(&rc);
+  if (!hs) return rc;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream), si = hs->in, so = hs->out;
+  uint64_t up_bytes = 0, down_bytes = 0;
+  // `height` rows of `width` bytes, `pitch` apart, from host h + off to device d + off
+  auto h2d = [&](void* d, const void* h, size_t off, size_t width, size_t pitch, size_t height) {
+    if (width == 0 || height == 0) return cudaSuccess;
+    up_bytes += (uint64_t)width * height;
+    uint8_t* dst = static_cast<uint8_t*>(d) + off;
+    const uint8_t* src = static_cast<const uint8_t*>(h) + off;
+    if (width == pitch || height == 1)
+      return cudaMemcpyAsync(dst, src, width * height, cudaMemcpyHostToDevice, si);
+    if (pitch <= (size_t)INT32_MAX)
+      return cudaMemcpy2DAsync(dst, pitch, src, pitch, width, height, cudaMemcpyHostToDevice, si);
+    for (size_t r = 0; r < height; ++r) {  // pitches past the 2-D copy's limit: one copy per row
+      cudaError_t err = cudaMemcpyAsync(dst + r * pitch, src + r * pitch, width, cudaMemcpyHostToDevice, si);
+      if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
   };
-  cudaEvent_t events[2 * kMaxHostPieces + 1];
+  // Only keys j < min(lsk, Sk) can be visible (attn_fwd's definition), and
+  // the kernels never let a cache slot or mask column past that reach the
+  // output: those are not uploaded.
+  auto key_rows = [&](int b) -> size_t {
+    if (!total_lengths) return (size_t)Sk;
+    return (size_t)std::min(std::max(total_lengths[b], 0), Sk);
+  };
+  cudaEvent_t events[2 * kMaxHostPieces + 3 + kHostComputeStreams];
   int n_events = 0;
   auto new_event = [&](cudaEvent_t* e) {
     cudaError_t err = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
     if (err == cudaSuccess) events[n_events++] = *e;
     return err;
   };
+  int used_compute = 0;  // compute streams that got a piece
   auto finish = [&](int status) {
-    // nothing of this call may still use the caller's buffers when it returns
-    cudaStreamSynchronize(si);
+    // `stream` joins the internal streams (work queued on it after this call
+    // is ordered after all of it) ...
+    cudaStream_t mine[2 + kHostComputeStreams] = {si, so};
+    for (int i = 0; i < used_compute; ++i) mine[2 + i] = hs->compute[i];
+    for (int i = 0; i < 2 + used_compute; ++i) {
+      cudaEvent_t j;
+      if (new_event(&j) == cudaSuccess && cudaEventRecord(j, mine[i]) == cudaSuccess)
+        cudaStreamWaitEvent(cs, j, 0);
+    }
+    // ... and nothing of this call may still use the caller's buffers when it returns
+    for (int i = 0; i < 2 + used_compute; ++i) cudaStreamSynchronize(mine[i]);
     cudaStreamSynchronize(cs);
-    cudaStreamSynchronize(so);
     for (int i = 0; i < n_events; ++i) cudaEventDestroy(events[i]);
+    if (copied_bytes && status == ATTN_OK) {
+      copied_bytes[0] = up_bytes;
+      copied_bytes[1] = down_bytes;
+    }
     return status;
   };
   cudaError_t e;
   cudaEvent_t start;
-  // the device buffers may still be in use by earlier work on the compute stream
-  if ((e = new_event(&start)) != cudaSuccess) return finish(cuda_fail(e));
-  if ((e = cudaEventRecord(start, cs)) != cudaSuccess || (e = cudaStreamWaitEvent(si, start, 0)) != cudaSuccess)
+  // the device buffers may still be in use by earlier work on `stream`
+  used_compute = std::min(n, kHostComputeStreams);
+  if ((e = new_event(&start)) != cudaSuccess || (e = cudaEventRecord(start, cs)) != cudaSuccess)
     return finish(cuda_fail(e));
-  if ((total_lengths && (e = h2d(dtotal, total_lengths, 0, (size_t)B * 4)) != cudaSuccess) ||
-      (past_lengths && (e = h2d(dpast, past_lengths, 0, (size_t)B * 4)) != cudaSuccess) ||
-      (mask && !per_head_mask && !per_batch_mask && (e = h2d(dmask, mask, 0, m_plane)) != cudaSuccess))
+  if ((e = cudaStreamWaitEvent(si, start, 0)) != cudaSuccess || (e = cudaStreamWaitEvent(so, start, 0)) != cudaSuccess)
+    return finish(cuda_fail(e));
+  for (int i = 0; i < used_compute; ++i)
+    if ((e = cudaStreamWaitEvent(hs->compute[i], start, 0)) != cudaSuccess) return finish(cuda_fail(e));
+  size_t shared_cols = 0;  // a shared mask plane serves every batch: the widest key range
+  for (int b = 0; b < B && mask && !per_head_mask && !per_batch_mask; ++b)
+    shared_cols = std::max(shared_cols, key_rows(b));
+  const size_t m_row = (size_t)Sk * 4;
+  if ((total_lengths && (e = h2d(dtotal, total_lengths, 0, (size_t)B * 4, 0, 1)) != cudaSuccess) ||
+      (past_lengths && (e = h2d(dpast, past_lengths, 0, (size_t)B * 4, 0, 1)) != cudaSuccess) ||
+      (mask && !per_head_mask && !per_batch_mask &&
+       (e = h2d(dmask, mask, 0, shared_cols * 4, m_row, (size_t)Sq)) != cudaSuccess))
     return finish(cuda_fail(e));  // lengths, and a mask plane shared by every piece
-  int mask_batch = -1;  // batch whose plane went up last (one plane per batch)
+  int mask_next = 0;  // first batch whose plane has not gone up yet (one plane per batch)
   for (int i = 0; i < n; ++i) {
     const HostPiece& pc = pieces[i];
     const int nb = pc.b1 - pc.b0, hq = pc.h1 - pc.h0, hkv = pc.kv1 - pc.kv0;
     const size_t qo = ((size_t)pc.b0 * Hq + pc.h0) * q_head, ko = ((size_t)pc.b0 * Hkv + pc.kv0) * kv_head;
-    const size_t qb = (size_t)nb * hq * q_head, kb = (size_t)nb * hkv * kv_head;
+    const size_t qb = (size_t)nb * hq * q_head;
     float* m_dev = dmask;
     int planes = mask ? 1 : 0;
     size_t mo = 0;
     if (per_head_mask) {
       mo = ((size_t)pc.b0 * Hq + pc.h0) * m_plane;
       planes = nb * hq;
-      if ((e = h2d(dmask, mask, mo, (size_t)planes * m_plane)) != cudaSuccess) return finish(cuda_fail(e));
+      for (int b = pc.b0; b < pc.b1; ++b)
+        if ((e = h2d(dmask, mask, ((size_t)b * Hq + pc.h0) * m_plane, key_rows(b) * 4, m_row,
+                     (size_t)hq * Sq)) != cudaSuccess)
+          return finish(cuda_fail(e));
     } else if (per_batch_mask) {
       mo = (size_t)pc.b0 * m_plane;
       planes = nb;
-      if (pc.b0 != mask_batch) {  // a batch's plane goes up once, with its first piece
-        if ((e = h2d(dmask, mask, mo, (size_t)nb * m_plane)) != cudaSuccess) return finish(cuda_fail(e));
-        mask_batch = pc.b0;
-      }
+      for (int b = std::max(pc.b0, mask_next); b < pc.b1; ++b)  // once per batch, with its first piece
+        if ((e = h2d(dmask, mask, (size_t)b * m_plane, key_rows(b) * 4, m_row, (size_t)Sq)) != cudaSuccess)
+          return finish(cuda_fail(e));
+      mask_next = std::max(mask_next, pc.b1);
     }
     if (mask) m_dev = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dmask) + mo);
-    if ((e = h2d(dq, q, qo, qb)) != cudaSuccess || (e = h2d(dk, k, ko, kb)) != cudaSuccess ||
-        (e = h2d(dv, v, ko, kb)) != cudaSuccess)
-      return finish(cuda_fail(e));
+    if ((e = h2d(dq, q, qo, qb, qb, 1)) != cudaSuccess) return finish(cuda_fail(e));
+    const size_t row = (size_t)D * es;
+    for (int b = pc.b0; b < pc.b1; ++b) {
+      const size_t off = ((size_t)b * Hkv + pc.kv0) * kv_head, w = key_rows(b) * row;
+      if ((e = h2d(dk, k, off, w, kv_head, (size_t)hkv)) != cudaSuccess ||
+          (e = h2d(dv, v, off, w, kv_head, (size_t)hkv)) != cudaSuccess)
+        return finish(cuda_fail(e));
+    }
     cudaEvent_t up, done;
     if ((e = new_event(&up)) != cudaSuccess || (e = new_event(&done)) != cudaSuccess) return finish(cuda_fail(e));
-    if ((e = cudaEventRecord(up, si)) != cudaSuccess || (e = cudaStreamWaitEvent(cs, up, 0)) != cudaSuccess)
+    cudaStream_t ks = hs->compute[i % kHostComputeStreams];
+    if ((e = cudaEventRecord(up, si)) != cudaSuccess || (e = cudaStreamWaitEvent(ks, up, 0)) != cudaSuccess)
       return finish(cuda_fail(e));
     const bool head_major = out_layout == ATTN_OUT_HEAD_MAJOR;
     const size_t oo = head_major ? qo : (size_t)pc.b0 * o_batch, ob = head_major ? qb : (size_t)nb * o_batch;
     rc = fwd_impl(static_cast<uint8_t*>(dq) + qo, static_cast<uint8_t*>(dk) + ko, static_cast<uint8_t*>(dv) + ko,
                   m_dev, dtotal ? dtotal + pc.b0 : nullptr, dpast ? dpast + pc.b0 : nullptr,
                   static_cast<uint8_t*>(dout) + oo, nb, hq, hkv, Sq, Sk, kv_capacity, D, causal, local_window,
-                  scale, softcap, out_layout, planes, dtype, cs, false, 1, nullptr, nullptr, 0);
+                  scale, softcap, out_layout, planes, dtype, ks, false, 1, nullptr, nullptr, 0);
     if (rc != ATTN_OK) return finish(rc);
-    if ((e = cudaEventRecord(done, cs)) != cudaSuccess || (e = cudaStreamWaitEvent(so, done, 0)) != cudaSuccess)
+    if ((e = cudaEventRecord(done, ks)) != cudaSuccess || (e = cudaStreamWaitEvent(so, done, 0)) != cudaSuccess)
       return finish(cuda_fail(e));
     if ((e = cudaMemcpyAsync(static_cast<uint8_t*>(out) + oo, static_cast<const uint8_t*>(dout) + oo, ob,
                              cudaMemcpyDeviceToHost, so)) != cudaSuccess)
       return finish(cuda_fail(e));
+    down_bytes += ob;
   }
   return finish(ATTN_OK);
 }
