@@ -17,9 +17,10 @@
 // max and denominator, O rescaled when the max moves.  Work item = one
 // 128-row query tile of one (b, h); its key tiles (64 keys, 32 at D = 384)
 // run in order through two S buffers.
-//   warps 0-3   softmax: thread = query row.  At each item start they write
-//               the item's Q rows (split into pieces for fp32) to tensor
-//               memory (except at D = 384).
+//   warps 0-3   softmax: thread = query row.  They write each item's Q rows
+//               (split into pieces for fp32) to tensor memory (except at
+//               D = 384) as soon as the previous item's last P is written,
+//               ahead of that item's epilogue.
 //   warp 4      TMA producer: the K pieces of key tile g into K slot g % KS and
 //               the V pieces into V slot g % VS, one barrier per tile; it also
 //               prefetches each item's Q block into L2 (at D = 384: loads it
@@ -43,9 +44,9 @@ namespace gb300_attn {
 namespace lane1 {
 
 constexpr int FM = 128;          // query rows per item
-constexpr int kThreads = 192;    // 4 softmax warps + producer + MMA
 constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kMmaWarp = 5;      // issues every MMA, or QK^T only with a second issuer
+constexpr int kPvWarp = 6;       // the second issuer (P.V), where there is one
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;  // keep the old max while it is within 2^8
 constexpr float kLog2e = 1.4426950408889634f;
@@ -79,6 +80,12 @@ struct Cfg {
   // a key tile later than its K slot, so V has one stage more
   static constexpr int kKStages = (kKTileBytes <= 24576 && !kQSmem) ? 4 : 2;
   static constexpr int kVStages = kKStages + 1;
+  // S buffers: three where tensor memory has room for them (fp32 pieces),
+  // and then a second MMA warp issues the P.V products, so that neither
+  // issuer's barrier waits leave the tensor core without queued work
+  static constexpr int kSBufs = IN == kInF32Split ? 3 : 2;
+  static constexpr bool kTwoIssuers = kSBufs == 3;
+  static constexpr int kThreads = kTwoIssuers ? 224 : 192;
   // mask staging per softmax warp: 32 rows x kMaskKeys keys of f32
   static constexpr int kMaskKeys = kQSmem ? 16 : 32;
   static constexpr uint32_t kMaskBufBytes = 32 * kMaskKeys * 4;
@@ -87,9 +94,9 @@ struct Cfg {
   static constexpr uint32_t kOffV = kOffK + kKStages * kKTileBytes;
   static constexpr uint32_t kOffMaskBuf = kOffV + kVStages * kVTileBytes;
   static constexpr uint32_t kOffBar = kOffMaskBuf + 4 * kMaskBufBytes;
-  // kv_full[KS], k_empty[KS], v_empty[VS], q_full, q_empty, s_full[2],
-  // p_full[2], pv_done, o_final, drain
-  static constexpr int kNumBars = 2 * kKStages + kVStages + 2 + 2 + 2 + 3;
+  // kv_full[KS], k_empty[KS], v_empty[VS], q_full, q_empty, s_full[SB],
+  // p_full[SB], s_free[SB], pv_done, o_final, drain
+  static constexpr int kNumBars = 2 * kKStages + kVStages + 2 + 3 * kSBufs + 3;
   static constexpr uint32_t kOffSlot = kOffBar + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -97,14 +104,14 @@ struct Cfg {
   static constexpr uint32_t kQPiece = D / 2;                       // columns per piece of Q
   static constexpr uint32_t kColQ = 0;
   static constexpr uint32_t kColS = kQSmem ? 0 : (KP * kQPiece + 63) / 64 * 64;  // + buffer * 64
-  static constexpr uint32_t kColO = kColS + 128;
+  static constexpr uint32_t kColO = kColS + 64 * kSBufs;
   static_assert(kColO + D <= kTmemCols, "tensor memory columns");
 };
 
 template <int D, int IN>
 struct Smem {
   using C = Cfg<D, IN>;
-  static constexpr int KS = C::kKStages, VS = C::kVStages;
+  static constexpr int KS = C::kKStages, VS = C::kVStages, SB = C::kSBufs;
   static constexpr int kB = 2 * KS + VS;  // first barrier after the rings
   uint8_t* base;
   uint32_t sQ, sK, sV, bar0;
@@ -118,11 +125,13 @@ struct Smem {
   // written (p_full, 4 arrivals).  A buffer's next scores wait for the P.V of
   // its previous P, so neither barrier can run two phases ahead of its waiter.
   __device__ uint32_t s_full(int b) const { return bar0 + 8u * (kB + 2 + b); }
-  __device__ uint32_t p_full(int b) const { return bar0 + 8u * (kB + 4 + b); }
+  __device__ uint32_t p_full(int b) const { return bar0 + 8u * (kB + 2 + SB + b); }
+  // (two issuers) the P.V products of buffer b's P finished: its next S may go in
+  __device__ uint32_t s_free(int b) const { return bar0 + 8u * (kB + 2 + 2 * SB + b); }
   // one completion per P.V (the softmax waits on it only before rescaling O)
-  __device__ uint32_t pv_done() const { return bar0 + 8u * (kB + 6); }
-  __device__ uint32_t o_final() const { return bar0 + 8u * (kB + 7); }
-  __device__ uint32_t drain() const { return bar0 + 8u * (kB + 8); }
+  __device__ uint32_t pv_done() const { return bar0 + 8u * (kB + 2 + 3 * SB); }
+  __device__ uint32_t o_final() const { return bar0 + 8u * (kB + 3 + 3 * SB); }
+  __device__ uint32_t drain() const { return bar0 + 8u * (kB + 4 + 3 * SB); }
   __device__ uint8_t* mask_buf(int warp) const { return base + C::kOffMaskBuf + warp * C::kMaskBufBytes; }
 };
 
@@ -273,13 +282,24 @@ __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN
 
 // ------------------------------------------------------------------ MMA issuer
 // The whole warp runs this; elect.sync picks the issuing lane.  Step n of an
-// item: the scores of tile n into S buffer n % 2 (once its K / V are in), then
-// the P.V products of tile n - 1 (once its P is written).  One barrier wait
-// sits between consecutive issue blocks.  For inputs read straight from the
-// caller's cache (16-bit), V rows at or past the valid length may hold any
-// bits (NaN / Inf included): P is 0 there but 0 * NaN is not, so those rows
-// are zeroed in shared memory before the P.V products read them.
-template <int D, int IN>
+// item: the scores of tile n into an S buffer (once its K / V are in), then
+// the P.V products of tile n - 1 (once its P is written).
+//   ROLE 0 (one issuer, two S buffers): both; tile n uses buffer n % 2, and
+//     S(n) may overwrite the P of tile n - 2 because this warp issued that
+//     tile's P.V first (one thread's tensor-core operations run in order).
+//     One barrier wait sits between consecutive issue blocks; an issuing
+//     warp is held until only a few MMAs are queued, so each wait costs the
+//     tensor core most of its own duration.
+//   ROLE 1 / 2 (two issuers, three S buffers): ROLE 1 issues only the
+//     scores, ROLE 2 only the P.V products, each on the CTA's running key
+//     tile count g (buffer g % 3).  The scores of tile g wait until the P.V
+//     products of tile g - 3 finished (s_free), since they run on another
+//     thread.  While one issuer waits, the other's MMAs keep the queue busy.
+// For inputs read straight from the caller's cache (16-bit), V rows at or
+// past the valid length may hold any bits (NaN / Inf included): P is 0 there
+// but 0 * NaN is not, so those rows are zeroed in shared memory before the
+// P.V products read them.
+template <int D, int IN, int ROLE>
 __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm, uint32_t tmem, int n_items,
                                       int lane) {
   using C = Cfg<D, IN>;
@@ -287,6 +307,9 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
   constexpr int KP = C::KP, VP = C::VP;
   constexpr bool kBF16 = In<IN>::kBF16;
   constexpr int FN = C::FN;
+  constexpr int SB = C::kSBufs;
+  constexpr bool kQK = ROLE != 2, kPV = ROLE != 1;
+  static_assert(ROLE == 0 || C::kTwoIssuers, "two issuers need three S buffers");
   constexpr uint32_t id_qk = make_idesc_f16kind(kBF16, FM, FN, false);
   // one MMA's N is at most 256: D = 384 runs as N = 256 and N = 128 parts
   constexpr int kN0 = D > 256 ? 256 : D;
@@ -295,26 +318,33 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
   const CommonParams& p = P.c;
   int g0 = 0;          // ring position of the item's first key tile
   int q_items = 0;     // items whose Q was consumed
-  int pb[2] = {0, 0};  // P tiles consumed per S buffer (all items)
+  int pb[3] = {0, 0, 0};  // P tiles consumed per S buffer (all items)
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int idx = f_item_of_round(r, n_items);
     if (idx < 0) break;
     const FItem it = make_fitem<C::FN>(p, idx);
     if (it.N == 0) continue;
-    if (!mbar_wait_warp(sm.q_full(), q_items & 1, p.timeout_ns, p.status)) break;
-    ++q_items;
-    tc_fence_after();
+    if constexpr (kQK) {
+      if (!mbar_wait_warp(sm.q_full(), q_items & 1, p.timeout_ns, p.status)) break;
+      ++q_items;
+      tc_fence_after();
+    }
     int64_t zero_from = it.L.lsk < (int64_t)p.Sk ? it.L.lsk : (int64_t)p.Sk;
     if (zero_from < 0) zero_from = 0;
     for (int n = 0; ok && n <= it.N; ++n) {
-      if (n < it.N) {
-        // S_{n%2} = Q K_n^T (pieces: q0k0 + q0k1 + q1k0 + q0k2 + q1k1 + q2k0)
+      if (kQK && n < it.N) {
+        // S = Q K_n^T (pieces: q0k0 + q0k1 + q1k0 + q0k2 + q1k1 + q2k0)
         const int gs = g0 + n;
+        const int bs = SB == 3 ? gs % 3 : (n & 1);
         if (!mbar_wait_warp(sm.kv_full(gs % KS), (gs / KS) & 1, p.timeout_ns, p.status)) { ok = false; break; }
+        if (ROLE == 1 && gs >= 3 && !mbar_wait_warp(sm.s_free(bs), ((gs / 3) - 1) & 1, p.timeout_ns, p.status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t kb = sm.sK + (gs % KS) * C::kKTileBytes;
-        const uint32_t sd = tmem + C::kColS + 64 * (n & 1);
+        const uint32_t sd = tmem + C::kColS + 64 * bs;
         if constexpr (KP == 3) {
           uint64_t kd[3];
 #pragma unroll
@@ -349,17 +379,18 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
                           s > 0 ? 1u : 0u);
           }
         }
-        tc_commit_elect(sm.s_full(n & 1));
+        tc_commit_elect(sm.s_full(bs));
         tc_commit_elect(sm.k_empty(gs % KS));
         // the item's last QK^T products are issued: Q may be replaced once they finish
         if (n == it.N - 1) tc_commit_elect(sm.q_empty());
       }
-      if (n >= 1) {
+      if (kPV && n >= 1) {
         // O (+)= P_{n-1} V_{n-1} (pieces: p0 v0 + p0 v1 + p1 v0)
         const int m = n - 1;
         const int gv = g0 + m;
-        if (!mbar_wait_warp(sm.p_full(m & 1), pb[m & 1] & 1, p.timeout_ns, p.status)) { ok = false; break; }
-        ++pb[m & 1];
+        const int bp = SB == 3 ? gv % 3 : (m & 1);
+        if (!mbar_wait_warp(sm.p_full(bp), pb[bp] & 1, p.timeout_ns, p.status)) { ok = false; break; }
+        ++pb[bp];
         const uint32_t vb = sm.sV + (gv % VS) * C::kVTileBytes;
         if constexpr (IN != kInF32Split) {
           const int64_t key0 = (int64_t)(it.tb + m) * FN;
@@ -380,7 +411,7 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
         // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B apart,
         // 64-column blocks kSubBytes apart
         const uint64_t d0 = make_sdesc_sw128(vb, C::kSubBytes, 1024);
-        const uint32_t pa = tmem + C::kColS + 64 * (m & 1);  // P piece t over 32 columns from pa + 32 t
+        const uint32_t pa = tmem + C::kColS + 64 * bp;  // P piece t over 32 columns from pa + 32 t
         if constexpr (VP == 2) {
           const uint64_t d1 = make_sdesc_sw128(vb + C::kPieceBytes, C::kSubBytes, 1024);
           // two K steps (16 keys each, 2048 bytes of V apart) per issue block
@@ -404,6 +435,7 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
                         m == 0 ? 0u : 1u);
         }
         tc_commit_elect(sm.v_empty(gv % VS));
+        if constexpr (ROLE == 2) tc_commit_elect(sm.s_free(bp));
         tc_commit_elect(sm.pv_done());
         if (m == it.N - 1) tc_commit_elect(sm.o_final());  // the item's last P.V
       }
@@ -442,33 +474,66 @@ __device__ __forceinline__ float minn(const float (&x)[N]) {
   return fminf(fmin3(m[0], m[1], m[2]), fmin3(m[3], m[4], fmin3(m[5], m[6], m[7])));
 }
 
+// Rows of a warp move between global memory and the threads that own them
+// (thread = row) through the warp's staging buffer, 32 columns at a time:
+// each global load or store instruction then covers whole 32-column row
+// segments of several rows (128 bytes of fp32 or 64 of 16-bit per row)
+// instead of one 16-byte piece of 32 rows.  Segment chunks are XOR-swizzled
+// by row, so both the row-wise and the lane-per-row accesses are free of
+// bank conflicts.
+template <int ES>
+struct RowStage {
+  static constexpr int kSegBytes = 32 * ES;      // one row's 32 columns
+  static constexpr int kCps = kSegBytes / 16;    // 16-byte chunks per segment
+  static constexpr int kRpi = 32 / kCps;         // rows per instruction
+  static constexpr int kInstr = 32 / kRpi;       // instructions per 32 rows
+  __device__ static int swz(int r) { return kCps == 8 ? (r & 7) : ((r >> 1) & 3); }
+  __device__ static uint32_t at(int r, int c) { return (uint32_t)(r * kSegBytes + ((c ^ swz(r)) << 4)); }
+};
+
 // This thread's Q row in tensor memory: piece t over columns [t D/2,
 // (t+1) D/2), column c holding d = 2c, 2c + 1.  fp32 rows are split into KP
-// bf16 pieces; 16-bit rows are stored as they are.
+// bf16 pieces; 16-bit rows are stored as they are.  The warp's 32 rows are
+// read with coalesced loads (all in flight at once) and handed to their
+// threads through `buf` (at least 32 rows x 32 columns).
 template <int D, int IN>
-__device__ __forceinline__ void store_q_row(const CommonParams& p, const void* q, const FItem& it, int64_t qi,
-                                            uint32_t tlane) {
+__device__ __forceinline__ void store_q_row(const CommonParams& p, const void* q, const FItem& it, int warp,
+                                            int lane, uint32_t tlane, uint8_t* buf) {
   using C = Cfg<D, IN>;
-  const int64_t row = ((int64_t)it.b * p.Hq + it.h) * p.Sq + qi;
-  if constexpr (IN == kInF32Split) {
-    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(q) + row * D);
-    // the whole row in flight at once (D / 4 independent 16-byte loads)
-    float4 rowv[D / 4];
-    const uint64_t stream = l2_evict_first_policy();
+  constexpr int ES = IN == kInF32Split ? 4 : 2;
+  using RS = RowStage<ES>;
+  constexpr int kChunks = D / 32;
+  const int rsub = lane / RS::kCps, csub = lane % RS::kCps;
+  const int64_t qw0 = it.q0 + warp * 32;  // first row of the warp
+  const uint8_t* base =
+      static_cast<const uint8_t*>(q) + ((((int64_t)it.b * p.Hq + it.h) * p.Sq + qw0) * D) * ES + csub * 16;
+  const uint64_t stream = l2_evict_first_policy();
+  uint4 v[kChunks][RS::kInstr];
 #pragma unroll
-    for (int i = 0; i < D / 4; ++i) {
-      const uint4 u = qi < p.Sq ? ld_nc_hint(src + i, stream) : make_uint4(0u, 0u, 0u, 0u);
-      rowv[i] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+  for (int ch = 0; ch < kChunks; ++ch)
+#pragma unroll
+    for (int i = 0; i < RS::kInstr; ++i) {
+      const int r = i * RS::kRpi + rsub;
+      v[ch][i] = qw0 + r < p.Sq ? ld_nc_hint(base + (int64_t)r * D * ES + ch * RS::kSegBytes, stream)
+                                : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
+  for (int ch = 0; ch < kChunks; ++ch) {
+#pragma unroll
+    for (int i = 0; i < RS::kInstr; ++i)
+      *reinterpret_cast<uint4*>(buf + RS::at(i * RS::kRpi + rsub, csub)) = v[ch][i];
+    __syncwarp();
+    uint4 mine[RS::kCps];
+#pragma unroll
+    for (int c = 0; c < RS::kCps; ++c) mine[c] = *reinterpret_cast<const uint4*>(buf + RS::at(lane, c));
+    __syncwarp();
+    if constexpr (IN == kInF32Split) {
       uint32_t pcs[C::KP][16];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float4 v = rowv[ch * 8 + i];
         uint32_t a[C::KP], b[C::KP];
-        split_pair<C::KP>(v.x, v.y, a);
-        split_pair<C::KP>(v.z, v.w, b);
+        split_pair<C::KP>(__uint_as_float(mine[i].x), __uint_as_float(mine[i].y), a);
+        split_pair<C::KP>(__uint_as_float(mine[i].z), __uint_as_float(mine[i].w), b);
 #pragma unroll
         for (int t = 0; t < C::KP; ++t) {
           pcs[t][2 * i] = a[t];
@@ -477,23 +542,14 @@ __device__ __forceinline__ void store_q_row(const CommonParams& p, const void* q
       }
 #pragma unroll
       for (int t = 0; t < C::KP; ++t) tmem_st16(tlane + C::kColQ + t * C::kQPiece + ch * 16, pcs[t]);
-    }
-  } else {
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(q) + row * D);
-    uint4 rowv[D / 8];
-    const uint64_t stream = l2_evict_first_policy();
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) rowv[i] = qi < p.Sq ? ld_nc_hint(src + i, stream) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
+    } else {
       uint32_t w[16];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint4 v = rowv[ch * 4 + i];
-        w[4 * i] = v.x;
-        w[4 * i + 1] = v.y;
-        w[4 * i + 2] = v.z;
-        w[4 * i + 3] = v.w;
+        w[4 * i] = mine[i].x;
+        w[4 * i + 1] = mine[i].y;
+        w[4 * i + 2] = mine[i].z;
+        w[4 * i + 3] = mine[i].w;
       }
       tmem_st16(tlane + C::kColQ + ch * 16, w);
     }
@@ -565,11 +621,33 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
   const int row = warp * 32 + lane;
   const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
   const uint32_t o_addr = tlane + C::kColO;
-  int sb[2] = {0, 0};  // S tiles consumed per buffer (all items)
+  int sb[3] = {0, 0, 0};  // S tiles consumed per buffer (all items)
   int tiles = 0;       // key tiles consumed (all items): P.V completions to wait for
   int qn = 0;          // items whose Q was stored
   int on = 0;          // o_final completions
+  // Q rows of the first item at or after round r0 that has keys, into tensor
+  // memory once the QK^T products of the item before it have finished.  The
+  // next item's Q goes in right after this item's last P, before its
+  // epilogue, so the MMA warp starts the next item's QK^T while the
+  // epilogue runs.  Warp-collective; false on a timeout.
+  auto stage_q = [&](int r0) -> bool {
+    for (int r2 = r0;; ++r2) {
+      const int idx2 = f_item_of_round(r2, n_items);
+      if (idx2 < 0) return true;
+      const FItem it2 = make_fitem<C::FN>(p, idx2);
+      if (it2.N == 0) continue;
+      if (qn > 0 && !mbar_wait_warp(sm.q_empty(), (qn - 1) & 1, p.timeout_ns, p.status)) return false;
+      ++qn;
+      store_q_row<D, IN>(p, P.q, it2, warp, lane, tlane, sm.mask_buf(warp));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.q_full());
+      return true;
+    }
+  };
   bool ok = true;
+  if constexpr (!C::kQSmem) ok = stage_q(0);
   for (int r = 0; ok; ++r) {
     const int idx = f_item_of_round(r, n_items);
     if (idx < 0) break;
@@ -587,16 +665,6 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
       }
       continue;
     }
-    if constexpr (!C::kQSmem) {
-      // Q of this item into tensor memory once the previous item's QK^T finished
-      if (qn > 0 && !mbar_wait_warp(sm.q_empty(), (qn - 1) & 1, p.timeout_ns, p.status)) { ok = false; break; }
-      ++qn;
-      store_q_row<D, IN>(p, P.q, it, qi, tlane);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.q_full());
-    }
 
     const RowLimits R = row_limits(p, it.L, qi);
     const float* mwarp = nullptr;
@@ -613,7 +681,9 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
     float m_run = -INFINITY;  // running max, log2 units
     float l_run = 0.0f;
     for (int n = 0; n < it.N; ++n, ++tiles) {
-      const int bsel = n & 1;
+      // the MMA warp's buffer order: the running tile count with three
+      // buffers, the tile within the item with two
+      const int bsel = C::kSBufs == 3 ? tiles % 3 : (n & 1);
       const uint32_t s_addr = tlane + C::kColS + 64 * bsel;
       const int64_t key0 = (int64_t)(it.tb + n) * FN;
       float x[FN];
@@ -759,42 +829,62 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
       if (lane == 0) mbar_arrive(sm.p_full(bsel));
     }
     if (!ok) break;
+    if constexpr (!C::kQSmem) {
+      if (!stage_q(r + 1)) { ok = false; break; }
+    }
 
     // ------------------------------------------------------------ epilogue
     if (!mbar_wait_warp(sm.o_final(), on & 1, p.timeout_ns, p.status)) { ok = false; break; }
     ++on;
     tc_fence_after();
     const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+    // O is written once: evict_first, so it does not displace K / V in L2
     const uint64_t o_policy = l2_evict_first_policy();
     const uint64_t w2 = f2(inv_l, inv_l);
+    {
+      // through the staging buffer: coalesced row segments (see RowStage)
+      using RS = RowStage<kF32 ? 4 : 2>;
+      uint8_t* buf = sm.mask_buf(warp);
+      const int rsub = lane / RS::kCps, csub = lane % RS::kCps;
+      const int64_t qw0 = it.q0 + warp * 32;
+      uint8_t* odst[RS::kInstr];
 #pragma unroll
-    for (int k = 0; k < D / 32; ++k) {
-      uint32_t o[32];
-      tmem_ld32(o_addr + k * 32, o);
-      tmem_wait_ld();
-      if (qi < p.Sq) {
+      for (int i = 0; i < RS::kInstr; ++i) {
+        const int64_t qr = qw0 + i * RS::kRpi + rsub;
+        const int64_t e = p.out_layout == 0 ? (((int64_t)it.b * p.Hq + it.h) * p.Sq + qr) * D
+                                            : (((int64_t)it.b * p.Sq + qr) * p.Hq + it.h) * D;
+        odst[i] = qr < p.Sq ? static_cast<uint8_t*>(p.out) + e * (kF32 ? 4 : 2) + csub * 16 : nullptr;
+      }
+#pragma unroll
+      for (int k = 0; k < D / 32; ++k) {
+        uint32_t o[32];
+        tmem_ld32(o_addr + k * 32, o);
+        tmem_wait_ld();
         float r[32];
 #pragma unroll
         for (int i = 0; i < 32; i += 2)
           f2_split(fmul2(f2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), w2), r[i], r[i + 1]);
-        // O is written once: evict_first, so it does not displace K / V in L2
-        if constexpr (kF32) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            st_hint(orow + k * 8 + i,
-                    make_uint4(__float_as_uint(r[4 * i]), __float_as_uint(r[4 * i + 1]),
-                               __float_as_uint(r[4 * i + 2]), __float_as_uint(r[4 * i + 3])),
-                    o_policy);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            st_hint(orow + k * 4 + i,
-                    make_uint4(pack16<In<IN>::kBF16>(r[8 * i], r[8 * i + 1]),
-                               pack16<In<IN>::kBF16>(r[8 * i + 2], r[8 * i + 3]),
-                               pack16<In<IN>::kBF16>(r[8 * i + 4], r[8 * i + 5]),
-                               pack16<In<IN>::kBF16>(r[8 * i + 6], r[8 * i + 7])),
-                    o_policy);
+        for (int c = 0; c < RS::kCps; ++c) {
+          uint4 u;
+          if constexpr (kF32) {
+            u = make_uint4(__float_as_uint(r[4 * c]), __float_as_uint(r[4 * c + 1]), __float_as_uint(r[4 * c + 2]),
+                           __float_as_uint(r[4 * c + 3]));
+          } else {
+            u = make_uint4(pack16<In<IN>::kBF16>(r[8 * c], r[8 * c + 1]),
+                           pack16<In<IN>::kBF16>(r[8 * c + 2], r[8 * c + 3]),
+                           pack16<In<IN>::kBF16>(r[8 * c + 4], r[8 * c + 5]),
+                           pack16<In<IN>::kBF16>(r[8 * c + 6], r[8 * c + 7]));
+          }
+          *reinterpret_cast<uint4*>(buf + RS::at(lane, c)) = u;
         }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < RS::kInstr; ++i) {
+          const uint4 u = *reinterpret_cast<const uint4*>(buf + RS::at(i * RS::kRpi + rsub, csub));
+          if (odst[i]) st_hint(odst[i] + k * RS::kSegBytes, u, o_policy);
+        }
+        __syncwarp();
       }
     }
     // The next item's first P.V (which overwrites O) waits for this
@@ -805,7 +895,7 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
 
 // ------------------------------------------------------------------ kernel
 template <int D, int IN, bool SOFTCAP, bool MASK>
-__global__ void __launch_bounds__(kThreads, 1) attn_fwd_lane1_kernel(const __grid_constant__ LaneParams P) {
+__global__ void __launch_bounds__(Cfg<D, IN>::kThreads, 1) attn_fwd_lane1_kernel(const __grid_constant__ LaneParams P) {
   using C = Cfg<D, IN>;
   const CommonParams& p = P.c;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -829,13 +919,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_lane1_kernel(const __gri
     for (int s = 0; s < C::kVStages; ++s) mbar_init(sm.v_empty(s), 1);
     mbar_init(sm.q_full(), C::kQSmem ? 1 : 4);  // the producer's TMA, or one arrival per softmax warp
     mbar_init(sm.q_empty(), 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kSBufs; ++b) {
       mbar_init(sm.s_full(b), 1);
       mbar_init(sm.p_full(b), 4);  // one arrival per softmax warp
+      mbar_init(sm.s_free(b), 1);
     }
     mbar_init(sm.pv_done(), 1);
     mbar_init(sm.o_final(), 1);
-    mbar_init(sm.drain(), 1);
+    mbar_init(sm.drain(), C::kTwoIssuers ? 2 : 1);  // one commit per issuing warp
     mbar_init_fence();
   }
   if (warp == kTmaWarp && lane == 0) {
@@ -855,7 +946,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_lane1_kernel(const __gri
   if (warp == kTmaWarp) {
     if (lane == 0) f_producer<D, IN>(P, sm, n_items);
   } else if (warp == kMmaWarp) {
-    f_mma<D, IN>(P, sm, tmem, n_items, lane);
+    f_mma<D, IN, C::kTwoIssuers ? 1 : 0>(P, sm, tmem, n_items, lane);
+  } else if (warp == kPvWarp) {
+    if constexpr (C::kTwoIssuers) f_mma<D, IN, 2>(P, sm, tmem, n_items, lane);
   } else {
     f_softmax<D, IN, SOFTCAP, MASK>(P, sm, tmem, n_items, warp, lane);
   }
@@ -880,7 +973,7 @@ cudaError_t launch_lane1_variant(const LaneParams& P, cudaStream_t stream) {
   const int64_t n_items = (int64_t)((P.c.Sq + FM - 1) / FM) * P.c.B * P.c.Hq;
   if (n_items > INT32_MAX) return cudaErrorInvalidConfiguration;
   const int grid = (int)(n_items < sms ? n_items : sms);  // one persistent CTA per SM
-  kernel<<<grid, kThreads, smem, stream>>>(P);
+  kernel<<<grid, Cfg<D, IN>::kThreads, smem, stream>>>(P);
   return cudaGetLastError();
 }
 
