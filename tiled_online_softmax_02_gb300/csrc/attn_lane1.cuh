@@ -81,10 +81,10 @@ struct Cfg {
   static constexpr int kKStages = (kKTileBytes <= 24576 && !kQSmem) ? 4 : 2;
   static constexpr int kVStages = kKStages + 1;
   // S buffers: three where tensor memory has room for them (fp32 pieces),
-  // and then a second MMA warp issues the P.V products, so that neither
-  // issuer's barrier waits leave the tensor core without queued work
+  // else two.  A second MMA warp issues the P.V products, so that neither
+  // issuer's barrier waits leave the tensor core without queued work.
   static constexpr int kSBufs = IN == kInF32Split ? 3 : 2;
-  static constexpr bool kTwoIssuers = kSBufs == 3;
+  static constexpr bool kTwoIssuers = true;
   static constexpr int kThreads = kTwoIssuers ? 224 : 192;
   // mask staging per softmax warp: 32 rows x kMaskKeys keys of f32
   static constexpr int kMaskKeys = kQSmem ? 16 : 32;
@@ -290,11 +290,12 @@ __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN
 //     One barrier wait sits between consecutive issue blocks; an issuing
 //     warp is held until only a few MMAs are queued, so each wait costs the
 //     tensor core most of its own duration.
-//   ROLE 1 / 2 (two issuers, three S buffers): ROLE 1 issues only the
-//     scores, ROLE 2 only the P.V products, each on the CTA's running key
-//     tile count g (buffer g % 3).  The scores of tile g wait until the P.V
-//     products of tile g - 3 finished (s_free), since they run on another
-//     thread.  While one issuer waits, the other's MMAs keep the queue busy.
+//   ROLE 1 / 2 (two issuers, SB = two or three S buffers): ROLE 1 issues
+//     only the scores, ROLE 2 only the P.V products, each on the CTA's
+//     running key tile count g (buffer g % SB).  The scores of tile g wait
+//     until the P.V products of tile g - SB finished (s_free), since they
+//     run on another thread.  While one issuer waits, the other's MMAs keep
+//     the queue busy.
 // For inputs read straight from the caller's cache (16-bit), V rows at or
 // past the valid length may hold any bits (NaN / Inf included): P is 0 there
 // but 0 * NaN is not, so those rows are zeroed in shared memory before the
@@ -309,7 +310,7 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
   constexpr int FN = C::FN;
   constexpr int SB = C::kSBufs;
   constexpr bool kQK = ROLE != 2, kPV = ROLE != 1;
-  static_assert(ROLE == 0 || C::kTwoIssuers, "two issuers need three S buffers");
+  static_assert(ROLE == 0 || C::kTwoIssuers, "issuer roles");
   constexpr uint32_t id_qk = make_idesc_f16kind(kBF16, FM, FN, false);
   // one MMA's N is at most 256: D = 384 runs as N = 256 and N = 128 parts
   constexpr int kN0 = D > 256 ? 256 : D;
@@ -336,9 +337,9 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
       if (kQK && n < it.N) {
         // S = Q K_n^T (pieces: q0k0 + q0k1 + q1k0 + q0k2 + q1k1 + q2k0)
         const int gs = g0 + n;
-        const int bs = SB == 3 ? gs % 3 : (n & 1);
+        const int bs = ROLE == 0 ? (n & 1) : gs % SB;
         if (!mbar_wait_warp(sm.kv_full(gs % KS), (gs / KS) & 1, p.timeout_ns, p.status)) { ok = false; break; }
-        if (ROLE == 1 && gs >= 3 && !mbar_wait_warp(sm.s_free(bs), ((gs / 3) - 1) & 1, p.timeout_ns, p.status)) {
+        if (ROLE == 1 && gs >= SB && !mbar_wait_warp(sm.s_free(bs), ((gs / SB) - 1) & 1, p.timeout_ns, p.status)) {
           ok = false;
           break;
         }
@@ -388,7 +389,7 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
         // O (+)= P_{n-1} V_{n-1} (pieces: p0 v0 + p0 v1 + p1 v0)
         const int m = n - 1;
         const int gv = g0 + m;
-        const int bp = SB == 3 ? gv % 3 : (m & 1);
+        const int bp = ROLE == 0 ? (m & 1) : gv % SB;
         if (!mbar_wait_warp(sm.p_full(bp), pb[bp] & 1, p.timeout_ns, p.status)) { ok = false; break; }
         ++pb[bp];
         const uint32_t vb = sm.sV + (gv % VS) * C::kVTileBytes;
@@ -681,9 +682,9 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
     float m_run = -INFINITY;  // running max, log2 units
     float l_run = 0.0f;
     for (int n = 0; n < it.N; ++n, ++tiles) {
-      // the MMA warp's buffer order: the running tile count with three
-      // buffers, the tile within the item with two
-      const int bsel = C::kSBufs == 3 ? tiles % 3 : (n & 1);
+      // the MMA warps' buffer order: the running tile count with two
+      // issuers, the tile within the item with one
+      const int bsel = C::kTwoIssuers ? tiles % C::kSBufs : (n & 1);
       const uint32_t s_addr = tlane + C::kColS + 64 * bsel;
       const int64_t key0 = (int64_t)(it.tb + n) * FN;
       float x[FN];
