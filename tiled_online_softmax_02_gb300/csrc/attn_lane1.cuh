@@ -1,7 +1,7 @@
 #pragma once
 // attn_lane1.cuh -- single-lane tensor-core attention forward for sm_103a:
-// one softmax warpgroup per CTA, Q in tensor memory, two S buffers.  Used
-// where the ping-pong tile kernel's tensor-memory layout does not fit:
+// one softmax warpgroup per CTA, two MMA issuers, two or three S buffers.
+// Used where the ping-pong tile kernel's tensor-memory layout does not fit:
 //   - fp32 inputs as error-compensated bf16 pieces (attn_f32tc.cu, D 64 /
 //     128): Q and K in three pieces, P and V in two, six products for QK^T
 //     and three for P.V;
@@ -16,25 +16,26 @@
 // `flash_attention_body`): scores of one key tile at a time, running row
 // max and denominator, O rescaled when the max moves.  Work item = one
 // 128-row query tile of one (b, h); its key tiles (64 keys, 32 at D = 384)
-// run in order through two S buffers.
+// run in order; key tile g of the CTA (counted over all its items) uses S
+// buffer g % SB.
 //   warps 0-3   softmax: thread = query row.  They write each item's Q rows
 //               (split into pieces for fp32) to tensor memory (except at
 //               D = 384) as soon as the previous item's last P is written,
 //               ahead of that item's epilogue.
-//   warp 4      TMA producer: the K pieces of key tile g into K slot g % KS and
-//               the V pieces into V slot g % VS, one barrier per tile; it also
-//               prefetches each item's Q block into L2 (at D = 384: loads it
-//               into shared memory).
-//   warp 5      MMA issuer (converged warp, elect.sync) and owner of tensor
-//               memory.  Step n of an item: S_{n%2} = Q K_n^T, then
-//               O += P_{n-1} V_{n-1}.  S(n) overwrites the P of tile n - 2, whose
-//               P.V this warp issued one step earlier (tensor-core operations of
-//               one thread run in issue order).
-// Tensor memory (512 columns): Q pieces [0, KP D/2), S_0 / S_1 (64 columns
-// apart; a 32-key tile uses half) from kColS, O (D columns) from kColS + 128;
-// P_b over S_b (as VP bf16 / f16 pieces of FN / 2 columns).  Every barrier
-// wait is bounded; a timeout sets ATTN_ERR_TIMEOUT in the device status word
-// and the kernel drains and exits.
+//   warp 4      TMA producer: the K pieces of key tile g into K slot g % KS
+//               and the V pieces into V slot g % VS, each ring with its own
+//               barriers, V one tile behind K; it also prefetches each
+//               item's Q block into L2 (at D = 384: loads it into shared
+//               memory).
+//   warp 5      QK^T issuer (converged warp, elect.sync) and owner of tensor
+//               memory: S_g = Q K_g^T once K_g is in and the P.V of tile
+//               g - SB (whose P the buffer holds) has finished.
+//   warp 6      P.V issuer: O += P_g V_g once P_g is written.
+// Tensor memory (512 columns): Q pieces [0, KP D/2), SB S buffers 64 columns
+// apart (a 32-key tile uses half) from kColS, O (D columns) after them; P_b
+// over S_b (as VP bf16 / f16 pieces of FN / 2 columns).  Every barrier wait
+// is bounded; a timeout sets ATTN_ERR_TIMEOUT in the device status word and
+// the kernel drains and exits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -76,16 +77,17 @@ struct Cfg {
   static constexpr uint32_t kVTileBytes = VP * kPieceBytes;
   static constexpr uint32_t kQSubBytes = FM * 128;             // [128 rows][64 cols] of 16-bit
   static constexpr uint32_t kQBytes = kQSmem ? kSub * kQSubBytes : 0;
-  // K and V of a key tile arrive together (one barrier); a V slot is freed
-  // a key tile later than its K slot, so V has one stage more
-  static constexpr int kKStages = (kKTileBytes <= 24576 && !kQSmem) ? 4 : 2;
-  static constexpr int kVStages = kKStages + 1;
+  // K and V have rings and barriers of their own.  A K slot is freed by its
+  // tile's QK^T, a V slot by its P.V about a tile later; the producer loads
+  // V one tile behind K.  Stages as shared memory allows: 4 / 5 at fp32
+  // D = 64, 2 / 3 at fp32 D = 128, 3 / 3 at D = 256, 2 / 3 at D = 384.
+  static constexpr int kKStages = kQSmem ? 2 : (kKTileBytes <= 24576 ? 4 : (IN == kInF32Split ? 2 : 3));
+  static constexpr int kVStages = (IN != kInF32Split && !kQSmem) ? kKStages : kKStages + 1;
   // S buffers: three where tensor memory has room for them (fp32 pieces),
-  // else two.  A second MMA warp issues the P.V products, so that neither
-  // issuer's barrier waits leave the tensor core without queued work.
+  // else two.  Two MMA warps issue (QK^T and P.V), so that neither issuer's
+  // barrier waits leave the tensor core without queued work.
   static constexpr int kSBufs = IN == kInF32Split ? 3 : 2;
-  static constexpr bool kTwoIssuers = true;
-  static constexpr int kThreads = kTwoIssuers ? 224 : 192;
+  static constexpr int kThreads = 224;  // 4 softmax warps, producer, two MMA issuers
   // mask staging per softmax warp: 32 rows x kMaskKeys keys of f32
   static constexpr int kMaskKeys = kQSmem ? 16 : 32;
   static constexpr uint32_t kMaskBufBytes = 32 * kMaskKeys * 4;
@@ -94,9 +96,9 @@ struct Cfg {
   static constexpr uint32_t kOffV = kOffK + kKStages * kKTileBytes;
   static constexpr uint32_t kOffMaskBuf = kOffV + kVStages * kVTileBytes;
   static constexpr uint32_t kOffBar = kOffMaskBuf + 4 * kMaskBufBytes;
-  // kv_full[KS], k_empty[KS], v_empty[VS], q_full, q_empty, s_full[SB],
-  // p_full[SB], s_free[SB], pv_done, o_final, drain
-  static constexpr int kNumBars = 2 * kKStages + kVStages + 2 + 3 * kSBufs + 3;
+  // k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], q_full, q_empty,
+  // s_full[SB], p_full[SB], s_free[SB], pv_done, o_final, drain
+  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 3 * kSBufs + 3;
   static constexpr uint32_t kOffSlot = kOffBar + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -112,13 +114,14 @@ template <int D, int IN>
 struct Smem {
   using C = Cfg<D, IN>;
   static constexpr int KS = C::kKStages, VS = C::kVStages, SB = C::kSBufs;
-  static constexpr int kB = 2 * KS + VS;  // first barrier after the rings
+  static constexpr int kB = 2 * KS + 2 * VS;  // first barrier after the rings
   uint8_t* base;
   uint32_t sQ, sK, sV, bar0;
-  // K and V of key tile g, on ring index g % KS (V slot g % VS)
-  __device__ uint32_t kv_full(int s) const { return bar0 + 8u * s; }
+  // K of key tile g in K slot g % KS, V in V slot g % VS
+  __device__ uint32_t k_full(int s) const { return bar0 + 8u * s; }
   __device__ uint32_t k_empty(int s) const { return bar0 + 8u * (KS + s); }
-  __device__ uint32_t v_empty(int s) const { return bar0 + 8u * (2 * KS + s); }
+  __device__ uint32_t v_full(int s) const { return bar0 + 8u * (2 * KS + s); }
+  __device__ uint32_t v_empty(int s) const { return bar0 + 8u * (2 * KS + VS + s); }
   __device__ uint32_t q_full() const { return bar0 + 8u * kB; }
   __device__ uint32_t q_empty() const { return bar0 + 8u * (kB + 1); }
   // per S buffer b: the scores of its next tile are in (s_full), its P is
@@ -211,16 +214,17 @@ __device__ __forceinline__ int f_item_of_round(int r, int n_items) {
 }
 
 // ------------------------------------------------------------------ producer
-// One thread.  Per key tile g: the K pieces into K slot g % KS and the V
-// pieces into V slot g % VS, both completing kv_full(g % KS).  A K slot is
-// freed by its tile's QK^T products, a V slot by its P.V products.  At each
-// item start it also prefetches the item's Q rows into L2, so the softmax
-// warps' Q loads come from L2.  K / V tiles are read by every query tile of
-// their kv head, Q and O once: K / V are loaded as L2 evict_last, and the
-// softmax warps read Q and write O as evict_first, so a Q / O stream larger
-// than L2 does not push K / V out between the query tiles that share them
-// (the prefetch keeps the default policy: an evict_first prefetch measured a
-// few MB more DRAM reads).
+// One thread.  Per key tile g: the K pieces into K slot g % KS (k_full) and
+// the V pieces into V slot g % VS (v_full).  A K slot is freed by its tile's
+// QK^T products, a V slot by its P.V products; since P.V runs about a tile
+// after QK^T, V is loaded one tile behind K, so a wait for a V slot never
+// holds back the next K.  At each item start it also prefetches the item's Q
+// rows into L2, so the softmax warps' Q loads come from L2.  K / V tiles are
+// read by every query tile of their kv head, Q and O once: K / V are loaded
+// as L2 evict_last, and the softmax warps read Q and write O as evict_first,
+// so a Q / O stream larger than L2 does not push K / V out between the query
+// tiles that share them (the prefetch keeps the default policy: an
+// evict_first prefetch measured a few MB more DRAM reads).
 template <int D, int IN>
 __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN>& sm, int n_items) {
   using C = Cfg<D, IN>;
@@ -232,6 +236,20 @@ __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN
   int g = 0;
   int q_items = 0;  // items whose Q was loaded into shared memory (kQSmem)
   const uint64_t keep = l2_evict_last_policy(), stream = l2_evict_first_policy();
+  int k_issued = 0, v_issued = 0;  // tiles whose K / V copies were started
+  // V of tile g - 1, not yet loaded: key0 and plane, or vplane < 0
+  int vkey0 = 0, vplane = -1;
+  auto load_v = [&](int gv) -> bool {
+    const int vs = gv % VS;
+    if (gv >= VS && !mbar_wait(sm.v_empty(vs), ((gv / VS) - 1) & 1, p.timeout_ns, p.status)) return false;
+    mbar_arrive_expect_tx(sm.v_full(vs), C::kVTileBytes);
+    ++v_issued;
+    for (int pc = 0; pc < VP; ++pc)
+      for (int s = 0; s < C::kSub; ++s)
+        tma_load_3d_hint(sm.sV + vs * C::kVTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_v,
+                         sm.v_full(vs), s * 64, vkey0, P.v_plane0 + pc * kvp + vplane, keep);
+    return true;
+  };
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int idx = f_item_of_round(r, n_items);
@@ -254,48 +272,44 @@ __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN
     }
     const int kv_plane = it.b * p.Hkv + it.kvh;
     for (int n = 0; n < it.N; ++n, ++g) {
-      const int ks = g % KS, vs = g % VS;
+      const int ks = g % KS;
       const int key0 = (it.tb + n) * FN;
       if (g >= KS && !mbar_wait(sm.k_empty(ks), ((g / KS) - 1) & 1, p.timeout_ns, p.status)) {
         ok = false;
         break;
       }
-      if (g >= VS && !mbar_wait(sm.v_empty(vs), ((g / VS) - 1) & 1, p.timeout_ns, p.status)) {
-        ok = false;
-        break;
-      }
-      mbar_arrive_expect_tx(sm.kv_full(ks), C::kKTileBytes + C::kVTileBytes);
+      mbar_arrive_expect_tx(sm.k_full(ks), C::kKTileBytes);
+      ++k_issued;
       for (int pc = 0; pc < KP; ++pc)
         for (int s = 0; s < C::kSub; ++s)
           tma_load_3d_hint(sm.sK + ks * C::kKTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_k,
-                           sm.kv_full(ks), s * 64, key0, pc * kvp + kv_plane, keep);
-      for (int pc = 0; pc < VP; ++pc)
-        for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d_hint(sm.sV + vs * C::kVTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_v,
-                           sm.kv_full(ks), s * 64, key0, P.v_plane0 + pc * kvp + kv_plane, keep);
+                           sm.k_full(ks), s * 64, key0, pc * kvp + kv_plane, keep);
+      if (vplane >= 0 && !load_v(g - 1)) {
+        ok = false;
+        break;
+      }
+      vkey0 = key0;
+      vplane = kv_plane;
     }
   }
+  if (ok && vplane >= 0) ok = load_v(g - 1);
   // Let every copy this thread started land before the CTA can exit.
-  for (int n = (g > KS ? g - KS : 0); n < g; ++n) mbar_wait(sm.kv_full(n % KS), (n / KS) & 1, p.timeout_ns, p.status);
+  for (int n = (k_issued > KS ? k_issued - KS : 0); n < k_issued; ++n)
+    mbar_wait(sm.k_full(n % KS), (n / KS) & 1, p.timeout_ns, p.status);
+  for (int n = (v_issued > VS ? v_issued - VS : 0); n < v_issued; ++n)
+    mbar_wait(sm.v_full(n % VS), (n / VS) & 1, p.timeout_ns, p.status);
   if (C::kQSmem && q_items > 0) mbar_wait(sm.q_full(), (q_items - 1) & 1, p.timeout_ns, p.status);
 }
 
-// ------------------------------------------------------------------ MMA issuer
-// The whole warp runs this; elect.sync picks the issuing lane.  Step n of an
-// item: the scores of tile n into an S buffer (once its K / V are in), then
-// the P.V products of tile n - 1 (once its P is written).
-//   ROLE 0 (one issuer, two S buffers): both; tile n uses buffer n % 2, and
-//     S(n) may overwrite the P of tile n - 2 because this warp issued that
-//     tile's P.V first (one thread's tensor-core operations run in order).
-//     One barrier wait sits between consecutive issue blocks; an issuing
-//     warp is held until only a few MMAs are queued, so each wait costs the
-//     tensor core most of its own duration.
-//   ROLE 1 / 2 (two issuers, SB = two or three S buffers): ROLE 1 issues
-//     only the scores, ROLE 2 only the P.V products, each on the CTA's
-//     running key tile count g (buffer g % SB).  The scores of tile g wait
-//     until the P.V products of tile g - SB finished (s_free), since they
-//     run on another thread.  While one issuer waits, the other's MMAs keep
-//     the queue busy.
+// ------------------------------------------------------------------ MMA issuers
+// Two warps issue: ROLE 1 the scores S = Q K^T of every key tile, ROLE 2 the
+// products O += P V, both on the CTA's running key tile count g, tile g in S
+// buffer g % SB.  The whole warp runs this; elect.sync picks the issuing lane.
+// An issuing warp is held until only a few MMAs are queued, so a single
+// issuer's barrier waits would each leave the tensor core idle for most of
+// their duration; with two, one issuer's MMAs keep the queue busy while the
+// other waits.  The scores of tile g go into the buffer of tile g - SB's P,
+// so they wait until that tile's P.V products finished (s_free).
 // For inputs read straight from the caller's cache (16-bit), V rows at or
 // past the valid length may hold any bits (NaN / Inf included): P is 0 there
 // but 0 * NaN is not, so those rows are zeroed in shared memory before the
@@ -309,8 +323,8 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
   constexpr bool kBF16 = In<IN>::kBF16;
   constexpr int FN = C::FN;
   constexpr int SB = C::kSBufs;
-  constexpr bool kQK = ROLE != 2, kPV = ROLE != 1;
-  static_assert(ROLE == 0 || C::kTwoIssuers, "issuer roles");
+  constexpr bool kQK = ROLE == 1, kPV = ROLE == 2;
+  static_assert(ROLE == 1 || ROLE == 2, "issuer roles");
   constexpr uint32_t id_qk = make_idesc_f16kind(kBF16, FM, FN, false);
   // one MMA's N is at most 256: D = 384 runs as N = 256 and N = 128 parts
   constexpr int kN0 = D > 256 ? 256 : D;
@@ -337,9 +351,9 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
       if (kQK && n < it.N) {
         // S = Q K_n^T (pieces: q0k0 + q0k1 + q1k0 + q0k2 + q1k1 + q2k0)
         const int gs = g0 + n;
-        const int bs = ROLE == 0 ? (n & 1) : gs % SB;
-        if (!mbar_wait_warp(sm.kv_full(gs % KS), (gs / KS) & 1, p.timeout_ns, p.status)) { ok = false; break; }
-        if (ROLE == 1 && gs >= SB && !mbar_wait_warp(sm.s_free(bs), ((gs / SB) - 1) & 1, p.timeout_ns, p.status)) {
+        const int bs = gs % SB;
+        if (!mbar_wait_warp(sm.k_full(gs % KS), (gs / KS) & 1, p.timeout_ns, p.status)) { ok = false; break; }
+        if (gs >= SB && !mbar_wait_warp(sm.s_free(bs), ((gs / SB) - 1) & 1, p.timeout_ns, p.status)) {
           ok = false;
           break;
         }
@@ -389,7 +403,8 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
         // O (+)= P_{n-1} V_{n-1} (pieces: p0 v0 + p0 v1 + p1 v0)
         const int m = n - 1;
         const int gv = g0 + m;
-        const int bp = ROLE == 0 ? (m & 1) : gv % SB;
+        const int bp = gv % SB;
+        if (!mbar_wait_warp(sm.v_full(gv % VS), (gv / VS) & 1, p.timeout_ns, p.status)) { ok = false; break; }
         if (!mbar_wait_warp(sm.p_full(bp), pb[bp] & 1, p.timeout_ns, p.status)) { ok = false; break; }
         ++pb[bp];
         const uint32_t vb = sm.sV + (gv % VS) * C::kVTileBytes;
@@ -436,7 +451,7 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
                         m == 0 ? 0u : 1u);
         }
         tc_commit_elect(sm.v_empty(gv % VS));
-        if constexpr (ROLE == 2) tc_commit_elect(sm.s_free(bp));
+        tc_commit_elect(sm.s_free(bp));
         tc_commit_elect(sm.pv_done());
         if (m == it.N - 1) tc_commit_elect(sm.o_final());  // the item's last P.V
       }
@@ -682,9 +697,8 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
     float m_run = -INFINITY;  // running max, log2 units
     float l_run = 0.0f;
     for (int n = 0; n < it.N; ++n, ++tiles) {
-      // the MMA warps' buffer order: the running tile count with two
-      // issuers, the tile within the item with one
-      const int bsel = C::kTwoIssuers ? tiles % C::kSBufs : (n & 1);
+      // the MMA warps' buffer order: the running key tile count
+      const int bsel = tiles % C::kSBufs;
       const uint32_t s_addr = tlane + C::kColS + 64 * bsel;
       const int64_t key0 = (int64_t)(it.tb + n) * FN;
       float x[FN];
@@ -914,10 +928,13 @@ __global__ void __launch_bounds__(Cfg<D, IN>::kThreads, 1) attn_fwd_lane1_kernel
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kKStages; ++s) {
-      mbar_init(sm.kv_full(s), 1);
+      mbar_init(sm.k_full(s), 1);
       mbar_init(sm.k_empty(s), 1);
     }
-    for (int s = 0; s < C::kVStages; ++s) mbar_init(sm.v_empty(s), 1);
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(sm.v_full(s), 1);
+      mbar_init(sm.v_empty(s), 1);
+    }
     mbar_init(sm.q_full(), C::kQSmem ? 1 : 4);  // the producer's TMA, or one arrival per softmax warp
     mbar_init(sm.q_empty(), 1);
     for (int b = 0; b < C::kSBufs; ++b) {
@@ -927,7 +944,7 @@ __global__ void __launch_bounds__(Cfg<D, IN>::kThreads, 1) attn_fwd_lane1_kernel
     }
     mbar_init(sm.pv_done(), 1);
     mbar_init(sm.o_final(), 1);
-    mbar_init(sm.drain(), C::kTwoIssuers ? 2 : 1);  // one commit per issuing warp
+    mbar_init(sm.drain(), 2);  // one commit per issuing warp
     mbar_init_fence();
   }
   if (warp == kTmaWarp && lane == 0) {
@@ -947,9 +964,9 @@ __global__ void __launch_bounds__(Cfg<D, IN>::kThreads, 1) attn_fwd_lane1_kernel
   if (warp == kTmaWarp) {
     if (lane == 0) f_producer<D, IN>(P, sm, n_items);
   } else if (warp == kMmaWarp) {
-    f_mma<D, IN, C::kTwoIssuers ? 1 : 0>(P, sm, tmem, n_items, lane);
+    f_mma<D, IN, 1>(P, sm, tmem, n_items, lane);
   } else if (warp == kPvWarp) {
-    if constexpr (C::kTwoIssuers) f_mma<D, IN, 2>(P, sm, tmem, n_items, lane);
+    f_mma<D, IN, 2>(P, sm, tmem, n_items, lane);
   } else {
     f_softmax<D, IN, SOFTCAP, MASK>(P, sm, tmem, n_items, warp, lane);
   }
