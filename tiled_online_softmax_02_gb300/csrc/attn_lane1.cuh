@@ -870,11 +870,16 @@ __device__ __forceinline__ void f_softmax(const LaneParams& P, const Smem<D, IN>
                                             : (((int64_t)it.b * p.Sq + qr) * p.Hq + it.h) * D;
         odst[i] = qr < p.Sq ? static_cast<uint8_t*>(p.out) + e * (kF32 ? 4 : 2) + csub * 16 : nullptr;
       }
+      // the next 32 columns' tensor-memory load is in flight while these
+      // are converted and stored (tcgen05.wait::ld waits for every earlier
+      // load, so the load of chunk k + 1 is issued right after the wait for k)
+      uint32_t ob[2][32];
+      tmem_ld32(o_addr, ob[0]);
 #pragma unroll
       for (int k = 0; k < D / 32; ++k) {
-        uint32_t o[32];
-        tmem_ld32(o_addr + k * 32, o);
         tmem_wait_ld();
+        if (k + 1 < D / 32) tmem_ld32(o_addr + (k + 1) * 32, ob[(k + 1) & 1]);
+        const uint32_t(&o)[32] = ob[k & 1];
         float r[32];
 #pragma unroll
         for (int i = 0; i < 32; i += 2)
