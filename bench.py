@@ -47,17 +47,19 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # attn_fwd_splitkv entry), with the hash of that kernel's sources at the time;
 # reported as null once those sources change.
 NCU_TRAFFIC = {
-    "gqa_causal_bf16": {"bytes_per_launch": 127524096, "source_hash": "026bc7d58294bb1a"},
-    "window_softcap_bf16": {"bytes_per_launch": 396008704, "source_hash": "026bc7d58294bb1a"},
-    "ragged_kvcache_f16": {"bytes_per_launch": 48547584, "source_hash": "026bc7d58294bb1a"},
-    "dit_f32": {"bytes_per_launch": 57955840, "source_hash": "eae79b8b5b3f0a83"},
-    "dit_f32+f32split": {"bytes_per_launch": 76163072, "source_hash": "1734554f5cdad589"},
-    "decode_bf16": {"bytes_per_launch": 775665920, "source_hash": "aee60e800bf42d81"},
-    "decode_bf16+splitkv": {"bytes_per_launch": 777046272, "source_hash": "aee60e800bf42d81"},
-    "gqa_causal_bf16_d256": {"bytes_per_launch": 435266560, "source_hash": "6b4b5aabb41779d5"},
+    "gqa_causal_bf16": {"bytes_per_launch": 127725056, "source_hash": "64665e6852457495"},
+    "window_softcap_bf16": {"bytes_per_launch": 396390912, "source_hash": "64665e6852457495"},
+    "ragged_kvcache_f16": {"bytes_per_launch": 48563968, "source_hash": "64665e6852457495"},
+    "dit_f32": {"bytes_per_launch": 57926656, "source_hash": "1a2421def8d9be91"},
+    "dit_f32+f32split": {"bytes_per_launch": 69472000, "source_hash": "2ef5be24af3dacb8"},
+    "decode_bf16": {"bytes_per_launch": 775945472, "source_hash": "c05337b007be4581"},
+    "decode_bf16+splitkv": {"bytes_per_launch": 777069568, "source_hash": "c05337b007be4581"},
+    "gqa_causal_bf16_d256": {"bytes_per_launch": 372647168, "source_hash": "d23f60cee55ca08d"},
+    "gqa_causal_bf16_d384": {"bytes_per_launch": 888843264, "source_hash": "d23f60cee55ca08d"},
+    "vae_f32_d384": {"bytes_per_launch": 18940672, "source_hash": "1a2421def8d9be91"},
     # the DSA indexer: the tile score kernel (the selection kernel's traffic is in its profile)
-    "dsa_prefill_bf16": {"bytes_per_launch": 139407616, "source_hash": "9717cc89f81595d7"},
-    "dsa_decode_bf16": {"bytes_per_launch": 34638080, "source_hash": "9717cc89f81595d7"},
+    "dsa_prefill_bf16": {"bytes_per_launch": 139367680, "source_hash": "4c0afd2437582ac7"},
+    "dsa_decode_bf16": {"bytes_per_launch": 34638080, "source_hash": "4c0afd2437582ac7"},
 }
 
 
