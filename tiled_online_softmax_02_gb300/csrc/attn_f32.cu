@@ -13,6 +13,9 @@
 //                     (i < 4, j < BN / 16), 16 FFMA per 8 shared-memory
 //                     vector loads at BN = 64;
 //   O tile (64 x D):  thread owns rows ty + 16 i and columns 4 tx + 64 g.
+// At head dims 256 and 384, whose CTAs take a whole SM, a grid of 64-row
+// tiles smaller than the SM count runs as 32-row CTAs instead (i < 2), twice
+// as many.
 // Row max / sum reductions run over the 16 lanes that share a row.
 // Head dims are padded to DP = 64, 128, 256 or 384 (the page's wider VAE
 // variant compiles the same kernel for head dims up to 384, "Kernel
@@ -28,8 +31,11 @@ constexpr int BM = kF32BlockM;  // 64 query rows
 constexpr int kThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int DP>
+// RI = query rows per thread: a CTA owns 16 RI rows (64, or 32 where 64-row
+// tiles would leave SMs without a CTA).
+template <int DP, int RI = 4>
 struct F32Config {
+  static constexpr int BMr = 16 * RI;             // query rows per CTA
   static constexpr int BN = DP <= 256 ? 64 : 32;  // keys per tile
   static constexpr int kKeysPerThread = BN / 16;
   static constexpr int kQStride = DP + 4;  // padded rows: conflict-free float4 reads
@@ -38,7 +44,7 @@ struct F32Config {
   static constexpr int kPStride = BN + 4;
   static constexpr int kGroups = DP / 64;  // float4 column groups per O row per thread
   static constexpr size_t kSmemFloats =
-      (size_t)BM * kQStride + (size_t)BN * kKStride + (size_t)BN * kVStride + (size_t)BM * kPStride;
+      (size_t)BMr * kQStride + (size_t)BN * kKStride + (size_t)BN * kVStride + (size_t)BMr * kPStride;
   static constexpr size_t kSmemBytes = kSmemFloats * sizeof(float);
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
@@ -69,9 +75,10 @@ __device__ __forceinline__ void load_rows(float* dst, int sstride, const float* 
   }
 }
 
-template <int DP, bool SOFTCAP, bool MASK>
+template <int DP, int RI, bool SOFTCAP, bool MASK>
 __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_constant__ F32Params P) {
-  using Cfg = F32Config<DP>;
+  using Cfg = F32Config<DP, RI>;
+  constexpr int BM = Cfg::BMr;
   constexpr int BN = Cfg::BN;
   constexpr int KJ = Cfg::kKeysPerThread;
   const CommonParams& p = P.c;
@@ -102,10 +109,10 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
   const float* vplane = P.v + ((int64_t)b * p.Hkv + kvh) * (int64_t)p.kv_capacity * D;
   load_rows<DP>(Qs, Cfg::kQStride, qplane, q0, BM, p.Sq, D, vec4);
 
-  RowLimits R[4];
-  const float* mrow[4];
+  RowLimits R[RI];
+  const float* mrow[RI];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < RI; ++i) {
     const int64_t qi = q0 + ty + 16 * i;
     R[i] = row_limits(p, L, qi);
     mrow[i] = nullptr;
@@ -117,10 +124,10 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
     }
   }
 
-  float m[4], l[4];
-  float o[4][Cfg::kGroups][4];
+  float m[RI], l[RI];
+  float o[RI][Cfg::kGroups][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < RI; ++i) {
     m[i] = -INFINITY;
     l[i] = 0.f;
 #pragma unroll
@@ -136,23 +143,23 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
     load_rows<DP>(Vs, Cfg::kVStride, vplane, key0, BN, zero_from, D, vec4);
     __syncthreads();
 
-    // S = Q K^T for this thread's 4 x KJ block
-    float s[4][KJ];
+    // S = Q K^T for this thread's RI x KJ block
+    float s[RI][KJ];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < RI; ++i)
 #pragma unroll
       for (int j = 0; j < KJ; ++j) s[i][j] = 0.f;
 #pragma unroll 4
     for (int d0 = 0; d0 < DP; d0 += 4) {
-      float4 qa[4], kb[KJ];
+      float4 qa[RI], kb[KJ];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < RI; ++i)
         qa[i] = *reinterpret_cast<const float4*>(Qs + (ty + 16 * i) * Cfg::kQStride + d0);
 #pragma unroll
       for (int j = 0; j < KJ; ++j)
         kb[j] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * j) * Cfg::kKStride + d0);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < RI; ++i)
 #pragma unroll
         for (int j = 0; j < KJ; ++j) {
           s[i][j] = fmaf(qa[i].x, kb[j].x, s[i][j]);
@@ -165,7 +172,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
     // scores in log2 units; invisible keys -> -inf (a select)
     const bool need_mask = !(key0 >= T.full_lo && key0 + BN <= T.full_hi);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < RI; ++i) {
 #pragma unroll
       for (int j = 0; j < KJ; ++j) {
         const int64_t kj = key0 + tx + 16 * j;
@@ -187,7 +194,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
 
     // online softmax update per row (the tile update of the page's kernel)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < RI; ++i) {
       float mt = s[i][0];
 #pragma unroll
       for (int j = 1; j < KJ; ++j) mt = fmaxf(mt, s[i][j]);
@@ -219,9 +226,9 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
     // O += P V
 #pragma unroll 2
     for (int k0 = 0; k0 < BN; k0 += 4) {
-      float4 pa[4];
+      float4 pa[RI];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < RI; ++i)
         pa[i] = *reinterpret_cast<const float4*>(Ps + (ty + 16 * i) * Cfg::kPStride + k0);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
@@ -229,7 +236,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
         for (int g = 0; g < Cfg::kGroups; ++g) {
           const float4 vb = *reinterpret_cast<const float4*>(Vs + (k0 + kk) * Cfg::kVStride + g * 64 + tx * 4);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < RI; ++i) {
             const float pk = kk == 0 ? pa[i].x : kk == 1 ? pa[i].y : kk == 2 ? pa[i].z : pa[i].w;
             o[i][g][0] = fmaf(pk, vb.x, o[i][g][0]);
             o[i][g][1] = fmaf(pk, vb.y, o[i][g][1]);
@@ -244,7 +251,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
   // normalise and store
   float* out = reinterpret_cast<float*>(p.out);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < RI; ++i) {
     const int64_t qi = q0 + ty + 16 * i;
     if (qi >= p.Sq) continue;
     const float inv = l[i] > 0.f ? 1.0f / l[i] : 0.f;
@@ -269,25 +276,41 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
   }
 }
 
-template <int DP, bool SOFTCAP, bool MASK>
+template <int DP, int RI, bool SOFTCAP, bool MASK>
 cudaError_t launch_variant(const F32Params& P, cudaStream_t stream) {
-  auto kernel = attn_fwd_f32_kernel<DP, SOFTCAP, MASK>;
-  constexpr size_t smem = F32Config<DP>::kSmemBytes;
+  auto kernel = attn_fwd_f32_kernel<DP, RI, SOFTCAP, MASK>;
+  constexpr size_t smem = F32Config<DP, RI>::kSmemBytes;
+  constexpr int rows = F32Config<DP, RI>::BMr;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((P.c.Sq + BM - 1) / BM), (unsigned)P.c.Hq, (unsigned)P.c.B);
+  const dim3 grid((unsigned)((P.c.Sq + rows - 1) / rows), (unsigned)P.c.Hq, (unsigned)P.c.B);
   kernel<<<grid, kThreads, smem, stream>>>(P);
   return cudaGetLastError();
 }
 
-template <int DP>
-cudaError_t launch_dp(const F32Params& P, cudaStream_t stream) {
+template <int DP, int RI>
+cudaError_t launch_dp_ri(const F32Params& P, cudaStream_t stream) {
   const bool sc = P.c.softcap > 0.0f;
   const bool mk = P.c.mask != nullptr && P.c.mask_planes > 0;
-  if (sc && mk) return launch_variant<DP, true, true>(P, stream);
-  if (sc) return launch_variant<DP, true, false>(P, stream);
-  if (mk) return launch_variant<DP, false, true>(P, stream);
-  return launch_variant<DP, false, false>(P, stream);
+  if (sc && mk) return launch_variant<DP, RI, true, true>(P, stream);
+  if (sc) return launch_variant<DP, RI, true, false>(P, stream);
+  if (mk) return launch_variant<DP, RI, false, true>(P, stream);
+  return launch_variant<DP, RI, false, false>(P, stream);
+}
+
+// 64-row CTAs, or (wide head dims, whose CTAs take a whole SM) 32-row CTAs
+// when 64-row tiles would leave SMs without a CTA.
+template <int DP>
+cudaError_t launch_dp(const F32Params& P, cudaStream_t stream) {
+  if constexpr (DP >= 256) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles64 = (int64_t)((P.c.Sq + 63) / 64) * P.c.Hq * P.c.B;
+    if (tiles64 < sms) return launch_dp_ri<DP, 2>(P, stream);
+  }
+  return launch_dp_ri<DP, 4>(P, stream);
 }
 
 }  // namespace
