@@ -27,7 +27,6 @@
 namespace gb300_attn {
 namespace {
 
-constexpr int BM = kF32BlockM;  // 64 query rows
 constexpr int kThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
