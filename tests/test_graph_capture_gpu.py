@@ -105,3 +105,25 @@ def test_attn_fwd_graph(name, kw):
     out = torch.empty_like(ref)
     g = _capture(lambda: attn.attn_fwd(g_in["q"], g_in["k"], g_in["v"], out=out, **args))
     _replay_twice(g, [out], [ref])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(B=1, Hq=4, Hkv=4, Sq=300, Sk=300, kv_capacity=300, D=128),
+    dict(B=2, Hq=4, Hkv=2, Sq=200, Sk=260, kv_capacity=272, D=64, causal=True, ragged=True, garbage="nonfinite"),
+])
+def test_f32_split_graph(kw):
+    """fp32 on the tensor cores: the attention kernel is a programmatic
+    dependent of the K / V pre-pass (it starts its prologue and Q rows during
+    the pre-pass and waits for it before reading the pieces)."""
+    w = WORKLOADS["dit_f32"].replace(**kw)
+    g_in = to_dev(make_inputs(w))
+    args = dict(mask=g_in["mask"], total_lengths=g_in["total_lengths"], past_lengths=g_in["past_lengths"],
+                causal=w.causal, local_window=w.local_window, scale=w.softmax_scale, softcap=w.softcap,
+                out_layout=w.out_layout, seq_k=w.Sk)
+    ref = attn.attn_fwd_f32_split(g_in["q"], g_in["k"], g_in["v"], **args)
+    lib = attn.load_library()
+    ws = torch.empty(max(lib.attn_f32_split_workspace_bytes(w.B, w.Hkv, w.kv_capacity, w.D), 16),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(ref)
+    g = _capture(lambda: attn.attn_fwd_f32_split(g_in["q"], g_in["k"], g_in["v"], out=out, workspace=ws, **args))
+    _replay_twice(g, [out], [ref])

@@ -40,6 +40,9 @@ __global__ void __launch_bounds__(256) f32_split_kv_kernel(const float* __restri
                                                            const int32_t* __restrict__ total_lengths,
                                                            int Hkv, int kv_capacity, int Sk, int D,
                                                            int64_t n_elems) {
+  // the attention kernel (a programmatic dependent) may start its prologue
+  // and its first Q rows now; it waits for this grid before reading the pieces
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t n4 = n_elems / 4;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t e = i * 4;

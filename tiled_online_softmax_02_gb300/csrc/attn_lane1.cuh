@@ -237,6 +237,10 @@ __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN
   int q_items = 0;  // items whose Q was loaded into shared memory (kQSmem)
   const uint64_t keep = l2_evict_last_policy(), stream = l2_evict_first_policy();
   int k_issued = 0, v_issued = 0;  // tiles whose K / V copies were started
+  // fp32: K / V pieces come from the pre-pass grid; wait until it finished
+  // (its writes are then visible).  Everything before this point, and Q,
+  // is independent of it.
+  if constexpr (IN == kInF32Split) asm volatile("griddepcontrol.wait;" ::: "memory");
   // V of tile g - 1, not yet loaded: key0 and plane, or vplane < 0
   int vkey0 = 0, vplane = -1;
   auto load_v = [&](int gv) -> bool {
@@ -996,8 +1000,20 @@ cudaError_t launch_lane1_variant(const LaneParams& P, cudaStream_t stream) {
   const int64_t n_items = (int64_t)((P.c.Sq + FM - 1) / FM) * P.c.B * P.c.Hq;
   if (n_items > INT32_MAX) return cudaErrorInvalidConfiguration;
   const int grid = (int)(n_items < sms ? n_items : sms);  // one persistent CTA per SM
-  kernel<<<grid, Cfg<D, IN>::kThreads, smem, stream>>>(P);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(Cfg<D, IN>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  // fp32: a programmatic dependent of the K / V pre-pass, so the prologue and
+  // the first item's Q rows overlap its tail (the producer waits for it in
+  // hardware before the first K / V load)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = IN == kInF32Split ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, P);
 }
 
 // One head dim and input kind: the four soft-cap / mask variants.
