@@ -35,9 +35,10 @@
 // length limits), so the diagonal and window edges cost no extra MMAs.
 //
 // Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384),
-// O_1 [384,512).  Shared memory: Q_0, Q_1, kStages x (K, V) tiles, barriers;
-// every tile is stored as 64-column (128-byte) blocks in the 128-byte swizzle
-// TMA writes.
+// O_1 [384,512).  Shared memory: Q_0, Q_1, the K and V rings (2 + 2 stages
+// at D = 128 with a mask, 2 + 3 without, 4 + 4 at D = 64), barriers and the
+// per-warp mask buffers; every tile is stored as 64-column (128-byte) blocks
+// in the 128-byte swizzle TMA writes.
 //
 // Every barrier wait is bounded (mbar_wait); on a timeout the kernel records
 // ATTN_ERR_TIMEOUT in the status word, drains what it issued, frees tensor
@@ -65,51 +66,61 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxOrderB = 64;   // batches ranked by cost when B <= this
 constexpr uint32_t kMaskBufBytes = 32 * 32 * 4;  // per softmax warp: 32 rows x 32 keys of f32
 
-template <int D>
+// MB: the variant stages the mask through per-warp buffers.  Without a mask
+// (MB false) that space holds a third V stage at D = 128, and K and V of key
+// tile g complete one barrier (k_full of K's slot): the QK^T products of a
+// tile already wait for it, so the MMA warp's wait before the P.V products
+// of that tile, a step later, goes away (with three V stages V's load starts
+// about two steps before its P.V, so a tile's barrier is not held back by
+// its V).  With a mask, K and V keep their own barriers and two stages each.
+template <int D, bool MB = true>
 struct TcConfig {
   static constexpr int kSub = D / 64;                   // 128-byte column blocks per row
   static constexpr uint32_t kSubBytes = BM * 128;       // [128 rows][64 cols] of 16-bit
   static constexpr uint32_t kTileBytes = kSub * kSubBytes;
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kKStages = (D == 64) ? 4 : 2;
+  static constexpr int kVStages = (D == 64) ? 4 : (MB ? 2 : 3);
+  static constexpr bool kCombined = !MB;  // V(g) completes k_full(g % kKStages)
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffK = kOffQ + kQTiles * kTileBytes;
-  static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
-  static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
-  // q_full, q_empty, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2],
-  // o_final[2], drain, merge_full, merge_done
-  static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 3;
+  static constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
+  // q_full, q_empty, k_full[SK], v_full[SV], k_empty[SK], v_empty[SV], s_full[2],
+  // p_full[2], o_final[2], drain, merge_full, merge_done
+  static constexpr int kNumBars = 2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 3;
   static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffMerge = kOffTmemSlot + 16;          // float2 [128] (key-split merge)
   static constexpr uint32_t kOffOrder = kOffMerge + BM * 8;         // int [kMaxOrderB] batch order
   static constexpr uint32_t kOffMaskBuf = (kOffOrder + kMaxOrderB * 4 + 127) / 128 * 128;
-  static constexpr uint32_t kSmemBytes = kOffMaskBuf + 8 * kMaskBufBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kSmemBytes = kOffMaskBuf + (MB ? 8 * kMaskBufBytes : 0) + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 // Shared-memory addresses of the tiles and barriers.
-template <int D>
+template <int D, bool MB = true>
 struct Smem {
-  using Cfg = TcConfig<D>;
-  static constexpr int S = Cfg::kStages;
+  using Cfg = TcConfig<D, MB>;
+  static constexpr int SK = Cfg::kKStages, SV = Cfg::kVStages;
+  static constexpr int kR = 2 + 2 * SK + 2 * SV;  // first barrier after the rings
   uint8_t* base;
   uint32_t sQ, sK, sV, bar0;
   __device__ uint32_t q_full() const { return bar0; }
   __device__ uint32_t q_empty() const { return bar0 + 8u; }
   __device__ uint32_t k_full(int s) const { return bar0 + 8u * (2 + s); }
-  __device__ uint32_t v_full(int s) const { return bar0 + 8u * (2 + S + s); }
+  __device__ uint32_t v_full(int s) const { return bar0 + 8u * (2 + SK + s); }
   // K and V slots are released separately: a K tile is free once both
   // query tiles' QK^T products read it, one key tile before its V is
-  __device__ uint32_t k_empty(int s) const { return bar0 + 8u * (2 + 2 * S + s); }
-  __device__ uint32_t v_empty(int s) const { return bar0 + 8u * (2 + 3 * S + s); }
-  __device__ uint32_t s_full(int t) const { return bar0 + 8u * (2 + 4 * S + t); }
-  __device__ uint32_t p_full(int t) const { return bar0 + 8u * (2 + 4 * S + 2 + t); }
+  __device__ uint32_t k_empty(int s) const { return bar0 + 8u * (2 + SK + SV + s); }
+  __device__ uint32_t v_empty(int s) const { return bar0 + 8u * (2 + 2 * SK + SV + s); }
+  __device__ uint32_t s_full(int t) const { return bar0 + 8u * (kR + t); }
+  __device__ uint32_t p_full(int t) const { return bar0 + 8u * (kR + 2 + t); }
   // completes once per item, after query tile t's last P.V (the epilogue's wait)
-  __device__ uint32_t o_final(int t) const { return bar0 + 8u * (2 + 4 * S + 4 + t); }
-  __device__ uint32_t drain() const { return bar0 + 8u * (2 + 4 * S + 6); }
+  __device__ uint32_t o_final(int t) const { return bar0 + 8u * (kR + 4 + t); }
+  __device__ uint32_t drain() const { return bar0 + 8u * (kR + 6); }
   // key-split merge hand-over: lane 1's row max / sum written (128 arrivals),
   // then lane 1's O read by warpgroup 0 (128 arrivals)
-  __device__ uint32_t merge_full() const { return bar0 + 8u * (2 + 4 * S + 7); }
-  __device__ uint32_t merge_done() const { return bar0 + 8u * (2 + 4 * S + 8); }
+  __device__ uint32_t merge_full() const { return bar0 + 8u * (kR + 7); }
+  __device__ uint32_t merge_done() const { return bar0 + 8u * (kR + 8); }
   __device__ float2* merge() const { return reinterpret_cast<float2*>(base + Cfg::kOffMerge); }
   __device__ const int* order() const { return reinterpret_cast<const int*>(base + Cfg::kOffOrder); }
   __device__ uint8_t* mask_buf(int warp) const { return base + Cfg::kOffMaskBuf + warp * kMaskBufBytes; }
@@ -269,12 +280,13 @@ __device__ __forceinline__ float min128(const float (&x)[BN]) {
 // One thread.  Q tiles per item (after the previous item's QK^T products
 // released them), then the item's K / V tiles into the stage ring; the ring
 // index g runs on across items.
-template <int D, bool KSPLIT>
-__device__ __forceinline__ void producer_role(const TcParams& P, const Smem<D>& sm, int n_items) {
-  using Cfg = TcConfig<D>;
-  constexpr int S = Cfg::kStages;
+template <int D, bool KSPLIT, bool MB>
+__device__ __forceinline__ void producer_role(const TcParams& P, const Smem<D, MB>& sm, int n_items) {
+  using Cfg = TcConfig<D, MB>;
+  constexpr int SK = Cfg::kKStages, SV = Cfg::kVStages;
   const CommonParams& p = P.c;
   int g = 0;        // K / V tiles issued so far (ring position)
+  int k_issued = 0, v_issued = 0;  // tiles whose K / V copies were started
   int q_items = 0;  // items whose Q was loaded
   // batch ranking only in the key-split variant (short query ranges, where
   // ragged lengths decide the cost); elsewhere the pointer stays out of registers
@@ -297,43 +309,48 @@ __device__ __forceinline__ void producer_role(const TcParams& P, const Smem<D>& 
                     (int)it.row0(t), q_plane);
     ++q_items;
     for (int n = 0; n < it.N; ++n, ++g) {
-      const int st = g % S;
+      const int sk = g % SK, sv = g % SV;
       const int key0 = (it.tb + n) * BN;
-      // K(g) reuses the slot of K(g - S), freed after that tile's QK^T
-      // products; V(g) the slot of V(g - S), freed one key tile later (after
-      // its P.V products).  So K runs a key tile further ahead than V.
-      if (g >= S && !mbar_wait(sm.k_empty(st), ((g / S) - 1) & 1, p.timeout_ns, p.status)) {
+      // K(g) reuses the slot of K(g - SK), freed after that tile's QK^T
+      // products; V(g) the slot of V(g - SV), freed after its P.V products,
+      // which come a key tile later.  So K runs ahead of V.
+      if (g >= SK && !mbar_wait(sm.k_empty(sk), ((g / SK) - 1) & 1, p.timeout_ns, p.status)) {
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(sm.k_full(st), Cfg::kTileBytes);
+      // combined: this phase of k_full(sk) completes when K and V both landed
+      mbar_arrive_expect_tx(sm.k_full(sk), Cfg::kCombined ? 2 * Cfg::kTileBytes : Cfg::kTileBytes);
       for (int s = 0; s < Cfg::kSub; ++s)
-        tma_load_3d(sm.sK + st * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_k, sm.k_full(st), s * 64,
+        tma_load_3d(sm.sK + sk * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_k, sm.k_full(sk), s * 64,
                     key0, kv_plane);
-      if (g >= S && !mbar_wait(sm.v_empty(st), ((g / S) - 1) & 1, p.timeout_ns, p.status)) {
+      ++k_issued;
+      if (g >= SV && !mbar_wait(sm.v_empty(sv), ((g / SV) - 1) & 1, p.timeout_ns, p.status)) {
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(sm.v_full(st), Cfg::kTileBytes);
+      const uint32_t vbar = Cfg::kCombined ? sm.k_full(sk) : sm.v_full(sv);
+      if (!Cfg::kCombined) mbar_arrive_expect_tx(vbar, Cfg::kTileBytes);
       for (int s = 0; s < Cfg::kSub; ++s)
-        tma_load_3d(sm.sV + st * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_v, sm.v_full(st), s * 64,
-                    key0, kv_plane);
+        tma_load_3d(sm.sV + sv * Cfg::kTileBytes + s * Cfg::kSubBytes, &P.tmap_v, vbar, s * 64, key0, kv_plane);
+      ++v_issued;
     }
   }
-  // Let every copy this thread started land before the CTA can exit.
-  for (int n = (g > S ? g - S : 0); n < g; ++n) {
-    mbar_wait(sm.k_full(n % S), (n / S) & 1, p.timeout_ns, p.status);
-    mbar_wait(sm.v_full(n % S), (n / S) & 1, p.timeout_ns, p.status);
-  }
+  // Let every copy this thread started land before the CTA can exit (with
+  // the combined barrier, k_full covers V as well).
+  for (int n = (k_issued > SK ? k_issued - SK : 0); n < k_issued; ++n)
+    mbar_wait(sm.k_full(n % SK), (n / SK) & 1, p.timeout_ns, p.status);
+  if (!Cfg::kCombined)
+    for (int n = (v_issued > SV ? v_issued - SV : 0); n < v_issued; ++n)
+      mbar_wait(sm.v_full(n % SV), (n / SV) & 1, p.timeout_ns, p.status);
   if (q_items > 0) mbar_wait(sm.q_full(), (q_items - 1) & 1, p.timeout_ns, p.status);
 }
 
 // S_t = Q K^T for one key tile (K tile at kaddr, Q from query tile slot qt:
 // t, or 0 for both lanes of a lane-split item), then commit s_full(t).
 // Warp-collective: the whole MMA warp calls it, one elected lane issues.
-template <int D, bool BF16>
-__device__ __forceinline__ void issue_qk(const Smem<D>& sm, uint32_t tmem, int t, int qt, uint32_t kaddr) {
-  using Cfg = TcConfig<D>;
+template <int D, bool BF16, bool MB>
+__device__ __forceinline__ void issue_qk(const Smem<D, MB>& sm, uint32_t tmem, int t, int qt, uint32_t kaddr) {
+  using Cfg = TcConfig<D, MB>;
   constexpr uint32_t idesc_qk = make_idesc_f16kind(BF16, BM, BN, false);
   const uint64_t adesc0 = make_sdesc_sw128(sm.sQ + qt * Cfg::kTileBytes, 16, 1024);
   const uint64_t bdesc0 = make_sdesc_sw128(kaddr, 16, 1024);
@@ -351,10 +368,10 @@ __device__ __forceinline__ void issue_qk(const Smem<D>& sm, uint32_t tmem, int t
 // O_t (+)= P_t V for one key tile (V tile at vaddr; P_t in tensor memory over
 // the first half of S_t).
 // Warp-collective, like issue_qk.
-template <int D, bool BF16>
-__device__ __forceinline__ void issue_pv(const Smem<D>& sm, uint32_t tmem, int t, uint32_t vaddr,
+template <int D, bool BF16, bool MB>
+__device__ __forceinline__ void issue_pv(const Smem<D, MB>& sm, uint32_t tmem, int t, uint32_t vaddr,
                                          bool accumulate) {
-  using Cfg = TcConfig<D>;
+  using Cfg = TcConfig<D, MB>;
   constexpr uint32_t idesc_pv = make_idesc_f16kind(BF16, BM, D, true);
   // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B apart, 64-column
   // blocks kSubBytes apart.
@@ -372,11 +389,11 @@ __device__ __forceinline__ void issue_pv(const Smem<D>& sm, uint32_t tmem, int t
 // Whole warp waits; lane 0 issues.  Per item and key tile j (iteration n):
 // the P.V products of tile j-1, then the QK^T products of tile j, per query
 // tile in turn.  Returns after every MMA it issued has completed.
-template <int D, bool BF16, bool KSPLIT>
-__device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, uint32_t tmem,
+template <int D, bool BF16, bool KSPLIT, bool MB>
+__device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D, MB>& sm, uint32_t tmem,
                                          int n_items, int lane) {
-  using Cfg = TcConfig<D>;
-  constexpr int S = Cfg::kStages;
+  using Cfg = TcConfig<D, MB>;
+  constexpr int SK = Cfg::kKStages, SV = Cfg::kVStages;
   const CommonParams& p = P.c;
   int g0 = 0;                 // ring position of the item's first key tile
   int q_items = 0;            // items whose Q was consumed
@@ -400,8 +417,13 @@ __device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, u
       bool k_ready = false;  // K(j) is waited for only before its first use
       if (n >= 1) {
         const int gp = g0 + n - 1;
-        const int ps = gp % S;
-        if (!mbar_wait_warp(sm.v_full(ps), (gp / S) & 1, p.timeout_ns, p.status)) { ok = false; break; }
+        const int ps = gp % SV;
+        // combined barrier: V(j - 1) landed with K(j - 1), which this warp
+        // waited for before that tile's QK^T products
+        if (!Cfg::kCombined && !mbar_wait_warp(sm.v_full(ps), (gp / SV) & 1, p.timeout_ns, p.status)) {
+          ok = false;
+          break;
+        }
         const int64_t key0 = (int64_t)(j - 1) * BN;
         if (zero_from < key0 + BN && zero_from < (int64_t)p.kv_capacity) {
           // Cache slots past the valid length may hold NaN / Inf; P is 0
@@ -422,14 +444,14 @@ __device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, u
       tc_fence_after();
       const bool pv0 = n >= 1 && it.active(0, j - 1), pv1 = n >= 1 && it.active(1, j - 1);
       const bool s0 = n < it.N && it.active(0, j), s1 = n < it.N && it.active(1, j);
-      const uint32_t kaddr = sm.sK + ((g0 + n) % S) * Cfg::kTileBytes;
-      const uint32_t vaddr = sm.sV + ((g0 + n - 1 + S) % S) * Cfg::kTileBytes;
+      const uint32_t kaddr = sm.sK + ((g0 + n) % SK) * Cfg::kTileBytes;
+      const uint32_t vaddr = sm.sV + ((g0 + n - 1 + SV) % SV) * Cfg::kTileBytes;
       // K(j) is waited for only right before the first S that reads it, so a
       // late K never holds back the P.V products of tile j-1.
       auto wait_k = [&]() -> bool {
         if (k_ready) return true;
         const int gs = g0 + n;
-        if (!mbar_wait_warp(sm.k_full(gs % S), (gs / S) & 1, p.timeout_ns, p.status)) return false;
+        if (!mbar_wait_warp(sm.k_full(gs % SK), (gs / SK) & 1, p.timeout_ns, p.status)) return false;
         tc_fence_after();
         k_ready = true;
         return true;
@@ -443,68 +465,68 @@ __device__ __forceinline__ void mma_role(const TcParams& P, const Smem<D>& sm, u
         if (pv0) {
           if (!mbar_wait_warp(sm.p_full(0), pc[0] & 1, p.timeout_ns, p.status)) { ok = false; break; }
           tc_fence_after();
-          issue_pv<D, BF16>(sm, tmem, 0, vaddr, !first_pv[0]);
+          issue_pv<D, BF16, MB>(sm, tmem, 0, vaddr, !first_pv[0]);
           if (it.last(0, j - 1)) tc_commit_elect(sm.o_final(0));  // lane 0 has seen its last key tile
           first_pv[0] = false;
           ++pc[0];
         }
         if (s0) {
           if (!wait_k()) { ok = false; break; }
-          issue_qk<D, BF16>(sm, tmem, 0, 0, kaddr);
+          issue_qk<D, BF16, MB>(sm, tmem, 0, 0, kaddr);
         }
         __syncwarp();
         if (pv1) {
           if (!mbar_wait_warp(sm.p_full(1), pc[1] & 1, p.timeout_ns, p.status)) { ok = false; break; }
           tc_fence_after();
-          issue_pv<D, BF16>(sm, tmem, 1, vaddr, !first_pv[1]);
+          issue_pv<D, BF16, MB>(sm, tmem, 1, vaddr, !first_pv[1]);
           if (it.last(1, j - 1)) tc_commit_elect(sm.o_final(1));
           first_pv[1] = false;
           ++pc[1];
         }
         if (s1) {
           if (!wait_k()) { ok = false; break; }
-          issue_qk<D, BF16>(sm, tmem, 1, it.lanesplit ? 0 : 1, kaddr);
+          issue_qk<D, BF16, MB>(sm, tmem, 1, it.lanesplit ? 0 : 1, kaddr);
         }
         __syncwarp();
       } else {
       if (s0 && !pv0) {
         if (!wait_k()) { ok = false; break; }
-        issue_qk<D, BF16>(sm, tmem, 0, 0, kaddr);
+        issue_qk<D, BF16, MB>(sm, tmem, 0, 0, kaddr);
       }
       if (s1 && !pv1) {
         if (!wait_k()) { ok = false; break; }
-        issue_qk<D, BF16>(sm, tmem, 1, it.lanesplit ? 0 : 1, kaddr);
+        issue_qk<D, BF16, MB>(sm, tmem, 1, it.lanesplit ? 0 : 1, kaddr);
       }
       if (pv0) {
         if (!mbar_wait_warp(sm.p_full(0), pc[0] & 1, p.timeout_ns, p.status)) { ok = false; break; }
         tc_fence_after();
-        issue_pv<D, BF16>(sm, tmem, 0, vaddr, !first_pv[0]);
+        issue_pv<D, BF16, MB>(sm, tmem, 0, vaddr, !first_pv[0]);
         if (it.last(0, j - 1)) tc_commit_elect(sm.o_final(0));  // lane 0 has seen its last key tile
         first_pv[0] = false;
         ++pc[0];
         if (s0) {
           if (!wait_k()) { ok = false; break; }
-          issue_qk<D, BF16>(sm, tmem, 0, 0, kaddr);
+          issue_qk<D, BF16, MB>(sm, tmem, 0, 0, kaddr);
         }
       }
       if (pv1) {
         if (!mbar_wait_warp(sm.p_full(1), pc[1] & 1, p.timeout_ns, p.status)) { ok = false; break; }
         tc_fence_after();
-        issue_pv<D, BF16>(sm, tmem, 1, vaddr, !first_pv[1]);
+        issue_pv<D, BF16, MB>(sm, tmem, 1, vaddr, !first_pv[1]);
         if (it.last(1, j - 1)) tc_commit_elect(sm.o_final(1));
         first_pv[1] = false;
         ++pc[1];
         if (s1) {
           if (!wait_k()) { ok = false; break; }
-          issue_qk<D, BF16>(sm, tmem, 1, it.lanesplit ? 0 : 1, kaddr);
+          issue_qk<D, BF16, MB>(sm, tmem, 1, it.lanesplit ? 0 : 1, kaddr);
         }
       }
       }  // KSPLIT
       __syncwarp();
       if (!ok) break;
       // K(j) was read by this iteration's QK^T products, V(j-1) by its P.V
-      if (n < it.N) tc_commit_elect(sm.k_empty((g0 + n) % S));
-      if (n >= 1) tc_commit_elect(sm.v_empty((g0 + n - 1) % S));
+      if (n < it.N) tc_commit_elect(sm.k_empty((g0 + n) % SK));
+      if (n >= 1) tc_commit_elect(sm.v_empty((g0 + n - 1) % SV));
       // the item's last QK^T products are issued: Q may be replaced once they finish
       if (n == it.N - 1) tc_commit_elect(sm.q_empty());
       __syncwarp();
@@ -616,9 +638,9 @@ __device__ __forceinline__ void mask_chunk_read(float (&x)[BN], const uint8_t* b
 // ------------------------------------------------------------------ softmax
 // Warpgroup t (warps 4t..4t+3); thread = one query row of query tile t.
 template <int D, bool BF16, bool SOFTCAP, bool MASK, bool KSPLIT, bool SPLITKV>
-__device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& sm, uint32_t tmem,
+__device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D, MASK>& sm, uint32_t tmem,
                                              int n_items, int warp, int lane) {
-  using Cfg = TcConfig<D>;
+  using Cfg = TcConfig<D, MASK>;
   const CommonParams& p = P.c;
   const int t = warp >> 2;  // query tile of this warpgroup
   const int wq = warp & 3;  // TMEM lane quarter
@@ -957,12 +979,11 @@ __device__ __forceinline__ void softmax_role(const TcParams& P, const Smem<D>& s
 
 template <int D, bool BF16, bool SOFTCAP, bool MASK, bool KSPLIT, bool SPLITKV>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_constant__ TcParams P) {
-  using Cfg = TcConfig<D>;
-  constexpr int S = Cfg::kStages;
+  using Cfg = TcConfig<D, MASK>;
   const CommonParams& p = P.c;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  Smem<D> sm;
+  Smem<D, MASK> sm;
   sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm.base);
   sm.sQ = sbase + Cfg::kOffQ;
@@ -978,10 +999,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
   if (threadIdx.x == 0) {
     mbar_init(sm.q_full(), 1);
     mbar_init(sm.q_empty(), 1);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < Cfg::kKStages; ++s) {
       mbar_init(sm.k_full(s), 1);
-      mbar_init(sm.v_full(s), 1);
       mbar_init(sm.k_empty(s), 1);
+    }
+    for (int s = 0; s < Cfg::kVStages; ++s) {
+      mbar_init(sm.v_full(s), 1);
       mbar_init(sm.v_empty(s), 1);
     }
     for (int t = 0; t < kQTiles; ++t) {
@@ -1010,9 +1033,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
   if (warp == kTmaWarp) {
-    if (lane == 0) producer_role<D, KSPLIT>(P, sm, n_items);
+    if (lane == 0) producer_role<D, KSPLIT, MASK>(P, sm, n_items);
   } else if (warp == kMmaWarp) {
-    mma_role<D, BF16, KSPLIT>(P, sm, tmem, n_items, lane);
+    mma_role<D, BF16, KSPLIT, MASK>(P, sm, tmem, n_items, lane);
   } else {
     softmax_role<D, BF16, SOFTCAP, MASK, KSPLIT, SPLITKV>(P, sm, tmem, n_items, warp, lane);
   }
@@ -1028,7 +1051,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const __grid_c
 template <int D, bool BF16, bool SOFTCAP, bool MASK, bool KSPLIT, bool SPLITKV>
 cudaError_t launch_variant(const TcParams& P, cudaStream_t stream) {
   auto kernel = attn_fwd_tc_kernel<D, BF16, SOFTCAP, MASK, KSPLIT, SPLITKV>;
-  constexpr uint32_t smem = TcConfig<D>::kSmemBytes;
+  constexpr uint32_t smem = TcConfig<D, MASK>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
