@@ -47,16 +47,16 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # attn_fwd_splitkv entry), with the hash of that kernel's sources at the time;
 # reported as null once those sources change.
 NCU_TRAFFIC = {
-    "gqa_causal_bf16": {"bytes_per_launch": 127725056, "source_hash": "64665e6852457495"},
-    "window_softcap_bf16": {"bytes_per_launch": 396390912, "source_hash": "64665e6852457495"},
-    "ragged_kvcache_f16": {"bytes_per_launch": 48563968, "source_hash": "64665e6852457495"},
-    "dit_f32": {"bytes_per_launch": 57926656, "source_hash": "1a2421def8d9be91"},
-    "dit_f32+f32split": {"bytes_per_launch": 69472000, "source_hash": "2ef5be24af3dacb8"},
+    "gqa_causal_bf16": {"bytes_per_launch": 127968000, "source_hash": "d45751564600e637"},
+    "window_softcap_bf16": {"bytes_per_launch": 395893248, "source_hash": "d45751564600e637"},
+    "ragged_kvcache_f16": {"bytes_per_launch": 48668928, "source_hash": "d45751564600e637"},
+    "dit_f32": {"bytes_per_launch": 58309120, "source_hash": "7ebe6da14ee3c322"},
+    "dit_f32+f32split": {"bytes_per_launch": 69578496, "source_hash": "a413190c34ccf856"},
     "decode_bf16": {"bytes_per_launch": 775945472, "source_hash": "c05337b007be4581"},
     "decode_bf16+splitkv": {"bytes_per_launch": 777069568, "source_hash": "c05337b007be4581"},
-    "gqa_causal_bf16_d256": {"bytes_per_launch": 372647168, "source_hash": "d23f60cee55ca08d"},
-    "gqa_causal_bf16_d384": {"bytes_per_launch": 888843264, "source_hash": "d23f60cee55ca08d"},
-    "vae_f32_d384": {"bytes_per_launch": 18940672, "source_hash": "1a2421def8d9be91"},
+    "gqa_causal_bf16_d256": {"bytes_per_launch": 363525888, "source_hash": "7509e3c42009082f"},
+    "gqa_causal_bf16_d384": {"bytes_per_launch": 880826368, "source_hash": "7509e3c42009082f"},
+    "vae_f32_d384": {"bytes_per_launch": 18926336, "source_hash": "7ebe6da14ee3c322"},
     # the DSA indexer: the tile score kernel (the selection kernel's traffic is in its profile)
     "dsa_prefill_bf16": {"bytes_per_launch": 139367680, "source_hash": "4c0afd2437582ac7"},
     "dsa_decode_bf16": {"bytes_per_launch": 34638080, "source_hash": "4c0afd2437582ac7"},
