@@ -334,9 +334,10 @@ int fwd_impl(const void* q, const void* k, const void* v, const float* mask,
     lp.q = q;
     lp.c = c;
     lp.v_plane0 = 0;
-    const int key_box = D == 384 ? 32 : 64;  // keys per tile of the single-lane kernel
-    int rc = encode_map(&lp.tmap_k, k, bf16, (int64_t)B * Hkv, kv_capacity, D, key_box);
-    if (rc == ATTN_OK) rc = encode_map(&lp.tmap_v, v, bf16, (int64_t)B * Hkv, kv_capacity, D, key_box);
+    // 64-key tiles; at D = 384 V streams in 16-key units (one box of 16 rows)
+    const int v_box = D == 384 ? 16 : 64;
+    int rc = encode_map(&lp.tmap_k, k, bf16, (int64_t)B * Hkv, kv_capacity, D, 64);
+    if (rc == ATTN_OK) rc = encode_map(&lp.tmap_v, v, bf16, (int64_t)B * Hkv, kv_capacity, D, v_box);
     if (rc == ATTN_OK && D == 384) rc = encode_map(&lp.tmap_q, q, bf16, BHq, Sq, D);  // Q by TMA
     if (rc != ATTN_OK) return rc;
     e = launch_attn_lane16(lp, bf16, st);

@@ -7,32 +7,32 @@
 //     and three for P.V;
 //   - bf16 / f16 inputs with D = 256 or 384 (attn_lane16.cu): one piece
 //     each.  At D = 384, O alone takes 384 of the 512 tensor-memory columns,
-//     so Q goes to shared memory by TMA instead (QK^T as an SS-MMA) and key
-//     tiles hold 32 keys, which keeps Q, the K / V rings and the mask
-//     buffers within the 227 KB of shared memory a CTA may use.
+//     so Q goes to shared memory by TMA instead (QK^T as an SS-MMA, 96 KB),
+//     and K and V stream through their rings in units (K in 128-dim chunks
+//     of 16 KB, V in 16-key sub-tiles of 12 KB), which keeps Q, the rings
+//     and the mask buffers within the 227 KB of shared memory a CTA may use.
 //
 // The method is the tiled online softmax of "onnx-runtime-ep-cuda
 // 0.1.0-dev.5, src/kernels/flash_attention.rs" (module doc and
 // `flash_attention_body`): scores of one key tile at a time, running row
 // max and denominator, O rescaled when the max moves.  Work item = one
-// 128-row query tile of one (b, h); its key tiles (64 keys, 32 at D = 384)
-// run in order; key tile g of the CTA (counted over all its items) uses S
-// buffer g % SB.
+// 128-row query tile of one (b, h); its 64-key tiles run in order; key tile
+// g of the CTA (counted over all its items) uses S buffer g % SB.
 //   warps 0-3   softmax: thread = query row.  They write each item's Q rows
 //               (split into pieces for fp32) to tensor memory (except at
 //               D = 384) as soon as the previous item's last P is written,
 //               ahead of that item's epilogue.
-//   warp 4      TMA producer: the K pieces of key tile g into K slot g % KS
-//               and the V pieces into V slot g % VS, each ring with its own
-//               barriers, V one tile behind K; it also prefetches each
+//   warp 4      TMA producer: the K and V units of each key tile into their
+//               rings (unit u in slot u % KS or u % VS), each ring with its
+//               own barriers, V one tile behind K; it also prefetches each
 //               item's Q block into L2 (at D = 384: loads it into shared
 //               memory).
 //   warp 5      QK^T issuer (converged warp, elect.sync) and owner of tensor
 //               memory: S_g = Q K_g^T once K_g is in and the P.V of tile
 //               g - SB (whose P the buffer holds) has finished.
 //   warp 6      P.V issuer: O += P_g V_g once P_g is written.
-// Tensor memory (512 columns): Q pieces [0, KP D/2), SB S buffers 64 columns
-// apart (a 32-key tile uses half) from kColS, O (D columns) after them; P_b
+// Tensor memory (512 columns): Q pieces [0, KP D/2), SB S buffers of 64
+// columns from kColS, O (D columns) after them; P_b
 // over S_b (as VP bf16 / f16 pieces of FN / 2 columns).  Every barrier wait
 // is bounded; a timeout sets ATTN_ERR_TIMEOUT in the device status word and
 // the kernel drains and exits.
@@ -69,7 +69,7 @@ struct Cfg {
   static constexpr int KP = In<IN>::KP, VP = In<IN>::VP;
   // Q in shared memory (SS-MMA) when O leaves no tensor-memory room for it
   static constexpr bool kQSmem = IN != kInF32Split && D > 256;
-  static constexpr int FN = kQSmem ? 32 : 64;                  // keys per key tile
+  static constexpr int FN = 64;                                // keys per key tile
   static constexpr int kSub = D / 64;                          // 128-byte column blocks per row
   static constexpr uint32_t kSubBytes = FN * 128;              // [FN rows][64 cols] of 16-bit
   static constexpr uint32_t kPieceBytes = kSub * kSubBytes;    // one piece of one tile
@@ -77,12 +77,20 @@ struct Cfg {
   static constexpr uint32_t kVTileBytes = VP * kPieceBytes;
   static constexpr uint32_t kQSubBytes = FM * 128;             // [128 rows][64 cols] of 16-bit
   static constexpr uint32_t kQBytes = kQSmem ? kSub * kQSubBytes : 0;
-  // K and V have rings and barriers of their own.  A K slot is freed by its
-  // tile's QK^T, a V slot by its P.V about a tile later; the producer loads
-  // V one tile behind K.  Stages as shared memory allows: 4 / 5 at fp32
-  // D = 64, 2 / 3 at fp32 D = 128, 3 / 3 at D = 256, 2 / 3 at D = 384.
-  static constexpr int kKStages = kQSmem ? 2 : (kKTileBytes <= 24576 ? 4 : (IN == kInF32Split ? 2 : 3));
-  static constexpr int kVStages = (IN != kInF32Split && !kQSmem) ? kKStages : kKStages + 1;
+  // The K and V rings hold units: a whole key tile, or at D = 384 (whose Q
+  // takes 96 KB of shared memory) K in chunks of 128 dims (16 KB) and V in
+  // sub-tiles of 16 keys (12 KB), so that 64-key tiles still stream through
+  // a few slots.  A K unit is freed by its QK^T products, a V unit by its
+  // P.V products; the producer loads V one tile behind K.
+  static constexpr int kKUnits = kQSmem ? D / 128 : 1;         // K units per key tile
+  static constexpr int kVUnits = kQSmem ? FN / 16 : 1;         // V units per key tile
+  static constexpr uint32_t kKUnitBytes = kKTileBytes / kKUnits;
+  static constexpr uint32_t kVUnitBytes = kVTileBytes / kVUnits;
+  static constexpr uint32_t kVUnitSubBytes = kSubBytes / kVUnits;  // [16 rows][64 cols] at D = 384
+  // ring slots (units): 4 / 5 at fp32 D = 64, 2 / 3 at fp32 D = 128, 3 / 3 at
+  // D = 256, 4 / 4 at D = 384
+  static constexpr int kKStages = kQSmem ? 4 : (kKTileBytes <= 24576 ? 4 : (IN == kInF32Split ? 2 : 3));
+  static constexpr int kVStages = kQSmem ? 4 : (IN != kInF32Split ? kKStages : kKStages + 1);
   // S buffers: three where tensor memory has room for them (fp32 pieces),
   // else two.  Two MMA warps issue (QK^T and P.V), so that neither issuer's
   // barrier waits leave the tensor core without queued work.
@@ -93,8 +101,8 @@ struct Cfg {
   static constexpr uint32_t kMaskBufBytes = 32 * kMaskKeys * 4;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffK = kOffQ + kQBytes;
-  static constexpr uint32_t kOffV = kOffK + kKStages * kKTileBytes;
-  static constexpr uint32_t kOffMaskBuf = kOffV + kVStages * kVTileBytes;
+  static constexpr uint32_t kOffV = kOffK + kKStages * kKUnitBytes;
+  static constexpr uint32_t kOffMaskBuf = kOffV + kVStages * kVUnitBytes;
   static constexpr uint32_t kOffBar = kOffMaskBuf + 4 * kMaskBufBytes;
   // k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], q_full, q_empty,
   // s_full[SB], p_full[SB], s_free[SB], pv_done, o_final, drain
@@ -117,7 +125,7 @@ struct Smem {
   static constexpr int kB = 2 * KS + 2 * VS;  // first barrier after the rings
   uint8_t* base;
   uint32_t sQ, sK, sV, bar0;
-  // K of key tile g in K slot g % KS, V in V slot g % VS
+  // K unit u (counted over the CTA's key tiles) in K slot u % KS, V unit u in V slot u % VS
   __device__ uint32_t k_full(int s) const { return bar0 + 8u * s; }
   __device__ uint32_t k_empty(int s) const { return bar0 + 8u * (KS + s); }
   __device__ uint32_t v_full(int s) const { return bar0 + 8u * (2 * KS + s); }
@@ -214,17 +222,18 @@ __device__ __forceinline__ int f_item_of_round(int r, int n_items) {
 }
 
 // ------------------------------------------------------------------ producer
-// One thread.  Per key tile g: the K pieces into K slot g % KS (k_full) and
-// the V pieces into V slot g % VS (v_full).  A K slot is freed by its tile's
-// QK^T products, a V slot by its P.V products; since P.V runs about a tile
-// after QK^T, V is loaded one tile behind K, so a wait for a V slot never
-// holds back the next K.  At each item start it also prefetches the item's Q
-// rows into L2, so the softmax warps' Q loads come from L2.  K / V tiles are
-// read by every query tile of their kv head, Q and O once: K / V are loaded
-// as L2 evict_last, and the softmax warps read Q and write O as evict_first,
-// so a Q / O stream larger than L2 does not push K / V out between the query
-// tiles that share them (the prefetch keeps the default policy: an
-// evict_first prefetch measured a few MB more DRAM reads).
+// One thread.  Per key tile: its K units into the K ring (k_full) and its V
+// units into the V ring (v_full).  A K unit is freed by its QK^T products, a
+// V unit by its P.V products; since P.V runs about a tile after QK^T, V is
+// loaded one tile behind K, so a wait for a V slot never holds back the next
+// K.  At each item start it also prefetches the item's Q rows into L2, so
+// the softmax warps' Q loads come from L2 (at D = 384 it loads Q into shared
+// memory instead).  K / V tiles are read by every query tile of their kv
+// head, Q and O once: K / V are loaded as L2 evict_last, and the softmax
+// warps read Q and write O as evict_first, so a Q / O stream larger than L2
+// does not push K / V out between the query tiles that share them (the
+// prefetch keeps the default policy: an evict_first prefetch measured a few
+// MB more DRAM reads).
 template <int D, int IN>
 __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN>& sm, int n_items) {
   using C = Cfg<D, IN>;
@@ -236,24 +245,52 @@ __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN
   int g = 0;
   int q_items = 0;  // items whose Q was loaded into shared memory (kQSmem)
   const uint64_t keep = l2_evict_last_policy(), stream = l2_evict_first_policy();
-  int k_issued = 0, v_issued = 0;  // tiles whose K / V copies were started
+  int k_issued = 0, v_issued = 0;  // units whose K / V copies were started
   // fp32: K / V pieces come from the pre-pass grid; wait until it finished
   // (its writes are then visible).  Everything before this point, and Q,
   // is independent of it.
   if constexpr (IN == kInF32Split) asm volatile("griddepcontrol.wait;" ::: "memory");
-  // V of tile g - 1, not yet loaded: key0 and plane, or vplane < 0
-  int vkey0 = 0, vplane = -1;
-  auto load_v = [&](int gv) -> bool {
-    const int vs = gv % VS;
-    if (gv >= VS && !mbar_wait(sm.v_empty(vs), ((gv / VS) - 1) & 1, p.timeout_ns, p.status)) return false;
-    mbar_arrive_expect_tx(sm.v_full(vs), C::kVTileBytes);
-    ++v_issued;
-    for (int pc = 0; pc < VP; ++pc)
-      for (int s = 0; s < C::kSub; ++s)
-        tma_load_3d_hint(sm.sV + vs * C::kVTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_v,
-                         sm.v_full(vs), s * 64, vkey0, P.v_plane0 + pc * kvp + vplane, keep);
+  // K unit c of key tile gt (key0, kv plane) into K slot (gt kKUnits + c) % KS
+  auto load_k = [&](int gt, int c, int key0, int kv_plane) -> bool {
+    const int gu = gt * C::kKUnits + c, ks = gu % KS;
+    if (gu >= KS && !mbar_wait(sm.k_empty(ks), ((gu / KS) - 1) & 1, p.timeout_ns, p.status)) return false;
+    mbar_arrive_expect_tx(sm.k_full(ks), C::kKUnitBytes);
+    ++k_issued;
+    const uint32_t dst = sm.sK + ks * C::kKUnitBytes;
+    if constexpr (C::kKUnits == 1) {
+      for (int pc = 0; pc < KP; ++pc)
+        for (int s = 0; s < C::kSub; ++s)
+          tma_load_3d_hint(dst + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_k, sm.k_full(ks), s * 64, key0,
+                           pc * kvp + kv_plane, keep);
+    } else {
+      // dims [128 c, 128 c + 128): two 64-column blocks
+      for (int s = 0; s < 2; ++s)
+        tma_load_3d_hint(dst + s * C::kSubBytes, &P.tmap_k, sm.k_full(ks), (2 * c + s) * 64, key0, kv_plane, keep);
+    }
     return true;
   };
+  // V unit u of key tile gt into V slot (gt kVUnits + u) % VS
+  auto load_v = [&](int gt, int u, int key0, int kv_plane) -> bool {
+    const int gu = gt * C::kVUnits + u, vs = gu % VS;
+    if (gu >= VS && !mbar_wait(sm.v_empty(vs), ((gu / VS) - 1) & 1, p.timeout_ns, p.status)) return false;
+    mbar_arrive_expect_tx(sm.v_full(vs), C::kVUnitBytes);
+    ++v_issued;
+    const uint32_t dst = sm.sV + vs * C::kVUnitBytes;
+    if constexpr (C::kVUnits == 1) {
+      for (int pc = 0; pc < VP; ++pc)
+        for (int s = 0; s < C::kSub; ++s)
+          tma_load_3d_hint(dst + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_v, sm.v_full(vs), s * 64, key0,
+                           P.v_plane0 + pc * kvp + kv_plane, keep);
+    } else {
+      // keys [key0 + 16 u, + 16): kSub [16 rows][64 cols] blocks
+      for (int s = 0; s < C::kSub; ++s)
+        tma_load_3d_hint(dst + s * C::kVUnitSubBytes, &P.tmap_v, sm.v_full(vs), s * 64, key0 + 16 * u, kv_plane,
+                         keep);
+    }
+    return true;
+  };
+  // V of tile g - 1, not yet loaded: key0 and plane, or vplane < 0
+  int vkey0 = 0, vplane = -1;
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int idx = f_item_of_round(r, n_items);
@@ -276,27 +313,15 @@ __device__ __forceinline__ void f_producer(const LaneParams& P, const Smem<D, IN
     }
     const int kv_plane = it.b * p.Hkv + it.kvh;
     for (int n = 0; n < it.N; ++n, ++g) {
-      const int ks = g % KS;
       const int key0 = (it.tb + n) * FN;
-      if (g >= KS && !mbar_wait(sm.k_empty(ks), ((g / KS) - 1) & 1, p.timeout_ns, p.status)) {
-        ok = false;
-        break;
-      }
-      mbar_arrive_expect_tx(sm.k_full(ks), C::kKTileBytes);
-      ++k_issued;
-      for (int pc = 0; pc < KP; ++pc)
-        for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d_hint(sm.sK + ks * C::kKTileBytes + pc * C::kPieceBytes + s * C::kSubBytes, &P.tmap_k,
-                           sm.k_full(ks), s * 64, key0, pc * kvp + kv_plane, keep);
-      if (vplane >= 0 && !load_v(g - 1)) {
-        ok = false;
-        break;
-      }
+      for (int c = 0; c < C::kKUnits && ok; ++c) ok = load_k(g, c, key0, kv_plane);
+      for (int u = 0; u < C::kVUnits && ok && vplane >= 0; ++u) ok = load_v(g - 1, u, vkey0, vplane);
+      if (!ok) break;
       vkey0 = key0;
       vplane = kv_plane;
     }
   }
-  if (ok && vplane >= 0) ok = load_v(g - 1);
+  for (int u = 0; u < C::kVUnits && ok && vplane >= 0; ++u) ok = load_v(g - 1, u, vkey0, vplane);
   // Let every copy this thread started land before the CTA can exit.
   for (int n = (k_issued > KS ? k_issued - KS : 0); n < k_issued; ++n)
     mbar_wait(sm.k_full(n % KS), (n / KS) & 1, p.timeout_ns, p.status);
@@ -356,105 +381,137 @@ __device__ __forceinline__ void f_mma(const LaneParams& P, const Smem<D, IN>& sm
         // S = Q K_n^T (pieces: q0k0 + q0k1 + q1k0 + q0k2 + q1k1 + q2k0)
         const int gs = g0 + n;
         const int bs = gs % SB;
-        if (!mbar_wait_warp(sm.k_full(gs % KS), (gs / KS) & 1, p.timeout_ns, p.status)) { ok = false; break; }
-        if (gs >= SB && !mbar_wait_warp(sm.s_free(bs), ((gs / SB) - 1) & 1, p.timeout_ns, p.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t kb = sm.sK + (gs % KS) * C::kKTileBytes;
+        // Of the two waits before a tile's first products, the one measured
+        // to complete later goes last, so the products follow it at once:
+        // the buffer (s_free) with two S buffers, K with three.
+        auto wait_buffer = [&]() -> bool {
+          return gs < SB || mbar_wait_warp(sm.s_free(bs), ((gs / SB) - 1) & 1, p.timeout_ns, p.status);
+        };
+        if (SB == 3 && !wait_buffer()) { ok = false; break; }
         const uint32_t sd = tmem + C::kColS + 64 * bs;
-        if constexpr (KP == 3) {
-          uint64_t kd[3];
+        if constexpr (C::kKUnits == 1) {
+          const int ks = gs % KS;
+          if (!mbar_wait_warp(sm.k_full(ks), (gs / KS) & 1, p.timeout_ns, p.status)) { ok = false; break; }
+          if (SB != 3 && !wait_buffer()) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kb = sm.sK + ks * C::kKUnitBytes;
+          if constexpr (KP == 3) {
+            uint64_t kd[3];
 #pragma unroll
-          for (int pc = 0; pc < 3; ++pc) kd[pc] = make_sdesc_sw128(kb + pc * C::kPieceBytes, 16, 1024);
+            for (int pc = 0; pc < 3; ++pc) kd[pc] = make_sdesc_sw128(kb + pc * C::kPieceBytes, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            // K step kk: 32 bytes into a 128-byte row, 64-column blocks kSubBytes apart
-            const uint32_t off16 = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
-            const uint32_t q0 = tmem + C::kColQ + kk * 8, q1 = q0 + C::kQPiece, q2 = q0 + 2 * C::kQPiece;
-            mma_ts6_elect(sd, q0, kd[0] + off16, q0, kd[1] + off16, q1, kd[0] + off16, q0, kd[2] + off16,
-                          q1, kd[1] + off16, q2, kd[0] + off16, id_qk, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              // K step kk: 32 bytes into a 128-byte row, 64-column blocks kSubBytes apart
+              const uint32_t off16 = ((kk >> 2) * C::kSubBytes + (kk & 3) * 32) >> 4;
+              const uint32_t q0 = tmem + C::kColQ + kk * 8, q1 = q0 + C::kQPiece, q2 = q0 + 2 * C::kQPiece;
+              mma_ts6_elect(sd, q0, kd[0] + off16, q0, kd[1] + off16, q1, kd[0] + off16, q0, kd[2] + off16,
+                            q1, kd[1] + off16, q2, kd[0] + off16, id_qk, kk > 0 ? 1u : 0u);
+            }
+          } else {
+            const uint64_t kd = make_sdesc_sw128(kb, 16, 1024);
+            // K steps 4s..4s+3 lie in 64-column block s
+#pragma unroll
+            for (int s = 0; s < D / 64; ++s) {
+              const uint32_t o = (s * C::kSubBytes) >> 4;
+              const uint32_t q = tmem + C::kColQ + s * 32;
+              mma_ts4_elect(sd, q, kd + o, q + 8, kd + o + 2, q + 16, kd + o + 4, q + 24, kd + o + 6, id_qk,
+                            s > 0 ? 1u : 0u);
+            }
           }
-        } else if constexpr (C::kQSmem) {
-          // Q and K both K-major in shared memory; K steps 4s..4s+3 lie in
-          // 64-column block s of each (blocks kQSubBytes / kSubBytes apart)
-          const uint64_t qd = make_sdesc_sw128(sm.sQ, 16, 1024);
-          const uint64_t kd = make_sdesc_sw128(kb, 16, 1024);
-#pragma unroll
-          for (int s = 0; s < D / 64; ++s) {
-            const uint32_t oq = (s * C::kQSubBytes) >> 4, okk = (s * C::kSubBytes) >> 4;
-            mma_ss4_elect(sd, qd + oq, kd + okk, qd + oq + 2, kd + okk + 2, qd + oq + 4, kd + okk + 4,
-                          qd + oq + 6, kd + okk + 6, id_qk, s > 0 ? 1u : 0u);
-          }
+          tc_commit_elect(sm.k_empty(ks));
         } else {
-          const uint64_t kd = make_sdesc_sw128(kb, 16, 1024);
-          // K steps 4s..4s+3 lie in 64-column block s
+          // D = 384: Q and K both K-major in shared memory.  K unit c holds
+          // dims [128 c, 128 c + 128) as two 64-column blocks (kSubBytes
+          // apart); Q's 64-column blocks are kQSubBytes apart.  Each unit is
+          // freed as soon as its products finish.
+          const uint64_t qd = make_sdesc_sw128(sm.sQ, 16, 1024);
 #pragma unroll
-          for (int s = 0; s < D / 64; ++s) {
-            const uint32_t o = (s * C::kSubBytes) >> 4;
-            const uint32_t q = tmem + C::kColQ + s * 32;
-            mma_ts4_elect(sd, q, kd + o, q + 8, kd + o + 2, q + 16, kd + o + 4, q + 24, kd + o + 6, id_qk,
-                          s > 0 ? 1u : 0u);
+          for (int c = 0; c < C::kKUnits; ++c) {
+            const int gu = gs * C::kKUnits + c, ks = gu % KS;
+            if (!mbar_wait_warp(sm.k_full(ks), (gu / KS) & 1, p.timeout_ns, p.status)) { ok = false; break; }
+            if (SB != 3 && c == 0 && !wait_buffer()) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t kd = make_sdesc_sw128(sm.sK + ks * C::kKUnitBytes, 16, 1024);
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              const uint32_t oq = ((2 * c + s) * C::kQSubBytes) >> 4, okk = (s * C::kSubBytes) >> 4;
+              mma_ss4_elect(sd, qd + oq, kd + okk, qd + oq + 2, kd + okk + 2, qd + oq + 4, kd + okk + 4,
+                            qd + oq + 6, kd + okk + 6, id_qk, (c > 0 || s > 0) ? 1u : 0u);
+            }
+            tc_commit_elect(sm.k_empty(ks));
           }
+          if (!ok) break;
         }
         tc_commit_elect(sm.s_full(bs));
-        tc_commit_elect(sm.k_empty(gs % KS));
         // the item's last QK^T products are issued: Q may be replaced once they finish
         if (n == it.N - 1) tc_commit_elect(sm.q_empty());
       }
       if (kPV && n >= 1) {
-        // O (+)= P_{n-1} V_{n-1} (pieces: p0 v0 + p0 v1 + p1 v0)
+        // O (+)= P_{n-1} V_{n-1} (pieces: p0 v0 + p0 v1 + p1 v0), V unit by unit
         const int m = n - 1;
         const int gv = g0 + m;
         const int bp = gv % SB;
-        if (!mbar_wait_warp(sm.v_full(gv % VS), (gv / VS) & 1, p.timeout_ns, p.status)) { ok = false; break; }
-        if (!mbar_wait_warp(sm.p_full(bp), pb[bp] & 1, p.timeout_ns, p.status)) { ok = false; break; }
-        ++pb[bp];
-        const uint32_t vb = sm.sV + (gv % VS) * C::kVTileBytes;
-        if constexpr (IN != kInF32Split) {
-          const int64_t key0 = (int64_t)(it.tb + m) * FN;
-          if (zero_from < key0 + FN && zero_from < (int64_t)p.kv_capacity) {
-            const int r0 = zero_from > key0 ? (int)(zero_from - key0) : 0;
-            const int chunks = (FN - r0) * 8;  // 16-byte chunks of whole 128-byte rows
-            for (int s = 0; s < C::kSub; ++s) {
-              uint8_t* blk = sm.base + C::kOffV + (gv % VS) * C::kVTileBytes + s * C::kSubBytes;
-              for (int c = lane; c < chunks; c += 32)
-                *reinterpret_cast<uint4*>(blk + (size_t)(r0 + (c >> 3)) * 128 + (c & 7) * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
-        }
-        tc_fence_after();
-        // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B apart,
-        // 64-column blocks kSubBytes apart
-        const uint64_t d0 = make_sdesc_sw128(vb, C::kSubBytes, 1024);
         const uint32_t pa = tmem + C::kColS + 64 * bp;  // P piece t over 32 columns from pa + 32 t
-        if constexpr (VP == 2) {
-          const uint64_t d1 = make_sdesc_sw128(vb + C::kPieceBytes, C::kSubBytes, 1024);
-          // two K steps (16 keys each, 2048 bytes of V apart) per issue block
+        // P and the first V unit, the one measured to complete later last:
+        // V with the fp32 pieces (three S buffers), P otherwise
+        auto wait_p = [&]() -> bool {
+          if (!mbar_wait_warp(sm.p_full(bp), pb[bp] & 1, p.timeout_ns, p.status)) return false;
+          ++pb[bp];
+          return true;
+        };
+        if (SB == 3 && !wait_p()) { ok = false; break; }
+        constexpr int kUKeys = FN / C::kVUnits;          // keys per V unit
+        const int64_t key0 = (int64_t)(it.tb + m) * FN;
 #pragma unroll
-          for (int kk = 0; kk < FN / 16; kk += 2) {
-            const uint32_t o0 = (uint32_t)(kk * 2048) >> 4, o1 = (uint32_t)((kk + 1) * 2048) >> 4;
-            mma_ts6_elect(tmem + C::kColO, pa + kk * 8, d0 + o0, pa + kk * 8, d1 + o0, pa + 32 + kk * 8, d0 + o0,
-                          pa + (kk + 1) * 8, d0 + o1, pa + (kk + 1) * 8, d1 + o1, pa + 32 + (kk + 1) * 8,
-                          d0 + o1, id_pv, (m == 0 && kk == 0) ? 0u : 1u);
+        for (int u = 0; u < C::kVUnits; ++u) {
+          const int gu = gv * C::kVUnits + u, vs = gu % VS;
+          if (!mbar_wait_warp(sm.v_full(vs), (gu / VS) & 1, p.timeout_ns, p.status)) { ok = false; break; }
+          if (SB != 3 && u == 0 && !wait_p()) { ok = false; break; }
+          const uint32_t vb = sm.sV + vs * C::kVUnitBytes;
+          if constexpr (IN != kInF32Split) {
+            const int64_t ukey0 = key0 + u * kUKeys;
+            if (zero_from < ukey0 + kUKeys && zero_from < (int64_t)p.kv_capacity) {
+              const int r0 = zero_from > ukey0 ? (int)(zero_from - ukey0) : 0;
+              const int chunks = (kUKeys - r0) * 8;  // 16-byte chunks of whole 128-byte rows
+              for (int s = 0; s < C::kSub; ++s) {
+                uint8_t* blk = sm.base + C::kOffV + vs * C::kVUnitBytes + s * C::kVUnitSubBytes;
+                for (int c = lane; c < chunks; c += 32)
+                  *reinterpret_cast<uint4*>(blk + (size_t)(r0 + (c >> 3)) * 128 + (c & 7) * 16) =
+                      make_uint4(0u, 0u, 0u, 0u);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+            }
           }
-        } else if constexpr (D > 256) {
-          // 32 keys = two K steps (2048 bytes of V apart); columns [0, 256)
-          // from V blocks 0-3, [256, D) from blocks 4.. into O + 256
-          const uint64_t d1 = make_sdesc_sw128(vb + 4 * C::kSubBytes, C::kSubBytes, 1024);
-          static_assert(FN == 32, "two K steps per key tile");
-          mma_ts2x2_elect(tmem + C::kColO, tmem + C::kColO + 256, pa, pa + 8, d0, d0 + 128, d1, d1 + 128, id_pv,
-                          id_pv1, m == 0 ? 0u : 1u);
-        } else {
-          static_assert(FN == 64, "four K steps per key tile");
-          mma_ts4_elect(tmem + C::kColO, pa, d0, pa + 8, d0 + 128, pa + 16, d0 + 256, pa + 24, d0 + 384, id_pv,
-                        m == 0 ? 0u : 1u);
+          tc_fence_after();
+          // B = V[keys 16kk.., 0..D): MN-major; 8-key groups 1024 B apart,
+          // 64-column blocks kVUnitSubBytes apart
+          const uint64_t d0 = make_sdesc_sw128(vb, C::kVUnitSubBytes, 1024);
+          if constexpr (VP == 2) {
+            const uint64_t d1 = make_sdesc_sw128(vb + C::kPieceBytes, C::kSubBytes, 1024);
+            // two K steps (16 keys each, 2048 bytes of V apart) per issue block
+#pragma unroll
+            for (int kk = 0; kk < FN / 16; kk += 2) {
+              const uint32_t o0 = (uint32_t)(kk * 2048) >> 4, o1 = (uint32_t)((kk + 1) * 2048) >> 4;
+              mma_ts6_elect(tmem + C::kColO, pa + kk * 8, d0 + o0, pa + kk * 8, d1 + o0, pa + 32 + kk * 8, d0 + o0,
+                            pa + (kk + 1) * 8, d0 + o1, pa + (kk + 1) * 8, d1 + o1, pa + 32 + (kk + 1) * 8,
+                            d0 + o1, id_pv, (m == 0 && kk == 0) ? 0u : 1u);
+            }
+          } else if constexpr (D > 256) {
+            // one K step (16 keys): columns [0, 256) from V blocks 0-3 (N = 256),
+            // [256, D) from blocks 4.. into O + 256
+            const uint64_t d1 = make_sdesc_sw128(vb + 4 * C::kVUnitSubBytes, C::kVUnitSubBytes, 1024);
+            const uint32_t acc = (m == 0 && u == 0) ? 0u : 1u;
+            mma_ts_elect(tmem + C::kColO, pa + 8 * u, d0, id_pv, acc);
+            mma_ts_elect(tmem + C::kColO + 256, pa + 8 * u, d1, id_pv1, acc);
+          } else {
+            static_assert(FN == 64, "four K steps per key tile");
+            mma_ts4_elect(tmem + C::kColO, pa, d0, pa + 8, d0 + 128, pa + 16, d0 + 256, pa + 24, d0 + 384, id_pv,
+                          m == 0 ? 0u : 1u);
+          }
+          tc_commit_elect(sm.v_empty(vs));
         }
-        tc_commit_elect(sm.v_empty(gv % VS));
+        if (!ok) break;
         tc_commit_elect(sm.s_free(bp));
         tc_commit_elect(sm.pv_done());
         if (m == it.N - 1) tc_commit_elect(sm.o_final());  // the item's last P.V

@@ -11,9 +11,9 @@
 // K and V tiles come straight from the caller's tensors by TMA; V rows past
 // the valid length are zeroed in shared memory before the P.V products.
 // For D = 384 (the page's widest variant) O takes 384 columns, so Q moves to
-// shared memory (by TMA, read by an SS-MMA), two 32-column S buffers sit
-// below O, key tiles hold 32 keys, and the P.V product runs as N = 256 and
-// N = 128 parts.
+// shared memory (by TMA, read by an SS-MMA), two 64-column S buffers sit
+// below O, K and V stream in units (128-dim K chunks, 16-key V sub-tiles),
+// and each 16-key step of P.V runs as N = 256 and N = 128 parts.
 #include "attn_lane1.cuh"
 
 namespace gb300_attn {
