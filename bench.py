@@ -51,11 +51,11 @@ NCU_TRAFFIC = {
     "window_softcap_bf16": {"bytes_per_launch": 395893248, "source_hash": "d45751564600e637"},
     "ragged_kvcache_f16": {"bytes_per_launch": 48668928, "source_hash": "d45751564600e637"},
     "dit_f32": {"bytes_per_launch": 58309120, "source_hash": "7ebe6da14ee3c322"},
-    "dit_f32+f32split": {"bytes_per_launch": 69578496, "source_hash": "a413190c34ccf856"},
+    "dit_f32+f32split": {"bytes_per_launch": 69670144, "source_hash": "d1b6b5d41e1fa827"},
     "decode_bf16": {"bytes_per_launch": 775945472, "source_hash": "c05337b007be4581"},
     "decode_bf16+splitkv": {"bytes_per_launch": 777069568, "source_hash": "c05337b007be4581"},
-    "gqa_causal_bf16_d256": {"bytes_per_launch": 363525888, "source_hash": "7509e3c42009082f"},
-    "gqa_causal_bf16_d384": {"bytes_per_launch": 880826368, "source_hash": "7509e3c42009082f"},
+    "gqa_causal_bf16_d256": {"bytes_per_launch": 364062720, "source_hash": "ef80f339777c4d37"},
+    "gqa_causal_bf16_d384": {"bytes_per_launch": 872332032, "source_hash": "ef80f339777c4d37"},
     "vae_f32_d384": {"bytes_per_launch": 18926336, "source_hash": "7ebe6da14ee3c322"},
     # the DSA indexer: the tile score kernel (the selection kernel's traffic is in its profile)
     "dsa_prefill_bf16": {"bytes_per_launch": 139367680, "source_hash": "4c0afd2437582ac7"},
