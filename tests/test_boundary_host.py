@@ -277,3 +277,45 @@ def test_dsa_binding_rejects_bad_tensors():
         attn.dsa_index_select(q, k[:, :4], w, b, top_k=2, scale=1.0)        # T mismatch
     with pytest.raises(ValueError):
         attn.dsa_index_select(q[0], k, w, b, top_k=2, scale=1.0)            # rank
+
+
+# attn_fwd_host: host buffers (fake addresses: never read before validation
+# passes) plus device buffers of the same sizes
+HQ, HK, HV, HOUT, HMASK, HTOT, HPAST = (0x11000000, 0x21000000, 0x31000000, 0x41000000, 0x51000000,
+                                        0x61000000, 0x71000000)
+
+
+def call_host(lib, hmask=None, htot=None, hpast=None, **kw):
+    a = dict(GOOD, **kw)
+    copied = (ctypes.c_uint64 * 2)(7, 7)
+    rc = lib.attn_fwd_host(HQ, HK, HV, hmask, htot, hpast, HOUT,
+                           a["q"], a["k"], a["v"], a["mask"], a["total"], a["past"], a["out"],
+                           a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Sk"], a["cap"], a["D"], a["causal"],
+                           a["window"], a["scale"], a["softcap"], a["layout"], a["planes"], a["dtype"],
+                           None, copied)
+    return rc, (copied[0], copied[1])
+
+
+@pytest.mark.parametrize("case", ["dtype", "Hq_not_multiple", "Sk_over_capacity", "nan_scale",
+                                  "bad_plane_count", "out_overlaps_q", "null_out"])
+def test_host_entry_validates_like_attn_fwd(lib, case):
+    """attn_fwd_host checks the whole problem as attn_fwd would, on its device
+    buffers, before any copy or CUDA call; nothing is reported copied."""
+    kw = dict(INVALID[case])
+    hm = HMASK if kw.get("mask") else None
+    rc, copied = call_host(lib, hmask=hm, **kw)
+    assert rc == attn.ATTN_ERR_INVALID_ARG
+    assert copied == (0, 0)
+
+
+def test_host_entry_pairs_host_and_device_buffers(lib):
+    """A mask or length array must be given on both sides or on neither."""
+    assert call_host(lib, hmask=HMASK)[0] == attn.ATTN_ERR_INVALID_ARG          # no device mask
+    assert call_host(lib, mask=MASK, planes=2)[0] == attn.ATTN_ERR_INVALID_ARG  # no host mask
+    assert call_host(lib, htot=HTOT)[0] == attn.ATTN_ERR_INVALID_ARG
+    assert call_host(lib, past=PAST)[0] == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_host_entry_unsupported_and_empty(lib):
+    assert call_host(lib, D=96)[0] == attn.ATTN_ERR_UNSUPPORTED
+    assert call_host(lib, B=0, q=None, k=None, v=None, out=None) == (attn.ATTN_OK, (0, 0))
