@@ -275,28 +275,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Warp-collective forms: every lane of the warp executes the call and one
 // lane, chosen by elect.sync (the lowest active lane, so always the same one
 // for a converged warp), issues the instruction.  Keeping the issuing warp
@@ -379,24 +357,6 @@ __device__ __forceinline__ void mma_ts6_elect(uint32_t d, uint32_t a0, uint64_t 
       "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%11], %12, %13, 1;\n\t}" ::"r"(d),
       "r"(a0), "l"(b0), "r"(a1), "l"(b1), "r"(a2), "l"(b2), "r"(a3), "l"(b3), "r"(a4), "l"(b4),
       "r"(a5), "l"(b5), "r"(idesc), "r"(acc0)
-      : "memory");
-}
-
-// Two K steps of a product whose N is split in two parts (N = 384 as 256 +
-// 128: one MMA's N is at most 256), A in tensor memory: part j of step k is
-// D_j (+)= A_k B_jk with instruction descriptor id_j.
-__device__ __forceinline__ void mma_ts2x2_elect(uint32_t d0, uint32_t d1, uint32_t a0, uint32_t a1,
-                                                uint64_t b00, uint64_t b01, uint64_t b10, uint64_t b11,
-                                                uint32_t id0, uint32_t id1, uint32_t acc0) {
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "elect.sync _|p, 0xffffffff;\n\t"
-      "setp.ne.b32 q, %10, 0;\n\t"
-      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %4, %8, q;\n\t"
-      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %6, %9, q;\n\t"
-      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %5, %8, 1;\n\t"
-      "@p tcgen05.mma.cta_group::1.kind::f16 [%1], [%3], %7, %9, 1;\n\t}" ::"r"(d0),
-      "r"(d1), "r"(a0), "r"(a1), "l"(b00), "l"(b01), "l"(b10), "l"(b11), "r"(id0), "r"(id1), "r"(acc0)
       : "memory");
 }
 
