@@ -276,6 +276,14 @@ __device__ __forceinline__ float min128(const float (&x)[BN]) {
   return fminf(fmin3(m[0], m[1], m[2]), fmin3(m[3], m[4], fmin3(m[5], m[6], m[7])));
 }
 
+// Prefetch of one box of a 3-D tensor map into L2 (no shared memory, no
+// completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(c0),
+               "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // ------------------------------------------------------------------ producer
 // One thread.  Q tiles per item (after the previous item's QK^T products
 // released them), then the item's K / V tiles into the stage ring; the ring
@@ -297,11 +305,19 @@ __device__ __forceinline__ void producer_role(const TcParams& P, const Smem<D, M
     if (idx < 0) break;
     const Item it = make_item<KSPLIT>(p, idx, border);
     if (it.N == 0) continue;
-    if (q_items > 0 && !mbar_wait(sm.q_empty(), (q_items - 1) & 1, p.timeout_ns, p.status)) break;
     const int q_plane = it.b * p.Hq + it.h;
     const int kv_plane = it.b * p.Hkv + it.kvh;
     // a lane-split item's two lanes share query tile 0's rows: one Q tile
     const int nq = it.lanesplit ? 1 : kQTiles;
+    // This point is reached once the previous item's K / V are all issued,
+    // a few key tiles before its last QK^T frees the Q buffer: the Q rows go
+    // into L2 now, so the load below (which a whole item boundary waits for)
+    // does not wait on DRAM.  Key-split items are a few key tiles long, too
+    // short for the prefetch to run ahead (measured slightly slower there).
+    if (!KSPLIT && q_items > 0)
+      for (int t = 0; t < nq; ++t)
+        for (int s = 0; s < Cfg::kSub; ++s) tma_prefetch_l2_3d(&P.tmap_q, s * 64, (int)it.row0(t), q_plane);
+    if (q_items > 0 && !mbar_wait(sm.q_empty(), (q_items - 1) & 1, p.timeout_ns, p.status)) break;
     mbar_arrive_expect_tx(sm.q_full(), nq * Cfg::kTileBytes);
     for (int t = 0; t < nq; ++t)
       for (int s = 0; s < Cfg::kSub; ++s)
