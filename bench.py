@@ -47,19 +47,19 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # attn_fwd_splitkv entry), with the hash of that kernel's sources at the time;
 # reported as null once those sources change.
 NCU_TRAFFIC = {
-    "gqa_causal_bf16": {"bytes_per_launch": 127968000, "source_hash": "d45751564600e637"},
-    "window_softcap_bf16": {"bytes_per_launch": 395893248, "source_hash": "d45751564600e637"},
-    "ragged_kvcache_f16": {"bytes_per_launch": 48668928, "source_hash": "d45751564600e637"},
-    "dit_f32": {"bytes_per_launch": 58309120, "source_hash": "7ebe6da14ee3c322"},
-    "dit_f32+f32split": {"bytes_per_launch": 69670144, "source_hash": "d1b6b5d41e1fa827"},
-    "decode_bf16": {"bytes_per_launch": 775945472, "source_hash": "c05337b007be4581"},
-    "decode_bf16+splitkv": {"bytes_per_launch": 777069568, "source_hash": "c05337b007be4581"},
-    "gqa_causal_bf16_d256": {"bytes_per_launch": 364062720, "source_hash": "ef80f339777c4d37"},
-    "gqa_causal_bf16_d384": {"bytes_per_launch": 872332032, "source_hash": "ef80f339777c4d37"},
-    "vae_f32_d384": {"bytes_per_launch": 18926336, "source_hash": "7ebe6da14ee3c322"},
+    "gqa_causal_bf16": {"bytes_per_launch": 127417600, "source_hash": "8b5647f515ca3d4a"},
+    "window_softcap_bf16": {"bytes_per_launch": 397537536, "source_hash": "8b5647f515ca3d4a"},
+    "ragged_kvcache_f16": {"bytes_per_launch": 48649472, "source_hash": "8b5647f515ca3d4a"},
+    "dit_f32": {"bytes_per_launch": 58648064, "source_hash": "abe01510bfbba6a1"},
+    "dit_f32+f32split": {"bytes_per_launch": 69517568, "source_hash": "297cd19ddfb9bc7b"},
+    "decode_bf16": {"bytes_per_launch": 775977216, "source_hash": "9febafcf1e6362f3"},
+    "decode_bf16+splitkv": {"bytes_per_launch": 777591040, "source_hash": "9febafcf1e6362f3"},
+    "gqa_causal_bf16_d256": {"bytes_per_launch": 365990656, "source_hash": "c52d466f411cd530"},
+    "gqa_causal_bf16_d384": {"bytes_per_launch": 884027136, "source_hash": "c52d466f411cd530"},
+    "vae_f32_d384": {"bytes_per_launch": 18926336, "source_hash": "abe01510bfbba6a1"},
     # the DSA indexer: the tile score kernel (the selection kernel's traffic is in its profile)
-    "dsa_prefill_bf16": {"bytes_per_launch": 139367680, "source_hash": "4c0afd2437582ac7"},
-    "dsa_decode_bf16": {"bytes_per_launch": 34638080, "source_hash": "4c0afd2437582ac7"},
+    "dsa_prefill_bf16": {"bytes_per_launch": 139097088, "source_hash": "fda2993782a35635"},
+    "dsa_decode_bf16": {"bytes_per_launch": 34638080, "source_hash": "fda2993782a35635"},
 }
 
 
