@@ -22,6 +22,11 @@
 // structure"); columns past D are zero in shared memory and never stored.
 // Q, a K tile, a V tile and P must fit in shared memory: BN = 64 keys up to
 // DP = 256 (211 KB), 32 keys at DP = 384 (203 KB).
+// With one 256-thread CTA per SM nothing else covers a tile's load latency,
+// so the loads run under the arithmetic: V of tile t is requested (cp.async,
+// global -> shared, no registers) before S of tile t is computed, and K of
+// tile t + 1 before the P.V products of tile t; each buffer is rewritten only
+// after the barrier that ends its last reads.
 #include "device_common.cuh"
 
 namespace gb300_attn {
@@ -72,6 +77,35 @@ __device__ __forceinline__ void load_rows(float* dst, int sstride, const float* 
       dst[r * sstride + c] = v;
     }
   }
+}
+
+// The same rows as load_rows, as 16-byte cp.async copies (rows of whole
+// 16-byte chunks: D % 4 == 0 and 16-byte aligned planes), zero-filled outside
+// the valid rows and past D; one commit group per call.  Without vec4 the
+// rows are loaded synchronously, and the barrier before their first use makes
+// them visible all the same.
+template <int DP>
+__device__ __forceinline__ void load_rows_async(float* dst, int sstride, const float* src, int64_t row0,
+                                                int nrows, int64_t valid_rows, int D, bool vec4) {
+  if (!vec4) {
+    load_rows<DP>(dst, sstride, src, row0, nrows, valid_rows, D, false);
+    return;
+  }
+  constexpr int kVecPerRow = DP / 4;
+  for (int idx = threadIdx.x; idx < nrows * kVecPerRow; idx += kThreads) {
+    const int r = idx / kVecPerRow;
+    const int c = (idx % kVecPerRow) * 4;
+    const bool valid = row0 + r < valid_rows && c < D;
+    const float* g = valid ? src + (row0 + r) * (int64_t)D + c : src;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst + r * sstride + c)), "l"(g),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void async_rows_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 template <int DP, int RI, bool SOFTCAP, bool MASK>
@@ -135,12 +169,14 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
       for (int u = 0; u < 4; ++u) o[i][g][u] = 0.f;
   }
 
+  if (T.t_begin < T.t_end)
+    load_rows_async<DP>(Ks, Cfg::kKStride, kplane, (int64_t)T.t_begin * BN, BN, zero_from, D, vec4);
   for (int t = T.t_begin; t < T.t_end; ++t) {
     const int64_t key0 = (int64_t)t * BN;
-    __syncthreads();  // previous tile's K / V / P no longer in use
-    load_rows<DP>(Ks, Cfg::kKStride, kplane, key0, BN, zero_from, D, vec4);
-    load_rows<DP>(Vs, Cfg::kVStride, vplane, key0, BN, zero_from, D, vec4);
-    __syncthreads();
+    const bool more = t + 1 < T.t_end;
+    async_rows_wait<0>();  // this thread's copies of K(t)
+    __syncthreads();       // K(t) (and Q) visible; the previous tile's P.V no longer reads V / P
+    load_rows_async<DP>(Vs, Cfg::kVStride, vplane, key0, BN, zero_from, D, vec4);
 
     // S = Q K^T for this thread's RI x KJ block
     float s[RI][KJ];
@@ -220,7 +256,11 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
 #pragma unroll
       for (int j = 0; j < KJ; ++j) Ps[(ty + 16 * i) * Cfg::kPStride + tx + 16 * j] = s[i][j];
     }
-    __syncthreads();
+    __syncthreads();  // P complete; S no longer reads K
+    if (more) load_rows_async<DP>(Ks, Cfg::kKStride, kplane, key0 + BN, BN, zero_from, D, vec4);
+    if (more) async_rows_wait<1>();  // V(t) landed; K(t + 1) may still be in flight
+    else async_rows_wait<0>();
+    __syncthreads();  // V(t) visible
 
     // O += P V
 #pragma unroll 2
