@@ -50,6 +50,13 @@ struct F32Config {
   static constexpr size_t kSmemFloats =
       (size_t)BMr * kQStride + (size_t)BN * kKStride + (size_t)BN * kVStride + (size_t)BMr * kPStride;
   static constexpr size_t kSmemBytes = kSmemFloats * sizeof(float);
+  // Head dims up to 128: the register budget of one CTA per SM (which shared
+  // memory allows anyway) and deeper unrolling of both product loops, so more
+  // shared-memory loads are in flight (measured 2.6% faster on DiT; at 256 and
+  // 384 the compiler's own choice measured faster).
+  static constexpr int kMinBlocks = DP <= 128 ? 1 : 0;
+  static constexpr int kUnrollS = DP <= 128 ? 8 : 4;
+  static constexpr int kUnrollPV = DP <= 128 ? 4 : 2;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
@@ -109,7 +116,7 @@ __device__ __forceinline__ void async_rows_wait() {
 }
 
 template <int DP, int RI, bool SOFTCAP, bool MASK>
-__global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_constant__ F32Params P) {
+__global__ void __launch_bounds__(kThreads, F32Config<DP, RI>::kMinBlocks) attn_fwd_f32_kernel(const __grid_constant__ F32Params P) {
   using Cfg = F32Config<DP, RI>;
   constexpr int BM = Cfg::BMr;
   constexpr int BN = Cfg::BN;
@@ -184,7 +191,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
     for (int i = 0; i < RI; ++i)
 #pragma unroll
       for (int j = 0; j < KJ; ++j) s[i][j] = 0.f;
-#pragma unroll 4
+#pragma unroll Cfg::kUnrollS
     for (int d0 = 0; d0 < DP; d0 += 4) {
       float4 qa[RI], kb[KJ];
 #pragma unroll
@@ -263,7 +270,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const __grid_con
     __syncthreads();  // V(t) visible
 
     // O += P V
-#pragma unroll 2
+#pragma unroll Cfg::kUnrollPV
     for (int k0 = 0; k0 < BN; k0 += 4) {
       float4 pa[RI];
 #pragma unroll
