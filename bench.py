@@ -50,13 +50,13 @@ NCU_TRAFFIC = {
     "gqa_causal_bf16": {"bytes_per_launch": 127417600, "source_hash": "8b5647f515ca3d4a"},
     "window_softcap_bf16": {"bytes_per_launch": 397537536, "source_hash": "8b5647f515ca3d4a"},
     "ragged_kvcache_f16": {"bytes_per_launch": 48649472, "source_hash": "8b5647f515ca3d4a"},
-    "dit_f32": {"bytes_per_launch": 58392576, "source_hash": "d78c720db74a9627"},
+    "dit_f32": {"bytes_per_launch": 57792000, "source_hash": "8808934b75c1e438"},
     "dit_f32+f32split": {"bytes_per_launch": 69517568, "source_hash": "297cd19ddfb9bc7b"},
     "decode_bf16": {"bytes_per_launch": 775977216, "source_hash": "9febafcf1e6362f3"},
     "decode_bf16+splitkv": {"bytes_per_launch": 777591040, "source_hash": "9febafcf1e6362f3"},
     "gqa_causal_bf16_d256": {"bytes_per_launch": 365990656, "source_hash": "c52d466f411cd530"},
     "gqa_causal_bf16_d384": {"bytes_per_launch": 884027136, "source_hash": "c52d466f411cd530"},
-    "vae_f32_d384": {"bytes_per_launch": 18931200, "source_hash": "d78c720db74a9627"},
+    "vae_f32_d384": {"bytes_per_launch": 18930944, "source_hash": "8808934b75c1e438"},
     # the DSA indexer: the tile score kernel (the selection kernel's traffic is in its profile)
     "dsa_prefill_bf16": {"bytes_per_launch": 139097088, "source_hash": "fda2993782a35635"},
     "dsa_decode_bf16": {"bytes_per_launch": 34638080, "source_hash": "fda2993782a35635"},

@@ -11,7 +11,7 @@
 // keys in tiles of BN, with both products register-tiled:
 //   S tile (64 x BN): thread (ty, tx) owns rows ty + 16 i and keys tx + 16 j
 //                     (i < 4, j < BN / 16), 16 FFMA per 8 shared-memory
-//                     vector loads at BN = 64;
+//                     vector loads at BN = 64, 12 per 7 at BN = 48;
 //   O tile (64 x D):  thread owns rows ty + 16 i and columns 4 tx + 64 g.
 // At head dims 256 and 384, whose CTAs take a whole SM, a grid of 64-row
 // tiles smaller than the SM count runs as 32-row CTAs instead (i < 2), twice
@@ -20,8 +20,9 @@
 // Head dims are padded to DP = 64, 128, 256 or 384 (the page's wider VAE
 // variant compiles the same kernel for head dims up to 384, "Kernel
 // structure"); columns past D are zero in shared memory and never stored.
-// Q, a K tile, a V tile and P must fit in shared memory: BN = 64 keys up to
-// DP = 256 (211 KB), 32 keys at DP = 384 (203 KB).
+// Q, a K tile, a V tile and P must fit in shared memory: BN = 48 keys up to
+// DP = 128 (95 KB, so two CTAs share an SM), 64 at DP = 256 (211 KB), 32 at
+// DP = 384 (203 KB).
 // With one 256-thread CTA per SM nothing else covers a tile's load latency,
 // so the loads run under the arithmetic: V of tile t is requested (cp.async,
 // global -> shared, no registers) before S of tile t is computed, and K of
@@ -40,7 +41,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int DP, int RI = 4>
 struct F32Config {
   static constexpr int BMr = 16 * RI;             // query rows per CTA
-  static constexpr int BN = DP <= 256 ? 64 : 32;  // keys per tile
+  static constexpr int BN = DP <= 128 ? 48 : DP <= 256 ? 64 : 32;  // keys per tile
   static constexpr int kKeysPerThread = BN / 16;
   static constexpr int kQStride = DP + 4;  // padded rows: conflict-free float4 reads
   static constexpr int kKStride = DP + 4;
@@ -50,13 +51,14 @@ struct F32Config {
   static constexpr size_t kSmemFloats =
       (size_t)BMr * kQStride + (size_t)BN * kKStride + (size_t)BN * kVStride + (size_t)BMr * kPStride;
   static constexpr size_t kSmemBytes = kSmemFloats * sizeof(float);
-  // Head dims up to 128: the register budget of one CTA per SM (which shared
-  // memory allows anyway) and deeper unrolling of both product loops, so more
-  // shared-memory loads are in flight (measured 2.6% faster on DiT; at 256 and
-  // 384 the compiler's own choice measured faster).
-  static constexpr int kMinBlocks = DP <= 128 ? 1 : 0;
-  static constexpr int kUnrollS = DP <= 128 ? 8 : 4;
-  static constexpr int kUnrollPV = DP <= 128 ? 4 : 2;
+  // Head dims up to 128: 48-key tiles leave room for two CTAs an SM, and the
+  // register budget is set to match (128 a thread), so 16 warps cover each
+  // other's shared-memory latency (measured 5% faster on DiT than one CTA with
+  // 64-key tiles and the full register budget); at 256 and 384 a CTA takes the
+  // SM and the compiler's own register choice measured fastest.
+  static constexpr int kMinBlocks = DP <= 128 ? 2 : 0;
+  static constexpr int kUnrollS = 4;
+  static constexpr int kUnrollPV = 2;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
