@@ -365,7 +365,8 @@ def reference_arm(args, world, rank):
             "warmup": args.warmup, "ms_per_step": tot_s * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, shaped like the pages' workloads)",
-            "config": workload_config(w, flops, flops_excl, 1),
+            # the same config as our arm at this world size (only rank 0 runs the oracle)
+            "config": workload_config(w, flops, flops_excl, world),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -654,7 +655,7 @@ def dsa_reference_arm(args, world, rank):
     line = {"metric": DSA_METRIC, "impl": "reference", "value": value, "unit": "TFLOP/s", "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_s * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic (seeded)", "config": dsa_config(w, flops, 1),
+            "data": "synthetic (seeded)", "config": dsa_config(w, flops, world),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
