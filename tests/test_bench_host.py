@@ -1,7 +1,8 @@
 """The bench's host-side bookkeeping on CPU: the attention FLOP count against
 the oracle's own visible keys, the DSA workloads' FLOP and byte counts against
-hand counts, and both reference arms (the CPU oracle timed on a bounded
-sample) printing a well-formed JSON line."""
+hand counts, both reference arms (the CPU oracle timed on a bounded sample)
+printing a well-formed JSON line, and the ncu traffic table belonging to the
+kernel sources in the tree."""
 import contextlib
 import io
 import json
@@ -112,3 +113,19 @@ def test_flop_count_matches_the_oracles_visible_keys(case):
         assert flops == 4 * w.D * w.Hq * int(vis.sum())
         assert excl == 4 * w.D * int(cnt.sum())
         assert excl < flops  # the case masks some visible keys
+
+
+def test_traffic_table_belongs_to_the_committed_sources():
+    """Every DRAM-traffic figure the bench reports was captured on the
+    kernel sources in the tree: its entry's source hash is that kernel
+    family's current hash (a kernel change without a new capture reports
+    traffic null, which this catches before a run does)."""
+    for key, ent in bench.NCU_TRAFFIC.items():
+        name, *flags = key.split("+")
+        if name in bench.DSA_WORKLOADS:
+            family = "dsa"
+        else:
+            w = bench.ALL_WORKLOADS[name]
+            family = bench.kernel_family(w, "splitkv" in flags, "f32split" in flags)
+        assert ent["bytes_per_launch"] > 0
+        assert ent["source_hash"] == bench.kernel_source_hash(family), key
